@@ -1,0 +1,21 @@
+"""Plain, slow, fp64 CPU oracle for batched draft verification.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this
+package: only the test suite, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it.  It shares no code with the CUDA
+library (no kernels, headers, helpers or constants) and imports nothing
+from it.
+
+Modules
+-------
+``verify``        the verification rules themselves (chain, tree, cascade),
+                  written step by step in float64 NumPy, one sequence at a time.
+``closed_forms``  the PipeSpec analytical model (expected tokens per step,
+                  steady-state verification probability and its recurrence).
+
+Every function states the passage it follows.  Points where the pages are
+silent or ambiguous follow the readings listed in the design notes; each is
+repeated in the docstring that depends on it.
+"""
+
+from . import closed_forms, verify  # noqa: F401

@@ -1,0 +1,332 @@
+"""Seeded synthetic workloads for batched draft verification.
+
+Shapes follow the five workloads the verification step is measured on:
+
+  greedy chain      B=4,   gamma=4,  V=1000,   float32, temperature ignored
+  sampling chain    B=32,  gamma=8,  V=32000,  bfloat16, T=1.0, alpha ~ 0.7
+  sampling chain    B=64,  gamma=5,  V=128256, bfloat16, T=0.7,
+                    alpha in {0.05, 0.3, 0.6, 0.9}
+  tree              B=16,  64 nodes (depth 6, branching 4/3/2/2/1/1),
+                    V=50257, bfloat16, T=1.0, alpha ~ 0.7
+  cascade           B=128, gamma1=8, gamma2=4, V=128256, bfloat16, T=1.0,
+                    alpha(M0,M1) ~ 0.8, alpha(M1,M2) ~ 0.6
+
+The vocabulary sizes stand in for the LLaMA-2 (32000), LLaMA-3 (128256) and
+GPT-2 (50257) families the pages use; the pages' datasets are not needed
+because the verification step consumes logits only.
+
+Logit model: draft logits Q ~ N(0, sigma_q^2); target logits
+P = a * Q + N(0, s^2).  Values are rounded to the stored dtype before anything
+reads them.  Drafted tokens are drawn from the draft softmax at the workload's
+temperature with the Gumbel-max trick (argmax of Q/T plus Gumbel noise), so
+that drafts follow q as speculative sampling assumes; the greedy workload
+drafts the draft argmax instead.  The noise scales were chosen by bisection on
+seeded calibration batches (tests/golden/make_calibration.py, which records
+the achieved mean acceptance next to each value) so that the mean acceptance
+sum_x min(p, q) lands near the stated alpha.
+
+Everything is NumPy on the host; callers move arrays to the device.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# bfloat16 storage
+# --------------------------------------------------------------------------
+
+def bf16_from_float32(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even.
+
+    Inputs here are finite, so no NaN special case is needed.
+    """
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))
+    return ((bits + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def float32_from_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float32 values (exact)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _store(x: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_from_float32(x) if dtype == "bf16" else np.ascontiguousarray(x, np.float32)
+
+
+def _values(stored: np.ndarray, dtype: str) -> np.ndarray:
+    return float32_from_bf16(stored) if dtype == "bf16" else stored
+
+
+def _gumbel_argmax(rng: np.random.Generator, scaled: np.ndarray) -> np.ndarray:
+    """argmax over the last axis of scaled + Gumbel(0, 1) noise."""
+    uni = rng.random(scaled.shape, dtype=np.float32)
+    with np.errstate(divide="ignore"):
+        g = -np.log(-np.log(uni))
+    return np.argmax(scaled + g, axis=-1)
+
+
+# --------------------------------------------------------------------------
+# specs
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class ChainSpec:
+    name: str
+    B: int
+    gamma: int
+    V: int
+    dtype: str            # "f32" | "bf16"
+    greedy: bool
+    temperature: float
+    sigma_q: float        # draft logit scale
+    a: float              # target = a * draft + noise
+    s: float              # target noise scale
+    alpha_target: float | None = None
+    pad: int = 0          # row stride = V + pad elements
+
+
+@dataclass(frozen=True)
+class TreeSpec:
+    name: str
+    B: int
+    V: int
+    dtype: str
+    greedy: bool
+    temperature: float
+    sigma_q: float
+    a: float
+    s: float
+    branching: tuple = (4, 3, 2, 2, 1, 1)
+    n_nodes: int = 64
+    alpha_target: float | None = None
+    pad: int = 0
+
+
+@dataclass(frozen=True)
+class CascadeSpec:
+    name: str
+    B: int
+    gamma1: int
+    gamma2: int
+    V: int
+    dtype: str
+    greedy: bool
+    temperature: float
+    sigma_q: float
+    a01: float
+    s01: float
+    a12: float
+    s12: float
+    alpha01_target: float | None = None
+    alpha12_target: float | None = None
+    pad: int = 0
+
+
+# Calibrated noise scales: see tests/golden/calibration.json for the achieved
+# mean acceptance of each value.
+SPECS = {
+    "greedy_chain_b4_g4_v1000_f32": ChainSpec(
+        "greedy_chain_b4_g4_v1000_f32", B=4, gamma=4, V=1000, dtype="f32",
+        greedy=True, temperature=1.0, sigma_q=2.0, a=1.0, s=0.5),
+    "sampling_chain_b32_g8_v32000_bf16": ChainSpec(
+        "sampling_chain_b32_g8_v32000_bf16", B=32, gamma=8, V=32000,
+        dtype="bf16", greedy=False, temperature=1.0, sigma_q=2.0, a=0.9,
+        s=0.748, alpha_target=0.7),
+    "sampling_chain_b64_g5_v128256_bf16_a05": ChainSpec(
+        "sampling_chain_b64_g5_v128256_bf16_a05", B=64, gamma=5, V=128256,
+        dtype="bf16", greedy=False, temperature=0.7, sigma_q=2.0, a=0.0535,
+        s=1.9971, alpha_target=0.05),
+    "sampling_chain_b64_g5_v128256_bf16_a30": ChainSpec(
+        "sampling_chain_b64_g5_v128256_bf16_a30", B=64, gamma=5, V=128256,
+        dtype="bf16", greedy=False, temperature=0.7, sigma_q=2.0, a=0.7402,
+        s=1.3448, alpha_target=0.3),
+    "sampling_chain_b64_g5_v128256_bf16_a60": ChainSpec(
+        "sampling_chain_b64_g5_v128256_bf16_a60", B=64, gamma=5, V=128256,
+        dtype="bf16", greedy=False, temperature=0.7, sigma_q=2.0, a=0.9331,
+        s=0.7192, alpha_target=0.6),
+    "sampling_chain_b64_g5_v128256_bf16_a90": ChainSpec(
+        "sampling_chain_b64_g5_v128256_bf16_a90", B=64, gamma=5, V=128256,
+        dtype="bf16", greedy=False, temperature=0.7, sigma_q=2.0, a=0.996,
+        s=0.1787, alpha_target=0.9),
+    "tree_b16_n64_v50257_bf16": TreeSpec(
+        "tree_b16_n64_v50257_bf16", B=16, V=50257, dtype="bf16", greedy=False,
+        temperature=1.0, sigma_q=2.0, a=0.9, s=0.75, alpha_target=0.7),
+    "cascade_b128_g8_g4_v128256_bf16": CascadeSpec(
+        "cascade_b128_g8_g4_v128256_bf16", B=128, gamma1=8, gamma2=4,
+        V=128256, dtype="bf16", greedy=False, temperature=1.0, sigma_q=2.0,
+        a01=0.9, s01=0.465, a12=0.9, s12=1.024, alpha01_target=0.8,
+        alpha12_target=0.6),
+}
+
+
+def with_sizes(spec, **kw):
+    """A copy of a spec with some fields replaced (e.g. a smaller B or V)."""
+    return dataclasses.replace(spec, **kw)
+
+
+# --------------------------------------------------------------------------
+# generators
+# --------------------------------------------------------------------------
+
+def _rng(seed: int, salt: int) -> np.random.Generator:
+    return np.random.default_rng([int(seed), int(salt)])
+
+
+def _pad(x: np.ndarray, pad: int) -> np.ndarray:
+    if pad == 0:
+        return x
+    width = list(x.shape)
+    width[-1] += pad
+    out = np.zeros(width, dtype=x.dtype)
+    out[..., : x.shape[-1]] = x
+    return out
+
+
+def make_chain(spec: ChainSpec, seed: int = 0) -> dict:
+    """Chain workload: target [B, gamma+1, V+pad], draft [B, gamma, V+pad],
+    tokens int32 [B, gamma], u float32 [B, gamma], v float32 [B],
+    prefix_len int32 [B]."""
+    rng = _rng(seed, 1)
+    B, g, V = spec.B, spec.gamma, spec.V
+    target = np.empty((B, g + 1, V), np.uint16 if spec.dtype == "bf16" else np.float32)
+    draft = np.empty((B, g, V), target.dtype)
+    tokens = np.empty((B, g), np.int32)
+    for b in range(B):  # one sequence at a time keeps the float32 temporaries small
+        q = rng.standard_normal((g + 1, V), dtype=np.float32) * np.float32(spec.sigma_q)
+        p = np.float32(spec.a) * q + rng.standard_normal((g + 1, V), dtype=np.float32) * np.float32(spec.s)
+        qs = _store(q[:g], spec.dtype)
+        draft[b] = qs
+        target[b] = _store(p, spec.dtype)
+        qv = _values(qs, spec.dtype)
+        if spec.greedy:
+            tokens[b] = np.argmax(qv, axis=-1)
+        else:
+            tokens[b] = _gumbel_argmax(rng, qv / np.float32(spec.temperature))
+    u = rng.random((B, g), dtype=np.float32)
+    v = rng.random(B, dtype=np.float32)
+    prefix = rng.integers(0, 4096, B, dtype=np.int32)
+    return dict(kind="chain", spec=spec, target=_pad(target, spec.pad),
+                draft=_pad(draft, spec.pad), tokens=tokens, u=u, v=v,
+                prefix_len=prefix)
+
+
+def tree_topology(branching=(4, 3, 2, 2, 1, 1), n_nodes=64) -> np.ndarray:
+    """Parent array of the draft tree used by the tree workload.
+
+    The full tree with the given per-depth branching is enumerated as paths of
+    0-based sibling ranks; the n_nodes paths with the smallest key
+    (sum of ranks, depth, path) are kept and numbered in key order, so that
+    parent[i] < i and the kept set is closed under parents.  For the default
+    arguments the kept nodes per depth are 1/4/9/11/13/13/13.
+    """
+    paths = [()]
+    frontier = [()]
+    for width in branching:
+        frontier = [p + (r,) for p in frontier for r in range(width)]
+        paths.extend(frontier)
+    paths.sort(key=lambda p: (sum(p), len(p), p))
+    kept = paths[:n_nodes]
+    index = {p: i for i, p in enumerate(kept)}
+    parent = np.array([-1] + [index[p[:-1]] for p in kept[1:]], dtype=np.int32)
+    return parent
+
+
+def make_tree(spec: TreeSpec, seed: int = 0) -> dict:
+    """Tree workload: parent int32 [B, N], tokens int32 [B, N] (tokens[:, 0]
+    unused), target / draft [B, N, V+pad], u float32 [B, N], v float32 [B],
+    prefix_len int32 [B].  Each child's token is drawn from the draft softmax
+    of its parent's row, independently of its siblings (with replacement)."""
+    rng = _rng(seed, 2)
+    B, V = spec.B, spec.V
+    parent1 = tree_topology(spec.branching, spec.n_nodes)
+    N = len(parent1)
+    parent = np.tile(parent1, (B, 1))
+    dt = np.uint16 if spec.dtype == "bf16" else np.float32
+    target = np.empty((B, N, V), dt)
+    draft = np.empty((B, N, V), dt)
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        q = rng.standard_normal((N, V), dtype=np.float32) * np.float32(spec.sigma_q)
+        p = np.float32(spec.a) * q + rng.standard_normal((N, V), dtype=np.float32) * np.float32(spec.s)
+        qs = _store(q, spec.dtype)
+        draft[b] = qs
+        target[b] = _store(p, spec.dtype)
+        qv = _values(qs, spec.dtype) / np.float32(spec.temperature)
+        if spec.greedy:
+            tokens[b, 1:] = np.argmax(qv[parent1[1:]], axis=-1)
+        else:
+            tokens[b, 1:] = _gumbel_argmax(rng, qv[parent1[1:]])
+    u = rng.random((B, N), dtype=np.float32)
+    v = rng.random(B, dtype=np.float32)
+    prefix = rng.integers(0, 4096, B, dtype=np.int32)
+    depth = np.zeros(N, np.int64)
+    for i in range(1, N):
+        depth[i] = depth[parent1[i]] + 1
+    return dict(kind="tree", spec=spec, parent=parent, tokens=tokens,
+                target=_pad(target, spec.pad), draft=_pad(draft, spec.pad),
+                u=u, v=v, prefix_len=prefix, max_depth=int(depth.max()))
+
+
+def make_cascade(spec: CascadeSpec, seed: int = 0) -> dict:
+    """Cascade workload: l0 [B, g1, V+pad] (M_0), l1 [B, g1+1, V+pad] (M_1),
+    l2 [B, g2, V+pad] (M_2), tokens int32 [B, g1] drawn from M_0, u1 [B, g1],
+    v1 [B], u2 [B, g2], v2 [B], base0 = base1 int32 [B]."""
+    rng = _rng(seed, 3)
+    B, g1, g2, V = spec.B, spec.gamma1, spec.gamma2, spec.V
+    dt = np.uint16 if spec.dtype == "bf16" else np.float32
+    l0 = np.empty((B, g1, V), dt)
+    l1 = np.empty((B, g1 + 1, V), dt)
+    l2 = np.empty((B, g2, V), dt)
+    tokens = np.empty((B, g1), np.int32)
+    for b in range(B):
+        m0 = rng.standard_normal((g1 + 1, V), dtype=np.float32) * np.float32(spec.sigma_q)
+        m1 = np.float32(spec.a01) * m0 + rng.standard_normal((g1 + 1, V), dtype=np.float32) * np.float32(spec.s01)
+        m2 = np.float32(spec.a12) * m1[:g2] + rng.standard_normal((g2, V), dtype=np.float32) * np.float32(spec.s12)
+        s0 = _store(m0[:g1], spec.dtype)
+        l0[b] = s0
+        l1[b] = _store(m1, spec.dtype)
+        l2[b] = _store(m2, spec.dtype)
+        v0 = _values(s0, spec.dtype)
+        if spec.greedy:
+            tokens[b] = np.argmax(v0, axis=-1)
+        else:
+            tokens[b] = _gumbel_argmax(rng, v0 / np.float32(spec.temperature))
+    u1 = rng.random((B, g1), dtype=np.float32)
+    v1 = rng.random(B, dtype=np.float32)
+    u2 = rng.random((B, g2), dtype=np.float32)
+    v2 = rng.random(B, dtype=np.float32)
+    base = rng.integers(0, 4096, B, dtype=np.int32)
+    return dict(kind="cascade", spec=spec, l0=_pad(l0, spec.pad),
+                l1=_pad(l1, spec.pad), l2=_pad(l2, spec.pad), tokens=tokens,
+                u1=u1, v1=v1, u2=u2, v2=v2, base0=base.copy(), base1=base.copy())
+
+
+def make(spec, seed: int = 0) -> dict:
+    if isinstance(spec, str):
+        spec = SPECS[spec]
+    if isinstance(spec, ChainSpec):
+        return make_chain(spec, seed)
+    if isinstance(spec, TreeSpec):
+        return make_tree(spec, seed)
+    if isinstance(spec, CascadeSpec):
+        return make_cascade(spec, seed)
+    raise TypeError(type(spec))
+
+
+def logit_bytes(w: dict) -> int:
+    """Bytes of logits handed to one verification call (rows x V x size)."""
+    spec = w["spec"]
+    es = 2 if spec.dtype == "bf16" else 4
+    if w["kind"] == "chain":
+        rows = spec.gamma + 1 + (0 if spec.greedy else spec.gamma)
+    elif w["kind"] == "tree":
+        rows = w["target"].shape[1] * (1 if spec.greedy else 2)
+    else:
+        rows = spec.gamma1 + 1 + spec.gamma2 + (0 if spec.greedy else spec.gamma1)
+    return spec.B * rows * spec.V * es
