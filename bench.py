@@ -1,0 +1,521 @@
+"""Benchmark of batched draft verification on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one verification call (row statistics + per-sequence walk) over one
+batch of the workload.  The default workload is the sampling chain
+B=32, gamma=8, V=32000, bf16, T=1.0, mean acceptance ~0.7; --workload selects
+any of workloads.synth.SPECS.  Inputs are synthetic and seeded.
+
+Timing: W warm-up steps, then a loaded soak of about one second (clocks are
+sampled over it and the timed region), then exactly K steps between CUDA
+events on the launching stream, with a barrier and a device synchronize on
+both sides; the max over ranks is reported.  Consecutive steps rotate over
+enough distinct copies of the input batch (more than 3x the L2 size in
+total) that every step reads its logits from HBM.  The steps are replayed
+from a CUDA graph that holds one call per input copy.
+
+Printed on rank 0: one JSON line with the metric (verified draft tokens/s),
+logits GB/s, the roofline of the row-statistics kernel (measured with CUDA
+events around that kernel alone), the end-to-end number through the public
+call with host buffers, and the CPU oracle timed on a bounded sample.
+
+--impl reference times the CPU oracle itself (the slow, plainly written
+reference) on the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "sampling_chain_b32_g8_v32000_bf16"
+METRIC = "verified draft tokens/sec and logits GB/s vs GB300 HBM peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+STATS_SOURCES = ["draft_verification_gb300/csrc/stats.cu", "draft_verification_gb300/csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# workload bookkeeping (sizes only)
+# --------------------------------------------------------------------------
+
+def draft_tokens_per_call(w) -> int:
+    s = w["spec"]
+    if w["kind"] == "chain":
+        return s.B * s.gamma
+    if w["kind"] == "tree":
+        return s.B * (w["parent"].shape[1] - 1)
+    return s.B * (s.gamma1 + s.gamma2)
+
+
+def workload_config(w) -> dict:
+    s = w["spec"]
+    cfg = {"workload": s.name, "kind": w["kind"], "batch": s.B, "vocab": s.V,
+           "logit_dtype": s.dtype, "mode": "greedy" if s.greedy else "sampling",
+           "temperature": s.temperature}
+    if w["kind"] == "chain":
+        cfg["gamma"] = s.gamma
+        cfg["alpha_target"] = s.alpha_target
+    elif w["kind"] == "tree":
+        cfg["nodes"] = int(w["parent"].shape[1])
+        cfg["max_depth"] = w["max_depth"]
+        cfg["alpha_target"] = s.alpha_target
+    else:
+        cfg.update(gamma1=s.gamma1, gamma2=s.gamma2, alpha01_target=s.alpha01_target,
+                   alpha12_target=s.alpha12_target)
+    return cfg
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            mp = json.load(fh)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if k in mp:
+                return float(mp[k]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def stats_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in STATS_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the statistics kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"row_stats_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("- ") and " = " in line:
+                k, v = line[2:].split(" = ", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_hash") != stats_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+        self.proc = None
+        props = torch.cuda.get_device_properties(device)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            self.gpu = "GPU-" + str(uuid)
+        else:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            self.gpu = vis.split(",")[device.index] if vis else str(device.index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_rate(w, budget_s: float):
+    """Verified draft tokens/s of the CPU oracle on whole calls of the
+    workload, repeated until about `budget_s` seconds of CPU work."""
+    from oracle import verify as V  # the reference is only used on this leg
+    s = w["spec"]
+    sample_B = s.B
+    done = 0
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        if w["kind"] == "chain":
+            V.verify_chain(w["target"], w["draft"], w["tokens"], w["u"], w["v"], w["prefix_len"],
+                           s.temperature, s.greedy, s.dtype, V=s.V)
+        elif w["kind"] == "tree":
+            V.verify_tree(w["parent"], w["tokens"], w["target"], w["draft"], w["u"], w["v"],
+                          w["prefix_len"], s.temperature, s.greedy, w["max_depth"], s.dtype, V=s.V)
+        else:
+            V.verify_cascade(w["l0"], w["l1"], w["l2"], w["tokens"], w["u1"], w["v1"], w["u2"],
+                             w["v2"], w["base0"], w["base1"], s.temperature, s.greedy, s.dtype, V=s.V)
+        calls += 1
+        done += draft_tokens_per_call(w)
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el, f"{calls} whole calls of {sample_B} sequences ({el:.1f} s, float64 NumPy)", el
+
+
+def subset(w, nseq):
+    """The first nseq sequences of a workload (for a bounded CPU sample)."""
+    import dataclasses
+    out = dict(w)
+    out["spec"] = dataclasses.replace(w["spec"], B=nseq)
+    for k, v in w.items():
+        if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w["spec"].B:
+            out[k] = v[:nseq]
+    return out
+
+
+def bounded_sample(w, budget_s):
+    """Shrink the batch so one oracle call takes at most about budget_s / 3."""
+    from oracle import verify as V  # noqa: F401
+    probe = subset(w, 1)
+    t0 = time.perf_counter()
+    oracle_rate(probe, 0.0)
+    per_seq = time.perf_counter() - t0
+    nseq = max(1, min(w["spec"].B, int(budget_s / 3 / max(per_seq, 1e-6))))
+    return subset(w, nseq), nseq
+
+
+def run_reference(args, w):
+    sample, nseq = bounded_sample(w, args.cpu_seconds)
+    rate, desc, el = oracle_rate(sample, args.cpu_seconds)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * draft_tokens_per_call(w) / rate,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {nseq} of {w['spec'].B} sequences; " + desc},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def device_inputs(w, dev):
+    import torch
+    s = w["spec"]
+
+    def logits(a):
+        if s.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    out = {}
+    for k, v in w.items():
+        if not isinstance(v, np.ndarray):
+            continue
+        if k in ("target", "draft", "l0", "l1", "l2"):
+            out[k] = logits(v)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v)).to(dev)
+    return out
+
+
+def make_plan(w, t, workspace=None):
+    import draft_verification_gb300 as dv
+    s = w["spec"]
+    if w["kind"] == "chain":
+        return dv.ChainPlan(t["target"], t["draft"], t["tokens"], t["u"], t["v"], t["prefix_len"],
+                            greedy=s.greedy, temperature=s.temperature, workspace=workspace)
+    if w["kind"] == "tree":
+        return dv.TreePlan(t["parent"], t["tokens"], t["target"], t["draft"], t["u"], t["v"],
+                           t["prefix_len"], max_depth=w["max_depth"], greedy=s.greedy,
+                           temperature=s.temperature, workspace=workspace)
+    return dv.CascadePlan(t["l0"], t["l1"], t["l2"], t["tokens"], t["u1"], t["v1"], t["u2"], t["v2"],
+                          t["base0"], t["base1"], greedy=s.greedy, temperature=s.temperature,
+                          workspace=workspace)
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+    import draft_verification_gb300 as dv
+    from workloads.synth import logit_bytes
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dv.build_library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    bytes_per_call = logit_bytes(w)
+    n_sets = max(2, math.ceil(3 * l2 / bytes_per_call) + 1)
+    n_sets = min(n_sets, max(2, int(0.5 * props.total_memory // max(bytes_per_call, 1))))
+
+    base = device_inputs(w, dev)
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
+    ws = torch.empty(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
+    plans = [make_plan(w, t, ws) for t in sets]
+    stream = torch.cuda.Stream(dev)
+
+    def one_pass(s):
+        for p in plans:
+            p.run(s)
+
+    # warm-up (eager), then capture one call per input copy into a graph
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            plans[i % n_sets].run(stream)
+    stream.synchronize()
+    launch = "cuda_graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            one_pass(stream)
+        stream.synchronize()
+    except Exception as exc:  # graph capture unavailable: time eager launches
+        launch = f"eager ({type(exc).__name__})"
+        graph = None
+
+    def run_steps(k):
+        full, rest = divmod(k, n_sets)
+        for _ in range(full):
+            if graph is not None:
+                graph.replay()
+            else:
+                one_pass(stream)
+        for i in range(rest):
+            plans[i].run(stream)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:  # loaded soak so the clocks settle
+            run_steps(n_sets * 20)
+            stream.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+    clock_info = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # the dominant kernel alone: CUDA events around the row-statistics launch
+    n_ev = min(200, max(20, args.steps))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        for i, (b, e) in enumerate(evs):
+            b.record(stream)
+            e.record(stream)
+        stream.synchronize()
+        for i, (b, e) in enumerate(evs):
+            p = plans[i % n_sets]
+            p.set_stats_events(b, e)
+            p.run(stream)
+            p.set_stats_events(None, None)
+        stream.synchronize()
+    stats_ms = statistics.mean(b.elapsed_time(e) for b, e in evs)
+
+    # end to end through the public call, host buffers in and out
+    e2e = e2e_rate(args, w, dev, stream)
+
+    tokens = draft_tokens_per_call(w)
+    value = tokens * world / (ms * 1e-3)
+    logits_gbs = bytes_per_call / (ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    stats_gbs = bytes_per_call / (stats_ms * 1e-3) / 1e9
+    check = plans[0].run(stream)
+    stream.synchronize()
+    s = w["spec"]
+    accepted = None
+    if w["kind"] == "chain":
+        accepted = float((check["accept_len"].float() + 1).mean().item())
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; shapes of the pages' model families)",
+        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       l2_policy=f"rotating {n_sets} input copies ({n_sets * bytes_per_call / 2**20:.0f} MB "
+                                 f"> 3 x L2 {l2 / 2**20:.0f} MB)", launch=launch),
+        "logits_gbs": logits_gbs,
+        "logits_frac_of_peak": logits_gbs / peak,
+        "accepted_tokens_per_s": None if accepted is None else accepted * s.B * world / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "row_stats", "achieved": stats_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": stats_gbs / peak, "peak_source": peak_src,
+                     "kernel_ms": stats_ms, "algorithmic_bytes": bytes_per_call,
+                     "traffic": profiled_traffic(s.name)},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clock_info,
+    }
+    return line
+
+
+def plan_workspace(w):
+    import draft_verification_gb300 as dv
+    s = w["spec"]
+    if w["kind"] == "chain":
+        return dv.workspace_bytes("chain", s.B, s.gamma, s.V)
+    if w["kind"] == "tree":
+        return dv.workspace_bytes("tree", s.B, int(w["parent"].shape[1]), s.V)
+    return dv.workspace_bytes("cascade", s.B, s.gamma1, s.gamma2, s.V)
+
+
+def e2e_rate(args, w, dev, stream):
+    """Same metric through the public verify_* call with pinned host tensors:
+    each step copies the step's inputs to the device and reads the results
+    back (both inside the timed region)."""
+    import torch
+    import draft_verification_gb300 as dv
+    s = w["spec"]
+    host = {}
+    for k, v in w.items():
+        if isinstance(v, np.ndarray):
+            t = torch.from_numpy(np.ascontiguousarray(v))
+            if k in ("target", "draft", "l0", "l1", "l2") and s.dtype == "bf16":
+                t = t.view(torch.int16).view(torch.bfloat16)
+            host[k] = t.pin_memory()
+    h2d = sum(t.numel() * t.element_size() for k, t in host.items()
+              if not (s.greedy and k in ("draft", "l0", "u", "v", "u1", "v1", "u2", "v2")))
+
+    def call():
+        with torch.cuda.stream(stream):
+            if w["kind"] == "chain":
+                o = dv.verify_chain(host["target"], None if s.greedy else host["draft"], host["tokens"],
+                                    host["u"], host["v"], host["prefix_len"], greedy=s.greedy,
+                                    temperature=s.temperature, device=dev, stream=stream)
+            elif w["kind"] == "tree":
+                o = dv.verify_tree(host["parent"], host["tokens"], host["target"], host["draft"],
+                                   host["u"], host["v"], host["prefix_len"], max_depth=w["max_depth"],
+                                   greedy=s.greedy, temperature=s.temperature, device=dev, stream=stream)
+            else:
+                o = dv.verify_cascade(host["l0"], host["l1"], host["l2"], host["tokens"], host["u1"],
+                                      host["v1"], host["u2"], host["v2"], host["base0"], host["base1"],
+                                      greedy=s.greedy, temperature=s.temperature, device=dev,
+                                      stream=stream)
+        return o
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    d2h = 0
+    for _ in range(n):
+        o = call()
+        stream.synchronize()
+        d2h = sum(v.numel() * v.element_size() for v in o.values())
+    el = time.perf_counter() - t0
+    return {"value": draft_tokens_per_call(w) / (el / n), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": 1000.0 * el / n, "steps": n}
+
+
+def main():
+    args = parse()
+    from workloads import synth
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.workload not in synth.SPECS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.SPECS)}")
+    w = synth.make(synth.SPECS[args.workload], seed=args.seed + rank)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, w, rank, world, dist)
+    if rank == 0 and not args.no_cpu_baseline:
+        sample, nseq = bounded_sample(w, args.cpu_seconds)
+        rate, desc, _ = oracle_rate(sample, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {nseq} of {w['spec'].B} sequences; " + desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,293 @@
+"""Torch-facing binding of the verification library (argument marshalling only).
+
+PyTorch supplies device memory and the current stream; every step of the
+verification runs in the CUDA kernels behind the C ABI (include/spec_verify.h).
+
+Two ways to call:
+  * ``verify_chain / verify_tree / verify_cascade``: one call, returns a dict
+    of output tensors.  Device tensors stay on the device; CPU tensors are
+    copied to ``device`` first and the results copied back (end-to-end use).
+  * ``ChainPlan / TreePlan / CascadePlan``: bind the input and output buffers
+    once, then ``plan.run()`` launches with no Python-side allocation (a
+    prebuilt argument struct and one ctypes call).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.float32: L.SPEC_F32, torch.bfloat16: L.SPEC_BF16}
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _rows(t: torch.Tensor, rows: int, name: str) -> int:
+    """Row stride (elements) of a [B, rows, V] logit view; checks the layout
+    the C ABI assumes: row (b, i) starts at (b * rows + i) * ld."""
+    if t.dim() != 3 or t.shape[1] != rows:
+        raise ValueError(f"{name}: expected [B, {rows}, V], got {tuple(t.shape)}")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"{name}: logits must be float32 or bfloat16")
+    if t.stride(2) != 1:
+        raise ValueError(f"{name}: logits must have unit element stride")
+    if rows == 1:  # one row per sequence: the row stride is the batch stride
+        return t.stride(0) if t.shape[0] > 1 else t.shape[2]
+    if t.shape[0] > 1 and t.stride(0) != rows * t.stride(1):
+        raise ValueError(f"{name}: rows must be evenly strided")
+    return t.stride(1)
+
+
+def _i32(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous int32 tensor")
+    return t
+
+
+def _f32(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous float32 tensor")
+    return t
+
+
+def _check(code: int, what: str):
+    if code != L.SPEC_OK:
+        raise RuntimeError(f"{what} failed: {L.status_string(code)} ({code})")
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _event_handle(ev):
+    if ev is None:
+        return None
+    if ev.cuda_event == 0:  # torch creates the event lazily on first record
+        ev.record()
+    return C.c_void_p(ev.cuda_event)
+
+
+class _Plan:
+    def run(self, stream=None):
+        _check(self._call(C.byref(self.args), _stream_handle(stream)), type(self).__name__)
+        return self.out
+
+    def set_stats_events(self, begin, end):
+        """Record these torch.cuda.Events around the row-statistics kernel."""
+        self.args.stats_begin = _event_handle(begin)
+        self.args.stats_end = _event_handle(end)
+
+
+class ChainPlan(_Plan):
+    """Chain verification bound to fixed buffers.  See spec_verify_chain."""
+
+    def __init__(self, target, draft, tokens, u=None, v=None, prefix_len=None, *,
+                 greedy=False, temperature=1.0, V=None, workspace=None, want_probs=True):
+        B, R, width = target.shape
+        gamma = R - 1
+        V = width if V is None else V
+        dev = target.device
+        ld = _rows(target, gamma + 1, "target")
+        if not greedy and gamma > 0:
+            if draft is None or draft.dtype != target.dtype or _rows(draft, gamma, "draft") != ld:
+                raise ValueError("draft: same dtype and row stride as target required")
+        lib = L.lib()
+        self.keep = [target, draft, tokens, u, v, prefix_len]
+        self.out = dict(
+            accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_token=torch.empty(B, dtype=torch.int32, device=dev),
+            rollback_idx=torch.empty(B, dtype=torch.int32, device=dev),
+            seq_error=torch.empty(B, dtype=torch.int32, device=dev),
+            error_word=torch.zeros(1, dtype=torch.int32, device=dev),
+        )
+        if want_probs:
+            self.out["p_at_draft"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+            self.out["q_at_draft"] = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+            self.out["resid_mass"] = torch.empty(B, dtype=torch.float32, device=dev)
+        need = lib.spec_chain_workspace_size(B, gamma, V)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        a = L.ChainArgs()
+        a.B, a.gamma, a.V, a.ld = B, gamma, V, ld
+        a.dtype = _DTYPES[target.dtype]
+        a.mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        a.temperature = float(temperature)
+        a.target_logits = _ptr(target)
+        a.draft_logits = _ptr(draft) if not greedy else None
+        a.draft_tokens = _ptr(_i32(tokens, "tokens"))
+        a.u = _ptr(_f32(u, "u")) if not greedy else None
+        a.v = _ptr(_f32(v, "v")) if not greedy else None
+        a.prefix_len = _ptr(_i32(prefix_len, "prefix_len"))
+        o = self.out
+        a.accept_len, a.out_token = _ptr(o["accept_len"]), _ptr(o["out_token"])
+        a.rollback_idx, a.seq_error = _ptr(o["rollback_idx"]), _ptr(o["seq_error"])
+        a.error_word = _ptr(o["error_word"])
+        a.p_at_draft = _ptr(o.get("p_at_draft"))
+        a.q_at_draft = _ptr(o.get("q_at_draft"))
+        a.resid_mass = _ptr(o.get("resid_mass"))
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_chain
+
+
+class TreePlan(_Plan):
+    """Tree verification bound to fixed buffers.  See spec_verify_tree."""
+
+    def __init__(self, parent, tokens, target, draft, u=None, v=None, prefix_len=None, *,
+                 max_depth, greedy=False, temperature=1.0, V=None, workspace=None):
+        B, N, width = target.shape
+        V = width if V is None else V
+        dev = target.device
+        ld = _rows(target, N, "target")
+        if not greedy:
+            if draft is None or draft.dtype != target.dtype or _rows(draft, N, "draft") != ld:
+                raise ValueError("draft: same dtype and row stride as target required")
+        lib = L.lib()
+        self.keep = [parent, tokens, target, draft, u, v, prefix_len]
+        self.out = dict(
+            path_len=torch.empty(B, dtype=torch.int32, device=dev),
+            path_nodes=torch.empty(B, max_depth + 1, dtype=torch.int32, device=dev),
+            out_token=torch.empty(B, dtype=torch.int32, device=dev),
+            rollback_idx=torch.empty(B, dtype=torch.int32, device=dev),
+            seq_error=torch.empty(B, dtype=torch.int32, device=dev),
+            error_word=torch.zeros(1, dtype=torch.int32, device=dev),
+        )
+        need = lib.spec_tree_workspace_size(B, N, V)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        a = L.TreeArgs()
+        a.B, a.N, a.max_depth, a.V, a.ld = B, N, int(max_depth), V, ld
+        a.dtype = _DTYPES[target.dtype]
+        a.mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        a.temperature = float(temperature)
+        a.parent = _ptr(_i32(parent, "parent"))
+        a.node_tokens = _ptr(_i32(tokens, "tokens"))
+        a.target_logits = _ptr(target)
+        a.draft_logits = _ptr(draft) if not greedy else None
+        a.u = _ptr(_f32(u, "u")) if not greedy else None
+        a.v = _ptr(_f32(v, "v")) if not greedy else None
+        a.prefix_len = _ptr(_i32(prefix_len, "prefix_len"))
+        o = self.out
+        a.path_len, a.path_nodes = _ptr(o["path_len"]), _ptr(o["path_nodes"])
+        a.out_token, a.rollback_idx = _ptr(o["out_token"]), _ptr(o["rollback_idx"])
+        a.seq_error, a.error_word = _ptr(o["seq_error"]), _ptr(o["error_word"])
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_tree
+
+
+class CascadePlan(_Plan):
+    """PipeSpec cascade snapshot bound to fixed buffers.  See spec_verify_cascade."""
+
+    def __init__(self, l0, l1, l2, tokens, u1=None, v1=None, u2=None, v2=None, base0=None,
+                 base1=None, *, greedy=False, temperature=1.0, V=None, workspace=None):
+        B, g1p1, width = l1.shape
+        g1 = g1p1 - 1
+        g2 = l2.shape[1]
+        V = width if V is None else V
+        dev = l1.device
+        ld = _rows(l1, g1 + 1, "l1")
+        if _rows(l2, g2, "l2") != ld or l2.dtype != l1.dtype:
+            raise ValueError("l2: same dtype and row stride as l1 required")
+        if not greedy and (l0 is None or l0.dtype != l1.dtype or _rows(l0, g1, "l0") != ld):
+            raise ValueError("l0: same dtype and row stride as l1 required")
+        lib = L.lib()
+        self.keep = [l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1]
+        names = ("a1", "t1", "a2", "w2", "t2", "t2_valid", "r0", "r1", "committed", "seq_error")
+        self.out = {k: torch.empty(B, dtype=torch.int32, device=dev) for k in names}
+        self.out["error_word"] = torch.zeros(1, dtype=torch.int32, device=dev)
+        need = lib.spec_cascade_workspace_size(B, g1, g2, V)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        a = L.CascadeArgs()
+        a.B, a.gamma1, a.gamma2, a.V, a.ld = B, g1, g2, V, ld
+        a.dtype = _DTYPES[l1.dtype]
+        a.mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        a.temperature = float(temperature)
+        a.l0 = _ptr(l0) if not greedy else None
+        a.l1, a.l2 = _ptr(l1), _ptr(l2)
+        a.draft_tokens = _ptr(_i32(tokens, "tokens"))
+        if not greedy:
+            a.u1, a.v1 = _ptr(_f32(u1, "u1")), _ptr(_f32(v1, "v1"))
+            a.u2, a.v2 = _ptr(_f32(u2, "u2")), _ptr(_f32(v2, "v2"))
+        a.base0, a.base1 = _ptr(_i32(base0, "base0")), _ptr(_i32(base1, "base1"))
+        for k in names:
+            setattr(a, k, _ptr(self.out[k]))
+        a.error_word = _ptr(self.out["error_word"])
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_cascade
+
+
+def _to_device(xs, device):
+    moved = []
+    for x in xs:
+        if isinstance(x, torch.Tensor) and x.device.type == "cpu":
+            x = x.to(device, non_blocking=True)
+        moved.append(x)
+    return moved
+
+
+def _finish(out, host):
+    if not host:
+        return out
+    return {k: v.to("cpu", non_blocking=True) for k, v in out.items()}
+
+
+def verify_chain(target, draft, tokens, u=None, v=None, prefix_len=None, *, greedy=False,
+                 temperature=1.0, V=None, device="cuda", stream=None):
+    """Verify B draft chains; returns accept_len, out_token, rollback_idx,
+    p_at_draft, q_at_draft, resid_mass, seq_error, error_word."""
+    host = target.device.type == "cpu"
+    if host:
+        target, draft, tokens, u, v, prefix_len = _to_device(
+            [target, draft, tokens, u, v, prefix_len], device)
+    plan = ChainPlan(target, draft, tokens, u, v, prefix_len, greedy=greedy,
+                     temperature=temperature, V=V)
+    return _finish(plan.run(stream), host)
+
+
+def verify_tree(parent, tokens, target, draft, u=None, v=None, prefix_len=None, *, max_depth,
+                greedy=False, temperature=1.0, V=None, device="cuda", stream=None):
+    """Walk B draft trees; returns path_len, path_nodes, out_token,
+    rollback_idx, seq_error, error_word."""
+    host = target.device.type == "cpu"
+    if host:
+        parent, tokens, target, draft, u, v, prefix_len = _to_device(
+            [parent, tokens, target, draft, u, v, prefix_len], device)
+    plan = TreePlan(parent, tokens, target, draft, u, v, prefix_len, max_depth=max_depth,
+                    greedy=greedy, temperature=temperature, V=V)
+    return _finish(plan.run(stream), host)
+
+
+def verify_cascade(l0, l1, l2, tokens, u1=None, v1=None, u2=None, v2=None, base0=None,
+                   base1=None, *, greedy=False, temperature=1.0, V=None, device="cuda",
+                   stream=None):
+    """One PipeSpec cascade snapshot; returns a1, t1, a2, w2, t2, t2_valid,
+    r0, r1, committed, seq_error, error_word."""
+    host = l1.device.type == "cpu"
+    if host:
+        l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1 = _to_device(
+            [l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1], device)
+    plan = CascadePlan(l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1, greedy=greedy,
+                       temperature=temperature, V=V)
+    return _finish(plan.run(stream), host)
+
+
+def workspace_bytes(kind: str, *sizes) -> int:
+    fn = {"chain": "spec_chain_workspace_size", "tree": "spec_tree_workspace_size",
+          "cascade": "spec_cascade_workspace_size"}[kind]
+    return int(getattr(L.lib(), fn)(*sizes))

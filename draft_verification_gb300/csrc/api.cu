@@ -1,0 +1,289 @@
+// C ABI of the verification library: argument checks, workspace sizing and
+// the two launches of every call (row statistics, then the per-sequence
+// walker cluster).  Nothing here allocates or synchronises.
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "spec_verify.h"
+
+namespace sv {
+
+cudaError_t launch_walker(const void* kernel, void** args, int B, int cluster, size_t dyn_smem,
+                          cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(cluster));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = dyn_smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
+namespace {
+
+constexpr int kMaxV = 8 * 256 * 2048;  // walker tiles per CTA bound (walk.cuh)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+spec_status check_common(int B, int V, long long ld, spec_dtype dtype, spec_mode mode,
+                         float temperature) {
+  if (B < 1 || B > (1 << 24)) return SPEC_EINVAL;
+  if (V < 1 || V > kMaxV) return SPEC_EINVAL;
+  if (ld < V || ld > (1LL << 40)) return SPEC_EINVAL;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EDTYPE;
+  if (mode != SPEC_GREEDY && mode != SPEC_SAMPLE) return SPEC_EDTYPE;
+  if (mode == SPEC_SAMPLE && !(temperature > 0.f && std::isfinite(temperature))) return SPEC_EINVAL;
+  return SPEC_OK;
+}
+
+// log2(e) / T, rounded once to float: the scale applied to every logit.
+float logit_scale(float temperature) {
+  return static_cast<float>(1.4426950408889634073599 / static_cast<double>(temperature));
+}
+
+spec_status run(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA; }
+
+spec_status record(cudaEvent_t ev, cudaStream_t s) {
+  if (ev == nullptr) return SPEC_OK;
+  return run(cudaEventRecord(ev, s));
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+const char* spec_status_string(spec_status status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_EDTYPE: return "unknown dtype or mode";
+    case SPEC_EALIGN: return "logit base address not 16-byte aligned";
+    case SPEC_EWORKSPACE: return "workspace missing or too small";
+    case SPEC_ECUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+size_t spec_chain_workspace_size(int B, int gamma, int V) {
+  if (B < 1 || gamma < 0 || V < 1) return 0;
+  return stats_workspace_bytes(B, 2 * gamma + 1, V);
+}
+
+size_t spec_tree_workspace_size(int B, int N, int V) {
+  if (B < 1 || N < 1 || V < 1) return 0;
+  return stats_workspace_bytes(B, 2 * N, V);
+}
+
+size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V) {
+  if (B < 1 || gamma1 < 1 || gamma2 < 1 || V < 1) return 0;
+  return stats_workspace_bytes(B, 2 * gamma1 + 1 + gamma2, V);
+}
+
+spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
+  if (a == nullptr) return SPEC_EINVAL;
+  spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
+  if (st != SPEC_OK) return st;
+  const bool greedy = a->mode == SPEC_GREEDY;
+  const bool bf16 = a->dtype == SPEC_BF16;
+  if (a->gamma < 0 || a->gamma > 32) return SPEC_EINVAL;
+  if (!a->target_logits || !a->accept_len || !a->out_token) return SPEC_EINVAL;
+  if (a->gamma > 0 && !a->draft_tokens) return SPEC_EINVAL;
+  if (!greedy && (!a->v || (a->gamma > 0 && (!a->draft_logits || !a->u)))) return SPEC_EINVAL;
+  if (!aligned16(a->target_logits) || (!greedy && a->gamma > 0 && !aligned16(a->draft_logits)))
+    return SPEC_EALIGN;
+  const int rows = greedy ? a->gamma + 1 : 2 * a->gamma + 1;
+  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
+  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+
+  StatsParams sp = {};
+  sp.set[0] = RowSet{a->target_logits, a->gamma + 1};
+  sp.set[1] = RowSet{a->draft_logits, a->gamma};
+  sp.nsets = (greedy || a->gamma == 0) ? 1 : 2;
+  sp.rows_per_seq = rows;
+  sp.B = a->B;
+  sp.V = a->V;
+  sp.ld = a->ld;
+  sp.chunks = stats_chunks(a->V);
+  sp.c = greedy ? 1.f : logit_scale(a->temperature);
+  sp.partials = static_cast<float2*>(a->workspace);
+
+  ChainParams cp = {};
+  cp.B = a->B;
+  cp.gamma = a->gamma;
+  cp.V = a->V;
+  cp.ld = a->ld;
+  cp.c = sp.c;
+  cp.target = a->target_logits;
+  cp.draft = a->draft_logits;
+  cp.tokens = a->draft_tokens;
+  cp.u = a->u;
+  cp.v = a->v;
+  cp.prefix = a->prefix_len;
+  cp.accept_len = a->accept_len;
+  cp.out_token = a->out_token;
+  cp.rollback = a->rollback_idx;
+  cp.p_at = a->p_at_draft;
+  cp.q_at = a->q_at_draft;
+  cp.resid = a->resid_mass;
+  cp.seq_error = a->seq_error;
+  cp.error_word = a->error_word;
+  cp.partials = sp.partials;
+  cp.chunks = sp.chunks;
+  cp.rows_per_seq = rows;
+  cp.cluster = walker_cluster(a->V);
+
+  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
+  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
+  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
+  return run(launch_chain_walk(cp, bf16, greedy, stream));
+}
+
+spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
+  if (a == nullptr) return SPEC_EINVAL;
+  spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
+  if (st != SPEC_OK) return st;
+  const bool greedy = a->mode == SPEC_GREEDY;
+  const bool bf16 = a->dtype == SPEC_BF16;
+  if (a->N < 1 || a->N > 1024) return SPEC_EINVAL;
+  if (a->max_depth < 0 || a->max_depth > a->N - 1) return SPEC_EINVAL;
+  if (!a->parent || !a->node_tokens || !a->target_logits || !a->path_len || !a->path_nodes ||
+      !a->out_token)
+    return SPEC_EINVAL;
+  if (!greedy && (!a->draft_logits || !a->u || !a->v)) return SPEC_EINVAL;
+  if (!aligned16(a->target_logits) || (!greedy && !aligned16(a->draft_logits))) return SPEC_EALIGN;
+  const int rows = greedy ? a->N : 2 * a->N;
+  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
+  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+
+  StatsParams sp = {};
+  sp.set[0] = RowSet{a->target_logits, a->N};
+  sp.set[1] = RowSet{a->draft_logits, a->N};
+  sp.nsets = greedy ? 1 : 2;
+  sp.rows_per_seq = rows;
+  sp.B = a->B;
+  sp.V = a->V;
+  sp.ld = a->ld;
+  sp.chunks = stats_chunks(a->V);
+  sp.c = greedy ? 1.f : logit_scale(a->temperature);
+  sp.partials = static_cast<float2*>(a->workspace);
+
+  TreeParams tp = {};
+  tp.B = a->B;
+  tp.N = a->N;
+  tp.max_depth = a->max_depth;
+  tp.V = a->V;
+  tp.ld = a->ld;
+  tp.c = sp.c;
+  tp.parent = a->parent;
+  tp.tokens = a->node_tokens;
+  tp.target = a->target_logits;
+  tp.draft = a->draft_logits;
+  tp.u = a->u;
+  tp.v = a->v;
+  tp.prefix = a->prefix_len;
+  tp.path_len = a->path_len;
+  tp.path_nodes = a->path_nodes;
+  tp.out_token = a->out_token;
+  tp.rollback = a->rollback_idx;
+  tp.seq_error = a->seq_error;
+  tp.error_word = a->error_word;
+  tp.partials = sp.partials;
+  tp.chunks = sp.chunks;
+  tp.rows_per_seq = rows;
+  tp.cluster = walker_cluster(a->V);
+
+  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
+  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
+  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
+  return run(launch_tree_walk(tp, bf16, greedy, stream));
+}
+
+spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream) {
+  if (a == nullptr) return SPEC_EINVAL;
+  spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
+  if (st != SPEC_OK) return st;
+  const bool greedy = a->mode == SPEC_GREEDY;
+  const bool bf16 = a->dtype == SPEC_BF16;
+  if (a->gamma1 < 1 || a->gamma1 > 32) return SPEC_EINVAL;
+  if (a->gamma2 < 1 || a->gamma2 > 32 || a->gamma2 > a->gamma1 + 1) return SPEC_EINVAL;
+  if (!a->l1 || !a->l2 || !a->draft_tokens) return SPEC_EINVAL;
+  if (!a->a1 || !a->t1 || !a->a2 || !a->w2 || !a->t2 || !a->t2_valid || !a->r0 || !a->r1 ||
+      !a->committed)
+    return SPEC_EINVAL;
+  if (!greedy && (!a->l0 || !a->u1 || !a->v1 || !a->u2 || !a->v2)) return SPEC_EINVAL;
+  if (!aligned16(a->l1) || !aligned16(a->l2) || (!greedy && !aligned16(a->l0))) return SPEC_EALIGN;
+  const int rows = greedy ? a->gamma1 + 1 + a->gamma2 : 2 * a->gamma1 + 1 + a->gamma2;
+  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
+  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+
+  StatsParams sp = {};
+  if (greedy) {
+    sp.set[0] = RowSet{a->l1, a->gamma1 + 1};
+    sp.set[1] = RowSet{a->l2, a->gamma2};
+    sp.nsets = 2;
+  } else {
+    sp.set[0] = RowSet{a->l0, a->gamma1};
+    sp.set[1] = RowSet{a->l1, a->gamma1 + 1};
+    sp.set[2] = RowSet{a->l2, a->gamma2};
+    sp.nsets = 3;
+  }
+  sp.rows_per_seq = rows;
+  sp.B = a->B;
+  sp.V = a->V;
+  sp.ld = a->ld;
+  sp.chunks = stats_chunks(a->V);
+  sp.c = greedy ? 1.f : logit_scale(a->temperature);
+  sp.partials = static_cast<float2*>(a->workspace);
+
+  CascadeParams cp = {};
+  cp.B = a->B;
+  cp.g1 = a->gamma1;
+  cp.g2 = a->gamma2;
+  cp.V = a->V;
+  cp.ld = a->ld;
+  cp.c = sp.c;
+  cp.l0 = a->l0;
+  cp.l1 = a->l1;
+  cp.l2 = a->l2;
+  cp.tokens = a->draft_tokens;
+  cp.u1 = a->u1;
+  cp.v1 = a->v1;
+  cp.u2 = a->u2;
+  cp.v2 = a->v2;
+  cp.base0 = a->base0;
+  cp.base1 = a->base1;
+  cp.a1 = a->a1;
+  cp.t1 = a->t1;
+  cp.a2 = a->a2;
+  cp.w2 = a->w2;
+  cp.t2 = a->t2;
+  cp.t2_valid = a->t2_valid;
+  cp.r0 = a->r0;
+  cp.r1 = a->r1;
+  cp.committed = a->committed;
+  cp.seq_error = a->seq_error;
+  cp.error_word = a->error_word;
+  cp.partials = sp.partials;
+  cp.chunks = sp.chunks;
+  cp.rows_per_seq = rows;
+  cp.cluster = walker_cluster(a->V);
+
+  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
+  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
+  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
+  return run(launch_cascade_walk(cp, bf16, greedy, stream));
+}
+
+}  // extern "C"

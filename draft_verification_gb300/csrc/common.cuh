@@ -1,0 +1,139 @@
+// Device helpers shared by the verification kernels (sm_103a).
+//
+// Numerical conventions used by every kernel, so that the row statistics,
+// the accept tests and the sampling passes agree bit for bit:
+//   c      = log2(e) / T, rounded once to float on the host
+//   M(m)   = __fmul_rn(m, c): the scaled maximum of a row with raw maximum m
+//   e(x)   = ex2(__fmaf_rn(x, c, -M)) = 2^(x c - M), the unnormalised weight
+//   s      = sum of e(x) over the row
+//   p(x)   = e(x) / s
+// The unrounded x c - M of one fused multiply-add keeps every weight relative
+// to the same shift M, so p(x) computed later from (M, s) is consistent with s.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;          // threads per CTA for every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 8192;           // row elements per row-statistics CTA
+constexpr int kTileElems = 8 * kThreads;  // walker tile: 8 contiguous elements per thread
+
+constexpr float kInf = __builtin_huge_valf();
+
+// bfloat16 is handled as raw 16-bit patterns: the value is the top half of
+// a float32 with the same bits.
+using bf16_t = uint16_t;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float load_elem(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_elem(const bf16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+// 16-byte streaming load that does not allocate in L1 (rows are read once
+// by the statistics pass).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// 16-byte load through the normal cache path (walker re-reads hit L2).
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max that returns NaN when either operand is NaN, so that a NaN logit
+// poisons the row statistics instead of disappearing.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+__device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
+
+// 2^(x c - M): the unnormalised softmax weight of logit x.
+__device__ __forceinline__ float weight(float x, float c, float M) {
+  return ex2(__fmaf_rn(x, c, -M));
+}
+
+// ---------------------------------------------------------------------------
+// (max, sum) pairs of the online softmax
+// ---------------------------------------------------------------------------
+struct MaxSum {
+  float m;  // raw maximum logit (-inf for an empty set)
+  float s;  // sum of 2^(x c - M(m))
+};
+
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b, float c) {
+  const float m = fmax_nan(a.m, b.m);
+  if (m == -kInf) return {m, 0.f};
+  const float M = scaled_max(m, c);
+  const float ea = ex2(scaled_max(a.m, c) - M);
+  const float eb = ex2(scaled_max(b.m, c) - M);
+  return {m, __fadd_rn(__fmul_rn(a.s, ea), __fmul_rn(b.s, eb))};
+}
+
+__device__ __forceinline__ MaxSum ms_warp_merge(MaxSum v, float c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MaxSum w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = ms_merge(v, w, c);  // commutative bit for bit, so every lane agrees
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// (value, index) pairs of the greedy argmax: larger value wins, ties go to
+// the lower index; index -1 means "nothing seen".
+// ---------------------------------------------------------------------------
+struct ArgMax {
+  float v;
+  int i;
+};
+
+__device__ __forceinline__ ArgMax am_merge(ArgMax a, ArgMax b) {
+  if (b.i < 0) return a;
+  if (a.i < 0) return b;
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+
+__device__ __forceinline__ ArgMax am_warp_merge(ArgMax v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax w{__shfl_xor_sync(0xffffffffu, v.v, o), __shfl_xor_sync(0xffffffffu, v.i, o)};
+    v = am_merge(v, w);
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace sv

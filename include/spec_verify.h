@@ -1,0 +1,236 @@
+/*
+ * spec_verify.h - batched draft verification for speculative decoding, GB300.
+ *
+ * One call verifies a batch of drafted continuations against target-model
+ * logits and returns, per sequence, how much of the draft is kept, the token
+ * emitted where verification stops, and the buffer length to roll back to.
+ *
+ * Sources:
+ *  - Pith review of "PipeSpec: Breaking Stage Dependencies in Hierarchical
+ *    LLM Decoding" (arXiv 2505.01572), "What carries the argument": a stage
+ *    verifies the previous buffer against its own prediction, appends the
+ *    longest matching prefix and, on a mismatch, rolls the earlier buffers
+ *    back to the last verified token.  "Circularity Check": the acceptance
+ *    formula is that of Leviathan et al.  "Reading between the lines": the
+ *    reported runs use greedy decoding.
+ *  - "Accelerating LLM Inference with Staged Speculative Decoding"
+ *    (arXiv 2308.04623), abstract: the speculative batch is a tree, and a
+ *    second speculative stage is added.
+ *  - Pith review of "CLaSp: In-Context Layer Skip for Self-Speculative
+ *    Decoding" (arXiv 2505.24196), "Assumptions & free parameters":
+ *    speculative sampling with a matching draft distribution is lossless.
+ *
+ * The rule (sampling mode).  p = softmax(target logits / T) and
+ * q = softmax(draft logits / T) per position.  A drafted token x is kept
+ * when u < min(1, p(x)/q(x)) for its uniform u in [0, 1) (strict; r >= 1
+ * always keeps; q(x) = 0 keeps when p(x) > 0 and rejects when both are 0).
+ * At the first rejection one token is drawn from max(0, p - q) / Z; when
+ * every draft is kept one bonus token is drawn from the next target row.
+ * A draw with uniform v returns the first index y (ascending) whose running
+ * sum exceeds v * Z.  Greedy mode keeps a draft while it equals the target
+ * argmax (ties to the lowest index) and emits the argmax where it stops;
+ * greedy compares raw logits and ignores the temperature.
+ *
+ * Conventions for every entry point.
+ *  - All array pointers are DEVICE pointers, row-major, caller-owned.  The
+ *    library never allocates, frees or synchronises; every call is
+ *    asynchronous on `stream`.  Inputs are only read; outputs are written
+ *    completely (including on a data error).
+ *  - Logit arrays hold float32 (SPEC_F32) or bfloat16 (SPEC_BF16) values.
+ *    Row r of a logit array starts at element r * ld; only the first V
+ *    elements of a row are read.  ld >= V.  Each logit array's base address
+ *    must be 16-byte aligned (any ld is accepted; misaligned rows are read
+ *    with realigned loads).
+ *  - int arrays are int32; uniform arrays are float32 in [0, 1).
+ *  - Argument errors (a NULL required pointer, a size out of range, T <= 0
+ *    in sampling mode, a misaligned logit base, a short workspace) return a
+ *    negative spec_status before anything is launched.  A launch failure
+ *    returns SPEC_ECUDA.
+ *  - Data errors found on the device never trap: they set bits in the
+ *    optional per-sequence `seq_error` array and are OR-ed into the optional
+ *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2 or 4 gets
+ *    empty outputs: accept length 0, tokens -1, rollback = prefix length.
+ *  - The workspace is scratch for one call; size it with the matching
+ *    *_workspace_size function.  Two calls in flight at the same time need
+ *    two workspaces.  Results are deterministic: the same inputs on the same
+ *    GPU give bit-identical outputs.
+ *  - stats_begin / stats_end: optional events (NULL to skip) recorded on
+ *    `stream` immediately before and after the row-statistics kernel, the
+ *    pass that streams every logit row once.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spec_status {
+  SPEC_OK = 0,
+  SPEC_EINVAL = -1,      /* a size or pointer argument is invalid            */
+  SPEC_EDTYPE = -2,      /* unknown dtype or mode                           */
+  SPEC_EALIGN = -3,      /* a logit base address is not 16-byte aligned     */
+  SPEC_EWORKSPACE = -4,  /* workspace NULL or smaller than required          */
+  SPEC_ECUDA = -5        /* a CUDA launch failed                             */
+} spec_status;
+
+typedef enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+typedef enum spec_mode { SPEC_GREEDY = 0, SPEC_SAMPLE = 1 } spec_mode;
+
+/* data-error bits (seq_error / error_word) */
+#define SPEC_ERR_TOKEN 1      /* a drafted / node token outside [0, V)          */
+#define SPEC_ERR_PARENT 2     /* malformed tree parent array or depth > max     */
+#define SPEC_ERR_NONFINITE 4  /* a logit row with NaN or +inf, or no finite entry */
+#define SPEC_ERR_ZERO_MASS 8  /* residual mass 0 after a rejection: the token was
+                                 drawn from p instead (outputs stay valid)       */
+
+/* ---------------------------------------------------------------------- */
+/* Chain verification: B sequences, each with a gamma-token draft.         */
+/* PipeSpec review, "What carries the argument" (longest kept prefix and   */
+/* rollback); the accept / residual / bonus rule cited in its Circularity  */
+/* Check.                                                                   */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_chain_args {
+  int B;                       /* sequences, >= 1                                  */
+  int gamma;                   /* drafted tokens per sequence, 0..32               */
+  int V;                       /* vocabulary size, >= 1                            */
+  long long ld;                /* row stride of the logit arrays (elements), >= V  */
+  spec_dtype dtype;
+  spec_mode mode;
+  float temperature;           /* > 0 and finite in SPEC_SAMPLE                     */
+  const void* target_logits;   /* [B, gamma+1, ld]: row i scores position i; row
+                                  gamma is the bonus position                       */
+  const void* draft_logits;    /* [B, gamma, ld]; SPEC_SAMPLE only (may be NULL in
+                                  greedy mode: it is not read)                      */
+  const int* draft_tokens;     /* [B, gamma]                                        */
+  const float* u;              /* [B, gamma] accept uniforms; SPEC_SAMPLE only      */
+  const float* v;              /* [B] draw uniform; SPEC_SAMPLE only                */
+  const int* prefix_len;       /* [B] tokens before the window; NULL = all 0        */
+  int* accept_len;             /* out [B]: kept drafts a, 0..gamma                  */
+  int* out_token;              /* out [B]: correction (a < gamma) or bonus token    */
+  int* rollback_idx;           /* out [B], optional: prefix_len + a                 */
+  float* p_at_draft;           /* out [B, gamma], optional: p_i(d_i) (0 in greedy)  */
+  float* q_at_draft;           /* out [B, gamma], optional: q_i(d_i) (0 in greedy)  */
+  float* resid_mass;           /* out [B], optional: mass Z of the distribution the
+                                  token was drawn from (0 in greedy)                */
+  int* seq_error;              /* out [B], optional: data-error bits                */
+  int* error_word;             /* in/out, optional: data-error bits OR-ed in        */
+  void* workspace;
+  size_t workspace_bytes;
+  cudaEvent_t stats_begin;     /* optional, see the file comment                    */
+  cudaEvent_t stats_end;
+} spec_chain_args;
+
+size_t spec_chain_workspace_size(int B, int gamma, int V);
+spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Tree verification: each sequence carries a draft tree of N nodes.       */
+/* Staged Speculative Decoding, abstract (the speculative batch as a       */
+/* tree).  Row n of the logit arrays is the distribution over the children */
+/* of node n; node 0 is the root (the last verified token).  Children are  */
+/* tried in ascending node index.  Sampling: a child c is kept when         */
+/* u[c] < min(1, p(tok_c)/q(tok_c)) for the current p; a rejected child    */
+/* replaces p with max(0, p - q) renormalised (q unchanged) before the next */
+/* sibling; when no child is kept the token is drawn from the current p     */
+/* (from the node's own target row at a leaf).  Greedy: the first child     */
+/* whose token is the target argmax is kept; otherwise the argmax is        */
+/* emitted.  The walk repeats from the kept child.                          */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_tree_args {
+  int B;                       /* sequences, >= 1                                  */
+  int N;                       /* nodes per tree including the root, 1..1024       */
+  int max_depth;               /* deepest node allowed, 0..N-1; path_nodes has
+                                  max_depth+1 entries per sequence                  */
+  int V;
+  long long ld;
+  spec_dtype dtype;
+  spec_mode mode;
+  float temperature;
+  const int* parent;           /* [B, N]: parent[0] = -1, 0 <= parent[i] < i      */
+  const int* node_tokens;      /* [B, N]: token of node i (entry 0 not read)        */
+  const void* target_logits;   /* [B, N, ld]                                        */
+  const void* draft_logits;    /* [B, N, ld]; SPEC_SAMPLE only                      */
+  const float* u;              /* [B, N]: u[c] for node c's own test; SPEC_SAMPLE   */
+  const float* v;              /* [B]; SPEC_SAMPLE only                             */
+  const int* prefix_len;       /* [B]; NULL = all 0                                 */
+  int* path_len;               /* out [B]: kept nodes on the root path, 0..max_depth */
+  int* path_nodes;             /* out [B, max_depth+1]: 0 (root), then the kept
+                                  nodes in order, -1 padded (all -1 on a data error) */
+  int* out_token;              /* out [B]                                           */
+  int* rollback_idx;           /* out [B], optional: prefix_len + path_len          */
+  int* seq_error;              /* out [B], optional                                 */
+  int* error_word;             /* in/out, optional                                  */
+  void* workspace;
+  size_t workspace_bytes;
+  cudaEvent_t stats_begin;
+  cudaEvent_t stats_end;
+} spec_tree_args;
+
+size_t spec_tree_workspace_size(int B, int N, int V);
+spec_status spec_verify_tree(const spec_tree_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* PipeSpec 3-model cascade, one synchronous snapshot: M_0 drafts O_0,     */
+/* M_1 verifies it (stage 1) and M_2 verifies the first tokens of O_1      */
+/* (stage 2).  PipeSpec review, "What carries the argument" and abstract;  */
+/* Staged Speculative Decoding, abstract (a second speculative stage).     */
+/* Stage 1: the chain rule with p = M_1, q = M_0 over the gamma1 drafts:    */
+/* a1 kept, t1 = correction or bonus (M_1 row gamma1); O_1 = d[0..a1) ++ t1. */
+/* Stage 2: the chain rule with p = M_2, q = M_1 over the first             */
+/* w2 = min(gamma2, a1+1) tokens of O_1: a2 kept; on a rejection t2 is drawn */
+/* from max(0, p2 - p1) (t2_valid = 1); when all w2 are kept no bonus is    */
+/* drawn (t2 = -1, t2_valid = 0).  Rollback: a final-stage rejection rolls  */
+/* O_0 back too: r0 = base0 + (rejected ? min(a1, a2) : a1),                */
+/* r1 = base1 + (rejected ? a2 : w2); committed = a2 + t2_valid.            */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_cascade_args {
+  int B;
+  int gamma1;                  /* stage-1 window, 1..32                             */
+  int gamma2;                  /* stage-2 window, 1..min(32, gamma1+1)              */
+  int V;
+  long long ld;
+  spec_dtype dtype;
+  spec_mode mode;
+  float temperature;
+  const void* l0;              /* [B, gamma1, ld]   M_0 logits; SPEC_SAMPLE only    */
+  const void* l1;              /* [B, gamma1+1, ld] M_1 logits                      */
+  const void* l2;              /* [B, gamma2, ld]   M_2 logits                      */
+  const int* draft_tokens;     /* [B, gamma1]: the O_0 window                       */
+  const float* u1;             /* [B, gamma1]; SPEC_SAMPLE only                     */
+  const float* v1;             /* [B]                                               */
+  const float* u2;             /* [B, gamma2]                                       */
+  const float* v2;             /* [B]                                               */
+  const int* base0;            /* [B] length of O_0 before the window; NULL = 0     */
+  const int* base1;            /* [B] length of O_1 before the window; NULL = 0     */
+  int* a1;                     /* out [B] each                                      */
+  int* t1;
+  int* a2;
+  int* w2;
+  int* t2;
+  int* t2_valid;
+  int* r0;
+  int* r1;
+  int* committed;
+  int* seq_error;              /* out [B], optional                                 */
+  int* error_word;             /* in/out, optional                                  */
+  void* workspace;
+  size_t workspace_bytes;
+  cudaEvent_t stats_begin;
+  cudaEvent_t stats_end;
+} spec_cascade_args;
+
+size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V);
+spec_status spec_verify_cascade(const spec_cascade_args* args, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* spec_status_string(spec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

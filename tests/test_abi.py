@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+symbol include/spec_verify.h declares, the ctypes structures match the C
+layout, and argument errors are reported before anything is launched."""
+
+import ctypes as C
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from draft_verification_gb300 import _lib, build
+    if shutil.which("nvcc") is None and not os.path.exists(build.lib_path()):
+        pytest.skip("neither nvcc nor a built library is available")
+    build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(spec_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) == 7, names
+    for n in names:
+        assert hasattr(lib, n), n
+    from draft_verification_gb300 import _lib
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_struct_layout_matches_header(tmp_path):
+    from draft_verification_gb300 import _lib
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or CUDA headers missing")
+    structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
+               "spec_cascade_args": _lib.CascadeArgs}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0;}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            s, f, v = line.split()
+            got[(s, f)] = int(v)
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == C.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_status_strings(lib):
+    from draft_verification_gb300 import _lib
+    assert _lib.status_string(0) == "ok"
+    assert "workspace" in _lib.status_string(-4)
+
+
+def test_workspace_sizes(lib):
+    # chain: (2 gamma + 1) rows x ceil(V / 8192) chunks x 8 bytes per sequence
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == 64 * 11 * 16 * 8
+    assert lib.spec_tree_workspace_size(16, 64, 50257) == 16 * 128 * 7 * 8
+    assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == 128 * 21 * 16 * 8
+    assert lib.spec_chain_workspace_size(0, 5, 10) == 0
+
+
+def _chain(**kw):
+    from draft_verification_gb300 import _lib
+    a = _lib.ChainArgs()
+    a.B, a.gamma, a.V, a.ld = 2, 3, 100, 100
+    a.dtype, a.mode, a.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
+    fake = 0x10000  # never dereferenced: validation fails first, or no launch happens
+    for f in ("target_logits", "draft_logits", "draft_tokens", "u", "v", "accept_len",
+              "out_token", "workspace"):
+        setattr(a, f, fake)
+    a.workspace_bytes = 1 << 20
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("B", 0, -1), ("V", 0, -1), ("ld", 50, -1), ("gamma", 33, -1), ("gamma", -1, -1),
+    ("temperature", 0.0, -1), ("temperature", float("inf"), -1), ("dtype", 7, -2),
+    ("mode", 5, -2), ("target_logits", 0x10002, -3), ("draft_logits", 0x10008, -3),
+    ("workspace_bytes", 8, -4), ("workspace", None, -4), ("accept_len", None, -1),
+    ("u", None, -1),
+])
+def test_chain_argument_errors_are_reported_before_launch(lib, field, value, code):
+    a = _chain(**{field: value})
+    assert lib.spec_verify_chain(C.byref(a), None) == code
+
+
+def test_tree_and_cascade_argument_errors(lib):
+    from draft_verification_gb300 import _lib
+    t = _lib.TreeArgs()
+    t.B, t.N, t.max_depth, t.V, t.ld = 1, 1025, 3, 10, 10
+    t.dtype, t.mode, t.temperature = 1, 1, 1.0
+    assert lib.spec_verify_tree(C.byref(t), None) == -1
+    t.N, t.max_depth = 8, 8  # max_depth > N - 1
+    assert lib.spec_verify_tree(C.byref(t), None) == -1
+    c = _lib.CascadeArgs()
+    c.B, c.gamma1, c.gamma2, c.V, c.ld = 1, 4, 6, 10, 10  # gamma2 > gamma1 + 1
+    c.dtype, c.mode, c.temperature = 1, 1, 1.0
+    assert lib.spec_verify_cascade(C.byref(c), None) == -1
+    assert lib.spec_verify_chain(None, None) == -1
