@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="plain eager loop for an ncu capture: warm-up + steps calls, one input copy")
     return ap.parse_args()
 
 
@@ -486,6 +488,19 @@ def e2e_rate(args, w, dev, stream):
             "ms_per_step": 1000.0 * el / n, "steps": n}
 
 
+def run_profile(args, w):
+    """W + K eager calls on one input copy, nothing else (an ncu target)."""
+    import torch
+    import draft_verification_gb300 as dv
+    dev = torch.device("cuda", 0)
+    dv.build_library()
+    plan = make_plan(w, device_inputs(w, dev))
+    for _ in range(args.warmup + args.steps):
+        plan.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": w["spec"].name, "calls": args.warmup + args.steps}))
+
+
 def main():
     args = parse()
     from workloads import synth
@@ -498,6 +513,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, w)
+        return
+
+    if args.profile:
+        run_profile(args, w)
         return
 
     dist = None
