@@ -2,8 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one verification call (row statistics + per-sequence walk) over one
-batch of the workload.  The default workload is the sampling chain
+One step = one verification call (one fused kernel: row statistics, then the
+per-sequence walk) over one batch of the workload.  The default workload is the sampling chain
 B=32, gamma=8, V=32000, bf16, T=1.0, mean acceptance ~0.7; --workload selects
 any of workloads.synth.SPECS.  Inputs are synthetic and seeded.
 
@@ -16,9 +16,9 @@ total) that every step reads its logits from HBM.  The steps are replayed
 from a CUDA graph that holds one call per input copy.
 
 Printed on rank 0: one JSON line with the metric (verified draft tokens/s),
-logits GB/s, the roofline of the row-statistics kernel (measured with CUDA
-events around that kernel alone), the end-to-end number through the public
-call with host buffers, and the CPU oracle timed on a bounded sample.
+logits GB/s, the roofline of the call's single kernel (measured with CUDA
+events around each launch), the end-to-end number through the public call
+with host buffers, and the CPU oracle timed on a bounded sample.
 
 --impl reference times the CPU oracle itself (the slow, plainly written
 reference) on the same workload and prints the same JSON line with
@@ -45,7 +45,9 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "sampling_chain_b32_g8_v32000_bf16"
 METRIC = "verified draft tokens/sec and logits GB/s vs GB300 HBM peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
-STATS_SOURCES = ["draft_verification_gb300/csrc/stats.cu", "draft_verification_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification_gb300/csrc/stats.cuh",
+                  "draft_verification_gb300/csrc/walk.cuh", "draft_verification_gb300/csrc/common.cuh"]
+KERNEL_NAME = {"chain": "chain_kernel", "tree": "tree_kernel", "cascade": "cascade_kernel"}
 
 
 def parse():
@@ -108,18 +110,18 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
 
 
-def stats_source_hash() -> str:
+def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for p in STATS_SOURCES:
+    for p in KERNEL_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the statistics kernel from the committed ncu
+    """DRAM bytes per launch of the verification kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"row_stats_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"verify_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -128,7 +130,7 @@ def profiled_traffic(workload: str):
             if line.startswith("- ") and " = " in line:
                 k, v = line[2:].split(" = ", 1)
                 fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_hash") != stats_source_hash():
+    if fields.get("source_hash") != kernel_source_hash():
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))
@@ -317,7 +319,7 @@ def run_ours(args, w, rank, world, dist):
 
     base = device_inputs(w, dev)
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
-    ws = torch.empty(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
     plans = [make_plan(w, t, ws) for t in sets]
     stream = torch.cuda.Stream(dev)
 
@@ -375,21 +377,16 @@ def run_ours(args, w, rank, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # the dominant kernel alone: CUDA events around the row-statistics launch
+    # the one kernel of a call, alone: CUDA events around each launch
     n_ev = min(200, max(20, args.steps))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
     with torch.cuda.stream(stream):
         for i, (b, e) in enumerate(evs):
             b.record(stream)
+            plans[i % n_sets].run(stream)
             e.record(stream)
         stream.synchronize()
-        for i, (b, e) in enumerate(evs):
-            p = plans[i % n_sets]
-            p.set_stats_events(b, e)
-            p.run(stream)
-            p.set_stats_events(None, None)
-        stream.synchronize()
-    stats_ms = statistics.mean(b.elapsed_time(e) for b, e in evs)
+    kernel_ms = statistics.mean(b.elapsed_time(e) for b, e in evs)
 
     # end to end through the public call, host buffers in and out
     e2e = e2e_rate(args, w, dev, stream)
@@ -398,7 +395,7 @@ def run_ours(args, w, rank, world, dist):
     value = tokens * world / (ms * 1e-3)
     logits_gbs = bytes_per_call / (ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    stats_gbs = bytes_per_call / (stats_ms * 1e-3) / 1e9
+    kernel_gbs = bytes_per_call / (kernel_ms * 1e-3) / 1e9
     check = plans[0].run(stream)
     stream.synchronize()
     s = w["spec"]
@@ -417,12 +414,12 @@ def run_ours(args, w, rank, world, dist):
         "logits_gbs": logits_gbs,
         "logits_frac_of_peak": logits_gbs / peak,
         "accepted_tokens_per_s": None if accepted is None else accepted * s.B * world / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "kernel": "row_stats", "achieved": stats_gbs, "peak": peak,
-                     "unit": "GB/s", "frac": stats_gbs / peak, "peak_source": peak_src,
-                     "kernel_ms": stats_ms, "algorithmic_bytes": bytes_per_call,
+        "roofline": {"bound": "hbm", "kernel": KERNEL_NAME[w["kind"]], "achieved": kernel_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak, "peak_source": peak_src,
+                     "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_per_call,
                      "traffic": profiled_traffic(s.name)},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clock_info,
     }
     return line

@@ -15,7 +15,7 @@ from .build import lib_path
 SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EALIGN, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, -4, -5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_GREEDY, SPEC_SAMPLE = 0, 1
-ERR_TOKEN, ERR_PARENT, ERR_NONFINITE, ERR_ZERO_MASS = 1, 2, 4, 8
+ERR_TOKEN, ERR_PARENT, ERR_NONFINITE, ERR_ZERO_MASS, ERR_INTERNAL = 1, 2, 4, 8, 16
 
 _vp = C.c_void_p
 
@@ -29,8 +29,7 @@ class ChainArgs(C.Structure):
         ("accept_len", _vp), ("out_token", _vp), ("rollback_idx", _vp),
         ("p_at_draft", _vp), ("q_at_draft", _vp), ("resid_mass", _vp),
         ("seq_error", _vp), ("error_word", _vp),
-        ("workspace", _vp), ("workspace_bytes", C.c_size_t),
-        ("stats_begin", _vp), ("stats_end", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
     ]
 
 
@@ -43,8 +42,7 @@ class TreeArgs(C.Structure):
         ("draft_logits", _vp), ("u", _vp), ("v", _vp), ("prefix_len", _vp),
         ("path_len", _vp), ("path_nodes", _vp), ("out_token", _vp),
         ("rollback_idx", _vp), ("seq_error", _vp), ("error_word", _vp),
-        ("workspace", _vp), ("workspace_bytes", C.c_size_t),
-        ("stats_begin", _vp), ("stats_end", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
     ]
 
 
@@ -59,8 +57,7 @@ class CascadeArgs(C.Structure):
         ("a1", _vp), ("t1", _vp), ("a2", _vp), ("w2", _vp), ("t2", _vp),
         ("t2_valid", _vp), ("r0", _vp), ("r1", _vp), ("committed", _vp),
         ("seq_error", _vp), ("error_word", _vp),
-        ("workspace", _vp), ("workspace_bytes", C.c_size_t),
-        ("stats_begin", _vp), ("stats_end", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
     ]
 
 

@@ -69,23 +69,10 @@ def _stream_handle(stream):
     return C.c_void_p(s.cuda_stream)
 
 
-def _event_handle(ev):
-    if ev is None:
-        return None
-    if ev.cuda_event == 0:  # torch creates the event lazily on first record
-        ev.record()
-    return C.c_void_p(ev.cuda_event)
-
-
 class _Plan:
     def run(self, stream=None):
         _check(self._call(C.byref(self.args), _stream_handle(stream)), type(self).__name__)
         return self.out
-
-    def set_stats_events(self, begin, end):
-        """Record these torch.cuda.Events around the row-statistics kernel."""
-        self.args.stats_begin = _event_handle(begin)
-        self.args.stats_end = _event_handle(end)
 
 
 class ChainPlan(_Plan):
@@ -116,7 +103,7 @@ class ChainPlan(_Plan):
             self.out["resid_mass"] = torch.empty(B, dtype=torch.float32, device=dev)
         need = lib.spec_chain_workspace_size(B, gamma, V)
         if workspace is None:
-            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.ChainArgs()
         a.B, a.gamma, a.V, a.ld = B, gamma, V, ld
@@ -165,7 +152,7 @@ class TreePlan(_Plan):
         )
         need = lib.spec_tree_workspace_size(B, N, V)
         if workspace is None:
-            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.TreeArgs()
         a.B, a.N, a.max_depth, a.V, a.ld = B, N, int(max_depth), V, ld
@@ -210,7 +197,7 @@ class CascadePlan(_Plan):
         self.out["error_word"] = torch.zeros(1, dtype=torch.int32, device=dev)
         need = lib.spec_cascade_workspace_size(B, g1, g2, V)
         if workspace is None:
-            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.CascadeArgs()
         a.B, a.gamma1, a.gamma2, a.V, a.ld = B, g1, g2, V, ld

@@ -1,6 +1,5 @@
 // C ABI of the verification library: argument checks, workspace sizing and
-// the two launches of every call (row statistics, then the per-sequence
-// walker cluster).  Nothing here allocates or synchronises.
+// the one launch of every call.  Nothing here allocates or synchronises.
 #include <cmath>
 #include <cstdint>
 
@@ -9,34 +8,16 @@
 
 namespace sv {
 
-cudaError_t launch_walker(const void* kernel, void** args, int B, int cluster, size_t dyn_smem,
-                          cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(cluster));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = dyn_smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelExC(&cfg, kernel, args);
-}
-
 namespace {
 
-constexpr int kMaxV = 8 * 256 * 2048;  // walker tiles per CTA bound (walk.cuh)
+constexpr int kMaxV = 512 * 4096;  // pass tiles per row bound (walk.cuh)
+constexpr int kMaxB = kMaxSeq;     // per-sequence state records
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 spec_status check_common(int B, int V, long long ld, spec_dtype dtype, spec_mode mode,
                          float temperature) {
-  if (B < 1 || B > (1 << 24)) return SPEC_EINVAL;
+  if (B < 1 || B > kMaxB) return SPEC_EINVAL;
   if (V < 1 || V > kMaxV) return SPEC_EINVAL;
   if (ld < V || ld > (1LL << 40)) return SPEC_EINVAL;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EDTYPE;
@@ -52,9 +33,26 @@ float logit_scale(float temperature) {
 
 spec_status run(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA; }
 
-spec_status record(cudaEvent_t ev, cudaStream_t s) {
-  if (ev == nullptr) return SPEC_OK;
-  return run(cudaEventRecord(ev, s));
+// Statistics geometry and workspace pointers shared by the three entry points.
+bool stats_params(StatsParams& sp, int B, int V, long long ld, bool bf16, bool greedy, float temperature,
+                  int rows, void* workspace) {
+  sp = StatsParams{};
+  sp.rows_per_seq = rows;
+  sp.B = B;
+  sp.V = V;
+  sp.ld = ld;
+  sp.chunks = stats_chunks(V, bf16);
+  sp.ntiles = pass_tiles(V);
+  sp.tps = kTilesPerSlice;
+  sp.c = greedy ? 1.f : logit_scale(temperature);
+  char* ws = static_cast<char*>(workspace);
+  const Layout L = workspace_layout(B, rows, V);
+  sp.state = ws + 256;
+  sp.specs = ws + L.specs;
+  sp.mid = ws + L.mid;
+  sp.sums = reinterpret_cast<float*>(ws + L.sums);
+  sp.partials = reinterpret_cast<float2*>(ws + L.partials);
+  return rows <= 65535 && sp.chunks <= 0x7fffffff;
 }
 
 }  // namespace
@@ -78,17 +76,17 @@ const char* spec_status_string(spec_status status) {
 
 size_t spec_chain_workspace_size(int B, int gamma, int V) {
   if (B < 1 || gamma < 0 || V < 1) return 0;
-  return stats_workspace_bytes(B, 2 * gamma + 1, V);
+  return workspace_bytes(B, 2 * gamma + 1, V);
 }
 
 size_t spec_tree_workspace_size(int B, int N, int V) {
   if (B < 1 || N < 1 || V < 1) return 0;
-  return stats_workspace_bytes(B, 2 * N, V);
+  return workspace_bytes(B, 2 * N, V);
 }
 
 size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V) {
   if (B < 1 || gamma1 < 1 || gamma2 < 1 || V < 1) return 0;
-  return stats_workspace_bytes(B, 2 * gamma1 + 1 + gamma2, V);
+  return workspace_bytes(B, 2 * gamma1 + 1 + gamma2, V);
 }
 
 spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
@@ -103,28 +101,24 @@ spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
   if (!greedy && (!a->v || (a->gamma > 0 && (!a->draft_logits || !a->u)))) return SPEC_EINVAL;
   if (!aligned16(a->target_logits) || (!greedy && a->gamma > 0 && !aligned16(a->draft_logits)))
     return SPEC_EALIGN;
+  // sampling reads the draft rows too; greedy reads the target rows only
   const int rows = greedy ? a->gamma + 1 : 2 * a->gamma + 1;
-  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
-  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+  if (!a->workspace || a->workspace_bytes < workspace_bytes(a->B, rows, a->V) ||
+      !aligned16(a->workspace))
+    return SPEC_EWORKSPACE;
 
-  StatsParams sp = {};
+  StatsParams sp;
+  if (!stats_params(sp, a->B, a->V, a->ld, bf16, greedy, a->temperature, rows, a->workspace))
+    return SPEC_EINVAL;
   sp.set[0] = RowSet{a->target_logits, a->gamma + 1};
   sp.set[1] = RowSet{a->draft_logits, a->gamma};
   sp.nsets = (greedy || a->gamma == 0) ? 1 : 2;
-  sp.rows_per_seq = rows;
-  sp.B = a->B;
-  sp.V = a->V;
-  sp.ld = a->ld;
-  sp.chunks = stats_chunks(a->V);
-  sp.c = greedy ? 1.f : logit_scale(a->temperature);
-  sp.partials = static_cast<float2*>(a->workspace);
 
   ChainParams cp = {};
   cp.B = a->B;
   cp.gamma = a->gamma;
   cp.V = a->V;
   cp.ld = a->ld;
-  cp.c = sp.c;
   cp.target = a->target_logits;
   cp.draft = a->draft_logits;
   cp.tokens = a->draft_tokens;
@@ -139,15 +133,7 @@ spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
   cp.resid = a->resid_mass;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
-  cp.partials = sp.partials;
-  cp.chunks = sp.chunks;
-  cp.rows_per_seq = rows;
-  cp.cluster = walker_cluster(a->V);
-
-  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
-  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
-  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
-  return run(launch_chain_walk(cp, bf16, greedy, stream));
+  return run(launch_chain(sp, cp, bf16, greedy, stream));
 }
 
 spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
@@ -164,20 +150,16 @@ spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
   if (!greedy && (!a->draft_logits || !a->u || !a->v)) return SPEC_EINVAL;
   if (!aligned16(a->target_logits) || (!greedy && !aligned16(a->draft_logits))) return SPEC_EALIGN;
   const int rows = greedy ? a->N : 2 * a->N;
-  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
-  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+  if (!a->workspace || a->workspace_bytes < workspace_bytes(a->B, rows, a->V) ||
+      !aligned16(a->workspace))
+    return SPEC_EWORKSPACE;
 
-  StatsParams sp = {};
+  StatsParams sp;
+  if (!stats_params(sp, a->B, a->V, a->ld, bf16, greedy, a->temperature, rows, a->workspace))
+    return SPEC_EINVAL;
   sp.set[0] = RowSet{a->target_logits, a->N};
   sp.set[1] = RowSet{a->draft_logits, a->N};
   sp.nsets = greedy ? 1 : 2;
-  sp.rows_per_seq = rows;
-  sp.B = a->B;
-  sp.V = a->V;
-  sp.ld = a->ld;
-  sp.chunks = stats_chunks(a->V);
-  sp.c = greedy ? 1.f : logit_scale(a->temperature);
-  sp.partials = static_cast<float2*>(a->workspace);
 
   TreeParams tp = {};
   tp.B = a->B;
@@ -185,7 +167,6 @@ spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
   tp.max_depth = a->max_depth;
   tp.V = a->V;
   tp.ld = a->ld;
-  tp.c = sp.c;
   tp.parent = a->parent;
   tp.tokens = a->node_tokens;
   tp.target = a->target_logits;
@@ -199,15 +180,7 @@ spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
   tp.rollback = a->rollback_idx;
   tp.seq_error = a->seq_error;
   tp.error_word = a->error_word;
-  tp.partials = sp.partials;
-  tp.chunks = sp.chunks;
-  tp.rows_per_seq = rows;
-  tp.cluster = walker_cluster(a->V);
-
-  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
-  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
-  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
-  return run(launch_tree_walk(tp, bf16, greedy, stream));
+  return run(launch_tree(sp, tp, bf16, greedy, stream));
 }
 
 spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream) {
@@ -225,10 +198,13 @@ spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream)
   if (!greedy && (!a->l0 || !a->u1 || !a->v1 || !a->u2 || !a->v2)) return SPEC_EINVAL;
   if (!aligned16(a->l1) || !aligned16(a->l2) || (!greedy && !aligned16(a->l0))) return SPEC_EALIGN;
   const int rows = greedy ? a->gamma1 + 1 + a->gamma2 : 2 * a->gamma1 + 1 + a->gamma2;
-  const size_t need = stats_workspace_bytes(a->B, rows, a->V);
-  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return SPEC_EWORKSPACE;
+  if (!a->workspace || a->workspace_bytes < workspace_bytes(a->B, rows, a->V) ||
+      !aligned16(a->workspace))
+    return SPEC_EWORKSPACE;
 
-  StatsParams sp = {};
+  StatsParams sp;
+  if (!stats_params(sp, a->B, a->V, a->ld, bf16, greedy, a->temperature, rows, a->workspace))
+    return SPEC_EINVAL;
   if (greedy) {
     sp.set[0] = RowSet{a->l1, a->gamma1 + 1};
     sp.set[1] = RowSet{a->l2, a->gamma2};
@@ -239,13 +215,6 @@ spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream)
     sp.set[2] = RowSet{a->l2, a->gamma2};
     sp.nsets = 3;
   }
-  sp.rows_per_seq = rows;
-  sp.B = a->B;
-  sp.V = a->V;
-  sp.ld = a->ld;
-  sp.chunks = stats_chunks(a->V);
-  sp.c = greedy ? 1.f : logit_scale(a->temperature);
-  sp.partials = static_cast<float2*>(a->workspace);
 
   CascadeParams cp = {};
   cp.B = a->B;
@@ -253,7 +222,6 @@ spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream)
   cp.g2 = a->gamma2;
   cp.V = a->V;
   cp.ld = a->ld;
-  cp.c = sp.c;
   cp.l0 = a->l0;
   cp.l1 = a->l1;
   cp.l2 = a->l2;
@@ -275,15 +243,7 @@ spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream)
   cp.committed = a->committed;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
-  cp.partials = sp.partials;
-  cp.chunks = sp.chunks;
-  cp.rows_per_seq = rows;
-  cp.cluster = walker_cluster(a->V);
-
-  if ((st = record(a->stats_begin, stream)) != SPEC_OK) return st;
-  if ((st = run(launch_row_stats(sp, bf16, greedy, stream))) != SPEC_OK) return st;
-  if ((st = record(a->stats_end, stream)) != SPEC_OK) return st;
-  return run(launch_cascade_walk(cp, bf16, greedy, stream));
+  return run(launch_cascade(sp, cp, bf16, greedy, stream));
 }
 
 }  // extern "C"

@@ -4,11 +4,13 @@
 // the accept tests and the sampling passes agree bit for bit:
 //   c      = log2(e) / T, rounded once to float on the host
 //   M(m)   = __fmul_rn(m, c): the scaled maximum of a row with raw maximum m
-//   e(x)   = ex2(__fmaf_rn(x, c, -M)) = 2^(x c - M), the unnormalised weight
+//   e(x)   = ex2(fma_rn(x, c, -M)) = 2^(x c - M), the unnormalised weight
 //   s      = sum of e(x) over the row
 //   p(x)   = e(x) / s
 // The unrounded x c - M of one fused multiply-add keeps every weight relative
 // to the same shift M, so p(x) computed later from (M, s) is consistent with s.
+// The packed (f32x2) forms below round each lane exactly like the scalar
+// intrinsics, so packed and scalar code give identical weights.
 #pragma once
 
 #include <cstdint>
@@ -16,10 +18,13 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;          // threads per CTA for every kernel
+constexpr int kStatsThreads = 256;       // row-statistics kernel: small CTAs, many per SM
+constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kVecPerThread = 8;         // 16-byte loads per thread per statistics unit
+constexpr int kThreads = 512;            // walk kernels
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 8192;           // row elements per row-statistics CTA
-constexpr int kTileElems = 8 * kThreads;  // walker tile: 8 contiguous elements per thread
+static_assert(kWarps <= 32 && kStatsWarps <= 32, "one warp reduces the per-warp partials");
+constexpr int kTileElems = 8 * kThreads; // pass tile: 8 contiguous elements per thread
 
 constexpr float kInf = __builtin_huge_valf();
 
@@ -39,18 +44,19 @@ __device__ __forceinline__ float load_elem(const bf16_t* p) {
 // by the statistics pass).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 
-// 16-byte load through the normal cache path (walker re-reads hit L2).
+// 16-byte load through L2 (the walker re-reads rows the statistics pass
+// brought into L2 moments earlier).
 __device__ __forceinline__ uint4 ld16(const void* p) {
   uint4 v;
-  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 
@@ -66,6 +72,31 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   float y;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
   return y;
+}
+
+// lane-wise max of two packed bfloat16 pairs, NaN-propagating
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 __device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
@@ -92,13 +123,18 @@ __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b, float c) {
   return {m, __fadd_rn(__fmul_rn(a.s, ea), __fmul_rn(b.s, eb))};
 }
 
-__device__ __forceinline__ MaxSum ms_warp_merge(MaxSum v, float c) {
+// Warp-wide (max, sum): max first, then every lane rescales its sum once and
+// the sums are added with a butterfly (fp addition is commutative, so every
+// lane ends with the same bits).
+__device__ __forceinline__ MaxSum ms_warp_reduce(MaxSum v, float c) {
+  float m = v.m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MaxSum w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-    v = ms_merge(v, w, c);  // commutative bit for bit, so every lane agrees
-  }
-  return v;
+  for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  if (m != -kInf) s = (v.m == -kInf) ? 0.f : __fmul_rn(v.s, ex2(scaled_max(v.m, c) - scaled_max(m, c)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return {m, s};
 }
 
 // ---------------------------------------------------------------------------
@@ -117,7 +153,7 @@ __device__ __forceinline__ ArgMax am_merge(ArgMax a, ArgMax b) {
   return a;
 }
 
-__device__ __forceinline__ ArgMax am_warp_merge(ArgMax v) {
+__device__ __forceinline__ ArgMax am_warp_reduce(ArgMax v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     ArgMax w{__shfl_xor_sync(0xffffffffu, v.v, o), __shfl_xor_sync(0xffffffffu, v.i, o)};
@@ -129,11 +165,12 @@ __device__ __forceinline__ ArgMax am_warp_merge(ArgMax v) {
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
+// Allow the next kernel in the stream to be scheduled now.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-__device__ __forceinline__ void pdl_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+// Wait until the previous kernel in the stream has completed and its memory
+// is visible (a no-op when this kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace sv

@@ -13,41 +13,65 @@ struct RowSet {
   int rows;
 };
 
-// One launch of the row-statistics kernel over up to three tensors.  The
-// rows of a sequence are numbered set by set: set 0's rows first.
+// Everything the kernels need besides the kind-specific arguments.
 struct StatsParams {
   RowSet set[3];
   int nsets;
-  int rows_per_seq;   // sum of set[k].rows
+  int rows_per_seq;     // sum of set[k].rows
   int B;
   int V;
   long long ld;
-  int chunks;         // row-statistics CTAs per row
-  float c;            // log2(e) / T (sampling); unused in greedy mode
-  float2* partials;   // [B][rows_per_seq][chunks]: (max, sum) or (value, index)
+  int chunks;           // statistics CTAs per row
+  int ntiles;           // pass tiles per row
+  int tps;              // pass tiles per slice CTA
+  float c;              // log2(e) / T (sampling); unused in greedy mode
+  void* state;          // [kMaxSeq] per-sequence counters, zero between calls
+  void* specs;          // [B] cascade: the stage-2 pass
+  void* mid;            // [B] cascade: stage-1 flags
+  float* sums;          // [B][2][ntiles] pass tile sums
+  float2* partials;     // [B][rows_per_seq][chunks]: (max, sum) or (value, index)
 };
 
-inline int stats_chunks(int V) { return (V + 8191) / 8192; }
+// Chunks per row for the dtype; the workspace is sized for the larger
+// (float32) count so one size serves both dtypes.
+int stats_chunks(int V, bool bf16);
+int pass_tiles(int V);
+constexpr int kTilesPerSlice = 4;
 
-// Workspace bytes for `rows_per_seq` statistics rows per sequence.
-inline size_t stats_workspace_bytes(int B, int rows_per_seq, int V) {
-  return static_cast<size_t>(B) * rows_per_seq * stats_chunks(V) * sizeof(float2);
+// Workspace layout.  A fixed head, zeroed once by the caller and left zero by
+// every call: 256 reserved bytes and one 32-byte record per possible sequence
+// index, so that calls of any batch size, mode or kind share it.  Then
+// per-call scratch, fully written before it is read.
+constexpr int kMaxSeq = 65535;
+constexpr size_t kSeqStateBytes = 32;
+constexpr size_t kSpecBytes = 48;
+constexpr size_t kHeadBytes = 256 + 65536 * kSeqStateBytes;
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t specs, mid, sums, partials, total;
+};
+inline Layout workspace_layout(int B, int rows_per_seq, int V) {
+  Layout L;
+  size_t off = kHeadBytes;
+  L.specs = off;
+  off = align256(off + static_cast<size_t>(B) * kSpecBytes);
+  L.mid = off;
+  off = align256(off + static_cast<size_t>(B) * 16);
+  L.sums = off;
+  off = align256(off + static_cast<size_t>(B) * 2 * pass_tiles(V) * 4);
+  L.partials = off;
+  off = align256(off + static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
+  L.total = off;
+  return L;
 }
-
-cudaError_t launch_row_stats(const StatsParams& p, bool bf16, bool greedy, cudaStream_t s);
-
-// Cluster size of the walker kernels: enough CTAs that each covers about
-// four 2048-element tiles of a row, at most 8 (the portable cluster size).
-inline int walker_cluster(int V) {
-  int tiles = (V + 2047) / 2048;
-  int cs = (tiles + 3) / 4;
-  return cs < 1 ? 1 : (cs > 8 ? 8 : cs);
+inline size_t workspace_bytes(int B, int rows_per_seq, int V) {
+  return workspace_layout(B, rows_per_seq, V).total;
 }
 
 struct ChainParams {
   int B, gamma, V;
   long long ld;
-  float c;                  // log2(e) / T
   const void* target;
   const void* draft;
   const int* tokens;
@@ -62,17 +86,11 @@ struct ChainParams {
   float* resid;
   int* seq_error;
   int* error_word;
-  const float2* partials;
-  int chunks;
-  int rows_per_seq;
-  int cluster;
 };
-cudaError_t launch_chain_walk(const ChainParams& p, bool bf16, bool greedy, cudaStream_t s);
 
 struct TreeParams {
   int B, N, max_depth, V;
   long long ld;
-  float c;
   const int* parent;
   const int* tokens;
   const void* target;
@@ -86,17 +104,11 @@ struct TreeParams {
   int* rollback;
   int* seq_error;
   int* error_word;
-  const float2* partials;
-  int chunks;
-  int rows_per_seq;
-  int cluster;
 };
-cudaError_t launch_tree_walk(const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
 
 struct CascadeParams {
   int B, g1, g2, V;
   long long ld;
-  float c;
   const void* l0;
   const void* l1;
   const void* l2;
@@ -118,17 +130,11 @@ struct CascadeParams {
   int* committed;
   int* seq_error;
   int* error_word;
-  const float2* partials;
-  int chunks;
-  int rows_per_seq;
-  int cluster;
 };
-cudaError_t launch_cascade_walk(const CascadeParams& p, bool bf16, bool greedy, cudaStream_t s);
 
-// Launch helper: `cluster` CTAs per sequence, with programmatic dependent
-// launch so the walker's CTAs are scheduled while the statistics kernel
-// drains.
-cudaError_t launch_walker(const void* kernel, void** args, int B, int cluster,
-                          size_t dyn_smem, cudaStream_t s);
+cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, bool greedy, cudaStream_t s);
+cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
+cudaError_t launch_cascade(const StatsParams& g, const CascadeParams& p, bool bf16, bool greedy,
+                           cudaStream_t s);
 
 }  // namespace sv

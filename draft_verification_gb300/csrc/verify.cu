@@ -1,0 +1,850 @@
+// Batched draft verification kernels and their launch sequence.
+//
+// Every call is a short chain of kernels on the caller's stream, each
+// launched with programmatic dependent launch so that it is resident and has
+// read its own inputs by the time its predecessor finishes:
+//
+//   1. stats_kernel  one CTA per (sequence, row, 16384-element chunk): the
+//                    online-softmax (max, sum) or the argmax of the chunk
+//                    (stats.cuh).  This streams every logit once; it is
+//                    the bandwidth-bound kernel.
+//   2. walk kernels  one CTA per (sequence, pass slice).  Every slice CTA of a
+//                    sequence merges the sequence's statistics and evaluates
+//                    the accept tests itself (a few hundred bytes), then sums
+//                    the residual / bonus weights of its tiles of the chosen
+//                    row pair (walk.cuh); the slice that arrives last on the
+//                    sequence's counter draws the token.  No CTA waits for
+//                    another.  The cascade runs a second walk kernel for its
+//                    second stage; trees and greedy calls use one CTA per
+//                    sequence.
+//
+// Rules (pages: the Pith review of PipeSpec, "What carries the argument" and
+// the acceptance rule of Leviathan et al. its Circularity Check cites; Staged
+// Speculative Decoding, abstract):
+//  * chain: keep drafts while u < min(1, p/q); draw from max(0, p - q) at the
+//    first rejection, from the bonus row when all are kept; greedy keeps
+//    drafts equal to the target argmax;
+//  * cascade: stage 1 (M_1 verifies M_0's drafts), then stage 2 (M_2 verifies
+//    the first tokens of stage 1's output);
+//  * tree: a serial walk from the root (each rejected sibling changes the
+//    distribution the next sibling is tested against).
+#include "common.cuh"
+#include "internal.h"
+#include "spec_verify.h"
+#include "stats.cuh"
+#include "walk.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kMaxGamma = 32;
+
+// ---------------------------------------------------------------------------
+// workspace records
+// ---------------------------------------------------------------------------
+struct SeqState {  // zero between calls
+  unsigned done1;  // slices of the first pass that have finished
+  unsigned done2;  // slices of the second pass (cascade)
+  int pad[6];
+};
+static_assert(sizeof(SeqState) == kSeqStateBytes, "state layout");
+
+struct SpecG {  // a pass handed from the first walk kernel to the second
+  const void* P;
+  const void* Q;
+  float MP, invSP, MQ, invSQ, cq;
+  int a;  // the decision that goes with it, or -1: no pass
+  int a1, t1;
+};
+static_assert(sizeof(SpecG) == kSpecBytes, "spec layout");
+
+__device__ __forceinline__ SeqState* seq_state(const StatsParams& G, int b) {
+  return reinterpret_cast<SeqState*>(G.state) + b;
+}
+
+template <typename T>
+__device__ __forceinline__ PassSpec<T> make_spec(const T* P, float mP, float sP, const T* Q, float mQ, float sQ,
+                                                 float cq, float c) {
+  PassSpec<T> S;
+  S.P = P;
+  S.MP = scaled_max(mP, c);
+  S.invSP = __fdiv_rn(1.f, sP);
+  S.Q = Q;
+  S.MQ = Q ? scaled_max(mQ, c) : 0.f;
+  S.invSQ = Q ? __fdiv_rn(1.f, sQ) : 0.f;
+  S.cq = Q ? cq : 0.f;
+  S.pad = 0;
+  return S;
+}
+
+template <typename T>
+__device__ __forceinline__ const T* stats_row(const StatsParams& G, int b, int r) {
+  int i = r;
+  const void* base = G.set[0].base;
+  int rows = G.set[0].rows;
+  if (G.nsets > 1 && i >= rows) {
+    i -= rows;
+    base = G.set[1].base;
+    rows = G.set[1].rows;
+    if (G.nsets > 2 && i >= rows) {
+      i -= rows;
+      base = G.set[2].base;
+      rows = G.set[2].rows;
+    }
+  }
+  return static_cast<const T*>(base) + (static_cast<long long>(b) * rows + i) * G.ld;
+}
+
+// Row statistics of sequence b into shared arrays; returns SPEC_ERR_NONFINITE
+// if a row is NaN / +inf / all -inf (or'ed into *err_s).
+template <bool kGreedy>
+__device__ int gather_stats(const StatsParams& G, int b, float* st_m, float* st_s, int* st_arg, int* err_s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float2* part = G.partials + static_cast<long long>(b) * G.rows_per_seq * G.chunks;
+  for (int r = warp; r < G.rows_per_seq; r += kWarps) {
+    if constexpr (kGreedy) {
+      bool bad;
+      const ArgMax am = combine_row_argmax(part + static_cast<long long>(r) * G.chunks, G.chunks, bad);
+      if (lane == 0) {
+        st_arg[r] = am.i;
+        if (bad || am.i < 0) atomicOr(err_s, SPEC_ERR_NONFINITE);
+      }
+    } else {
+      const MaxSum ms = combine_row(part + static_cast<long long>(r) * G.chunks, G.chunks, G.c);
+      if (lane == 0) {
+        st_m[r] = ms.m;
+        st_s[r] = ms.s;
+        if (!row_stats_ok(ms)) atomicOr(err_s, SPEC_ERR_NONFINITE);
+      }
+    }
+  }
+  __syncthreads();
+  return *err_s;
+}
+
+// Last-arriver test on a counter (all threads get the answer).  Every thread
+// fences first, so whatever this CTA wrote is visible before it is counted;
+// the last arriver resets the counter for the next call.
+__device__ bool arrive(unsigned* ctr, unsigned expected, int* sh) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(ctr, 1u);
+    *sh = (old + 1u == expected);
+    if (*sh) {
+      *ctr = 0u;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  return *sh != 0;
+}
+
+__device__ __forceinline__ float* pass_sums(const StatsParams& G, int b, int stage) {
+  return G.sums + (static_cast<long long>(b) * 2 + stage) * G.ntiles;
+}
+
+// Draw from a pass whose tile sums are all in `sums`; on a zero or
+// non-finite total, redo the pass on the target row alone (cq = 0) and set
+// *flag |= SPEC_ERR_ZERO_MASS.  Returns the token; *Z gets the mass drawn from.
+template <typename T>
+__device__ int finish_draw(const StatsParams& G, PassSpec<T> S, float* sums, float v, PassSmem& ps, int* flag,
+                           double* Z) {
+  double z = tile_prefix(sums, G.ntiles, ps);
+  if (!(z > 0.0) || !(z < INFINITY)) {
+    *flag |= SPEC_ERR_ZERO_MASS;
+    S.cq = 0.f;
+    S.Q = nullptr;
+    tile_sums(S, G.V, G.c, 0, G.ntiles, sums, ps);
+    __threadfence_block();
+    z = tile_prefix(sums, G.ntiles, ps);
+  }
+  *Z = z;
+  return draw(S, G.V, G.c, sums, G.ntiles, static_cast<double>(v) * z, ps);
+}
+
+// ===========================================================================
+// 1. statistics
+// ===========================================================================
+template <typename T, bool kGreedy>
+__global__ void __launch_bounds__(kStatsThreads, 5) stats_kernel(const StatsParams G) {
+  pdl_launch_dependents();
+  __shared__ StatsSmem sm;
+  const int k = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+  float2* out = G.partials + (static_cast<long long>(b) * G.rows_per_seq + r) * G.chunks + k;
+  stats_unit<T, kGreedy>(stats_row<T>(G, b, r), G.V, k, G.c, out, sm);
+}
+
+// ===========================================================================
+// 2a. chain
+// ===========================================================================
+struct ChainSmem {
+  float st_m[2 * kMaxGamma + 1], st_s[2 * kMaxGamma + 1];
+  int st_arg[kMaxGamma + 1];
+  int tok[kMaxGamma];
+  float gp[kMaxGamma], gq[kMaxGamma];
+  int err, a, last;
+};
+
+// Tokens and the logits at the drafted tokens (inputs only: safe before the
+// statistics are complete).
+template <typename T>
+__device__ void chain_inputs(const ChainParams& P, int b, ChainSmem& cs, bool sampling) {
+  const int g = P.gamma, tid = threadIdx.x;
+  if (tid == 0) cs.err = 0;
+  __syncthreads();
+  if (tid < g) {
+    const long long d0 = static_cast<long long>(b) * g;
+    const long long t0 = static_cast<long long>(b) * (g + 1);
+    const int t = P.tokens[d0 + tid];
+    cs.tok[tid] = t;
+    if (t < 0 || t >= P.V) {
+      atomicOr(&cs.err, SPEC_ERR_TOKEN);
+    } else if (sampling) {
+      cs.gp[tid] = load_elem(static_cast<const T*>(P.target) + (t0 + tid) * P.ld + t);
+      cs.gq[tid] = load_elem(static_cast<const T*>(P.draft) + (d0 + tid) * P.ld + t);
+    }
+  }
+}
+
+__device__ void chain_error_out(const ChainParams& P, int b, int err) {
+  const int tid = threadIdx.x, g = P.gamma;
+  if (tid == 0) {
+    P.accept_len[b] = 0;
+    P.out_token[b] = -1;
+    if (P.rollback) P.rollback[b] = P.prefix ? P.prefix[b] : 0;
+    if (P.resid) P.resid[b] = 0.f;
+    if (P.seq_error) P.seq_error[b] = err;
+    if (P.error_word) atomicOr(P.error_word, err);
+  }
+  if (tid < g) {
+    if (P.p_at) P.p_at[static_cast<long long>(b) * g + tid] = 0.f;
+    if (P.q_at) P.q_at[static_cast<long long>(b) * g + tid] = 0.f;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParams G, const ChainParams P) {
+  __shared__ ChainSmem cs;
+  const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = P.gamma;
+  chain_inputs<T>(P, b, cs, false);
+  pdl_wait();
+  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  if (err) {
+    chain_error_out(P, b, err);
+    return;
+  }
+  if (warp == 0) {
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < g && cs.tok[lane] != cs.st_arg[lane]);
+    const int a = rej ? __ffs(rej) - 1 : g;
+    if (lane == 0) {
+      P.accept_len[b] = a;
+      P.out_token[b] = cs.st_arg[a];
+      if (P.rollback) P.rollback[b] = (P.prefix ? P.prefix[b] : 0) + a;
+      if (P.resid) P.resid[b] = 0.f;
+      if (P.seq_error) P.seq_error[b] = 0;
+    }
+    if (lane < g) {
+      if (P.p_at) P.p_at[static_cast<long long>(b) * g + lane] = 0.f;
+      if (P.q_at) P.q_at[static_cast<long long>(b) * g + lane] = 0.f;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chain_walk_kernel(const StatsParams G, const ChainParams P) {
+  __shared__ ChainSmem cs;
+  __shared__ PassSmem ps;
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = P.gamma;
+  const float c = G.c;
+  const T* target = static_cast<const T*>(P.target);
+  const T* draft = static_cast<const T*>(P.draft);
+  const long long trow0 = static_cast<long long>(b) * (g + 1);
+  const long long drow0 = static_cast<long long>(b) * g;
+
+  chain_inputs<T>(P, b, cs, true);
+  pdl_wait();  // the statistics are complete and visible from here on
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  if (err) {  // every slice sees the same error; slice 0 reports it
+    if (j == 0) chain_error_out(P, b, err);
+    return;
+  }
+  if (warp == 0) {
+    bool keep = true;
+    if (lane < g) {
+      const float mq = cs.st_m[g + 1 + lane], sq = cs.st_s[g + 1 + lane];
+      keep = keeps(P.u[drow0 + lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
+      if (j == 0) {
+        if (P.p_at) P.p_at[drow0 + lane] = prob(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], c);
+        if (P.q_at) P.q_at[drow0 + lane] = prob(cs.gq[lane], mq, sq, c);
+      }
+    }
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < g && !keep);
+    if (lane == 0) cs.a = rej ? __ffs(rej) - 1 : g;
+  }
+  __syncthreads();
+  const int a = cs.a;
+  // residual max(0, p_a - q_a) after a rejection, the bonus row p_gamma otherwise
+  const PassSpec<T> S = make_spec(target + (trow0 + a) * P.ld, cs.st_m[a], cs.st_s[a],
+                                  a < g ? draft + (drow0 + a) * P.ld : nullptr, a < g ? cs.st_m[g + 1 + a] : 0.f,
+                                  a < g ? cs.st_s[g + 1 + a] : 1.f, 1.f, c);
+  float* sums = pass_sums(G, b, 0);
+  const int t0 = j * G.tps, t1 = min(G.ntiles, t0 + G.tps);
+  if (t0 < t1) tile_sums(S, G.V, c, t0, t1, sums, ps);
+  if (!arrive(&seq_state(G, b)->done1, gridDim.x, &cs.last)) return;
+
+  int flag = 0;
+  double Z;
+  const int y = finish_draw(G, S, sums, P.v[b], ps, &flag, &Z);
+  if (tid == 0) {
+    P.accept_len[b] = a;
+    P.out_token[b] = y;
+    if (P.rollback) P.rollback[b] = (P.prefix ? P.prefix[b] : 0) + a;
+    if (P.resid) P.resid[b] = static_cast<float>(Z);
+    if (P.seq_error) P.seq_error[b] = flag;
+    if (flag && P.error_word) atomicOr(P.error_word, flag);
+  }
+}
+
+// ===========================================================================
+// 2b. cascade
+// Statistics rows: sampling: M_0 [0, g1), M_1 [g1, 2 g1 + 1), M_2 after;
+// greedy (M_0 not read): M_1 [0, g1 + 1), M_2 [g1 + 1, ...).
+// ===========================================================================
+struct CascadeSmem {
+  float st_m[3 * kMaxGamma + 1], st_s[3 * kMaxGamma + 1];
+  int st_arg[3 * kMaxGamma + 1];
+  int tok[kMaxGamma];
+  float g1p[kMaxGamma], g1q[kMaxGamma];
+  int err, a1, a2, last;
+};
+
+struct CascadeOut {
+  const CascadeParams& P;
+  int b;
+  __device__ void write(int a1, int t1, int a2, int w2, int t2, int t2v, int flag) const {
+    const bool rej = a2 < w2;
+    const int base0 = P.base0 ? P.base0[b] : 0;
+    const int base1 = P.base1 ? P.base1[b] : 0;
+    P.a1[b] = a1;
+    P.t1[b] = t1;
+    P.a2[b] = a2;
+    P.w2[b] = w2;
+    P.t2[b] = t2;
+    P.t2_valid[b] = t2v;
+    P.r0[b] = base0 + (rej ? min(a1, a2) : a1);
+    P.r1[b] = base1 + (rej ? a2 : w2);
+    P.committed[b] = a2 + t2v;
+    if (P.seq_error) P.seq_error[b] = flag;
+    if (flag && P.error_word) atomicOr(P.error_word, flag);
+  }
+};
+
+template <typename T>
+__device__ void cascade_inputs(const CascadeParams& P, int b, CascadeSmem& cs, bool sampling) {
+  const int g1 = P.g1, tid = threadIdx.x;
+  if (tid == 0) cs.err = 0;
+  __syncthreads();
+  if (tid < g1) {
+    const long long b0 = static_cast<long long>(b) * g1, b1 = static_cast<long long>(b) * (g1 + 1);
+    const int t = P.tokens[b0 + tid];
+    cs.tok[tid] = t;
+    if (t < 0 || t >= P.V) {
+      atomicOr(&cs.err, SPEC_ERR_TOKEN);
+    } else if (sampling) {
+      cs.g1p[tid] = load_elem(static_cast<const T*>(P.l1) + (b1 + tid) * P.ld + t);
+      cs.g1q[tid] = load_elem(static_cast<const T*>(P.l0) + (b0 + tid) * P.ld + t);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) cascade_greedy_kernel(const StatsParams G, const CascadeParams P) {
+  __shared__ CascadeSmem cs;
+  const int b = blockIdx.x;
+  const int g1 = P.g1, g2 = P.g2;
+  cascade_inputs<T>(P, b, cs, false);
+  pdl_wait();
+  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  if (threadIdx.x != 0) return;
+  const CascadeOut out{P, b};
+  if (err) {
+    out.write(0, -1, 0, 0, -1, 0, err);
+    return;
+  }
+  const int r1 = 0, r2 = g1 + 1;
+  int a1 = g1;
+  for (int q = 0; q < g1; ++q)
+    if (cs.tok[q] != cs.st_arg[r1 + q]) {
+      a1 = q;
+      break;
+    }
+  const int t1 = cs.st_arg[r1 + a1];
+  const int w2 = min(g2, a1 + 1);
+  int a2 = w2;
+  for (int q = 0; q < w2; ++q) {
+    const int o = q < a1 ? cs.tok[q] : t1;
+    if (o != cs.st_arg[r2 + q]) {
+      a2 = q;
+      break;
+    }
+  }
+  out.write(a1, t1, a2, w2, a2 < w2 ? cs.st_arg[r2 + a2] : -1, a2 < w2 ? 1 : 0, 0);
+}
+
+// Stage 1, and the stage-2 decision by the slice that draws t1.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) cascade_walk1_kernel(const StatsParams G, const CascadeParams P) {
+  pdl_launch_dependents();
+  __shared__ CascadeSmem cs;
+  __shared__ PassSmem ps;
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g1 = P.g1, g2 = P.g2;
+  const float c = G.c;
+  const int r1 = g1, r2 = 2 * g1 + 1;
+  const T* L0 = static_cast<const T*>(P.l0);
+  const T* L1 = static_cast<const T*>(P.l1);
+  const T* L2 = static_cast<const T*>(P.l2);
+  const long long b0 = static_cast<long long>(b) * g1;
+  const long long b1 = static_cast<long long>(b) * (g1 + 1);
+  const long long b2 = static_cast<long long>(b) * g2;
+  SpecG* spec2 = reinterpret_cast<SpecG*>(G.specs) + b;
+  const CascadeOut out{P, b};
+
+  cascade_inputs<T>(P, b, cs, true);
+  pdl_wait();
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  if (err) {
+    if (j == 0 && tid == 0) {
+      out.write(0, -1, 0, 0, -1, 0, err);
+      spec2->a = -1;
+    }
+    return;
+  }
+  // stage 1: M_1 verifies O_0 against M_0
+  if (warp == 0) {
+    bool keep = true;
+    if (lane < g1)
+      keep = keeps(P.u1[b0 + lane], ratio(cs.g1p[lane], cs.st_m[r1 + lane], cs.st_s[r1 + lane], cs.g1q[lane],
+                                         cs.st_m[lane], cs.st_s[lane], c));
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < g1 && !keep);
+    if (lane == 0) cs.a1 = rej ? __ffs(rej) - 1 : g1;
+  }
+  __syncthreads();
+  const int a1 = cs.a1;
+  const PassSpec<T> S = make_spec(L1 + (b1 + a1) * P.ld, cs.st_m[r1 + a1], cs.st_s[r1 + a1],
+                                  a1 < g1 ? L0 + (b0 + a1) * P.ld : nullptr, a1 < g1 ? cs.st_m[a1] : 0.f,
+                                  a1 < g1 ? cs.st_s[a1] : 1.f, 1.f, c);
+  float* sums = pass_sums(G, b, 0);
+  const int t0 = j * G.tps, t1e = min(G.ntiles, t0 + G.tps);
+  if (t0 < t1e) tile_sums(S, G.V, c, t0, t1e, sums, ps);
+  if (!arrive(&seq_state(G, b)->done1, gridDim.x, &cs.last)) return;
+
+  int flag = 0;
+  double Z;
+  const int t1 = finish_draw(G, S, sums, P.v1[b], ps, &flag, &Z);
+  // stage 2: M_2 verifies the first w2 tokens of O_1 = d[0, a1) ++ t1 against M_1
+  const int w2 = min(g2, a1 + 1);
+  if (warp == 0) {
+    bool keep = true;
+    if (lane < w2) {
+      const int o = lane < a1 ? cs.tok[lane] : t1;
+      const float xp = load_elem(L2 + (b2 + lane) * P.ld + o);
+      const float xq = load_elem(L1 + (b1 + lane) * P.ld + o);
+      keep = keeps(P.u2[b2 + lane],
+                   ratio(xp, cs.st_m[r2 + lane], cs.st_s[r2 + lane], xq, cs.st_m[r1 + lane], cs.st_s[r1 + lane], c));
+    }
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < w2 && !keep);
+    if (lane == 0) cs.a2 = rej ? __ffs(rej) - 1 : w2;
+  }
+  __syncthreads();
+  const int a2 = cs.a2;
+  if (tid == 0) {
+    if (a2 < w2) {  // hand the residual max(0, p2 - p1) at position a2 to the stage-2 kernel
+      const PassSpec<T> S2 = make_spec(L2 + (b2 + a2) * P.ld, cs.st_m[r2 + a2], cs.st_s[r2 + a2],
+                                       L1 + (b1 + a2) * P.ld, cs.st_m[r1 + a2], cs.st_s[r1 + a2], 1.f, c);
+      SpecG sg;
+      sg.P = S2.P;
+      sg.Q = S2.Q;
+      sg.MP = S2.MP;
+      sg.invSP = S2.invSP;
+      sg.MQ = S2.MQ;
+      sg.invSQ = S2.invSQ;
+      sg.cq = S2.cq;
+      sg.a = a2;
+      sg.a1 = a1;
+      sg.t1 = t1;
+      *spec2 = sg;
+      reinterpret_cast<int*>(G.mid)[4 * b] = flag;  // stage-1 flags for the final outputs
+    } else {
+      out.write(a1, t1, a2, w2, -1, 0, flag);
+      spec2->a = -1;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) cascade_walk2_kernel(const StatsParams G, const CascadeParams P) {
+  __shared__ PassSmem ps;
+  __shared__ int last_s;
+  const int j = blockIdx.x, b = blockIdx.y;
+  pdl_wait();  // the stage-1 kernel is complete
+  const SpecG sg = reinterpret_cast<const SpecG*>(G.specs)[b];
+  if (sg.a < 0) return;  // no stage-2 pass for this sequence
+  PassSpec<T> S;
+  S.P = static_cast<const T*>(sg.P);
+  S.Q = static_cast<const T*>(sg.Q);
+  S.MP = sg.MP;
+  S.invSP = sg.invSP;
+  S.MQ = sg.MQ;
+  S.invSQ = sg.invSQ;
+  S.cq = sg.cq;
+  S.pad = 0;
+  float* sums = pass_sums(G, b, 1);
+  const int t0 = j * G.tps, t1 = min(G.ntiles, t0 + G.tps);
+  if (t0 < t1) tile_sums(S, G.V, G.c, t0, t1, sums, ps);
+  if (!arrive(&seq_state(G, b)->done2, gridDim.x, &last_s)) return;
+  int flag = reinterpret_cast<const int*>(G.mid)[4 * b];
+  double Z;
+  const int t2 = finish_draw(G, S, sums, P.v2[b], ps, &flag, &Z);
+  if (threadIdx.x == 0) {
+    const CascadeOut out{P, b};
+    out.write(sg.a1, sg.t1, sg.a, min(P.g2, sg.a1 + 1), t2, 1, flag);
+  }
+}
+
+// ===========================================================================
+// 2c. tree (one CTA per tree)
+//
+// After k rejected siblings at one node the current distribution is
+//     p_k = max(0, p - c_k q) / W_k,   c_0 = 0, W_0 = 1,
+//     c_{k+1} = c_k + W_k,             W_{k+1} = sum_x max(0, p - c_{k+1} q),
+// since max(0, max(0, p - c_k q)/W_k - q) = max(0, p - (c_k + W_k) q)/W_k
+// where the inner term is positive, and both sides are 0 elsewhere.  So each
+// rejection costs one pass with the scalar cq = c_{k+1}, and a final draw
+// searches the last pass with target v * W_k: the iterated renormalisation
+// of the rule, written in closed form.
+// ===========================================================================
+struct TreeSmem {
+  float2* st;  // [2N] (max, sum) of target rows then draft rows; greedy: argmax in .y
+  int* par;    // [N]
+  int* tk;     // [N]
+  float* gp;   // [N] target logit of node i's token in its parent's row
+  float* gq;   // [N] draft logit of the same
+  int* scr_a;  // [N] depth pointer jumping, then the children of the current node
+  int* scr_b;  // [N] depth pointer jumping, then the kept path
+};
+
+__device__ __forceinline__ TreeSmem tree_smem(char* base, int N) {
+  TreeSmem t;
+  t.st = reinterpret_cast<float2*>(base);
+  t.par = reinterpret_cast<int*>(base + 16 * N);
+  t.tk = t.par + N;
+  t.gp = reinterpret_cast<float*>(t.tk + N);
+  t.gq = t.gp + N;
+  t.scr_a = reinterpret_cast<int*>(t.gq + N);
+  t.scr_b = t.scr_a + N;
+  return t;
+}
+
+// Children of `node`, ascending, into kids[] (warp 0); count for all threads.
+__device__ int list_children(const int* par, int N, int node, int* kids, int* count_s) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    int count = 0;
+    for (int base = node + 1; base < N; base += 32) {
+      const int i = base + lane;
+      const bool ch = i < N && par[i] == node;
+      const unsigned m = __ballot_sync(0xffffffffu, ch);
+      if (ch) kids[count + __popc(m & ((1u << lane) - 1u))] = i;
+      count += __popc(m);
+    }
+    if (lane == 0) *count_s = count;
+  }
+  __syncthreads();
+  return *count_s;
+}
+
+template <typename T, bool kGreedy>
+__global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, const TreeParams P) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ PassSmem ps;
+  __shared__ int err_s, nk_s, keep_s;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = P.N;
+  const float c = G.c;
+  TreeSmem ts = tree_smem(reinterpret_cast<char*>(dyn), N);
+  const long long row0 = static_cast<long long>(b) * N;
+
+  // tree shape and tokens (inputs: read while the statistics finish)
+  if (tid == 0) err_s = 0;
+  for (int i = tid; i < N; i += kThreads) {
+    ts.par[i] = P.parent[row0 + i];
+    ts.tk[i] = P.tokens[row0 + i];
+  }
+  __syncthreads();
+  for (int i = tid; i < N; i += kThreads) {
+    const int p = ts.par[i];
+    if (i == 0 ? p != -1 : (p < 0 || p >= i)) atomicOr(&err_s, SPEC_ERR_PARENT);
+    if (i > 0 && (ts.tk[i] < 0 || ts.tk[i] >= P.V)) atomicOr(&err_s, SPEC_ERR_TOKEN);
+  }
+  __syncthreads();
+  if (!(err_s & SPEC_ERR_PARENT)) {
+    // depth by pointer jumping (N <= 1024, two nodes per thread):
+    // D[i] += D[A[i]], A[i] = A[A[i]]
+    constexpr int kPer = 1024 / kThreads;
+    for (int i = tid; i < N; i += kThreads) {
+      ts.scr_a[i] = i == 0 ? 0 : ts.par[i];
+      ts.scr_b[i] = i == 0 ? 0 : 1;
+    }
+    __syncthreads();
+    for (int span = 1; span < N; span <<= 1) {
+      int na[kPer], nd[kPer];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < N) {
+          const int a = ts.scr_a[i];
+          nd[q] = ts.scr_b[i] + ts.scr_b[a];
+          na[q] = ts.scr_a[a];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < N) {
+          ts.scr_a[i] = na[q];
+          ts.scr_b[i] = nd[q];
+        }
+      }
+      __syncthreads();
+    }
+    for (int i = tid; i < N; i += kThreads)
+      if (ts.scr_b[i] > P.max_depth) atomicOr(&err_s, SPEC_ERR_PARENT);
+    __syncthreads();
+    if (!kGreedy && err_s == 0) {
+      for (int i = tid + 1; i < N; i += kThreads) {
+        const long long off = (row0 + ts.par[i]) * P.ld + ts.tk[i];
+        ts.gp[i] = load_elem(static_cast<const T*>(P.target) + off);
+        ts.gq[i] = load_elem(static_cast<const T*>(P.draft) + off);
+      }
+    }
+  }
+  pdl_wait();
+  {
+    const float2* part = G.partials + static_cast<long long>(b) * G.rows_per_seq * G.chunks;
+    for (int rr = warp; rr < G.rows_per_seq; rr += kWarps) {
+      if constexpr (kGreedy) {
+        bool bad;
+        const ArgMax am = combine_row_argmax(part + static_cast<long long>(rr) * G.chunks, G.chunks, bad);
+        if (lane == 0) {
+          ts.st[rr] = make_float2(0.f, __int_as_float(am.i));
+          if (bad || am.i < 0) atomicOr(&err_s, SPEC_ERR_NONFINITE);
+        }
+      } else {
+        const MaxSum ms = combine_row(part + static_cast<long long>(rr) * G.chunks, G.chunks, c);
+        if (lane == 0) {
+          ts.st[rr] = make_float2(ms.m, ms.s);
+          if (!row_stats_ok(ms)) atomicOr(&err_s, SPEC_ERR_NONFINITE);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  const int err = err_s;
+  const int prefix = P.prefix ? P.prefix[b] : 0;
+  const int pn = P.max_depth + 1;
+  int* pnodes = P.path_nodes + static_cast<long long>(b) * pn;
+  if (err) {
+    if (tid == 0) {
+      P.path_len[b] = 0;
+      P.out_token[b] = -1;
+      if (P.rollback) P.rollback[b] = prefix;
+      if (P.seq_error) P.seq_error[b] = err;
+      if (P.error_word) atomicOr(P.error_word, err);
+    }
+    for (int q = tid; q < pn; q += kThreads) pnodes[q] = -1;
+    return;
+  }
+
+  const T* target = static_cast<const T*>(P.target);
+  const T* draft = static_cast<const T*>(P.draft);
+  int* kids = ts.scr_a;
+  int* path = ts.scr_b;
+  float* sums = pass_sums(G, b, 0);
+  int node = 0, plen = 0, flag = 0, token = -1;
+  while (true) {
+    const int nk = list_children(ts.par, N, node, kids, &nk_s);
+    if constexpr (kGreedy) {
+      const int best = __float_as_int(ts.st[node].y);
+      int kept = -1;
+      for (int q = 0; q < nk; ++q)
+        if (ts.tk[kids[q]] == best) {
+          kept = kids[q];
+          break;
+        }
+      __syncthreads();  // kids[] is rewritten by the next list_children
+      if (kept < 0) {
+        token = best;
+        break;
+      }
+      if (tid == 0) path[plen] = kept;
+      ++plen;
+      node = kept;
+    } else {
+      const float2 sp = ts.st[node];
+      const float2 sq = ts.st[N + node];
+      PassSpec<T> S = make_spec(target + (row0 + node) * P.ld, sp.x, sp.y, draft + (row0 + node) * P.ld, sq.x,
+                                sq.y, 1.f, c);
+      S.cq = 0.f;
+      double cc = 0.0, W = 1.0;
+      int kept = -1;
+      bool zero_mass = false;
+      for (int q = 0; q < nk; ++q) {
+        const int ch = kids[q];
+        if (tid == 0) {  // sibling test: p_k(tok) / q(tok) against u
+          const double pt = prob(ts.gp[ch], sp.x, sp.y, c);
+          const double qt = prob(ts.gq[ch], sq.x, sq.y, c);
+          const double pk = fmax(0.0, pt - cc * qt) / W;
+          const double rt = qt > 0.0 ? pk / qt : (pk > 0.0 ? INFINITY : 0.0);
+          keep_s = static_cast<double>(P.u[row0 + ch]) < fmin(1.0, rt);
+        }
+        __syncthreads();
+        if (keep_s) {
+          kept = ch;
+          break;
+        }
+        const double cn = cc + W;
+        S.cq = static_cast<float>(cn);
+        tile_sums(S, P.V, c, 0, G.ntiles, sums, ps);
+        __threadfence_block();
+        const double Wn = tile_prefix(sums, G.ntiles, ps);
+        if (!(Wn > 0.0) || !(Wn < INFINITY)) {
+          zero_mass = true;
+          break;
+        }
+        cc = cn;
+        W = Wn;
+      }
+      __syncthreads();  // kids[] is rewritten by the next list_children
+      if (kept >= 0) {
+        if (tid == 0) path[plen] = kept;
+        ++plen;
+        node = kept;
+        continue;
+      }
+      double Z = W;
+      if (zero_mass || nk == 0) {
+        if (zero_mass) flag = SPEC_ERR_ZERO_MASS;
+        S.cq = 0.f;  // draw from the node's own target distribution
+        tile_sums(S, P.V, c, 0, G.ntiles, sums, ps);
+        __threadfence_block();
+        Z = tile_prefix(sums, G.ntiles, ps);
+      }
+      token = draw(S, P.V, c, sums, G.ntiles, static_cast<double>(P.v[b]) * Z, ps);
+      break;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    P.out_token[b] = token;
+    P.path_len[b] = plen;
+    if (P.rollback) P.rollback[b] = prefix + plen;
+    if (P.seq_error) P.seq_error[b] = flag;
+    if (flag && P.error_word) atomicOr(P.error_word, flag);
+  }
+  for (int q = tid; q < pn; q += kThreads) pnodes[q] = q == 0 ? 0 : (q <= plen ? path[q - 1] : -1);
+}
+
+// ---------------------------------------------------------------------------
+// launches
+// ---------------------------------------------------------------------------
+template <typename K>
+cudaError_t launch_stats(K kernel, const StatsParams& G, cudaStream_t s) {
+  dim3 grid(G.chunks, G.rows_per_seq, G.B);
+  kernel<<<grid, kStatsThreads, 0, s>>>(G);
+  return cudaGetLastError();
+}
+
+// A dependent kernel: programmatic stream serialisation lets it start while
+// its predecessor drains; it reads the predecessor's results only after
+// griddepcontrol.wait.
+template <typename K, typename A>
+cudaError_t launch_dependent(K kernel, dim3 grid, size_t dyn, const StatsParams& G, const A& args, cudaStream_t s) {
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  if (dyn > 32 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  void* argv[] = {const_cast<StatsParams*>(&G), const_cast<A*>(&args)};
+  return cudaLaunchKernelExC(&cfg, fn, argv);
+}
+
+int slices(const StatsParams& G) { return (G.ntiles + G.tps - 1) / G.tps; }
+
+template <typename T>
+cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s) {
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+  if (e != cudaSuccess) return e;
+  if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, G, p, s);
+  return launch_dependent(chain_walk_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
+}
+
+template <typename T>
+cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, cudaStream_t s) {
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+  if (e != cudaSuccess) return e;
+  const size_t dyn = static_cast<size_t>(40) * p.N;  // TreeSmem arrays
+  if (greedy) return launch_dependent(tree_kernel<T, true>, dim3(G.B), dyn, G, p, s);
+  return launch_dependent(tree_kernel<T, false>, dim3(G.B), dyn, G, p, s);
+}
+
+template <typename T>
+cudaError_t cascade_impl(const StatsParams& G, const CascadeParams& p, bool greedy, cudaStream_t s) {
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+  if (e != cudaSuccess) return e;
+  if (greedy) return launch_dependent(cascade_greedy_kernel<T>, dim3(G.B), 0, G, p, s);
+  e = launch_dependent(cascade_walk1_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(cascade_walk2_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
+}
+
+}  // namespace
+
+int stats_chunks(int V, bool bf16) {
+  const int ce = bf16 ? chunk_elems<bf16_t>() : chunk_elems<float>();
+  return (V + ce - 1) / ce;
+}
+
+int pass_tiles(int V) { return (V + kTileElems - 1) / kTileElems; }
+
+cudaError_t launch_chain(const StatsParams& G, const ChainParams& p, bool bf16, bool greedy, cudaStream_t s) {
+  return bf16 ? chain_impl<bf16_t>(G, p, greedy, s) : chain_impl<float>(G, p, greedy, s);
+}
+
+cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s) {
+  return bf16 ? tree_impl<bf16_t>(G, p, greedy, s) : tree_impl<float>(G, p, greedy, s);
+}
+
+cudaError_t launch_cascade(const StatsParams& G, const CascadeParams& p, bool bf16, bool greedy, cudaStream_t s) {
+  return bf16 ? cascade_impl<bf16_t>(G, p, greedy, s) : cascade_impl<float>(G, p, greedy, s);
+}
+
+}  // namespace sv

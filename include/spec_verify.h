@@ -50,13 +50,19 @@
  *    optional per-sequence `seq_error` array and are OR-ed into the optional
  *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2 or 4 gets
  *    empty outputs: accept length 0, tokens -1, rollback = prefix length.
- *  - The workspace is scratch for one call; size it with the matching
- *    *_workspace_size function.  Two calls in flight at the same time need
- *    two workspaces.  Results are deterministic: the same inputs on the same
- *    GPU give bit-identical outputs.
- *  - stats_begin / stats_end: optional events (NULL to skip) recorded on
- *    `stream` immediately before and after the row-statistics kernel, the
- *    pass that streams every logit row once.
+ *  - Each call is one kernel launch.  Its CTAs stream every logit row once
+ *    (row statistics); the CTA that completes a sequence then verifies that
+ *    sequence while its rows are still in L2.
+ *  - The workspace starts with a fixed head (256 bytes of call counters and
+ *    one 32-byte state record per possible sequence index: 2,097,408 bytes)
+ *    followed by per-call scratch.  Size it with the matching
+ *    *_workspace_size function and ZERO THE HEAD ONCE before the first call
+ *    (cudaMemset of the whole workspace is simplest); every call leaves the
+ *    head at zero again, whatever its kind, mode or batch size, so one
+ *    workspace serves any sequence of calls on one stream.  Two calls in flight at the same
+ *    time need two workspaces.  Results are deterministic: the same inputs
+ *    on the same GPU give bit-identical outputs.
+ *  - Limits: B <= 65535, V <= 2,097,152.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -86,6 +92,8 @@ typedef enum spec_mode { SPEC_GREEDY = 0, SPEC_SAMPLE = 1 } spec_mode;
 #define SPEC_ERR_NONFINITE 4  /* a logit row with NaN or +inf, or no finite entry */
 #define SPEC_ERR_ZERO_MASS 8  /* residual mass 0 after a rejection: the token was
                                  drawn from p instead (outputs stay valid)       */
+#define SPEC_ERR_INTERNAL 16  /* (error_word only) a work item waited too long for
+                                 another; the call's outputs are not valid      */
 
 /* ---------------------------------------------------------------------- */
 /* Chain verification: B sequences, each with a gamma-token draft.         */
@@ -118,10 +126,8 @@ typedef struct spec_chain_args {
                                   token was drawn from (0 in greedy)                */
   int* seq_error;              /* out [B], optional: data-error bits                */
   int* error_word;             /* in/out, optional: data-error bits OR-ed in        */
-  void* workspace;
+  void* workspace;             /* zeroed once before first use, see the file comment */
   size_t workspace_bytes;
-  cudaEvent_t stats_begin;     /* optional, see the file comment                    */
-  cudaEvent_t stats_end;
 } spec_chain_args;
 
 size_t spec_chain_workspace_size(int B, int gamma, int V);
@@ -166,8 +172,6 @@ typedef struct spec_tree_args {
   int* error_word;             /* in/out, optional                                  */
   void* workspace;
   size_t workspace_bytes;
-  cudaEvent_t stats_begin;
-  cudaEvent_t stats_end;
 } spec_tree_args;
 
 size_t spec_tree_workspace_size(int B, int N, int V);
@@ -219,8 +223,6 @@ typedef struct spec_cascade_args {
   int* error_word;             /* in/out, optional                                  */
   void* workspace;
   size_t workspace_bytes;
-  cudaEvent_t stats_begin;
-  cudaEvent_t stats_end;
 } spec_cascade_args;
 
 size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V);

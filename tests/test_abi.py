@@ -74,10 +74,23 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # chain: (2 gamma + 1) rows x ceil(V / 8192) chunks x 8 bytes per sequence
-    assert lib.spec_chain_workspace_size(64, 5, 128256) == 64 * 11 * 16 * 8
-    assert lib.spec_tree_workspace_size(16, 64, 50257) == 16 * 128 * 7 * 8
-    assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == 128 * 21 * 16 * 8
+    # head (256 B + 65536 x 32 B sequence records), then per call, each
+    # region rounded up to 256 B: a 48 B pass record and 16 B per sequence,
+    # pass tile sums (2 x 4 B per 4096-element tile), chunk partials (8 B per
+    # row per 8192 elements: the float32 chunk of the statistics kernel).
+    head = 256 + 65536 * 32
+
+    def r256(x):
+        return (x + 255) // 256 * 256
+
+    def size(B, rows, V):
+        tiles, chunks = -(-V // 4096), -(-V // 8192)
+        return head + r256(B * 48) + r256(B * 16) + r256(B * 2 * tiles * 4) + r256(B * rows * chunks * 8)
+
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256)
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == head + 3072 + 1024 + 16384 + 90112
+    assert lib.spec_tree_workspace_size(16, 64, 50257) == size(16, 128, 50257)
+    assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == size(128, 21, 128256)
     assert lib.spec_chain_workspace_size(0, 5, 10) == 0
 
 
