@@ -5,7 +5,7 @@ include/spec_verify.h); this package only builds it and marshals arguments.
 """
 
 from .api import (  # noqa: F401
-    CascadePlan, ChainPlan, TreePlan, verify_cascade, verify_chain, verify_tree,
+    CascadePlan, ChainPlan, ChainPlanNoAlloc, TreePlan, verify_cascade, verify_chain, verify_tree,
     workspace_bytes,
 )
 from ._lib import ERR_NONFINITE, ERR_PARENT, ERR_TOKEN, ERR_ZERO_MASS  # noqa: F401

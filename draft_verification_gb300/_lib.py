@@ -15,6 +15,7 @@ from .build import lib_path
 SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EALIGN, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, -4, -5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_GREEDY, SPEC_SAMPLE = 0, 1
+SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 ERR_TOKEN, ERR_PARENT, ERR_NONFINITE, ERR_ZERO_MASS, ERR_INTERNAL = 1, 2, 4, 8, 16
 
 _vp = C.c_void_p
@@ -65,6 +66,7 @@ class CascadeArgs(C.Structure):
 SIGNATURES = {
     "spec_chain_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spec_verify_chain": (C.c_int, [C.POINTER(ChainArgs), _vp]),
+    "spec_verify_chain_noalloc": (C.c_int, [C.POINTER(ChainArgs), _vp]),
     "spec_tree_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spec_verify_tree": (C.c_int, [C.POINTER(TreeArgs), _vp]),
     "spec_cascade_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),

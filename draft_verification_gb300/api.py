@@ -128,6 +128,22 @@ class ChainPlan(_Plan):
         self._call = lib.spec_verify_chain
 
 
+class ChainPlanNoAlloc(ChainPlan):
+    """ChainPlan bound to spec_verify_chain_noalloc: the library's static
+    scratch replaces the workspace tensor, so neither this plan nor its runs
+    allocate scratch.  Runs that can overlap on the GPU race on that scratch;
+    the first run on a device should come before any stream capture."""
+
+    def __init__(self, target, *args, **kw):
+        if kw.get("workspace") is not None:
+            raise TypeError("ChainPlanNoAlloc takes no workspace")
+        # a zero-element tensor holds no device memory; the entry point
+        # ignores the workspace fields
+        kw["workspace"] = torch.empty(0, dtype=torch.uint8, device=target.device)
+        super().__init__(target, *args, **kw)
+        self._call = L.lib().spec_verify_chain_noalloc
+
+
 class TreePlan(_Plan):
     """Tree verification bound to fixed buffers.  See spec_verify_tree."""
 

@@ -134,6 +134,30 @@ size_t spec_chain_workspace_size(int B, int gamma, int V);
 spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* Chain verification with library-owned scratch.  None of the pages has a */
+/* counterpart: this is a deployment variant of spec_verify_chain for       */
+/* callers that cannot provide a workspace.  Same rule, arguments, outputs  */
+/* and results as spec_verify_chain, except that args->workspace and        */
+/* args->workspace_bytes are ignored: the scratch is one static device      */
+/* array of SPEC_NOALLOC_SCRATCH_BYTES per device, reserved when the        */
+/* library is loaded.  The call allocates and frees nothing.                */
+/*  - Size limit: the call returns SPEC_EWORKSPACE, launching nothing, when */
+/*    spec_chain_workspace_size(B, gamma, V) > SPEC_NOALLOC_SCRATCH_BYTES    */
+/*    (e.g. B = 64, gamma = 5, V = 128256 needs 2.2 MB and fits; B = 1024,  */
+/*    gamma = 8, V = 131072 needs 4.6 MB and fits; B = 8192 does not).      */
+/*  - The first call on a device looks up the array's device address (with  */
+/*    that device current) and keeps it; make that first call before any   */
+/*    stream capture.  Each call clears the completion counters it uses     */
+/*    (a memset node on `stream`) before its kernels run.                   */
+/*  - All calls on one device share the array: two calls that can overlap   */
+/*    on the GPU (other streams, other host threads) race on it and give    */
+/*    wrong results.  Serialise them, or use spec_verify_chain with one     */
+/*    workspace per stream.                                                 */
+/* ---------------------------------------------------------------------- */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Tree verification: each sequence carries a draft tree of N nodes.       */
 /* Staged Speculative Decoding, abstract (the speculative batch as a       */
 /* tree).  Row n of the logit arrays is the distribution over the children */

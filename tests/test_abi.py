@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 7, names
+    assert len(names) == 8, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -134,3 +134,16 @@ def test_tree_and_cascade_argument_errors(lib):
     c.dtype, c.mode, c.temperature = 1, 1, 1.0
     assert lib.spec_verify_cascade(C.byref(c), None) == -1
     assert lib.spec_verify_chain(None, None) == -1
+
+
+def test_noalloc_chain_rejects_before_touching_the_device(lib):
+    from draft_verification_gb300 import _lib
+    assert lib.spec_verify_chain_noalloc(None, None) == -1
+    assert lib.spec_verify_chain_noalloc(C.byref(_chain(B=0)), None) == -1
+    assert lib.spec_verify_chain_noalloc(C.byref(_chain(gamma=33)), None) == -1
+    # the static scratch is 8 MiB; a batch whose scratch exceeds it is refused
+    assert _lib.SPEC_NOALLOC_SCRATCH_BYTES == 8 << 20
+    big = _chain(B=8192, gamma=8, V=131072, ld=131072)
+    assert lib.spec_chain_workspace_size(8192, 8, 131072) > _lib.SPEC_NOALLOC_SCRATCH_BYTES
+    assert lib.spec_verify_chain_noalloc(C.byref(big), None) == -4
+    assert lib.spec_chain_workspace_size(1024, 8, 131072) <= _lib.SPEC_NOALLOC_SCRATCH_BYTES
