@@ -319,7 +319,7 @@ def run_ours(args, w, rank, world, dist):
 
     base = device_inputs(w, dev)
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
-    ws = torch.zeros(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
     plans = [make_plan(w, t, ws) for t in sets]
     stream = torch.cuda.Stream(dev)
 

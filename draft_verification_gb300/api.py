@@ -103,7 +103,7 @@ class ChainPlan(_Plan):
             self.out["resid_mass"] = torch.empty(B, dtype=torch.float32, device=dev)
         need = lib.spec_chain_workspace_size(B, gamma, V)
         if workspace is None:
-            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.ChainArgs()
         a.B, a.gamma, a.V, a.ld = B, gamma, V, ld
@@ -168,7 +168,7 @@ class TreePlan(_Plan):
         )
         need = lib.spec_tree_workspace_size(B, N, V)
         if workspace is None:
-            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.TreeArgs()
         a.B, a.N, a.max_depth, a.V, a.ld = B, N, int(max_depth), V, ld
@@ -213,7 +213,7 @@ class CascadePlan(_Plan):
         self.out["error_word"] = torch.zeros(1, dtype=torch.int32, device=dev)
         need = lib.spec_cascade_workspace_size(B, g1, g2, V)
         if workspace is None:
-            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.workspace = workspace
         a = L.CascadeArgs()
         a.B, a.gamma1, a.gamma2, a.V, a.ld = B, g1, g2, V, ld

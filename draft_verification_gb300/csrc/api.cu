@@ -10,8 +10,8 @@ namespace sv {
 
 namespace {
 
-constexpr int kMaxV = 512 * 4096;  // pass tiles per row bound (walk.cuh)
-constexpr int kMaxB = kMaxSeq;     // per-sequence state records
+constexpr int kMaxV = 2097152;  // tile sums of a whole row fit in shared memory (walk.cuh)
+constexpr int kMaxB = kMaxSeq;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -43,15 +43,8 @@ bool stats_params(StatsParams& sp, int B, int V, long long ld, bool bf16, bool g
   sp.ld = ld;
   sp.chunks = stats_chunks(V, bf16);
   sp.ntiles = pass_tiles(V);
-  sp.tps = kTilesPerSlice;
   sp.c = greedy ? 1.f : logit_scale(temperature);
-  char* ws = static_cast<char*>(workspace);
-  const Layout L = workspace_layout(B, rows, V);
-  sp.state = ws + 256;
-  sp.specs = ws + L.specs;
-  sp.mid = ws + L.mid;
-  sp.sums = reinterpret_cast<float*>(ws + L.sums);
-  sp.partials = reinterpret_cast<float2*>(ws + L.partials);
+  sp.partials = static_cast<float2*>(workspace);
   return rows <= 65535 && sp.chunks <= 0x7fffffff;
 }
 

@@ -21,7 +21,7 @@ namespace sv {
 constexpr int kStatsThreads = 256;       // row-statistics kernel: small CTAs, many per SM
 constexpr int kStatsWarps = kStatsThreads / 32;
 constexpr int kVecPerThread = 8;         // 16-byte loads per thread per statistics unit
-constexpr int kThreads = 512;            // walk kernels
+constexpr int kThreads = 256;            // walk kernels (one CTA of a per-sequence cluster)
 constexpr int kWarps = kThreads / 32;
 static_assert(kWarps <= 32 && kStatsWarps <= 32, "one warp reduces the per-warp partials");
 constexpr int kTileElems = 8 * kThreads; // pass tile: 8 contiguous elements per thread
@@ -90,6 +90,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   float2 d;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -104,6 +113,135 @@ __device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn
 // 2^(x c - M): the unnormalised softmax weight of logit x.
 __device__ __forceinline__ float weight(float x, float c, float M) {
   return ex2(__fmaf_rn(x, c, -M));
+}
+
+// ---------------------------------------------------------------------------
+// bulk copies (TMA engine) into shared memory, completed on an mbarrier
+// ---------------------------------------------------------------------------
+// Bound on an mbarrier wait: kMaxPolls polls, each suspending the thread for
+// at most kPollNs nanoseconds (about 65 ms in all) before the wait gives up.
+constexpr int kMaxPolls = 1 << 16;
+constexpr int kPollNs = 1000;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+// Make initialised mbarriers visible to the bulk-copy engine.
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// One arrival that also announces `bytes` of bulk-copy data to come.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(kPollNs)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete; false if it did not within
+// kMaxPolls polls (the caller records a fault instead of hanging).  The
+// arrival that completes the phase must already have been issued by a thread
+// that is not waiting: a thread issuing copies for a phase that lanes of its
+// own warp already wait on could be held back by their suspension.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  for (int i = 0; i < kMaxPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// One arrival, with release semantics at cluster scope, on the mbarrier at
+// the address of `local` in cluster CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* local, unsigned rank) {
+  const uint32_t a = smem_addr(local);
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(r) : "memory");
+}
+// Bounded wait, with acquire semantics at cluster scope, for phase `parity`
+// of a local mbarrier that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity) {
+  for (int i = 0; i < kMaxPolls; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kPollNs)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Order this thread's earlier shared-memory accesses before later bulk copies.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+// Store v at the address of `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_u32(int* local, unsigned rank, int v) {
+  const uint32_t a = smem_addr(local);
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(r), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// double-float numbers: hi + lo with |lo| <= ulp(hi) / 2, about 44 bits of
+// precision from float32 arithmetic only (FP64 throughput on GB300 is a small
+// fraction of FP32's).  Additions use Knuth's TwoSum, products the fused
+// multiply-add error term; every operation is an explicitly rounded
+// intrinsic, so the compiler cannot contract or reassociate them.
+// ---------------------------------------------------------------------------
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_norm(float s, float e) {  // |e| small against s
+  const float hi = __fadd_rn(s, e);
+  return {hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  return df_norm(s, e);
+}
+__device__ __forceinline__ DF df_add_f(DF a, float b) { return df_add(a, DF{b, 0.f}); }
+__device__ __forceinline__ DF df_neg(DF a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ DF df_mul_f(DF a, float v) {
+  const float p = __fmul_rn(a.hi, v);
+  float e = __fmaf_rn(a.hi, v, -p);
+  e = __fmaf_rn(a.lo, v, e);
+  return df_norm(p, e);
+}
+__device__ __forceinline__ float df_float(DF a) { return __fadd_rn(a.hi, a.lo); }
+__device__ __forceinline__ double df_double(DF a) {
+  return static_cast<double>(a.hi) + static_cast<double>(a.lo);
+}
+__device__ __forceinline__ DF df_shfl_up(DF a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
 }
 
 // ---------------------------------------------------------------------------
@@ -172,5 +310,39 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Wait until the previous kernel in the stream has completed and its memory
 // is visible (a no-op when this kernel was not launched as a dependent).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// thread-block clusters (one cluster per sequence in the sampling walks)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Split cluster barrier.  Every thread of every CTA of the cluster executes
+// the same sequence of arrives and waits (the kernels keep the control flow
+// around them uniform across the cluster).  Stores to other CTAs' shared
+// memory made before an arrive are visible after the matching wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+// Store v at the address of `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster(float* local, unsigned rank, float v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+}
 
 }  // namespace sv

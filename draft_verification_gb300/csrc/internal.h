@@ -23,12 +23,7 @@ struct StatsParams {
   long long ld;
   int chunks;           // statistics CTAs per row
   int ntiles;           // pass tiles per row
-  int tps;              // pass tiles per slice CTA
   float c;              // log2(e) / T (sampling); unused in greedy mode
-  void* state;          // [kMaxSeq] per-sequence counters, zero between calls
-  void* specs;          // [B] cascade: the stage-2 pass
-  void* mid;            // [B] cascade: stage-1 flags
-  float* sums;          // [B][2][ntiles] pass tile sums
   float2* partials;     // [B][rows_per_seq][chunks]: (max, sum) or (value, index)
 };
 
@@ -36,37 +31,15 @@ struct StatsParams {
 // (float32) count so one size serves both dtypes.
 int stats_chunks(int V, bool bf16);
 int pass_tiles(int V);
-constexpr int kTilesPerSlice = 4;
 
-// Workspace layout.  A fixed head, zeroed once by the caller and left zero by
-// every call: 256 reserved bytes and one 32-byte record per possible sequence
-// index, so that calls of any batch size, mode or kind share it.  Then
-// per-call scratch, fully written before it is read.
-constexpr int kMaxSeq = 65535;
-constexpr size_t kSeqStateBytes = 32;
-constexpr size_t kSpecBytes = 48;
-constexpr size_t kHeadBytes = 256 + 65536 * kSeqStateBytes;
+constexpr int kMaxSeq = 65535;  // statistics grid z extent
+
+// Workspace: the chunk partials of the statistics kernel, 8 bytes per
+// (sequence, row, chunk), written by the first kernel of a call and read by
+// the second; nothing in it outlives a call, so it needs no initialisation.
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-struct Layout {
-  size_t specs, mid, sums, partials, total;
-};
-inline Layout workspace_layout(int B, int rows_per_seq, int V) {
-  Layout L;
-  size_t off = kHeadBytes;
-  L.specs = off;
-  off = align256(off + static_cast<size_t>(B) * kSpecBytes);
-  L.mid = off;
-  off = align256(off + static_cast<size_t>(B) * 16);
-  L.sums = off;
-  off = align256(off + static_cast<size_t>(B) * 2 * pass_tiles(V) * 4);
-  L.partials = off;
-  off = align256(off + static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
-  L.total = off;
-  return L;
-}
 inline size_t workspace_bytes(int B, int rows_per_seq, int V) {
-  return workspace_layout(B, rows_per_seq, V).total;
+  return align256(static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
 }
 
 struct ChainParams {

@@ -1,22 +1,24 @@
 // Batched draft verification kernels and their launch sequence.
 //
-// Every call is a short chain of kernels on the caller's stream, each
-// launched with programmatic dependent launch so that it is resident and has
-// read its own inputs by the time its predecessor finishes:
+// Every call is two kernels on the caller's stream; the second is launched
+// with programmatic dependent launch, so it is resident and has read its own
+// inputs by the time the first finishes:
 //
 //   1. stats_kernel  one CTA per (sequence, row, 16384-element chunk): the
 //                    online-softmax (max, sum) or the argmax of the chunk
 //                    (stats.cuh).  This streams every logit once; it is
 //                    the bandwidth-bound kernel.
-//   2. walk kernels  one CTA per (sequence, pass slice).  Every slice CTA of a
-//                    sequence merges the sequence's statistics and evaluates
-//                    the accept tests itself (a few hundred bytes), then sums
-//                    the residual / bonus weights of its tiles of the chosen
-//                    row pair (walk.cuh); the slice that arrives last on the
-//                    sequence's counter draws the token.  No CTA waits for
-//                    another.  The cascade runs a second walk kernel for its
-//                    second stage; trees and greedy calls use one CTA per
-//                    sequence.
+//   2. walk kernel   sampling: one thread-block cluster of up to 8 CTAs per
+//                    sequence.  Every CTA merges the sequence's statistics
+//                    and evaluates the accept tests itself (a few hundred
+//                    bytes), then the cluster sums the residual / bonus
+//                    weights of the chosen row pair, each CTA a slice of
+//                    its tiles, exchanging the tile sums through distributed
+//                    shared memory (walk.cuh); the CTA holding the drawn
+//                    index's tile writes the result.  Greedy calls use one
+//                    CTA per sequence.  The cascade runs both of its stages
+//                    in the same cluster; a tree runs its serial walk in
+//                    every CTA of its cluster and splits each pass.
 //
 // Rules (pages: the Pith review of PipeSpec, "What carries the argument" and
 // the acceptance rule of Leviathan et al. its Circularity Check cites; Staged
@@ -28,6 +30,15 @@
 //    the first tokens of stage 1's output);
 //  * tree: a serial walk from the root (each rejected sibling changes the
 //    distribution the next sibling is tested against).
+//
+// Cluster discipline: all CTAs of a cluster read the same inputs and run the
+// same code on them, so they take the same branches; every cluster barrier
+// is therefore reached by all of them or by none.
+#include <array>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 #include "internal.h"
 #include "spec_verify.h"
@@ -38,44 +49,8 @@ namespace sv {
 namespace {
 
 constexpr int kMaxGamma = 32;
-
-// ---------------------------------------------------------------------------
-// workspace records
-// ---------------------------------------------------------------------------
-struct SeqState {  // zero between calls
-  unsigned done1;  // slices of the first pass that have finished
-  unsigned done2;  // slices of the second pass (cascade)
-  int pad[6];
-};
-static_assert(sizeof(SeqState) == kSeqStateBytes, "state layout");
-
-struct SpecG {  // a pass handed from the first walk kernel to the second
-  const void* P;
-  const void* Q;
-  float MP, invSP, MQ, invSQ, cq;
-  int a;  // the decision that goes with it, or -1: no pass
-  int a1, t1;
-};
-static_assert(sizeof(SpecG) == kSpecBytes, "spec layout");
-
-__device__ __forceinline__ SeqState* seq_state(const StatsParams& G, int b) {
-  return reinterpret_cast<SeqState*>(G.state) + b;
-}
-
-template <typename T>
-__device__ __forceinline__ PassSpec<T> make_spec(const T* P, float mP, float sP, const T* Q, float mQ, float sQ,
-                                                 float cq, float c) {
-  PassSpec<T> S;
-  S.P = P;
-  S.MP = scaled_max(mP, c);
-  S.invSP = __fdiv_rn(1.f, sP);
-  S.Q = Q;
-  S.MQ = Q ? scaled_max(mQ, c) : 0.f;
-  S.invSQ = Q ? __fdiv_rn(1.f, sQ) : 0.f;
-  S.cq = Q ? cq : 0.f;
-  S.pad = 0;
-  return S;
-}
+constexpr int kStage = 4 * kThreads;  // chunk partials staged per round (8 KB)
+static_assert(kMaxTiles * kTileElems >= 2097152, "tile sums of the largest row fit in shared memory");
 
 template <typename T>
 __device__ __forceinline__ const T* stats_row(const StatsParams& G, int b, int r) {
@@ -95,72 +70,104 @@ __device__ __forceinline__ const T* stats_row(const StatsParams& G, int b, int r
   return static_cast<const T*>(base) + (static_cast<long long>(b) * rows + i) * G.ld;
 }
 
-// Row statistics of sequence b into shared arrays; returns SPEC_ERR_NONFINITE
-// if a row is NaN / +inf / all -inf (or'ed into *err_s).
-template <bool kGreedy>
-__device__ int gather_stats(const StatsParams& G, int b, float* st_m, float* st_s, int* st_arg, int* err_s) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float2* part = G.partials + static_cast<long long>(b) * G.rows_per_seq * G.chunks;
-  for (int r = warp; r < G.rows_per_seq; r += kWarps) {
-    if constexpr (kGreedy) {
-      bool bad;
-      const ArgMax am = combine_row_argmax(part + static_cast<long long>(r) * G.chunks, G.chunks, bad);
-      if (lane == 0) {
-        st_arg[r] = am.i;
-        if (bad || am.i < 0) atomicOr(err_s, SPEC_ERR_NONFINITE);
-      }
-    } else {
-      const MaxSum ms = combine_row(part + static_cast<long long>(r) * G.chunks, G.chunks, G.c);
-      if (lane == 0) {
-        st_m[r] = ms.m;
-        st_s[r] = ms.s;
-        if (!row_stats_ok(ms)) atomicOr(err_s, SPEC_ERR_NONFINITE);
+// Row statistics of sequence b.  The chunk partials of a group of rows are
+// loaded at once (at most 4 per thread) into `stage`, then one thread merges
+// each row in chunk order and calls emit(row, stats, ok): stats is (max,
+// sum), or (unused, argmax bits) in greedy mode; ok is false for a row with a
+// NaN or +inf, or without a finite entry.
+template <bool kGreedy, typename Emit>
+__device__ void merge_stats(const StatsParams& G, int b, float2* stage, Emit emit) {
+  const int tid = threadIdx.x;
+  const int C = G.chunks, R = G.rows_per_seq;
+  const int rpg = max(1, kStage / C);
+  const float2* part = G.partials + static_cast<long long>(b) * R * C;
+  for (int r0 = 0; r0 < R; r0 += rpg) {
+    const int nr = min(rpg, R - r0);
+    const int n = nr * C;
+    const float2* src = part + static_cast<long long>(r0) * C;
+    float2 v[kStage / kThreads];
+#pragma unroll
+    for (int q = 0; q < kStage / kThreads; ++q) {
+      const int i = q * kThreads + tid;
+      if (i < n) v[q] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int q = 0; q < kStage / kThreads; ++q) {
+      const int i = q * kThreads + tid;
+      if (i < n) stage[i] = v[q];
+    }
+    __syncthreads();
+    for (int r = tid; r < nr; r += kThreads) {
+      if constexpr (kGreedy) {
+        bool bad;
+        const ArgMax am = combine_row_argmax(stage + r * C, C, bad);
+        emit(r0 + r, make_float2(0.f, __int_as_float(am.i)), !bad && am.i >= 0);
+      } else {
+        const MaxSum ms = combine_row(stage + r * C, C, G.c);
+        emit(r0 + r, make_float2(ms.m, ms.s), row_stats_ok(ms));
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
+}
+
+// Statistics into separate arrays; returns the error bits (or'ed into *err_s).
+template <bool kGreedy>
+__device__ int gather_stats(const StatsParams& G, int b, float* st_m, float* st_s, int* st_arg, int* err_s,
+                            float2* stage) {
+  merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
+    if (kGreedy) {
+      st_arg[r] = __float_as_int(v.y);
+    } else {
+      st_m[r] = v.x;
+      st_s[r] = v.y;
+    }
+    if (!ok) atomicOr(err_s, SPEC_ERR_NONFINITE);
+  });
   return *err_s;
 }
 
-// Last-arriver test on a counter (all threads get the answer).  Every thread
-// fences first, so whatever this CTA wrote is visible before it is counted;
-// the last arriver resets the counter for the next call.
-__device__ bool arrive(unsigned* ctr, unsigned expected, int* sh) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(ctr, 1u);
-    *sh = (old + 1u == expected);
-    if (*sh) {
-      *ctr = 0u;
-      __threadfence();
-    }
-  }
-  __syncthreads();
-  return *sh != 0;
+// Cluster entry and readiness: every CTA arrives when it starts (after
+// initialising its pass state) and waits before it first writes another
+// CTA's shared memory (or exits), so no CTA touches a peer that has not
+// started.
+__device__ __forceinline__ void cluster_enter() {
+  if (cluster_size() > 1) cluster_arrive();
+}
+__device__ __forceinline__ void cluster_ready() {
+  if (cluster_size() > 1) cluster_wait();
 }
 
-__device__ __forceinline__ float* pass_sums(const StatsParams& G, int b, int stage) {
-  return G.sums + (static_cast<long long>(b) * 2 + stage) * G.ntiles;
-}
-
-// Draw from a pass whose tile sums are all in `sums`; on a zero or
-// non-finite total, redo the pass on the target row alone (cq = 0) and set
-// *flag |= SPEC_ERR_ZERO_MASS.  Returns the token; *Z gets the mass drawn from.
 template <typename T>
-__device__ int finish_draw(const StatsParams& G, PassSpec<T> S, float* sums, float v, PassSmem& ps, int* flag,
-                           double* Z) {
-  double z = tile_prefix(sums, G.ntiles, ps);
-  if (!(z > 0.0) || !(z < INFINITY)) {
+__device__ __forceinline__ PassSpec<T> make_spec(const T* P, float mP, float sP, const T* Q, float mQ, float sQ,
+                                                 float cq, float c) {
+  PassSpec<T> S;
+  S.P = P;
+  S.MP = scaled_max(mP, c);
+  S.invSP = __fdiv_rn(1.f, sP);
+  S.Q = Q;
+  S.MQ = Q ? scaled_max(mQ, c) : 0.f;
+  S.invSQ = Q ? __fdiv_rn(1.f, sQ) : 0.f;
+  S.cq = Q ? cq : 0.f;
+  S.pad = 0;
+  return S;
+}
+
+// A pass over the cluster with the zero-mass fallback: if the residual has
+// no (finite) mass, the pass is redone on the target row alone (cq = 0) and
+// *flag gets SPEC_ERR_ZERO_MASS.  *buf is the buffer of the first pass on
+// entry and of the pass to draw from on return.
+template <typename T>
+__device__ DF pass_or_fallback(PassSpec<T>& S, int V, float c, int ntiles, int* buf, int* flag, PassSmem& ps) {
+  DF z = cluster_pass(S, V, c, ntiles, *buf, ps);
+  if (!pass_ok(z)) {
     *flag |= SPEC_ERR_ZERO_MASS;
     S.cq = 0.f;
     S.Q = nullptr;
-    tile_sums(S, G.V, G.c, 0, G.ntiles, sums, ps);
-    __threadfence_block();
-    z = tile_prefix(sums, G.ntiles, ps);
+    *buf ^= 1;
+    z = cluster_pass(S, V, c, ntiles, *buf, ps);
   }
-  *Z = z;
-  return draw(S, G.V, G.c, sums, G.ntiles, static_cast<double>(v) * z, ps);
+  return z;
 }
 
 // ===========================================================================
@@ -183,7 +190,7 @@ struct ChainSmem {
   int st_arg[kMaxGamma + 1];
   int tok[kMaxGamma];
   float gp[kMaxGamma], gq[kMaxGamma];
-  int err, a, last;
+  int err, a;
 };
 
 // Tokens and the logits at the drafted tokens (inputs only: safe before the
@@ -226,11 +233,12 @@ __device__ void chain_error_out(const ChainParams& P, int b, int err) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParams G, const ChainParams P) {
   __shared__ ChainSmem cs;
+  __shared__ float2 stage[kStage];
   const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = P.gamma;
   chain_inputs<T>(P, b, cs, false);
   pdl_wait();
-  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
   if (err) {
     chain_error_out(P, b, err);
     return;
@@ -252,24 +260,30 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParam
   }
 }
 
+// Sampling chain: one cluster per sequence (grid (S, B), cluster (S, 1, 1)).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) chain_walk_kernel(const StatsParams G, const ChainParams P) {
+__global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsParams G, const ChainParams P) {
   __shared__ ChainSmem cs;
   __shared__ PassSmem ps;
-  const int j = blockIdx.x, b = blockIdx.y;
+  __shared__ float2 stage[kStage];
+  const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = P.gamma;
   const float c = G.c;
+  const bool lead = cluster_rank() == 0;
   const T* target = static_cast<const T*>(P.target);
   const T* draft = static_cast<const T*>(P.draft);
   const long long trow0 = static_cast<long long>(b) * (g + 1);
   const long long drow0 = static_cast<long long>(b) * g;
 
+  pass_begin(ps);
+  cluster_enter();
   chain_inputs<T>(P, b, cs, true);
   pdl_wait();  // the statistics are complete and visible from here on
-  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
-  if (err) {  // every slice sees the same error; slice 0 reports it
-    if (j == 0) chain_error_out(P, b, err);
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  cluster_ready();
+  if (err) {  // every CTA of the cluster sees the same error; the lead reports it
+    if (lead) chain_error_out(P, b, err);
     return;
   }
   if (warp == 0) {
@@ -277,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) chain_walk_kernel(const StatsParams 
     if (lane < g) {
       const float mq = cs.st_m[g + 1 + lane], sq = cs.st_s[g + 1 + lane];
       keep = keeps(P.u[drow0 + lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
-      if (j == 0) {
+      if (lead) {
         if (P.p_at) P.p_at[drow0 + lane] = prob(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], c);
         if (P.q_at) P.q_at[drow0 + lane] = prob(cs.gq[lane], mq, sq, c);
       }
@@ -288,22 +302,19 @@ __global__ void __launch_bounds__(kThreads) chain_walk_kernel(const StatsParams 
   __syncthreads();
   const int a = cs.a;
   // residual max(0, p_a - q_a) after a rejection, the bonus row p_gamma otherwise
-  const PassSpec<T> S = make_spec(target + (trow0 + a) * P.ld, cs.st_m[a], cs.st_s[a],
-                                  a < g ? draft + (drow0 + a) * P.ld : nullptr, a < g ? cs.st_m[g + 1 + a] : 0.f,
-                                  a < g ? cs.st_s[g + 1 + a] : 1.f, 1.f, c);
-  float* sums = pass_sums(G, b, 0);
-  const int t0 = j * G.tps, t1 = min(G.ntiles, t0 + G.tps);
-  if (t0 < t1) tile_sums(S, G.V, c, t0, t1, sums, ps);
-  if (!arrive(&seq_state(G, b)->done1, gridDim.x, &cs.last)) return;
-
-  int flag = 0;
-  double Z;
-  const int y = finish_draw(G, S, sums, P.v[b], ps, &flag, &Z);
+  PassSpec<T> S = make_spec(target + (trow0 + a) * P.ld, cs.st_m[a], cs.st_s[a],
+                            a < g ? draft + (drow0 + a) * P.ld : nullptr, a < g ? cs.st_m[g + 1 + a] : 0.f,
+                            a < g ? cs.st_s[g + 1 + a] : 1.f, 1.f, c);
+  int buf = 0, flag = 0;
+  const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
+  const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, P.v[b]), false, ps);
+  if (y < 0) return;  // another CTA of the cluster holds the drawn tile
+  if (ps.fault) flag |= SPEC_ERR_INTERNAL;
   if (tid == 0) {
     P.accept_len[b] = a;
     P.out_token[b] = y;
     if (P.rollback) P.rollback[b] = (P.prefix ? P.prefix[b] : 0) + a;
-    if (P.resid) P.resid[b] = static_cast<float>(Z);
+    if (P.resid) P.resid[b] = df_float(Z);
     if (P.seq_error) P.seq_error[b] = flag;
     if (flag && P.error_word) atomicOr(P.error_word, flag);
   }
@@ -319,7 +330,7 @@ struct CascadeSmem {
   int st_arg[3 * kMaxGamma + 1];
   int tok[kMaxGamma];
   float g1p[kMaxGamma], g1q[kMaxGamma];
-  int err, a1, a2, last;
+  int err, a1, a2;
 };
 
 struct CascadeOut {
@@ -364,11 +375,12 @@ __device__ void cascade_inputs(const CascadeParams& P, int b, CascadeSmem& cs, b
 template <typename T>
 __global__ void __launch_bounds__(kThreads) cascade_greedy_kernel(const StatsParams G, const CascadeParams P) {
   __shared__ CascadeSmem cs;
+  __shared__ float2 stage[kStage];
   const int b = blockIdx.x;
   const int g1 = P.g1, g2 = P.g2;
   cascade_inputs<T>(P, b, cs, false);
   pdl_wait();
-  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
   if (threadIdx.x != 0) return;
   const CascadeOut out{P, b};
   if (err) {
@@ -395,34 +407,35 @@ __global__ void __launch_bounds__(kThreads) cascade_greedy_kernel(const StatsPar
   out.write(a1, t1, a2, w2, a2 < w2 ? cs.st_arg[r2 + a2] : -1, a2 < w2 ? 1 : 0, 0);
 }
 
-// Stage 1, and the stage-2 decision by the slice that draws t1.
+// Sampling cascade, both stages in one cluster per sequence.  Every CTA
+// draws t1 (the stage-2 tests need it); the CTA holding t2's tile writes.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) cascade_walk1_kernel(const StatsParams G, const CascadeParams P) {
-  pdl_launch_dependents();
+__global__ void __launch_bounds__(kThreads, 4) cascade_walk_kernel(const StatsParams G, const CascadeParams P) {
   __shared__ CascadeSmem cs;
   __shared__ PassSmem ps;
-  const int j = blockIdx.x, b = blockIdx.y;
+  __shared__ float2 stage[kStage];
+  const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g1 = P.g1, g2 = P.g2;
   const float c = G.c;
   const int r1 = g1, r2 = 2 * g1 + 1;
+  const bool lead = cluster_rank() == 0;
   const T* L0 = static_cast<const T*>(P.l0);
   const T* L1 = static_cast<const T*>(P.l1);
   const T* L2 = static_cast<const T*>(P.l2);
   const long long b0 = static_cast<long long>(b) * g1;
   const long long b1 = static_cast<long long>(b) * (g1 + 1);
   const long long b2 = static_cast<long long>(b) * g2;
-  SpecG* spec2 = reinterpret_cast<SpecG*>(G.specs) + b;
   const CascadeOut out{P, b};
 
+  pass_begin(ps);
+  cluster_enter();
   cascade_inputs<T>(P, b, cs, true);
   pdl_wait();
-  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err);
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  cluster_ready();
   if (err) {
-    if (j == 0 && tid == 0) {
-      out.write(0, -1, 0, 0, -1, 0, err);
-      spec2->a = -1;
-    }
+    if (lead && tid == 0) out.write(0, -1, 0, 0, -1, 0, err);
     return;
   }
   // stage 1: M_1 verifies O_0 against M_0
@@ -436,17 +449,13 @@ __global__ void __launch_bounds__(kThreads) cascade_walk1_kernel(const StatsPara
   }
   __syncthreads();
   const int a1 = cs.a1;
-  const PassSpec<T> S = make_spec(L1 + (b1 + a1) * P.ld, cs.st_m[r1 + a1], cs.st_s[r1 + a1],
-                                  a1 < g1 ? L0 + (b0 + a1) * P.ld : nullptr, a1 < g1 ? cs.st_m[a1] : 0.f,
-                                  a1 < g1 ? cs.st_s[a1] : 1.f, 1.f, c);
-  float* sums = pass_sums(G, b, 0);
-  const int t0 = j * G.tps, t1e = min(G.ntiles, t0 + G.tps);
-  if (t0 < t1e) tile_sums(S, G.V, c, t0, t1e, sums, ps);
-  if (!arrive(&seq_state(G, b)->done1, gridDim.x, &cs.last)) return;
+  PassSpec<T> S1 = make_spec(L1 + (b1 + a1) * P.ld, cs.st_m[r1 + a1], cs.st_s[r1 + a1],
+                             a1 < g1 ? L0 + (b0 + a1) * P.ld : nullptr, a1 < g1 ? cs.st_m[a1] : 0.f,
+                             a1 < g1 ? cs.st_s[a1] : 1.f, 1.f, c);
+  int buf = 0, flag = 0;
+  const DF Z1 = pass_or_fallback(S1, G.V, c, G.ntiles, &buf, &flag, ps);
+  const int t1 = cluster_draw(S1, G.V, c, G.ntiles, buf, df_mul_f(Z1, P.v1[b]), true, ps);
 
-  int flag = 0;
-  double Z;
-  const int t1 = finish_draw(G, S, sums, P.v1[b], ps, &flag, &Z);
   // stage 2: M_2 verifies the first w2 tokens of O_1 = d[0, a1) ++ t1 against M_1
   const int w2 = min(g2, a1 + 1);
   if (warp == 0) {
@@ -463,62 +472,22 @@ __global__ void __launch_bounds__(kThreads) cascade_walk1_kernel(const StatsPara
   }
   __syncthreads();
   const int a2 = cs.a2;
-  if (tid == 0) {
-    if (a2 < w2) {  // hand the residual max(0, p2 - p1) at position a2 to the stage-2 kernel
-      const PassSpec<T> S2 = make_spec(L2 + (b2 + a2) * P.ld, cs.st_m[r2 + a2], cs.st_s[r2 + a2],
-                                       L1 + (b1 + a2) * P.ld, cs.st_m[r1 + a2], cs.st_s[r1 + a2], 1.f, c);
-      SpecG sg;
-      sg.P = S2.P;
-      sg.Q = S2.Q;
-      sg.MP = S2.MP;
-      sg.invSP = S2.invSP;
-      sg.MQ = S2.MQ;
-      sg.invSQ = S2.invSQ;
-      sg.cq = S2.cq;
-      sg.a = a2;
-      sg.a1 = a1;
-      sg.t1 = t1;
-      *spec2 = sg;
-      reinterpret_cast<int*>(G.mid)[4 * b] = flag;  // stage-1 flags for the final outputs
-    } else {
-      out.write(a1, t1, a2, w2, -1, 0, flag);
-      spec2->a = -1;
-    }
+  if (a2 == w2) {  // all w2 kept: no stage-2 draw
+    if (lead && tid == 0) out.write(a1, t1, a2, w2, -1, 0, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0));
+    return;
   }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads) cascade_walk2_kernel(const StatsParams G, const CascadeParams P) {
-  __shared__ PassSmem ps;
-  __shared__ int last_s;
-  const int j = blockIdx.x, b = blockIdx.y;
-  pdl_wait();  // the stage-1 kernel is complete
-  const SpecG sg = reinterpret_cast<const SpecG*>(G.specs)[b];
-  if (sg.a < 0) return;  // no stage-2 pass for this sequence
-  PassSpec<T> S;
-  S.P = static_cast<const T*>(sg.P);
-  S.Q = static_cast<const T*>(sg.Q);
-  S.MP = sg.MP;
-  S.invSP = sg.invSP;
-  S.MQ = sg.MQ;
-  S.invSQ = sg.invSQ;
-  S.cq = sg.cq;
-  S.pad = 0;
-  float* sums = pass_sums(G, b, 1);
-  const int t0 = j * G.tps, t1 = min(G.ntiles, t0 + G.tps);
-  if (t0 < t1) tile_sums(S, G.V, G.c, t0, t1, sums, ps);
-  if (!arrive(&seq_state(G, b)->done2, gridDim.x, &last_s)) return;
-  int flag = reinterpret_cast<const int*>(G.mid)[4 * b];
-  double Z;
-  const int t2 = finish_draw(G, S, sums, P.v2[b], ps, &flag, &Z);
-  if (threadIdx.x == 0) {
-    const CascadeOut out{P, b};
-    out.write(sg.a1, sg.t1, sg.a, min(P.g2, sg.a1 + 1), t2, 1, flag);
-  }
+  // the residual max(0, p2 - p1) at position a2
+  PassSpec<T> S2 = make_spec(L2 + (b2 + a2) * P.ld, cs.st_m[r2 + a2], cs.st_s[r2 + a2], L1 + (b1 + a2) * P.ld,
+                             cs.st_m[r1 + a2], cs.st_s[r1 + a2], 1.f, c);
+  buf ^= 1;
+  const DF Z2 = pass_or_fallback(S2, G.V, c, G.ntiles, &buf, &flag, ps);
+  const int t2 = cluster_draw(S2, G.V, c, G.ntiles, buf, df_mul_f(Z2, P.v2[b]), false, ps);
+  if (t2 < 0) return;
+  if (tid == 0) out.write(a1, t1, a2, w2, t2, 1, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0));
 }
 
 // ===========================================================================
-// 2c. tree (one CTA per tree)
+// 2c. tree (one cluster per tree in sampling mode, one CTA in greedy mode)
 //
 // After k rejected siblings at one node the current distribution is
 //     p_k = max(0, p - c_k q) / W_k,   c_0 = 0, W_0 = 1,
@@ -538,6 +507,8 @@ struct TreeSmem {
   int* scr_a;  // [N] depth pointer jumping, then the children of the current node
   int* scr_b;  // [N] depth pointer jumping, then the kept path
 };
+constexpr int kTreeSmemPerNode = 40;
+constexpr int kMaxNodes = 1024;
 
 __device__ __forceinline__ TreeSmem tree_smem(char* base, int N) {
   TreeSmem t;
@@ -571,16 +542,19 @@ __device__ int list_children(const int* par, int N, int node, int* kids, int* co
 
 template <typename T, bool kGreedy>
 __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, const TreeParams P) {
-  extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ PassSmem ps;
+  __shared__ float2 stage[kStage];
   __shared__ int err_s, nk_s, keep_s;
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x;
   const int N = P.N;
   const float c = G.c;
-  TreeSmem ts = tree_smem(reinterpret_cast<char*>(dyn), N);
+  const bool lead = cluster_rank() == 0;
+  TreeSmem ts = tree_smem(reinterpret_cast<char*>(dyn_smem + (kGreedy ? 0 : kStageBytes)), N);
   const long long row0 = static_cast<long long>(b) * N;
 
+  pass_begin(ps);
+  cluster_enter();
   // tree shape and tokens (inputs: read while the statistics finish)
   if (tid == 0) err_s = 0;
   for (int i = tid; i < N; i += kThreads) {
@@ -595,9 +569,8 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   }
   __syncthreads();
   if (!(err_s & SPEC_ERR_PARENT)) {
-    // depth by pointer jumping (N <= 1024, two nodes per thread):
-    // D[i] += D[A[i]], A[i] = A[A[i]]
-    constexpr int kPer = 1024 / kThreads;
+    // depth by pointer jumping (N <= kMaxNodes): D[i] += D[A[i]], A[i] = A[A[i]]
+    constexpr int kPer = kMaxNodes / kThreads;
     for (int i = tid; i < N; i += kThreads) {
       ts.scr_a[i] = i == 0 ? 0 : ts.par[i];
       ts.scr_b[i] = i == 0 ? 0 : 1;
@@ -637,40 +610,27 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
     }
   }
   pdl_wait();
-  {
-    const float2* part = G.partials + static_cast<long long>(b) * G.rows_per_seq * G.chunks;
-    for (int rr = warp; rr < G.rows_per_seq; rr += kWarps) {
-      if constexpr (kGreedy) {
-        bool bad;
-        const ArgMax am = combine_row_argmax(part + static_cast<long long>(rr) * G.chunks, G.chunks, bad);
-        if (lane == 0) {
-          ts.st[rr] = make_float2(0.f, __int_as_float(am.i));
-          if (bad || am.i < 0) atomicOr(&err_s, SPEC_ERR_NONFINITE);
-        }
-      } else {
-        const MaxSum ms = combine_row(part + static_cast<long long>(rr) * G.chunks, G.chunks, c);
-        if (lane == 0) {
-          ts.st[rr] = make_float2(ms.m, ms.s);
-          if (!row_stats_ok(ms)) atomicOr(&err_s, SPEC_ERR_NONFINITE);
-        }
-      }
-    }
-  }
-  __syncthreads();
+  merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
+    ts.st[r] = v;
+    if (!ok) atomicOr(&err_s, SPEC_ERR_NONFINITE);
+  });
+  cluster_ready();
 
   const int err = err_s;
   const int prefix = P.prefix ? P.prefix[b] : 0;
   const int pn = P.max_depth + 1;
   int* pnodes = P.path_nodes + static_cast<long long>(b) * pn;
   if (err) {
-    if (tid == 0) {
-      P.path_len[b] = 0;
-      P.out_token[b] = -1;
-      if (P.rollback) P.rollback[b] = prefix;
-      if (P.seq_error) P.seq_error[b] = err;
-      if (P.error_word) atomicOr(P.error_word, err);
+    if (lead) {
+      if (tid == 0) {
+        P.path_len[b] = 0;
+        P.out_token[b] = -1;
+        if (P.rollback) P.rollback[b] = prefix;
+        if (P.seq_error) P.seq_error[b] = err;
+        if (P.error_word) atomicOr(P.error_word, err);
+      }
+      for (int q = tid; q < pn; q += kThreads) pnodes[q] = -1;
     }
-    for (int q = tid; q < pn; q += kThreads) pnodes[q] = -1;
     return;
   }
 
@@ -678,8 +638,8 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   const T* draft = static_cast<const T*>(P.draft);
   int* kids = ts.scr_a;
   int* path = ts.scr_b;
-  float* sums = pass_sums(G, b, 0);
-  int node = 0, plen = 0, flag = 0, token = -1;
+  int node = 0, plen = 0, flag = 0, token = -1, buf = 0;
+  bool writer = lead;
   while (true) {
     const int nk = list_children(ts.par, N, node, kids, &nk_s);
     if constexpr (kGreedy) {
@@ -705,6 +665,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
                                 sq.y, 1.f, c);
       S.cq = 0.f;
       double cc = 0.0, W = 1.0;
+      DF Wdf{1.f, 0.f};
       int kept = -1;
       bool zero_mass = false;
       for (int q = 0; q < nk; ++q) {
@@ -723,15 +684,15 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         }
         const double cn = cc + W;
         S.cq = static_cast<float>(cn);
-        tile_sums(S, P.V, c, 0, G.ntiles, sums, ps);
-        __threadfence_block();
-        const double Wn = tile_prefix(sums, G.ntiles, ps);
-        if (!(Wn > 0.0) || !(Wn < INFINITY)) {
+        buf ^= 1;
+        const DF Wn = cluster_pass(S, P.V, c, G.ntiles, buf, ps);
+        if (!pass_ok(Wn)) {
           zero_mass = true;
           break;
         }
         cc = cn;
-        W = Wn;
+        W = df_double(Wn);
+        Wdf = Wn;
       }
       __syncthreads();  // kids[] is rewritten by the next list_children
       if (kept >= 0) {
@@ -740,19 +701,21 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         node = kept;
         continue;
       }
-      double Z = W;
+      DF Z = Wdf;
       if (zero_mass || nk == 0) {
         if (zero_mass) flag = SPEC_ERR_ZERO_MASS;
         S.cq = 0.f;  // draw from the node's own target distribution
-        tile_sums(S, P.V, c, 0, G.ntiles, sums, ps);
-        __threadfence_block();
-        Z = tile_prefix(sums, G.ntiles, ps);
+        buf ^= 1;
+        Z = cluster_pass(S, P.V, c, G.ntiles, buf, ps);
       }
-      token = draw(S, P.V, c, sums, G.ntiles, static_cast<double>(P.v[b]) * Z, ps);
+      token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, P.v[b]), false, ps);
+      writer = token >= 0;
       break;
     }
   }
   __syncthreads();
+  if (!writer) return;
+  if (ps.fault) flag |= SPEC_ERR_INTERNAL;
   if (tid == 0) {
     P.out_token[b] = token;
     P.path_len[b] = plen;
@@ -768,62 +731,155 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
 // ---------------------------------------------------------------------------
 template <typename K>
 cudaError_t launch_stats(K kernel, const StatsParams& G, cudaStream_t s) {
-  dim3 grid(G.chunks, G.rows_per_seq, G.B);
-  kernel<<<grid, kStatsThreads, 0, s>>>(G);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G.chunks, G.rows_per_seq, G.B);
+  cfg.blockDim = dim3(kStatsThreads);
+  cfg.stream = s;
+  void* argv[] = {const_cast<StatsParams*>(&G)};
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), argv);
+}
+
+// Clusters of 1, 2, 4 and 8 CTAs of `fn` that can be resident at once on the
+// current device, cached per (kernel, device).
+cudaError_t resident_clusters(const void* fn, size_t dyn, std::array<int, 4>* out) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, std::array<int, 4>> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({fn, dev});
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  std::array<int, 4> n{};
+  for (int i = 0; i < 4; ++i) {
+    const int S = 1 << i;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int count = 0;
+    if (cudaOccupancyMaxActiveClusters(&count, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // a size the device cannot co-schedule: not used
+      count = 0;
+    }
+    n[i] = count;
+  }
+  cache[{fn, dev}] = n;
+  *out = n;
+  return cudaSuccess;
+}
+
+// Largest cluster (at most 8 CTAs, at most one per tile) for which all B
+// sequences' clusters are resident at once; 1 when even single CTAs need
+// more than one wave.
+int cluster_for(const std::array<int, 4>& resident, int B, int ntiles) {
+  for (int i = 3; i >= 1; --i) {
+    const int S = 1 << i;
+    if (S <= ntiles && B <= resident[i]) return S;
+  }
+  return 1;
 }
 
 // A dependent kernel: programmatic stream serialisation lets it start while
 // its predecessor drains; it reads the predecessor's results only after
-// griddepcontrol.wait.
+// griddepcontrol.wait.  cluster > 0 launches clusters of that many CTAs
+// along x.
 template <typename K, typename A>
-cudaError_t launch_dependent(K kernel, dim3 grid, size_t dyn, const StatsParams& G, const A& args, cudaStream_t s) {
+cudaError_t launch_dependent(K kernel, dim3 grid, int cluster, size_t dyn, const StatsParams& G, const A& args,
+                             cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(kernel);
-  if (dyn > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (cluster > 0) {
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = cluster;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    na = 2;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   void* argv[] = {const_cast<StatsParams*>(&G), const_cast<A*>(&args)};
   return cudaLaunchKernelExC(&cfg, fn, argv);
 }
 
-int slices(const StatsParams& G) { return (G.ntiles + G.tps - 1) / G.tps; }
+// Raise a kernel's dynamic shared memory limit to `bytes`, once per
+// (kernel, device).
+cudaError_t smem_limit(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({fn, dev});
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[{fn, dev}] = bytes;
+  return e;
+}
+
+// A sampling walk kernel with one cluster per sequence; `occupancy_dyn` is
+// the dynamic shared memory the cluster size is chosen for (at least dyn).
+template <typename K, typename A>
+cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsParams& G, const A& args,
+                        cudaStream_t s) {
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  cudaError_t e = smem_limit(fn, static_cast<int>(occupancy_dyn));
+  if (e != cudaSuccess) return e;
+  std::array<int, 4> resident;
+  e = resident_clusters(fn, occupancy_dyn, &resident);
+  if (e != cudaSuccess) return e;
+  const int S = cluster_for(resident, G.B, G.ntiles);
+  return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s);
+}
 
 template <typename T>
 cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s) {
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
   if (e != cudaSuccess) return e;
-  if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, G, p, s);
-  return launch_dependent(chain_walk_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
+  if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s);
+  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
 }
 
 template <typename T>
 cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, cudaStream_t s) {
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
   if (e != cudaSuccess) return e;
-  const size_t dyn = static_cast<size_t>(40) * p.N;  // TreeSmem arrays
-  if (greedy) return launch_dependent(tree_kernel<T, true>, dim3(G.B), dyn, G, p, s);
-  return launch_dependent(tree_kernel<T, false>, dim3(G.B), dyn, G, p, s);
+  const size_t nodes = static_cast<size_t>(kTreeSmemPerNode) * p.N;
+  if (greedy) {
+    e = smem_limit(reinterpret_cast<const void*>(tree_kernel<T, true>), kTreeSmemPerNode * kMaxNodes);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(tree_kernel<T, true>, dim3(1, G.B), 0, nodes, G, p, s);
+  }
+  // occupancy is evaluated once, at the largest tree's shared memory
+  return launch_walk(tree_kernel<T, false>, kStageBytes + nodes,
+                     static_cast<size_t>(kStageBytes) + static_cast<size_t>(kTreeSmemPerNode) * kMaxNodes, G, p, s);
 }
 
 template <typename T>
 cudaError_t cascade_impl(const StatsParams& G, const CascadeParams& p, bool greedy, cudaStream_t s) {
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
   if (e != cudaSuccess) return e;
-  if (greedy) return launch_dependent(cascade_greedy_kernel<T>, dim3(G.B), 0, G, p, s);
-  e = launch_dependent(cascade_walk1_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
-  if (e != cudaSuccess) return e;
-  return launch_dependent(cascade_walk2_kernel<T>, dim3(slices(G), G.B), 0, G, p, s);
+  if (greedy) return launch_dependent(cascade_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s);
+  return launch_walk(cascade_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
 }
 
 }  // namespace

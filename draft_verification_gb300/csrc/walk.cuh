@@ -10,21 +10,24 @@
 // ascending index order, exceeds v * sum(w).
 //
 // A pass is split into tiles of kTileElems = 8 * kThreads contiguous elements
-// (8 per thread).  Any CTA can compute the sums of any range of tiles, so a
-// pass is spread over many CTAs (slices), each writing its tiles' sums to
-// global memory; the CTA that finishes the last slice draws the token.
+// (8 per thread).  The CTAs of one thread-block cluster (one cluster per
+// sequence) each sum a slice of the tiles and store the sums into the shared
+// memory of every CTA of the cluster; after one cluster barrier every CTA
+// holds the whole row's tile sums, so the total and the tile of the draw are
+// found without another trip through global memory.
 //
 // Running sums: fp32 within a thread's 8 elements and within a warp (a fixed
 // shuffle scan), a fixed sequential fp32 combination of the per-warp totals
-// per tile, and fp64 across tiles.  The pass and the draw recompute a tile
-// with the same code, so a tile's total is bit-identical in both.
+// per tile, and double-float (two fp32 numbers) across tiles.  The pass and
+// the draw recompute a tile with the same code, so a tile's total is
+// bit-identical in both.
 #pragma once
 
 #include "common.cuh"
 
 namespace sv {
 
-constexpr int kMaxTiles = 512;  // V <= 512 * kTileElems
+constexpr int kMaxTiles = 1024;  // V <= kMaxTiles * kTileElems = 2,097,152
 
 // ---------------------------------------------------------------------------
 // the rows and scalars of one pass
@@ -146,18 +149,28 @@ __device__ __forceinline__ bool row_is_aligned(const T* row) {
   return (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
 }
 
-// Weights of 8 elements.
+// Weights of 8 elements, two at a time in packed f32x2 arithmetic (each lane
+// rounds exactly like the scalar intrinsics: fma, ex2, mul, fma, max).
 template <typename T>
 __device__ __forceinline__ void pass_weights(const PassSpec<T>& S, float c, const float* xp,
                                              const float* xq, float* w) {
+  const float2 cc = make_float2(c, c);
+  const float2 mp = make_float2(-S.MP, -S.MP), ip = make_float2(S.invSP, S.invSP);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float p = __fmul_rn(weight(xp[e], c, S.MP), S.invSP);
+  for (int e = 0; e < 8; e += 2) {
+    const float2 ap = ffma2(make_float2(xp[e], xp[e + 1]), cc, mp);
+    const float2 p = fmul2(make_float2(ex2(ap.x), ex2(ap.y)), ip);
     if (S.cq != 0.f) {
-      const float q = __fmul_rn(weight(xq[e], c, S.MQ), S.invSQ);
-      w[e] = fmaxf(__fmaf_rn(-S.cq, q, p), 0.f);
+      const float2 mq = make_float2(-S.MQ, -S.MQ), iq = make_float2(S.invSQ, S.invSQ);
+      const float2 ncq = make_float2(-S.cq, -S.cq);
+      const float2 aq = ffma2(make_float2(xq[e], xq[e + 1]), cc, mq);
+      const float2 q = fmul2(make_float2(ex2(aq.x), ex2(aq.y)), iq);
+      const float2 d = ffma2(ncq, q, p);
+      w[e] = fmaxf(d.x, 0.f);
+      w[e + 1] = fmaxf(d.y, 0.f);
     } else {
-      w[e] = p;
+      w[e] = p.x;
+      w[e + 1] = p.y;
     }
   }
 }
@@ -205,18 +218,69 @@ __device__ __forceinline__ void tile_weights(const PassSpec<T>& S, int V, float 
   pass_weights(S, c, xp, xq, w);
 }
 
+// Tiles a thread keeps in flight on the register path of tile_sums (two
+// 16-byte loads, target and draft row, per bf16 tile; four per float32
+// tile), kept small: the register path only serves misaligned rows and a
+// row's last partial tile.
+template <typename T>
+struct PassBatch {
+  static constexpr int k = 2;
+};
+template <>
+struct PassBatch<float> {
+  static constexpr int k = 1;
+};
+constexpr int kMaxBatch = 2;
+
+// Bulk-copy pipeline of the staged path: kStages buffers, each holding
+// kStageRowBytes of the target row and as much of the draft row.  They are
+// the first kStageBytes of the walk kernels' dynamic shared memory.
+constexpr int kStageRowBytes = 8192;
+constexpr int kStages = 2;
+constexpr int kStageBytes = kStages * 2 * kStageRowBytes;
+constexpr int kMaxCluster = 8;
+extern __shared__ __align__(128) unsigned char dyn_smem[];
+
 struct PassSmem {
-  float warp_tot[4][kWarps];
+  float warp_tot[2][kMaxBatch][kWarps];  // ring of per-warp tile totals
   float warp_excl[kWarps];
   float thr_incl[kThreads];
-  double tile_excl[kMaxTiles];
-  double total;
-  double E;
+  float all[2][kMaxTiles];  // tile sums of a whole pass, double-buffered
+  DF slice[2][kMaxCluster]; // total of each CTA's slice of tiles, double-buffered
+  DF lane_blk[32];          // sum of each lane's block of tiles of one slice
+  uint64_t bar[kStages];    // one mbarrier per stage buffer
+  uint64_t xbar[2];         // tile-sum exchange between the CTAs of the cluster
+  int staged;               // stages issued by earlier passes of this kernel
+  int exchanges;            // exchanges completed by earlier passes
+  int flt[kMaxCluster];     // fault state of each CTA of the cluster
+  int fault;                // a bulk copy here or in a peer did not complete
+  float rf;                 // target minus the prefix before the drawn tile
+  int owner;                // CTA whose slice holds the drawn tile
   int tile;
   int thread;
   int last_mode;
   int result;
 };
+
+// Before the first pass (thread 0; the kernel synchronises before any pass,
+// and peers write flt[] only after the cluster entry barrier).  The stage
+// mbarriers are initialised once per kernel: every pass continues their
+// phases (stage number `staged + k` uses buffer (staged + k) % kStages in
+// its ((staged + k) / kStages)-th phase).
+// The exchange barriers count one arrival from every CTA of the cluster per
+// pass; pass number x uses xbar[x & 1] in its (x >> 1)-th phase.
+__device__ __forceinline__ void pass_begin(PassSmem& sh) {
+  if (threadIdx.x == 0) {
+    sh.fault = 0;
+    sh.staged = 0;
+    sh.exchanges = 0;
+    for (int r = 0; r < kMaxCluster; ++r) sh.flt[r] = 0;
+    for (int s = 0; s < kStages; ++s) mbar_init(&sh.bar[s], 1);
+    mbar_init(&sh.xbar[0], cluster_size());
+    mbar_init(&sh.xbar[1], cluster_size());
+    mbar_fence_init();
+  }
+}
 
 // Sum of a tile's weights from the per-warp totals (fixed sequential order).
 __device__ __forceinline__ float tile_total(const float* warp_tot) {
@@ -226,20 +290,105 @@ __device__ __forceinline__ float tile_total(const float* warp_tot) {
   return s;
 }
 
-// Sums of tiles [t0, t1) into out[t0 .. t1) (global or shared).  All threads
-// call it.  Aligned rows keep 2 tiles (4 rows' loads) in flight per thread.
+// This thread's 8 elements of tile j of a staged row.
 template <typename T>
-__device__ void tile_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, float* out,
-                          PassSmem& sh) {
+__device__ __forceinline__ void stage_load8(const unsigned char* row, int j, uint32_t* r) {
+  const unsigned char* p = row + static_cast<size_t>(j * kTileElems + 8 * threadIdx.x) * sizeof(T);
+  const uint4 a = lds16(p);
+  r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
+  if constexpr (sizeof(T) == 4) {
+    const uint4 b = lds16(p + 16);
+    r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
+  }
+}
+
+// Staged path: full tiles [t0, t1) of rows whose addresses are 16-byte
+// aligned.  Thread 0 streams the tiles through kStages shared-memory buffers
+// with bulk copies (one mbarrier per buffer, up to kStages in flight) while
+// all threads compute the tiles already landed.  A buffer is refilled only
+// after the barrier that ends the computation on it.
+template <typename T>
+__device__ void staged_sums(const PassSpec<T>& S, float c, int t0, int t1, float* out, PassSmem& sh) {
+  constexpr int TPS = kStageRowBytes / (kTileElems * static_cast<int>(sizeof(T)));  // tiles per stage
+  static_assert(TPS >= 1 && TPS <= kMaxBatch, "stage geometry");
+  constexpr int R = Load8<T>::kRegs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool useQ = S.cq != 0.f;
+  const int nst = (t1 - t0 + TPS - 1) / TPS;
+  const int g0 = sh.staged;  // global number of this pass's first stage
+  auto issue = [&](int k) {  // thread 0
+    const int ta = t0 + k * TPS, te = min(t1, ta + TPS);
+    const unsigned bytes = static_cast<unsigned>((te - ta) * kTileElems * sizeof(T));
+    const int b = (g0 + k) % kStages;
+    unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
+    mbar_expect_tx(&sh.bar[b], useQ ? 2 * bytes : bytes);
+    bulk_load(buf, S.P + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
+    if (useQ) bulk_load(buf + kStageRowBytes, S.Q + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
+  };
+  if (tid == 0) {
+    fence_proxy_async();  // the buffers were last read by ordinary loads
+    for (int k = 0; k < min(kStages, nst); ++k) issue(k);
+  }
+  // Nobody waits before the first stages are issued (thread 0 shares a warp
+  // with waiting threads); later stages are issued after the barrier that
+  // ends a stage, long before anyone waits on them.
+  __syncthreads();
+  bool fault = false;
+  int slot = 0;
+  for (int k = 0; k < nst; ++k, slot ^= 1) {
+    const int ta = t0 + k * TPS, nb = min(TPS, t1 - ta);
+    const int b = (g0 + k) % kStages;
+    const unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
+    if (!mbar_wait(&sh.bar[b], ((g0 + k) / kStages) & 1)) fault = true;
+#pragma unroll
+    for (int j = 0; j < TPS; ++j) {
+      if (j < nb) {
+        uint32_t rp[R], rq[R];
+        float xp[8], xq[8], w[8];
+        stage_load8<T>(buf, j, rp);
+        Load8<T>::get(rp, xp);
+        if (useQ) {
+          stage_load8<T>(buf + kStageRowBytes, j, rq);
+          Load8<T>::get(rq, xq);
+        }
+        pass_weights(S, c, xp, xq, w);
+        const float incl = warp_incl_scan(sum8(w));
+        if (lane == 31) sh.warp_tot[slot][j][warp] = incl;
+      }
+    }
+    __syncthreads();  // buffer b is free; the warp totals are complete
+    if (tid < nb) out[ta + tid] = tile_total(sh.warp_tot[slot][tid]);
+    if (tid == 0 && k + kStages < nst) {
+      fence_proxy_async();
+      issue(k + kStages);
+    }
+  }
+  if (fault) {
+    // a copy that did not land in time may still be in flight: wait for the
+    // last use of every buffer once more (bounded) before it is reused
+    for (int k = max(0, nst - kStages); k < nst; ++k)
+      mbar_wait(&sh.bar[(g0 + k) % kStages], ((g0 + k) / kStages) & 1);
+    sh.fault = 1;
+  }
+  if (tid == 0) sh.staged = g0 + nst;  // read by the next pass after tile_sums' barrier
+}
+
+// Register path: tiles [t0, t1) loaded straight from global memory, NB
+// tiles per thread in flight (misaligned rows, and a row's last partial tile).
+template <typename T>
+__device__ void direct_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, float* out, PassSmem& sh) {
+  constexpr int NB = PassBatch<T>::k;
+  constexpr int R = Load8<T>::kRegs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool useQ = S.cq != 0.f;
   const bool aligned = row_is_aligned(S.P) && (!useQ || row_is_aligned(S.Q));
-  for (int tb = t0; tb < t1; tb += 2) {
-    const int nb = min(2, t1 - tb);
+  int slot = 0;
+  for (int tb = t0; tb < t1; tb += NB, slot ^= 1) {
+    const int nb = min(NB, t1 - tb);
     if (aligned) {
-      uint32_t rp[2][Load8<T>::kRegs], rq[2][Load8<T>::kRegs];
+      uint32_t rp[NB][R], rq[NB][R];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < NB; ++j) {
         if (j < nb) {
           const int e0 = (tb + j) * kTileElems + 8 * tid;
           Load8<T>::issue(S.P, e0, V, rp[j]);
@@ -247,14 +396,14 @@ __device__ void tile_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, 
         }
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < NB; ++j) {
         if (j < nb) {
           float xp[8], xq[8], w[8];
           Load8<T>::get(rp[j], xp);
           if (useQ) Load8<T>::get(rq[j], xq);
           pass_weights(S, c, xp, xq, w);
           const float incl = warp_incl_scan(sum8(w));
-          if (lane == 31) sh.warp_tot[j][warp] = incl;
+          if (lane == 31) sh.warp_tot[slot][j][warp] = incl;
         }
       }
     } else {
@@ -263,92 +412,236 @@ __device__ void tile_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, 
         float w[8];
         tile_weights(S, V, c, tb + j, w);
         const float incl = warp_incl_scan(sum8(w));
-        if (lane == 31) sh.warp_tot[j][warp] = incl;
+        if (lane == 31) sh.warp_tot[slot][j][warp] = incl;
       }
     }
     __syncthreads();
-    if (tid < nb) out[tb + tid] = tile_total(sh.warp_tot[tid]);
-    __syncthreads();
+    // the ring slot written next is the other one, so no second barrier
+    if (tid < nb) out[tb + tid] = tile_total(sh.warp_tot[slot][tid]);
   }
 }
 
-// fp64 exclusive prefix of ntiles tile sums (one warp; the sums are read
-// through L2 since other CTAs may have written them).  Leaves the prefix in
-// sh.tile_excl and returns the total to every thread.
-__device__ double tile_prefix(const float* sums, int ntiles, PassSmem& sh) {
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int per = (ntiles + 31) / 32;
-    const int j0 = min(ntiles, tid * per), j1 = min(ntiles, j0 + per);
-    double run = 0.0;
-    for (int j = j0; j < j1; ++j) run += static_cast<double>(__ldcg(sums + j));
-    double incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += y;
-    }
-    double acc = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (tid == 0) acc = 0.0;
-    for (int j = j0; j < j1; ++j) {
-      sh.tile_excl[j] = acc;
-      acc += static_cast<double>(__ldcg(sums + j));
-    }
-    if (tid == 31) sh.total = incl;
+// Sums of tiles [t0, t1) into out[t0 .. t1) (shared memory).  All threads
+// call it; out[] is complete when it returns.  Full tiles of aligned rows go
+// through the staged path, the rest through the register path.
+template <typename T>
+__device__ void tile_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, float* out, PassSmem& sh) {
+  const bool useQ = S.cq != 0.f;
+  const bool aligned = row_is_aligned(S.P) && (!useQ || row_is_aligned(S.Q));
+  int tb = t0;
+  if (aligned) {
+    const int tf = max(t0, min(t1, V / kTileElems));  // tiles before tf are full
+    if (tf > t0) staged_sums(S, c, t0, tf, out, sh);
+    tb = tf;
+  }
+  if (tb < t1) {
+    __syncthreads();  // the warp-total ring restarts at slot 0
+    direct_sums(S, V, c, tb, t1, out, sh);
   }
   __syncthreads();
-  return sh.total;
 }
 
-// Inverse-CDF draw over tile sums `sums` (prefix from tile_prefix): the first
-// index whose running sum exceeds `target`.  Recomputes the chosen tile with
-// the same code as tile_sums.  All threads call it; all get the index.
+// Contiguous block of tiles handled by one lane of the prefix.
+__device__ __forceinline__ void lane_block(int ntiles, int lane, int& j0, int& j1) {
+  const int per = (ntiles + 31) / 32;
+  j0 = min(ntiles, lane * per);
+  j1 = min(ntiles, j0 + per);
+}
+
+// Tiles [j0, j1) of the slice [s0, s0 + m) handled by one lane: the slice is
+// cut into at most 32 contiguous blocks.
+__device__ __forceinline__ void lane_block(int s0, int m, int lane, int& j0, int& j1, int& nblocks) {
+  const int per = max(1, (m + 31) / 32);
+  j0 = s0 + min(m, lane * per);
+  j1 = s0 + min(m, (lane + 1) * per);
+  nblocks = (m + per - 1) / per;
+}
+
+// Double-float sum of the tile sums all[s0 .. s0 + m), one warp: each lane
+// adds its block in order and publishes it, then every lane adds the block
+// sums in order (broadcast reads).  Every lane returns the same value.
+__device__ DF slice_sum(const float* all, int s0, int m, PassSmem& sh) {
+  const int lane = threadIdx.x & 31;
+  int j0, j1, nb;
+  lane_block(s0, m, lane, j0, j1, nb);
+  DF run{0.f, 0.f};
+  for (int j = j0; j < j1; ++j) run = df_add_f(run, all[j]);
+  sh.lane_blk[lane] = run;
+  __syncwarp();
+  DF acc{0.f, 0.f};
+  for (int l = 0; l < nb; ++l) acc = df_add(acc, sh.lane_blk[l]);
+  __syncwarp();  // lane_blk is reused by the next call
+  return acc;
+}
+
+__device__ __forceinline__ bool df_gt(DF a, DF b) { return df_add(a, df_neg(b)).hi > 0.f; }
+
+// One pass split over the CTAs of the cluster.  CTA `rank` sums its slice of
+// the tiles (tile sums into sh.all[buf], their total into
+// sh.slice[buf][rank]) and stores both into every CTA of the cluster, then
+// arrives on every CTA's exchange barrier (warp 0 does both); once its own
+// barrier has all arrivals, each CTA holds every tile sum and slice total.
+// Returns the pass total, the slice totals added in slice order (bit-
+// identical in every CTA).  Every CTA of the cluster calls it with the same
+// pass.  Consecutive passes alternate `buf`: a CTA can store into a peer's
+// buffer again only after that peer has arrived for the next pass, which it
+// does after it has finished reading this one.  A wait that gives up sets
+// the fault state instead of hanging.
 template <typename T>
-__device__ int draw(const PassSpec<T>& S, int V, float c, const float* sums, int ntiles, double target,
-                    PassSmem& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int buf, PassSmem& sh) {
+  const int tid = threadIdx.x;
+  const int rank = static_cast<int>(cluster_rank()), n = static_cast<int>(cluster_size());
+  const int tpc = (ntiles + n - 1) / n;
+  const int t0 = min(ntiles, rank * tpc), t1 = min(ntiles, t0 + tpc);
+  const int x = sh.exchanges;  // stable: updated only after the barriers below
+  float* all = sh.all[buf];
+  tile_sums(S, V, c, t0, t1, all, sh);
   if (tid < 32) {
-    // first tile with mass whose end passes the target, else the last with mass
-    int first = ntiles, last = -1;
-    for (int j = lane; j < ntiles; j += 32) {
-      const float s = __ldcg(sums + j);
-      if (s > 0.f) {
-        if (first == ntiles && sh.tile_excl[j] + static_cast<double>(s) > target) first = j;
-        last = j;
+    const DF mine = slice_sum(all, t0, t1 - t0, sh);
+    if (n > 1) {
+      const int nt = t1 - t0;
+      for (int i = tid; i < nt * (n - 1); i += 32) {
+        int d = i / nt;
+        const int k = i - d * nt;
+        if (d >= rank) ++d;
+        st_cluster(all + t0 + k, static_cast<unsigned>(d), all[t0 + k]);
       }
+      if (tid < n) {
+        st_cluster(&sh.slice[buf][rank].hi, static_cast<unsigned>(tid), mine.hi);
+        st_cluster(&sh.slice[buf][rank].lo, static_cast<unsigned>(tid), mine.lo);
+        st_cluster_u32(&sh.flt[rank], static_cast<unsigned>(tid), sh.fault);
+      }
+      fence_cluster();
+      __syncwarp();  // every store of this CTA precedes its arrivals
+      if (tid < n) mbar_arrive_cluster(&sh.xbar[x & 1], static_cast<unsigned>(tid));
+      if (!mbar_wait_cluster(&sh.xbar[x & 1], (x >> 1) & 1)) sh.fault = 1;
+    } else if (tid == 0) {
+      sh.slice[buf][0] = mine;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
-      last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  __syncthreads();
+  if (n > 1 && tid == 0) {
+    int f = sh.fault;
+    for (int r = 0; r < n; ++r) f |= sh.flt[r];
+    sh.fault = f;
+    sh.exchanges = x + 1;
+  }
+  DF z{0.f, 0.f};
+  for (int r = 0; r < n; ++r) z = df_add(z, sh.slice[buf][r]);
+  return z;
+}
+
+__device__ __forceinline__ bool pass_ok(DF z) { return z.hi > 0.f && z.hi < kInf; }
+
+// Inverse-CDF draw from the pass in sh.all[buf] / sh.slice[buf]: the first
+// index whose running sum exceeds `target`.  The prefix before a tile is the
+// slice totals before its slice plus the tile sums before it in its slice
+// (double-float, in order).  The owning slice is the first slice with mass
+// whose end passes the target (else the last slice with mass); in it, with
+// E_j the prefix before tile j and r_j = target - E_j rounded to float, the
+// drawn tile is the first tile with mass whose sum exceeds r_j (else the
+// last tile with mass), and inside the tile the first element whose float
+// running sum exceeds r_j (else its last element with mass).  Every CTA of
+// the cluster finds the tile; the CTA owning the slice, or every CTA when
+// all_ctas is set, recomputes that tile with the same code as tile_sums and
+// returns the index to all its threads.  The other CTAs return -1.
+template <typename T>
+__device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, int buf, DF target,
+                            bool all_ctas, PassSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = static_cast<int>(cluster_size());
+  const int tpc = (ntiles + n - 1) / n;
+  const float* all = sh.all[buf];
+  if (tid < 32) {
+    // the owning slice (every lane computes the same)
+    DF E{0.f, 0.f}, Ef{0.f, 0.f}, El{0.f, 0.f};
+    int rf_ = -1, rl = -1;
+    for (int r = 0; r < n; ++r) {
+      const DF Tr = sh.slice[buf][r];
+      if (Tr.hi > 0.f) {
+        if (rf_ < 0 && df_gt(df_add(E, Tr), target)) {
+          rf_ = r;
+          Ef = E;
+        }
+        rl = r;
+        El = E;
+      }
+      E = df_add(E, Tr);
     }
-    if (lane == 0) {
-      sh.last_mode = first == ntiles;
-      sh.tile = first < ntiles ? first : (last >= 0 ? last : 0);
-      sh.E = sh.tile_excl[sh.tile];
-      sh.thread = sh.last_mode ? -1 : kThreads;
+    bool last_mode = rf_ < 0;
+    const int owner = last_mode ? max(rl, 0) : rf_;
+    const DF Eo = last_mode ? El : Ef;
+    // inside the slice: blocks of tiles, then the tiles of one block
+    const int s0 = min(ntiles, owner * tpc), m = min(ntiles, s0 + tpc) - s0;
+    int j0, j1, nb;
+    lane_block(s0, m, lane, j0, j1, nb);
+    DF run{0.f, 0.f};
+    for (int j = j0; j < j1; ++j) run = df_add_f(run, all[j]);
+    sh.lane_blk[lane] = run;
+    __syncwarp();
+    DF e = Eo;
+    for (int l = 0; l < min(lane, nb); ++l) e = df_add(e, sh.lane_blk[l]);
+    int first = 0x7fffffff, last = -1;
+    float rf_first = 0.f, rf_last = 0.f;
+    for (int j = j0; j < j1; ++j) {
+      const float s = all[j];
+      if (s > 0.f) {
+        const float rf = df_float(df_add(target, df_neg(e)));
+        if (first == 0x7fffffff && s > rf) {
+          first = j;
+          rf_first = rf;
+        }
+        last = j;
+        rf_last = rf;
+      }
+      e = df_add_f(e, s);
     }
+    const int fmin = last_mode ? 0x7fffffff : __reduce_min_sync(0xffffffffu, first);
+    const int lmax = __reduce_max_sync(0xffffffffu, last);
+    if (fmin != 0x7fffffff) {
+      if (first == fmin) {
+        sh.tile = first;
+        sh.rf = rf_first;
+        sh.last_mode = 0;
+        sh.thread = kThreads;
+      }
+    } else if (lmax >= 0) {
+      if (last == lmax) {
+        sh.tile = last;
+        sh.rf = rf_last;
+        sh.last_mode = 1;
+        sh.thread = -1;
+      }
+    } else if (lane == 0) {
+      sh.tile = min(s0, ntiles - 1);
+      sh.rf = 0.f;
+      sh.last_mode = 1;
+      sh.thread = -1;
+    }
+    if (lane == 0) sh.owner = owner;
   }
   __syncthreads();
   const int tile = sh.tile;
+  if (!all_ctas && sh.owner != static_cast<int>(cluster_rank())) return -1;
   float w[8];
   tile_weights(S, V, c, tile, w);
   const float mine = sum8(w);
   const float incl_w = warp_incl_scan(mine);
-  if (lane == 31) sh.warp_tot[0][warp] = incl_w;
+  if (lane == 31) sh.warp_tot[0][0][warp] = incl_w;
   __syncthreads();
   if (tid == 0) {
     float s = 0.f;
     for (int k = 0; k < kWarps; ++k) {
       sh.warp_excl[k] = s;
-      s = (k == 0) ? sh.warp_tot[0][0] : __fadd_rn(s, sh.warp_tot[0][k]);
+      s = (k == 0) ? sh.warp_tot[0][0][0] : __fadd_rn(s, sh.warp_tot[0][0][k]);
     }
   }
   __syncthreads();
   const float incl = (warp == 0) ? incl_w : __fadd_rn(sh.warp_excl[warp], incl_w);
   sh.thr_incl[tid] = incl;
   const bool last_mode = sh.last_mode;
-  const bool pass_here = mine > 0.f && (last_mode || sh.E + static_cast<double>(incl) > target);
+  const float rf = sh.rf;
+  const bool pass_here = mine > 0.f && (last_mode || incl > rf);
   const unsigned bal = __ballot_sync(0xffffffffu, pass_here);
   if (bal != 0 && lane == 0) {
     if (last_mode) atomicMax(&sh.thread, warp * 32 + 31 - __clz(bal));
@@ -358,13 +651,13 @@ __device__ int draw(const PassSpec<T>& S, int V, float c, const float* sums, int
   int t = sh.thread;
   if (t < 0 || t >= kThreads) t = 0;
   if (tid == t) {
-    double run = sh.E + ((t == 0) ? 0.0 : static_cast<double>(sh.thr_incl[t - 1]));
+    float run = (t == 0) ? 0.f : sh.thr_incl[t - 1];
     int y = -1, lastpos = -1;
     for (int e = 0; e < 8; ++e) {
-      run += static_cast<double>(w[e]);
+      run = __fadd_rn(run, w[e]);
       if (w[e] > 0.f) {
         lastpos = e;
-        if (!last_mode && y < 0 && run > target) y = e;
+        if (!last_mode && y < 0 && run > rf) y = e;
       }
     }
     if (y < 0) y = lastpos < 0 ? 0 : lastpos;
@@ -399,29 +692,28 @@ __device__ __forceinline__ float ratio(float xp, float mP, float sP, float xq, f
 
 __device__ __forceinline__ bool keeps(float u, float r) { return u < fminf(1.f, r); }
 
-// Merge the chunk partials of one statistics row (one warp; partials were
-// written by other CTAs of this grid, so they are read past L1).
+// Merge the chunk partials of one statistics row in chunk order (one
+// thread; `part` points into shared memory, where the partials were staged).
 __device__ __forceinline__ MaxSum combine_row(const float2* part, int chunks, float c) {
-  const int lane = threadIdx.x & 31;
   MaxSum acc{-kInf, 0.f};
-  for (int k = lane; k < chunks; k += 32) {
-    const float2 p = __ldcg(part + k);
+  for (int k = 0; k < chunks; ++k) {
+    const float2 p = part[k];
     acc = ms_merge(acc, MaxSum{p.x, p.y}, c);
   }
-  return ms_warp_reduce(acc, c);
+  return acc;
 }
 
+// Argmax over the chunk partials of one row (one thread); `bad` is set when
+// a chunk saw a NaN or +inf.
 __device__ __forceinline__ ArgMax combine_row_argmax(const float2* part, int chunks, bool& bad) {
-  const int lane = threadIdx.x & 31;
   ArgMax acc{-kInf, -1};
-  bool b = false;
-  for (int k = lane; k < chunks; k += 32) {
-    const float2 p = __ldcg(part + k);
-    if (p.x != p.x) b = true;
+  bad = false;
+  for (int k = 0; k < chunks; ++k) {
+    const float2 p = part[k];
+    if (p.x != p.x) bad = true;
     acc = am_merge(acc, ArgMax{p.x, __float_as_int(p.y)});
   }
-  bad = __any_sync(0xffffffffu, b);
-  return am_warp_reduce(acc);
+  return acc;
 }
 
 __device__ __forceinline__ bool row_stats_ok(MaxSum ms) {

@@ -50,18 +50,16 @@
  *    optional per-sequence `seq_error` array and are OR-ed into the optional
  *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2 or 4 gets
  *    empty outputs: accept length 0, tokens -1, rollback = prefix length.
- *  - Each call is one kernel launch.  Its CTAs stream every logit row once
- *    (row statistics); the CTA that completes a sequence then verifies that
- *    sequence while its rows are still in L2.
- *  - The workspace starts with a fixed head (256 bytes of call counters and
- *    one 32-byte state record per possible sequence index: 2,097,408 bytes)
- *    followed by per-call scratch.  Size it with the matching
- *    *_workspace_size function and ZERO THE HEAD ONCE before the first call
- *    (cudaMemset of the whole workspace is simplest); every call leaves the
- *    head at zero again, whatever its kind, mode or batch size, so one
- *    workspace serves any sequence of calls on one stream.  Two calls in flight at the same
- *    time need two workspaces.  Results are deterministic: the same inputs
- *    on the same GPU give bit-identical outputs.
+ *  - Each call is two kernel launches on `stream`.  The first streams every
+ *    logit row once (row statistics); the second, one thread-block cluster
+ *    per sequence, verifies each sequence while its rows are still in L2.
+ *  - The workspace holds the row statistics passed from the first kernel of
+ *    a call to the second (8 bytes per sequence, row and 8192-element chunk).
+ *    Size it with the matching *_workspace_size function; it needs no
+ *    initialisation and nothing in it outlives a call.  Two calls that can
+ *    run at the same time (other streams) need two workspaces.  Results are
+ *    deterministic: the same inputs on the same GPU give bit-identical
+ *    outputs.
  *  - Limits: B <= 65535, V <= 2,097,152.
  */
 #ifndef SPEC_VERIFY_H
@@ -92,8 +90,9 @@ typedef enum spec_mode { SPEC_GREEDY = 0, SPEC_SAMPLE = 1 } spec_mode;
 #define SPEC_ERR_NONFINITE 4  /* a logit row with NaN or +inf, or no finite entry */
 #define SPEC_ERR_ZERO_MASS 8  /* residual mass 0 after a rejection: the token was
                                  drawn from p instead (outputs stay valid)       */
-#define SPEC_ERR_INTERNAL 16  /* (error_word only) a work item waited too long for
-                                 another; the call's outputs are not valid      */
+#define SPEC_ERR_INTERNAL 16  /* a bulk copy of logits into shared memory did not
+                                 complete in time; this sequence's outputs are
+                                 not valid (never expected; reported, not hung) */
 
 /* ---------------------------------------------------------------------- */
 /* Chain verification: B sequences, each with a gamma-token draft.         */
@@ -126,7 +125,7 @@ typedef struct spec_chain_args {
                                   token was drawn from (0 in greedy)                */
   int* seq_error;              /* out [B], optional: data-error bits                */
   int* error_word;             /* in/out, optional: data-error bits OR-ed in        */
-  void* workspace;             /* zeroed once before first use, see the file comment */
+  void* workspace;             /* 16-byte aligned, see the file comment             */
   size_t workspace_bytes;
 } spec_chain_args;
 
@@ -143,12 +142,11 @@ spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
 /* library is loaded.  The call allocates and frees nothing.                */
 /*  - Size limit: the call returns SPEC_EWORKSPACE, launching nothing, when */
 /*    spec_chain_workspace_size(B, gamma, V) > SPEC_NOALLOC_SCRATCH_BYTES    */
-/*    (e.g. B = 64, gamma = 5, V = 128256 needs 2.2 MB and fits; B = 1024,  */
-/*    gamma = 8, V = 131072 needs 4.6 MB and fits; B = 8192 does not).      */
+/*    (e.g. B = 1024, gamma = 8, V = 131072 needs 2.2 MB and fits;          */
+/*    B = 4096 at the same gamma and V needs 8.9 MB and does not).          */
 /*  - The first call on a device looks up the array's device address (with  */
 /*    that device current) and keeps it; make that first call before any   */
-/*    stream capture.  Each call clears the completion counters it uses     */
-/*    (a memset node on `stream`) before its kernels run.                   */
+/*    stream capture.                                                       */
 /*  - All calls on one device share the array: two calls that can overlap   */
 /*    on the GPU (other streams, other host threads) race on it and give    */
 /*    wrong results.  Serialise them, or use spec_verify_chain with one     */

@@ -74,21 +74,12 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # head (256 B + 65536 x 32 B sequence records), then per call, each
-    # region rounded up to 256 B: a 48 B pass record and 16 B per sequence,
-    # pass tile sums (2 x 4 B per 4096-element tile), chunk partials (8 B per
-    # row per 8192 elements: the float32 chunk of the statistics kernel).
-    head = 256 + 65536 * 32
-
-    def r256(x):
-        return (x + 255) // 256 * 256
-
+    # the chunk partials of the statistics kernel: 8 B per (sequence, row,
+    # 8192-element chunk: the float32 chunk), rounded up to 256 B
     def size(B, rows, V):
-        tiles, chunks = -(-V // 4096), -(-V // 8192)
-        return head + r256(B * 48) + r256(B * 16) + r256(B * 2 * tiles * 4) + r256(B * rows * chunks * 8)
+        return (B * rows * -(-V // 8192) * 8 + 255) // 256 * 256
 
-    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256)
-    assert lib.spec_chain_workspace_size(64, 5, 128256) == head + 3072 + 1024 + 16384 + 90112
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256) == 90112
     assert lib.spec_tree_workspace_size(16, 64, 50257) == size(16, 128, 50257)
     assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == size(128, 21, 128256)
     assert lib.spec_chain_workspace_size(0, 5, 10) == 0
@@ -143,7 +134,7 @@ def test_noalloc_chain_rejects_before_touching_the_device(lib):
     assert lib.spec_verify_chain_noalloc(C.byref(_chain(gamma=33)), None) == -1
     # the static scratch is 8 MiB; a batch whose scratch exceeds it is refused
     assert _lib.SPEC_NOALLOC_SCRATCH_BYTES == 8 << 20
-    big = _chain(B=8192, gamma=8, V=131072, ld=131072)
-    assert lib.spec_chain_workspace_size(8192, 8, 131072) > _lib.SPEC_NOALLOC_SCRATCH_BYTES
+    big = _chain(B=4096, gamma=8, V=131072, ld=131072)
+    assert lib.spec_chain_workspace_size(4096, 8, 131072) > _lib.SPEC_NOALLOC_SCRATCH_BYTES
     assert lib.spec_verify_chain_noalloc(C.byref(big), None) == -4
     assert lib.spec_chain_workspace_size(1024, 8, 131072) <= _lib.SPEC_NOALLOC_SCRATCH_BYTES

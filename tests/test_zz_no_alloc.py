@@ -78,7 +78,7 @@ def test_noalloc_oversize_is_refused(cuda_device):
     from draft_verification_gb300 import _lib
     import ctypes as C
     a = _lib.ChainArgs()
-    a.B, a.gamma, a.V, a.ld = 8192, 8, 131072, 131072
+    a.B, a.gamma, a.V, a.ld = 4096, 8, 131072, 131072
     a.dtype, a.mode, a.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
     code = _lib.lib().spec_verify_chain_noalloc(C.byref(a), None)
     assert code == _lib.SPEC_EWORKSPACE
