@@ -2,10 +2,13 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one verification call (one fused kernel: row statistics, then the
-per-sequence walk) over one batch of the workload.  The default workload is the sampling chain
-B=32, gamma=8, V=32000, bf16, T=1.0, mean acceptance ~0.7; --workload selects
-any of workloads.synth.SPECS.  Inputs are synthetic and seeded.
+One step = one verification call over one batch of the workload: two kernels
+on one stream, the row-statistics kernel (streams every logit once) and the
+walk kernel (one thread-block cluster per sequence: accept tests, residual
+or bonus pass, inverse-CDF draw), chained with programmatic dependent launch.
+The default workload is the sampling chain B=32, gamma=8, V=32000, bf16,
+T=1.0, mean acceptance ~0.7; --workload selects any of
+workloads.synth.SPECS.  Inputs are synthetic and seeded.
 
 Timing: W warm-up steps, then a loaded soak of about one second (clocks are
 sampled over it and the timed region), then exactly K steps between CUDA
@@ -16,9 +19,11 @@ total) that every step reads its logits from HBM.  The steps are replayed
 from a CUDA graph that holds one call per input copy.
 
 Printed on rank 0: one JSON line with the metric (verified draft tokens/s),
-logits GB/s, the roofline of the call's single kernel (measured with CUDA
-events around each launch), the end-to-end number through the public call
-with host buffers, and the CPU oracle timed on a bounded sample.
+logits GB/s, the HBM roofline of the verification call (algorithmic bytes
+over the call's duration, CUDA events around each call on the launching
+stream: both kernels, so a lower bound for the statistics kernel alone), the
+end-to-end number through the public call with host buffers, and the CPU
+oracle timed on a bounded sample.
 
 --impl reference times the CPU oracle itself (the slow, plainly written
 reference) on the same workload and prints the same JSON line with
@@ -47,7 +52,10 @@ METRIC = "verified draft tokens/sec and logits GB/s vs GB300 HBM peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification_gb300/csrc/stats.cuh",
                   "draft_verification_gb300/csrc/walk.cuh", "draft_verification_gb300/csrc/common.cuh"]
-KERNEL_NAME = {"chain": "chain_kernel", "tree": "tree_kernel", "cascade": "cascade_kernel"}
+# the kernels of one call (statistics, then walk); greedy calls use the
+# greedy walk kernels
+KERNELS = {"chain": ["stats_kernel", "chain_walk_kernel"], "tree": ["stats_kernel", "tree_kernel"],
+           "cascade": ["stats_kernel", "cascade_walk_kernel"]}
 
 
 def parse():
@@ -97,6 +105,30 @@ def workload_config(w) -> dict:
     return cfg
 
 
+# --------------------------------------------------------------------------
+# replicas: one process per GPU, each verifying its own batch (no exchange)
+# --------------------------------------------------------------------------
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each replica draws its own seeded batch."""
+    return seed + rank
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest replica's time (every rank gets it)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_call: float, world: int, ms_per_call: float) -> float:
+    """Units all replicas processed per second, timed by the slowest one."""
+    return units_per_call * world / (ms_per_call * 1e-3)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -119,9 +151,10 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the verification kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"verify_kernel_{workload}.md")
+    """DRAM bytes of one verification call (both kernels, caches flushed) from
+    the committed ncu launch-list summary, if it was taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"launches_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -133,7 +166,7 @@ def profiled_traffic(workload: str):
     if fields.get("source_hash") != kernel_source_hash():
         return None
     try:
-        return int(float(fields["dram_bytes_per_launch"]))
+        return int(float(fields["dram_bytes_per_call"]))
     except (KeyError, ValueError):
         return None
 
@@ -371,11 +404,7 @@ def run_ours(args, w, rank, world, dist):
         if dist is not None:
             dist.barrier()
     clock_info = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, dev)
 
     # the one kernel of a call, alone: CUDA events around each launch
     n_ev = min(200, max(20, args.steps))
@@ -392,7 +421,7 @@ def run_ours(args, w, rank, world, dist):
     e2e = e2e_rate(args, w, dev, stream)
 
     tokens = draft_tokens_per_call(w)
-    value = tokens * world / (ms * 1e-3)
+    value = whole_job_rate(tokens, world, ms)
     logits_gbs = bytes_per_call / (ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     kernel_gbs = bytes_per_call / (kernel_ms * 1e-3) / 1e9
@@ -414,12 +443,13 @@ def run_ours(args, w, rank, world, dist):
         "logits_gbs": logits_gbs,
         "logits_frac_of_peak": logits_gbs / peak,
         "accepted_tokens_per_s": None if accepted is None else accepted * s.B * world / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "kernel": KERNEL_NAME[w["kind"]], "achieved": kernel_gbs,
+        "roofline": {"bound": "hbm", "kernel": "+".join(KERNELS[w["kind"]]), "unit_of_work": "one verification call",
+                     "achieved": kernel_gbs,
                      "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak, "peak_source": peak_src,
                      "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_per_call,
                      "traffic": profiled_traffic(s.name)},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * len(KERNELS[w["kind"]]),
         "clocks": clock_info,
     }
     return line
@@ -505,7 +535,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.workload not in synth.SPECS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.SPECS)}")
-    w = synth.make(synth.SPECS[args.workload], seed=args.seed + rank)
+    w = synth.make(synth.SPECS[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":
         if rank == 0:

@@ -780,12 +780,16 @@ cudaError_t resident_clusters(const void* fn, size_t dyn, std::array<int, 4>* ou
 }
 
 // Largest cluster (at most 8 CTAs, at most one per tile) for which all B
-// sequences' clusters are resident at once; 1 when even single CTAs need
-// more than one wave.
+// sequences' clusters fit in 7/8 of the clusters the occupancy query reports
+// resident at once; 1 when even single CTAs need more than one wave.  The
+// margin is for placement: a cluster must fit inside one GPC, and the walk
+// is placed while the statistics kernel still drains, so the clusters that
+// really fit are fewer than on an empty GPU (a second wave of a few
+// clusters costs a whole walk).
 int cluster_for(const std::array<int, 4>& resident, int B, int ntiles) {
   for (int i = 3; i >= 1; --i) {
     const int S = 1 << i;
-    if (S <= ntiles && B <= resident[i]) return S;
+    if (S <= ntiles && 8 * B <= 7 * resident[i]) return S;
   }
   return 1;
 }
