@@ -53,36 +53,7 @@ bool stats_params(StatsParams& sp, int B, int V, long long ld, bool bf16, bool g
 
 using namespace sv;
 
-extern "C" {
-
-const char* spec_status_string(spec_status status) {
-  switch (status) {
-    case SPEC_OK: return "ok";
-    case SPEC_EINVAL: return "invalid argument";
-    case SPEC_EDTYPE: return "unknown dtype or mode";
-    case SPEC_EALIGN: return "logit base address not 16-byte aligned";
-    case SPEC_EWORKSPACE: return "workspace missing or too small";
-    case SPEC_ECUDA: return "CUDA launch failed";
-  }
-  return "unknown status";
-}
-
-size_t spec_chain_workspace_size(int B, int gamma, int V) {
-  if (B < 1 || gamma < 0 || V < 1) return 0;
-  return workspace_bytes(B, 2 * gamma + 1, V);
-}
-
-size_t spec_tree_workspace_size(int B, int N, int V) {
-  if (B < 1 || N < 1 || V < 1) return 0;
-  return workspace_bytes(B, 2 * N, V);
-}
-
-size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V) {
-  if (B < 1 || gamma1 < 1 || gamma2 < 1 || V < 1) return 0;
-  return workspace_bytes(B, 2 * gamma1 + 1 + gamma2, V);
-}
-
-spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
+spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool grouped) {
   if (a == nullptr) return SPEC_EINVAL;
   spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
   if (st != SPEC_OK) return st;
@@ -126,7 +97,40 @@ spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
   cp.resid = a->resid_mass;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
-  return run(launch_chain(sp, cp, bf16, greedy, stream));
+  return run(launch_chain(sp, cp, bf16, greedy, grouped, stream));
+}
+
+extern "C" {
+
+const char* spec_status_string(spec_status status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_EDTYPE: return "unknown dtype or mode";
+    case SPEC_EALIGN: return "logit base address not 16-byte aligned";
+    case SPEC_EWORKSPACE: return "workspace missing or too small";
+    case SPEC_ECUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+size_t spec_chain_workspace_size(int B, int gamma, int V) {
+  if (B < 1 || gamma < 0 || V < 1) return 0;
+  return workspace_bytes(B, 2 * gamma + 1, V);
+}
+
+size_t spec_tree_workspace_size(int B, int N, int V) {
+  if (B < 1 || N < 1 || V < 1) return 0;
+  return workspace_bytes(B, 2 * N, V);
+}
+
+size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V) {
+  if (B < 1 || gamma1 < 1 || gamma2 < 1 || V < 1) return 0;
+  return workspace_bytes(B, 2 * gamma1 + 1 + gamma2, V);
+}
+
+spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
+  return sv::verify_chain(a, stream, true);
 }
 
 spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "spec_verify.h"
+
 namespace sv {
 
 // Logit rows of one tensor: row (b, i) starts at base + (b * rows + i) * ld.
@@ -41,6 +43,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 inline size_t workspace_bytes(int B, int rows_per_seq, int V) {
   return align256(static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
 }
+
 
 struct ChainParams {
   int B, gamma, V;
@@ -105,9 +108,18 @@ struct CascadeParams {
   int* error_word;
 };
 
-cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, bool greedy, cudaStream_t s);
+// `grouped` allows a large call to be split into batch groups on library
+// streams (forked from and joined into s); false keeps every launch on s.
+cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, bool greedy, bool grouped,
+                         cudaStream_t s);
 cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
 cudaError_t launch_cascade(const StatsParams& g, const CascadeParams& p, bool bf16, bool greedy,
                            cudaStream_t s);
 
+}  // namespace sv
+
+namespace sv {
+// spec_verify_chain with batch groups allowed or not (the no-allocation
+// entry point runs everything on the caller's stream).
+spec_status verify_chain(const spec_chain_args* a, cudaStream_t stream, bool grouped);
 }  // namespace sv

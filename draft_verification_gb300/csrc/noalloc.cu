@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "internal.h"
 #include "spec_verify.h"
 
 namespace {
@@ -65,5 +66,5 @@ extern "C" spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cu
   spec_chain_args a = *args;
   a.workspace = scratch;
   a.workspace_bytes = SPEC_NOALLOC_SCRATCH_BYTES;
-  return spec_verify_chain(&a, stream);
+  return sv::verify_chain(&a, stream, false);  // no library streams or events
 }

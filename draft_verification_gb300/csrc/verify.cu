@@ -729,12 +729,30 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
 // ---------------------------------------------------------------------------
 // launches
 // ---------------------------------------------------------------------------
+// Scheduling priority of rank r (0 = most urgent): the device's greatest
+// priority for r = 0, one level less per rank, never below the least.
+int launch_priority(int r) {
+  static int least = 0, greatest = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) least = greatest = 0;
+  });
+  return min(least, greatest + r);
+}
+
 template <typename K>
-cudaError_t launch_stats(K kernel, const StatsParams& G, cudaStream_t s) {
+cudaError_t launch_stats(K kernel, const StatsParams& G, cudaStream_t s, int rank = -1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G.chunks, G.rows_per_seq, G.B);
   cfg.blockDim = dim3(kStatsThreads);
   cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  if (rank >= 0) {
+    at[0].id = cudaLaunchAttributePriority;
+    at[0].val.priority = launch_priority(rank);
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  }
   void* argv[] = {const_cast<StatsParams*>(&G)};
   return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), argv);
 }
@@ -800,23 +818,28 @@ int cluster_for(const std::array<int, 4>& resident, int B, int ntiles) {
 // along x.
 template <typename K, typename A>
 cudaError_t launch_dependent(K kernel, dim3 grid, int cluster, size_t dyn, const StatsParams& G, const A& args,
-                             cudaStream_t s) {
+                             cudaStream_t s, int rank = -1) {
   const void* fn = reinterpret_cast<const void*>(kernel);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   int na = 1;
   if (cluster > 0) {
-    at[1].id = cudaLaunchAttributeClusterDimension;
-    at[1].val.clusterDim.x = cluster;
-    at[1].val.clusterDim.y = 1;
-    at[1].val.clusterDim.z = 1;
-    na = 2;
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = cluster;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (rank >= 0) {
+    at[na].id = cudaLaunchAttributePriority;
+    at[na].val.priority = launch_priority(rank);
+    ++na;
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
@@ -844,7 +867,7 @@ cudaError_t smem_limit(const void* fn, int bytes) {
 // the dynamic shared memory the cluster size is chosen for (at least dyn).
 template <typename K, typename A>
 cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsParams& G, const A& args,
-                        cudaStream_t s) {
+                        cudaStream_t s, int rank = -1) {
   const void* fn = reinterpret_cast<const void*>(kernel);
   cudaError_t e = smem_limit(fn, static_cast<int>(occupancy_dyn));
   if (e != cudaSuccess) return e;
@@ -852,15 +875,150 @@ cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsP
   e = resident_clusters(fn, occupancy_dyn, &resident);
   if (e != cudaSuccess) return e;
   const int S = cluster_for(resident, G.B, G.ntiles);
-  return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s);
+  return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s, rank);
+}
+
+// ---------------------------------------------------------------------------
+// batch groups: large calls are split into up to kMaxGroups groups of
+// sequences, each verified by its own statistics kernel and walk on a
+// library-owned stream forked from (and joined back into) the caller's
+// stream.  The statistics kernels of all groups stream back to back, and
+// each group's walk runs as soon as that group's statistics are complete,
+// alongside the statistics of the later groups; only the last group's walk
+// is left after the logits have been read.  A group is a smaller batch:
+// its pointers are offsets into the caller's arrays and its partials a
+// disjoint part of the workspace.
+// ---------------------------------------------------------------------------
+constexpr int kMaxGroups = 4;
+constexpr double kGroupBytes = 40e6;  // logits per group at least
+constexpr int kGroupSeqs = 16;        // sequences per group at least
+
+struct Groups {
+  int n;
+  int b0[kMaxGroups + 1];
+};
+
+Groups plan_groups(int B, double bytes) {
+  Groups g{};
+  int n = min(kMaxGroups, B / kGroupSeqs);
+  n = min(n, static_cast<int>(bytes / kGroupBytes));
+  g.n = max(n, 1);
+  for (int i = 0; i <= g.n; ++i) g.b0[i] = static_cast<int>((static_cast<long long>(B) * i) / g.n);
+  return g;
+}
+
+cudaError_t group_streams(cudaStream_t* out) {
+  static std::mutex mu;
+  static std::map<int, std::array<cudaStream_t, kMaxGroups>> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    std::array<cudaStream_t, kMaxGroups> st{};
+    for (int i = 0; i < kMaxGroups; ++i) {
+      e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return e;
+    }
+    it = cache.emplace(dev, st).first;
+  }
+  for (int i = 0; i < kMaxGroups; ++i) out[i] = it->second[i];
+  return cudaSuccess;
+}
+
+// Fork the caller's stream into one library stream per group, run
+// launch_group(i, stream) on each, and join them back.  The join is recorded
+// even when a launch fails, so the caller's stream never runs ahead of work
+// that was enqueued.
+template <typename F>
+cudaError_t run_groups(const Groups& gr, cudaStream_t s, F launch_group) {
+  cudaStream_t side[kMaxGroups];
+  cudaError_t e = group_streams(side);
+  if (e != cudaSuccess) return e;
+  cudaEvent_t fork;
+  e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(fork, s);
+  cudaError_t first = e;
+  for (int i = 0; i < gr.n && first == cudaSuccess; ++i) {
+    cudaEvent_t done;
+    e = cudaStreamWaitEvent(side[i], fork, 0);
+    if (e == cudaSuccess) e = launch_group(i, side[i]);
+    if (e != cudaSuccess) first = e;
+    if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess) {
+      if (cudaEventRecord(done, side[i]) == cudaSuccess) {
+        e = cudaStreamWaitEvent(s, done, 0);
+        if (e != cudaSuccess && first == cudaSuccess) first = e;
+      }
+      cudaEventDestroy(done);
+    }
+  }
+  cudaEventDestroy(fork);
+  return first;
 }
 
 template <typename T>
-cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s) {
-  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+StatsParams stats_group(const StatsParams& G, int b0, int nb) {
+  StatsParams g = G;
+  g.B = nb;
+  for (int k = 0; k < G.nsets; ++k)
+    g.set[k].base = static_cast<const T*>(G.set[k].base) + static_cast<long long>(b0) * G.set[k].rows * G.ld;
+  g.partials = G.partials + static_cast<long long>(b0) * G.rows_per_seq * G.chunks;
+  return g;
+}
+
+template <typename X>
+X* at_seq(X* p, int b0, long long per) {
+  return p ? p + static_cast<long long>(b0) * per : nullptr;
+}
+
+template <typename T>
+ChainParams chain_group(const ChainParams& p, int b0, int nb) {
+  ChainParams g = p;
+  const long long gam = p.gamma;
+  g.B = nb;
+  g.target = static_cast<const T*>(p.target) + static_cast<long long>(b0) * (gam + 1) * p.ld;
+  g.draft = p.draft ? static_cast<const T*>(p.draft) + static_cast<long long>(b0) * gam * p.ld : nullptr;
+  g.tokens = at_seq(p.tokens, b0, gam);
+  g.u = at_seq(p.u, b0, gam);
+  g.v = at_seq(p.v, b0, 1);
+  g.prefix = at_seq(p.prefix, b0, 1);
+  g.accept_len = at_seq(p.accept_len, b0, 1);
+  g.out_token = at_seq(p.out_token, b0, 1);
+  g.rollback = at_seq(p.rollback, b0, 1);
+  g.p_at = at_seq(p.p_at, b0, gam);
+  g.q_at = at_seq(p.q_at, b0, gam);
+  g.resid = at_seq(p.resid, b0, 1);
+  g.seq_error = at_seq(p.seq_error, b0, 1);
+  return g;
+}
+
+double logit_bytes(const StatsParams& G, size_t elt) {
+  return static_cast<double>(G.B) * G.rows_per_seq * G.V * static_cast<double>(elt);
+}
+
+// One group: its statistics, then its walk.  With group >= 0 the launches
+// carry priorities: every walk above every statistics kernel, and the
+// statistics of earlier groups above later ones, so that groups finish
+// their statistics in order and each walk starts as soon as it can.
+template <typename T>
+cudaError_t chain_one(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s, int group) {
+  const int sr = group < 0 ? -1 : 1 + group, wr = group < 0 ? -1 : 0;
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s, sr) : launch_stats(stats_kernel<T, false>, G, s, sr);
   if (e != cudaSuccess) return e;
-  if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s);
-  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
+  if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s, wr);
+  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s, wr);
+}
+
+template <typename T>
+cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, bool grouped, cudaStream_t s) {
+  const Groups gr = plan_groups(G.B, logit_bytes(G, sizeof(T)));
+  if (!grouped || gr.n == 1) return chain_one<T>(G, p, greedy, s, -1);
+  return run_groups(gr, s, [&](int i, cudaStream_t si) {
+    const int b0 = gr.b0[i], nb = gr.b0[i + 1] - b0;
+    return chain_one<T>(stats_group<T>(G, b0, nb), chain_group<T>(p, b0, nb), greedy, si, i);
+  });
 }
 
 template <typename T>
@@ -879,11 +1037,20 @@ cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, cu
 }
 
 template <typename T>
-cudaError_t cascade_impl(const StatsParams& G, const CascadeParams& p, bool greedy, cudaStream_t s) {
-  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+cudaError_t cascade_one(const StatsParams& G, const CascadeParams& p, bool greedy, cudaStream_t s, int group) {
+  const int sr = group < 0 ? -1 : 1 + group, wr = group < 0 ? -1 : 0;
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s, sr) : launch_stats(stats_kernel<T, false>, G, s, sr);
   if (e != cudaSuccess) return e;
-  if (greedy) return launch_dependent(cascade_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s);
-  return launch_walk(cascade_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
+  if (greedy) return launch_dependent(cascade_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s, wr);
+  return launch_walk(cascade_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s, wr);
+}
+
+// The cascade is not split into groups: its walk (two passes per sequence)
+// holds the SMs long enough that running it beside later groups'
+// statistics costs more than it hides.
+template <typename T>
+cudaError_t cascade_impl(const StatsParams& G, const CascadeParams& p, bool greedy, cudaStream_t s) {
+  return cascade_one<T>(G, p, greedy, s, -1);
 }
 
 }  // namespace
@@ -895,8 +1062,9 @@ int stats_chunks(int V, bool bf16) {
 
 int pass_tiles(int V) { return (V + kTileElems - 1) / kTileElems; }
 
-cudaError_t launch_chain(const StatsParams& G, const ChainParams& p, bool bf16, bool greedy, cudaStream_t s) {
-  return bf16 ? chain_impl<bf16_t>(G, p, greedy, s) : chain_impl<float>(G, p, greedy, s);
+cudaError_t launch_chain(const StatsParams& G, const ChainParams& p, bool bf16, bool greedy, bool grouped,
+                         cudaStream_t s) {
+  return bf16 ? chain_impl<bf16_t>(G, p, greedy, grouped, s) : chain_impl<float>(G, p, greedy, grouped, s);
 }
 
 cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s) {

@@ -533,31 +533,30 @@ __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int
 
 __device__ __forceinline__ bool pass_ok(DF z) { return z.hi > 0.f && z.hi < kInf; }
 
-// Inverse-CDF draw from the pass in sh.all[buf] / sh.slice[buf]: the first
-// index whose running sum exceeds `target`.  The prefix before a tile is the
-// slice totals before its slice plus the tile sums before it in its slice
-// (double-float, in order).  The owning slice is the first slice with mass
-// whose end passes the target (else the last slice with mass); in it, with
-// E_j the prefix before tile j and r_j = target - E_j rounded to float, the
-// drawn tile is the first tile with mass whose sum exceeds r_j (else the
-// last tile with mass), and inside the tile the first element whose float
-// running sum exceeds r_j (else its last element with mass).  Every CTA of
-// the cluster finds the tile; the CTA owning the slice, or every CTA when
-// all_ctas is set, recomputes that tile with the same code as tile_sums and
-// returns the index to all its threads.  The other CTAs return -1.
-template <typename T>
-__device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, int buf, DF target,
-                            bool all_ctas, PassSmem& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = static_cast<int>(cluster_size());
+// Inverse-CDF draw from a pass given as tile sums `all` (ntiles, shared
+// memory) and the totals `slices` of its n slices of tpc = ceil(ntiles / n)
+// tiles: the first index whose running sum exceeds `target`.  The prefix
+// before a tile is the slice totals before its slice plus the tile sums
+// before it in its slice (double-float, in order).  The owning slice is the
+// first slice with mass whose end passes the target (else the last slice
+// with mass); in it, with E_j the prefix before tile j and r_j = target -
+// E_j rounded to float, the drawn tile is the first tile with mass whose sum
+// exceeds r_j (else the last tile with mass), and inside the tile the first
+// element whose float running sum exceeds r_j (else its last element with
+// mass).
+//
+// locate_tile finds the slice and tile (warp 0; every CTA gets the same
+// result); draw_in_tile recomputes that tile with the same code as the pass
+// and returns the index to all threads.
+__device__ void locate_tile(const float* all, const DF* slices, int n, int ntiles, DF target, PassSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31;
   const int tpc = (ntiles + n - 1) / n;
-  const float* all = sh.all[buf];
   if (tid < 32) {
     // the owning slice (every lane computes the same)
     DF E{0.f, 0.f}, Ef{0.f, 0.f}, El{0.f, 0.f};
     int rf_ = -1, rl = -1;
     for (int r = 0; r < n; ++r) {
-      const DF Tr = sh.slice[buf][r];
+      const DF Tr = slices[r];
       if (Tr.hi > 0.f) {
         if (rf_ < 0 && df_gt(df_add(E, Tr), target)) {
           rf_ = r;
@@ -621,8 +620,12 @@ __device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, in
     if (lane == 0) sh.owner = owner;
   }
   __syncthreads();
+}
+
+template <typename T>
+__device__ int draw_in_tile(const PassSpec<T>& S, int V, float c, PassSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = sh.tile;
-  if (!all_ctas && sh.owner != static_cast<int>(cluster_rank())) return -1;
   float w[8];
   tile_weights(S, V, c, tile, w);
   const float mine = sum8(w);
@@ -667,6 +670,17 @@ __device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, in
   }
   __syncthreads();
   return sh.result;
+}
+
+// The draw from a cluster pass (sh.all[buf] / sh.slice[buf]): every CTA
+// locates the tile; the CTA owning its slice, or every CTA when all_ctas is
+// set, recomputes the tile and returns the index; the others return -1.
+template <typename T>
+__device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, int buf, DF target,
+                            bool all_ctas, PassSmem& sh) {
+  locate_tile(sh.all[buf], sh.slice[buf], static_cast<int>(cluster_size()), ntiles, target, sh);
+  if (!all_ctas && sh.owner != static_cast<int>(cluster_rank())) return -1;
+  return draw_in_tile(S, V, c, sh);
 }
 
 // ---------------------------------------------------------------------------

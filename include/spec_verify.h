@@ -50,9 +50,10 @@
  *    optional per-sequence `seq_error` array and are OR-ed into the optional
  *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2 or 4 gets
  *    empty outputs: accept length 0, tokens -1, rollback = prefix length.
- *  - Each call is two kernel launches on `stream`.  The first streams every
- *    logit row once (row statistics); the second, one thread-block cluster
- *    per sequence, verifies each sequence while its rows are still in L2.
+ *  - Each call is two kernel launches (row statistics, then the per-sequence
+ *    walk) per batch group; large sampling chain calls are split into
+ *    groups that run on library streams forked from `stream` and joined
+ *    back into it, so the call is ordered on `stream` like any other work.
  *  - The workspace holds the row statistics passed from the first kernel of
  *    a call to the second (8 bytes per sequence, row and 8192-element chunk).
  *    Size it with the matching *_workspace_size function; it needs no
