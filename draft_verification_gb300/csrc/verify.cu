@@ -640,6 +640,12 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   int* path = ts.scr_b;
   int node = 0, plen = 0, flag = 0, token = -1, buf = 0;
   bool writer = lead;
+  // this CTA's tiles; when they fit, a node's rows are loaded into shared
+  // memory once and every pass at the node reads them there
+  const int ncl = static_cast<int>(cluster_size());
+  const int tpc = (G.ntiles + ncl - 1) / ncl;
+  const int t0 = min(G.ntiles, static_cast<int>(cluster_rank()) * tpc), t1 = min(G.ntiles, t0 + tpc);
+  const bool res_ok = !kGreedy && slice_fits<T>(tpc);
   while (true) {
     const int nk = list_children(ts.par, N, node, kids, &nk_s);
     if constexpr (kGreedy) {
@@ -667,15 +673,18 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
       double cc = 0.0, W = 1.0;
       DF Wdf{1.f, 0.f};
       int kept = -1;
-      bool zero_mass = false;
+      bool zero_mass = false, resident = false;
       for (int q = 0; q < nk; ++q) {
         const int ch = kids[q];
-        if (tid == 0) {  // sibling test: p_k(tok) / q(tok) against u
+        if (tid == 0) {
+          // sibling test u < min(1, r) with r = max(0, p - c_k q) / (W_k q) at
+          // the child's token; since u < 1 it is u W_k q < max(0, p - c_k q),
+          // which needs no division and keeps exactly when p - c_k q > 0 if
+          // q = 0
           const double pt = prob(ts.gp[ch], sp.x, sp.y, c);
           const double qt = prob(ts.gq[ch], sq.x, sq.y, c);
-          const double pk = fmax(0.0, pt - cc * qt) / W;
-          const double rt = qt > 0.0 ? pk / qt : (pk > 0.0 ? INFINITY : 0.0);
-          keep_s = static_cast<double>(P.u[row0 + ch]) < fmin(1.0, rt);
+          const double num = fmax(0.0, pt - cc * qt);
+          keep_s = static_cast<double>(P.u[row0 + ch]) * W * qt < num;
         }
         __syncthreads();
         if (keep_s) {
@@ -685,7 +694,11 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         const double cn = cc + W;
         S.cq = static_cast<float>(cn);
         buf ^= 1;
-        const DF Wn = cluster_pass(S, P.V, c, G.ntiles, buf, ps);
+        if (res_ok && !resident) {
+          slice_load(S, true, P.V, t0, t1, ps);
+          resident = true;
+        }
+        const DF Wn = cluster_pass(S, P.V, c, G.ntiles, buf, ps, res_ok);
         if (!pass_ok(Wn)) {
           zero_mass = true;
           break;
@@ -706,7 +719,11 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         if (zero_mass) flag = SPEC_ERR_ZERO_MASS;
         S.cq = 0.f;  // draw from the node's own target distribution
         buf ^= 1;
-        Z = cluster_pass(S, P.V, c, G.ntiles, buf, ps);
+        if (res_ok && !resident) {
+          slice_load(S, false, P.V, t0, t1, ps);
+          resident = true;
+        }
+        Z = cluster_pass(S, P.V, c, G.ntiles, buf, ps, res_ok);
       }
       token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, P.v[b]), false, ps);
       writer = token >= 0;

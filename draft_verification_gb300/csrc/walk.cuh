@@ -250,6 +250,8 @@ struct PassSmem {
   DF lane_blk[32];          // sum of each lane's block of tiles of one slice
   uint64_t bar[kStages];    // one mbarrier per stage buffer
   uint64_t xbar[2];         // tile-sum exchange between the CTAs of the cluster
+  uint64_t lbar;            // loads of a resident slice
+  int loads;                // resident slices loaded so far (phase of lbar)
   int staged;               // stages issued by earlier passes of this kernel
   int exchanges;            // exchanges completed by earlier passes
   int flt[kMaxCluster];     // fault state of each CTA of the cluster
@@ -274,8 +276,10 @@ __device__ __forceinline__ void pass_begin(PassSmem& sh) {
     sh.fault = 0;
     sh.staged = 0;
     sh.exchanges = 0;
+    sh.loads = 0;
     for (int r = 0; r < kMaxCluster; ++r) sh.flt[r] = 0;
     for (int s = 0; s < kStages; ++s) mbar_init(&sh.bar[s], 1);
+    mbar_init(&sh.lbar, 1);
     mbar_init(&sh.xbar[0], cluster_size());
     mbar_init(&sh.xbar[1], cluster_size());
     mbar_fence_init();
@@ -421,6 +425,105 @@ __device__ void direct_sums(const PassSpec<T>& S, int V, float c, int t0, int t1
   }
 }
 
+// ---------------------------------------------------------------------------
+// resident slices: a CTA's tiles [t0, t1) of a (target, draft) row pair kept
+// in the stage region of shared memory, so that several passes over the same
+// rows (the sibling passes at one tree node) read the logits once
+// ---------------------------------------------------------------------------
+// Whether `nt` tiles of both rows fit in the stage region.
+template <typename T>
+__device__ __forceinline__ bool slice_fits(int nt) {
+  return 2 * static_cast<size_t>(nt) * kTileElems * sizeof(T) <= static_cast<size_t>(kStageBytes);
+}
+
+// This thread's 8 elements of local tile j of a resident row as floats.
+template <typename T>
+__device__ __forceinline__ void slice_get8(const unsigned char* buf, int j, float* x) {
+  uint32_t r[Load8<T>::kRegs];
+  stage_load8<T>(buf, j, r);
+  Load8<T>::get(r, x);
+}
+
+// Store 8 floats that are values of T into local tile j of a resident row.
+template <typename T>
+__device__ __forceinline__ void slice_put8(unsigned char* buf, int j, const float* x) {
+  T* p = reinterpret_cast<T*>(buf) + j * kTileElems + 8 * threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if constexpr (sizeof(T) == 2) p[e] = static_cast<bf16_t>(__float_as_uint(x[e]) >> 16);
+    else p[e] = x[e];
+  }
+}
+
+// Tiles [t0, t1) of `row` into buf (local tile 0 = t0).  Full tiles of a
+// 16-byte-aligned row by bulk copy, issued by thread 0 on `bar` (the byte
+// count is returned); the rest (misaligned rows, a row's last partial tile)
+// by plain loads, with -inf past V.
+template <typename T>
+__device__ unsigned slice_issue(const T* row, int V, int t0, int t1, unsigned char* buf, uint64_t* bar) {
+  const int tf = row_is_aligned(row) ? max(t0, min(t1, V / kTileElems)) : t0;
+  unsigned bytes = 0;
+  if (tf > t0) {
+    bytes = static_cast<unsigned>((tf - t0) * kTileElems * sizeof(T));
+    if (threadIdx.x == 0) bulk_load(buf, row + static_cast<long long>(t0) * kTileElems, bytes, bar);
+  }
+  for (int t = tf; t < t1; ++t) {
+    float x[8];
+    const int e0 = t * kTileElems + 8 * threadIdx.x;
+    if (row_is_aligned(row)) {
+      uint32_t r[Load8<T>::kRegs];
+      Load8<T>::issue(row, e0, V, r);
+      Load8<T>::get(r, x);
+    } else {
+      load8_misaligned(row, e0, V, x);
+    }
+    slice_put8<T>(buf, t - t0, x);
+  }
+  return bytes;
+}
+
+// Load this CTA's slice of the pass's rows (the draft row only when
+// `with_q`) into the stage region; every thread returns after the data is
+// in place.  A load that does not complete in time sets the fault state.
+template <typename T>
+__device__ void slice_load(const PassSpec<T>& S, bool with_q, int V, int t0, int t1, PassSmem& sh) {
+  const int tpc = t1 - t0;
+  unsigned char* pbuf = dyn_smem;
+  unsigned char* qbuf = dyn_smem + static_cast<size_t>(tpc) * kTileElems * sizeof(T);
+  __syncthreads();  // earlier passes have finished with the stage region
+  if (threadIdx.x == 0) fence_proxy_async();
+  unsigned bytes = slice_issue(S.P, V, t0, t1, pbuf, &sh.lbar);
+  if (with_q) bytes += slice_issue(S.Q, V, t0, t1, qbuf, &sh.lbar);
+  const int phase = sh.loads;
+  if (threadIdx.x == 0) mbar_expect_tx(&sh.lbar, bytes);
+  __syncthreads();  // armed and issued before anyone waits; plain stores visible
+  if (!mbar_wait(&sh.lbar, phase & 1)) sh.fault = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) sh.loads = phase + 1;
+}
+
+// Sums of the resident tiles (local 0 .. t1 - t0) into out[t0 .. t1), with
+// the same arithmetic as the other paths.
+template <typename T>
+__device__ void resident_sums(const PassSpec<T>& S, float c, int t0, int t1, float* out, PassSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tpc = t1 - t0;
+  const unsigned char* pbuf = dyn_smem;
+  const unsigned char* qbuf = dyn_smem + static_cast<size_t>(tpc) * kTileElems * sizeof(T);
+  const bool useQ = S.cq != 0.f;
+  for (int j = 0; j < tpc; ++j) {
+    float xp[8], xq[8], w[8];
+    slice_get8<T>(pbuf, j, xp);
+    if (useQ) slice_get8<T>(qbuf, j, xq);
+    pass_weights(S, c, xp, xq, w);
+    const float incl = warp_incl_scan(sum8(w));
+    if (lane == 31) sh.warp_tot[j & 1][0][warp] = incl;
+    __syncthreads();
+    if (tid == 0) out[t0 + j] = tile_total(sh.warp_tot[j & 1][0]);
+  }
+  __syncthreads();
+}
+
 // Sums of tiles [t0, t1) into out[t0 .. t1) (shared memory).  All threads
 // call it; out[] is complete when it returns.  Full tiles of aligned rows go
 // through the staged path, the rest through the register path.
@@ -476,8 +579,10 @@ __device__ DF slice_sum(const float* all, int s0, int m, PassSmem& sh) {
 
 __device__ __forceinline__ bool df_gt(DF a, DF b) { return df_add(a, df_neg(b)).hi > 0.f; }
 
-// One pass split over the CTAs of the cluster.  CTA `rank` sums its slice of
-// the tiles (tile sums into sh.all[buf], their total into
+// One pass split over the CTAs of the cluster (from the resident slice when
+// `resident`, which then holds this CTA's tiles of the pass's rows).  CTA
+// `rank` sums its slice of the tiles (tile sums into sh.all[buf], their
+// total into
 // sh.slice[buf][rank]) and stores both into every CTA of the cluster, then
 // arrives on every CTA's exchange barrier (warp 0 does both); once its own
 // barrier has all arrivals, each CTA holds every tile sum and slice total.
@@ -488,14 +593,16 @@ __device__ __forceinline__ bool df_gt(DF a, DF b) { return df_add(a, df_neg(b)).
 // does after it has finished reading this one.  A wait that gives up sets
 // the fault state instead of hanging.
 template <typename T>
-__device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int buf, PassSmem& sh) {
+__device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int buf, PassSmem& sh,
+                           bool resident = false) {
   const int tid = threadIdx.x;
   const int rank = static_cast<int>(cluster_rank()), n = static_cast<int>(cluster_size());
   const int tpc = (ntiles + n - 1) / n;
   const int t0 = min(ntiles, rank * tpc), t1 = min(ntiles, t0 + tpc);
   const int x = sh.exchanges;  // stable: updated only after the barriers below
   float* all = sh.all[buf];
-  tile_sums(S, V, c, t0, t1, all, sh);
+  if (resident) resident_sums(S, c, t0, t1, all, sh);
+  else tile_sums(S, V, c, t0, t1, all, sh);
   if (tid < 32) {
     const DF mine = slice_sum(all, t0, t1 - t0, sh);
     if (n > 1) {
