@@ -188,6 +188,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity
 }
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
+// Hint the bulk-copy engine to bring `bytes` (a multiple of 16, 16-byte
+// aligned) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Order this thread's earlier shared-memory accesses before later bulk copies.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

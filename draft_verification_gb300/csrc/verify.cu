@@ -648,6 +648,19 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   const bool res_ok = !kGreedy && slice_fits<T>(tpc);
   while (true) {
     const int nk = list_children(ts.par, N, node, kids, &nk_s);
+    if (!kGreedy && res_ok && tid < nk) {
+      // whichever child is kept next, its rows' slice of this CTA will come
+      // from L2: hint the bulk-copy engine to bring every child's in now
+      const int ch = kids[tid];
+      const T* cp = target + (row0 + ch) * P.ld;
+      const T* cq = draft + (row0 + ch) * P.ld;
+      const int tf = min(t1, P.V / kTileElems);
+      if (tf > t0 && row_is_aligned(cp) && row_is_aligned(cq)) {
+        const unsigned bytes = static_cast<unsigned>((tf - t0) * kTileElems * sizeof(T));
+        prefetch_l2(cp + static_cast<long long>(t0) * kTileElems, bytes);
+        prefetch_l2(cq + static_cast<long long>(t0) * kTileElems, bytes);
+      }
+    }
     if constexpr (kGreedy) {
       const int best = __float_as_int(ts.st[node].y);
       int kept = -1;

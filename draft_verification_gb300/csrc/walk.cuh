@@ -239,10 +239,12 @@ constexpr int kStageRowBytes = 8192;
 constexpr int kStages = 2;
 constexpr int kStageBytes = kStages * 2 * kStageRowBytes;
 constexpr int kMaxCluster = 8;
+constexpr int kResidentTiles = kStageBytes / (2 * kTileElems * 2);  // bf16 tiles of both rows
 extern __shared__ __align__(128) unsigned char dyn_smem[];
 
 struct PassSmem {
   float warp_tot[2][kMaxBatch][kWarps];  // ring of per-warp tile totals
+  float res_tot[kResidentTiles][kWarps]; // per-warp totals of the resident tiles
   float warp_excl[kWarps];
   float thr_incl[kThreads];
   float all[2][kMaxTiles];  // tile sums of a whole pass, double-buffered
@@ -503,7 +505,8 @@ __device__ void slice_load(const PassSpec<T>& S, bool with_q, int V, int t0, int
 }
 
 // Sums of the resident tiles (local 0 .. t1 - t0) into out[t0 .. t1), with
-// the same arithmetic as the other paths.
+// the same arithmetic as the other paths.  Every tile's per-warp totals are
+// formed before one barrier; then one thread per tile adds them.
 template <typename T>
 __device__ void resident_sums(const PassSpec<T>& S, float c, int t0, int t1, float* out, PassSmem& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -517,10 +520,10 @@ __device__ void resident_sums(const PassSpec<T>& S, float c, int t0, int t1, flo
     if (useQ) slice_get8<T>(qbuf, j, xq);
     pass_weights(S, c, xp, xq, w);
     const float incl = warp_incl_scan(sum8(w));
-    if (lane == 31) sh.warp_tot[j & 1][0][warp] = incl;
-    __syncthreads();
-    if (tid == 0) out[t0 + j] = tile_total(sh.warp_tot[j & 1][0]);
+    if (lane == 31) sh.res_tot[j][warp] = incl;
   }
+  __syncthreads();
+  if (tid < tpc) out[t0 + tid] = tile_total(sh.res_tot[tid]);
   __syncthreads();
 }
 
