@@ -63,6 +63,19 @@ def test_chain_full_size(cuda_device, name):
         H.compare_chain(H.gpu_chain(w, cuda_device, greedy=True), H.oracle_chain(w, greedy=True), True)
 
 
+def test_chain_batch_groups_ragged(cuda_device):
+    # B = 37 rows of 128256 logits is large enough to be split into two
+    # groups of sequences (18 and 19) on library streams; every sequence,
+    # including those at the group boundary, must match the oracle, and a
+    # data error in the second group must stay with its sequence
+    spec = W(S["sampling_chain_b64_g5_v128256_bf16_a60"], B=37)
+    w = synth.make(spec, seed=9)
+    w["tokens"][20, 2] = spec.V  # out of range, in the second group
+    g = H.gpu_chain(w, cuda_device)
+    H.compare_chain(g, H.oracle_chain(w), False)
+    assert g["seq_error"][20] == 1 and (np.delete(g["seq_error"], 20) & 1).sum() == 0
+
+
 def test_chain_data_errors(cuda_device):
     spec = W(S["sampling_chain_b32_g8_v32000_bf16"], B=6, gamma=4, V=3000)
     w = synth.make(spec, seed=2)
