@@ -163,16 +163,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-// One arrival, with release semantics at cluster scope, on the mbarrier at
-// the address of `local` in cluster CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* local, unsigned rank) {
-  const uint32_t a = smem_addr(local);
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(r) : "memory");
-}
 // Bounded wait, with acquire semantics at cluster scope, for phase `parity`
-// of a local mbarrier that other CTAs of the cluster arrive on.
+// of a local mbarrier that other CTAs of the cluster send bytes to.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity) {
   for (int i = 0; i < kMaxPolls; ++i) {
     uint32_t ok;
@@ -186,7 +178,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, unsigned parity
   }
   return false;
 }
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Store v at the address of `local` in cluster CTA `rank`, counting its 4
+// bytes on that CTA's mbarrier at the address of `bar` (one network trip:
+// the receiver's wait on the barrier makes the value visible).
+__device__ __forceinline__ void st_async_cluster(const void* local, unsigned rank, uint32_t v, const uint64_t* bar) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra), "r"(v), "r"(rb)
+               : "memory");
+}
 
 // Hint the bulk-copy engine to bring `bytes` (a multiple of 16, 16-byte
 // aligned) at `src` into L2.
@@ -203,13 +204,6 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(smem_addr(p)));
   return v;
-}
-// Store v at the address of `local` in the shared memory of cluster CTA `rank`.
-__device__ __forceinline__ void st_cluster_u32(int* local, unsigned rank, int v) {
-  const uint32_t a = smem_addr(local);
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(r), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -342,13 +336,6 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 __device__ __forceinline__ void cluster_sync() {
   cluster_arrive();
   cluster_wait();
-}
-// Store v at the address of `local` in the shared memory of cluster CTA `rank`.
-__device__ __forceinline__ void st_cluster(float* local, unsigned rank, float v) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
 }
 
 }  // namespace sv

@@ -271,8 +271,9 @@ struct PassSmem {
 // mbarriers are initialised once per kernel: every pass continues their
 // phases (stage number `staged + k` uses buffer (staged + k) % kStages in
 // its ((staged + k) / kStages)-th phase).
-// The exchange barriers count one arrival from every CTA of the cluster per
-// pass; pass number x uses xbar[x & 1] in its (x >> 1)-th phase.
+// The exchange barriers complete when the CTA itself has armed them with the
+// bytes its peers will send for the pass and all those bytes have landed;
+// pass number x uses xbar[x & 1] in its (x >> 1)-th phase.
 __device__ __forceinline__ void pass_begin(PassSmem& sh) {
   if (threadIdx.x == 0) {
     sh.fault = 0;
@@ -282,8 +283,8 @@ __device__ __forceinline__ void pass_begin(PassSmem& sh) {
     for (int r = 0; r < kMaxCluster; ++r) sh.flt[r] = 0;
     for (int s = 0; s < kStages; ++s) mbar_init(&sh.bar[s], 1);
     mbar_init(&sh.lbar, 1);
-    mbar_init(&sh.xbar[0], cluster_size());
-    mbar_init(&sh.xbar[1], cluster_size());
+    mbar_init(&sh.xbar[0], 1);
+    mbar_init(&sh.xbar[1], 1);
     mbar_fence_init();
   }
 }
@@ -585,16 +586,18 @@ __device__ __forceinline__ bool df_gt(DF a, DF b) { return df_add(a, df_neg(b)).
 // One pass split over the CTAs of the cluster (from the resident slice when
 // `resident`, which then holds this CTA's tiles of the pass's rows).  CTA
 // `rank` sums its slice of the tiles (tile sums into sh.all[buf], their
-// total into
-// sh.slice[buf][rank]) and stores both into every CTA of the cluster, then
-// arrives on every CTA's exchange barrier (warp 0 does both); once its own
-// barrier has all arrivals, each CTA holds every tile sum and slice total.
+// total into sh.slice[buf][rank]) and sends both to every other CTA of the
+// cluster by asynchronous stores that count on the receiver's exchange
+// barrier (warp 0); once its own barrier has every peer's bytes, each CTA
+// holds every tile sum and slice total.
 // Returns the pass total, the slice totals added in slice order (bit-
 // identical in every CTA).  Every CTA of the cluster calls it with the same
-// pass.  Consecutive passes alternate `buf`: a CTA can store into a peer's
-// buffer again only after that peer has arrived for the next pass, which it
-// does after it has finished reading this one.  A wait that gives up sets
-// the fault state instead of hanging.
+// pass.  Consecutive passes alternate `buf` and the exchange barrier: a CTA
+// can send into a peer's buffer or barrier again only after it has received
+// that peer's data for the next pass, which the peer sends after it has
+// finished reading this one (fault states are not double-buffered: they only
+// go from 0 to 1, so reading a later one is harmless).  A wait that gives up
+// sets the fault state instead of hanging.
 template <typename T>
 __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int buf, PassSmem& sh,
                            bool resident = false) {
@@ -609,22 +612,30 @@ __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int
   if (tid < 32) {
     const DF mine = slice_sum(all, t0, t1 - t0, sh);
     if (n > 1) {
+      // every peer's tile sums, slice total and fault state arrive by
+      // asynchronous stores counted on this CTA's exchange barrier
+      uint64_t* xb = &sh.xbar[x & 1];
+      if (tid == 0) {
+        unsigned expect = 0;
+        for (int d = 0; d < n; ++d)
+          if (d != rank) expect += 4u * static_cast<unsigned>(min(ntiles, d * tpc + tpc) - min(ntiles, d * tpc)) + 12u;
+        mbar_expect_tx(xb, expect);
+        sh.slice[buf][rank] = mine;
+        sh.flt[rank] = sh.fault;
+      }
       const int nt = t1 - t0;
       for (int i = tid; i < nt * (n - 1); i += 32) {
         int d = i / nt;
         const int k = i - d * nt;
         if (d >= rank) ++d;
-        st_cluster(all + t0 + k, static_cast<unsigned>(d), all[t0 + k]);
+        st_async_cluster(all + t0 + k, static_cast<unsigned>(d), __float_as_uint(all[t0 + k]), xb);
       }
-      if (tid < n) {
-        st_cluster(&sh.slice[buf][rank].hi, static_cast<unsigned>(tid), mine.hi);
-        st_cluster(&sh.slice[buf][rank].lo, static_cast<unsigned>(tid), mine.lo);
-        st_cluster_u32(&sh.flt[rank], static_cast<unsigned>(tid), sh.fault);
+      if (tid < n && tid != rank) {
+        st_async_cluster(&sh.slice[buf][rank].hi, static_cast<unsigned>(tid), __float_as_uint(mine.hi), xb);
+        st_async_cluster(&sh.slice[buf][rank].lo, static_cast<unsigned>(tid), __float_as_uint(mine.lo), xb);
+        st_async_cluster(&sh.flt[rank], static_cast<unsigned>(tid), static_cast<uint32_t>(sh.fault), xb);
       }
-      fence_cluster();
-      __syncwarp();  // every store of this CTA precedes its arrivals
-      if (tid < n) mbar_arrive_cluster(&sh.xbar[x & 1], static_cast<unsigned>(tid));
-      if (!mbar_wait_cluster(&sh.xbar[x & 1], (x >> 1) & 1)) sh.fault = 1;
+      if (!mbar_wait_cluster(xb, (x >> 1) & 1)) sh.fault = 1;
     } else if (tid == 0) {
       sh.slice[buf][0] = mine;
     }
