@@ -55,15 +55,19 @@ def logits_view(t: torch.Tensor, V: int) -> torch.Tensor:
 # chain
 # --------------------------------------------------------------------------
 
-def gpu_chain(w, device, greedy=None):
+def chain_plan(w, device, greedy=None, workspace=None):
     from draft_verification_gb300 import ChainPlan
     s = w["spec"]
     greedy = s.greedy if greedy is None else greedy
     tgt = logits_view(dev_logits(w["target"], s.dtype, device), s.V)
     drf = logits_view(dev_logits(w["draft"], s.dtype, device), s.V)
-    plan = ChainPlan(tgt, drf, dev(w["tokens"], device), dev(w["u"], device), dev(w["v"], device),
-                     dev(w["prefix_len"], device), greedy=greedy, temperature=s.temperature)
-    return to_np(plan.run())
+    return ChainPlan(tgt, drf, dev(w["tokens"], device), dev(w["u"], device), dev(w["v"], device),
+                     dev(w["prefix_len"], device), greedy=greedy, temperature=s.temperature,
+                     workspace=workspace)
+
+
+def gpu_chain(w, device, greedy=None, workspace=None):
+    return to_np(chain_plan(w, device, greedy, workspace).run())
 
 
 def oracle_chain(w, greedy=None):
@@ -108,7 +112,7 @@ def compare_chain(g, o, greedy):
 # tree
 # --------------------------------------------------------------------------
 
-def gpu_tree(w, device, greedy=None):
+def gpu_tree(w, device, greedy=None, workspace=None):
     from draft_verification_gb300 import TreePlan
     s = w["spec"]
     greedy = s.greedy if greedy is None else greedy
@@ -116,7 +120,8 @@ def gpu_tree(w, device, greedy=None):
     drf = logits_view(dev_logits(w["draft"], s.dtype, device), s.V)
     plan = TreePlan(dev(w["parent"], device), dev(w["tokens"], device), tgt, drf,
                     dev(w["u"], device), dev(w["v"], device), dev(w["prefix_len"], device),
-                    max_depth=w["max_depth"], greedy=greedy, temperature=s.temperature)
+                    max_depth=w["max_depth"], greedy=greedy, temperature=s.temperature,
+                    workspace=workspace)
     return to_np(plan.run())
 
 

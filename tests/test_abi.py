@@ -138,3 +138,40 @@ def test_noalloc_chain_rejects_before_touching_the_device(lib):
     assert lib.spec_chain_workspace_size(4096, 8, 131072) > _lib.SPEC_NOALLOC_SCRATCH_BYTES
     assert lib.spec_verify_chain_noalloc(C.byref(big), None) == -4
     assert lib.spec_chain_workspace_size(1024, 8, 131072) <= _lib.SPEC_NOALLOC_SCRATCH_BYTES
+
+
+def test_each_kind_accepts_exactly_its_workspace_size(lib):
+    # a workspace of exactly the reported size passes validation (the call
+    # then fails at the launch: there is no GPU here), one byte less does not
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on placeholder pointers")
+    from draft_verification_gb300 import _lib
+    fake = 0x10000
+    a = _chain()
+    a.workspace_bytes = lib.spec_chain_workspace_size(a.B, a.gamma, a.V)
+    assert lib.spec_verify_chain(C.byref(a), None) == _lib.SPEC_ECUDA
+    a.workspace_bytes -= 1
+    assert lib.spec_verify_chain(C.byref(a), None) == -4
+
+    t = _lib.TreeArgs()
+    t.B, t.N, t.max_depth, t.V, t.ld = 2, 6, 3, 100, 100
+    t.dtype, t.mode, t.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
+    for f in ("parent", "node_tokens", "target_logits", "draft_logits", "u", "v", "path_len",
+              "path_nodes", "out_token", "workspace"):
+        setattr(t, f, fake)
+    t.workspace_bytes = lib.spec_tree_workspace_size(t.B, t.N, t.V)
+    assert lib.spec_verify_tree(C.byref(t), None) == _lib.SPEC_ECUDA
+    t.workspace_bytes -= 1
+    assert lib.spec_verify_tree(C.byref(t), None) == -4
+
+    c = _lib.CascadeArgs()
+    c.B, c.gamma1, c.gamma2, c.V, c.ld = 2, 4, 3, 100, 100
+    c.dtype, c.mode, c.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
+    for f in ("l0", "l1", "l2", "draft_tokens", "u1", "v1", "u2", "v2", "a1", "t1", "a2", "w2",
+              "t2", "t2_valid", "r0", "r1", "committed", "workspace"):
+        setattr(c, f, fake)
+    c.workspace_bytes = lib.spec_cascade_workspace_size(c.B, c.gamma1, c.gamma2, c.V)
+    assert lib.spec_verify_cascade(C.byref(c), None) == _lib.SPEC_ECUDA
+    c.workspace_bytes -= 1
+    assert lib.spec_verify_cascade(C.byref(c), None) == -4

@@ -76,6 +76,49 @@ def test_chain_batch_groups_ragged(cuda_device):
     assert g["seq_error"][20] == 1 and (np.delete(g["seq_error"], 20) & 1).sum() == 0
 
 
+def test_chain_workspace_reused_across_shapes(cuda_device):
+    # one workspace (sized for the largest call) serves chain and tree calls
+    # of different sizes, dtypes and modes in turn: whatever an earlier call
+    # left in it never passes for the current call's statistics
+    import draft_verification_gb300 as dv
+    big = W(S["sampling_chain_b32_g8_v32000_bf16"], B=24, gamma=6, V=40000)
+    tree = W(S["tree_b16_n64_v50257_bf16"], B=3, V=5000, n_nodes=20, branching=(3, 3, 2))
+    need = max(dv.workspace_bytes("chain", 24, 6, 40000), dv.workspace_bytes("tree", 3, 20, 5000))
+    ws = torch.zeros(need, dtype=torch.uint8, device=cuda_device)
+    calls = [(big, 1), (W(big, B=5, V=9000), 2), (big, 3), (tree, 4), (W(big, greedy=True), 5),
+             (W(big, B=7, gamma=3, dtype="f32", V=12001), 6), (big, 7)]
+    for spec, seed in calls:
+        w = synth.make(spec, seed=seed)
+        if w["kind"] == "tree":
+            H.compare_tree(H.gpu_tree(w, cuda_device, workspace=ws), H.oracle_tree(w), False)
+        else:
+            H.compare_chain(H.gpu_chain(w, cuda_device, workspace=ws), H.oracle_chain(w), spec.greedy)
+
+
+def test_chain_graph_replays(cuda_device):
+    # a call captured once in a CUDA graph and replayed on new inputs copied
+    # into the same buffers (the way the benchmark runs it): every replay is
+    # verified against the oracle
+    spec = W(S["sampling_chain_b64_g5_v128256_bf16_a60"], B=12)
+    ws = [synth.make(spec, seed=20 + i) for i in range(3)]
+    plan = H.chain_plan(ws[0], cuda_device)
+    tgt, drf = plan.keep[0], plan.keep[1]
+    stream = torch.cuda.Stream(cuda_device)
+    plan.run(stream)  # first call outside the capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.run(stream)
+    for w in ws[1:] + ws[:1]:
+        tgt.copy_(H.logits_view(H.dev_logits(w["target"], spec.dtype, cuda_device), spec.V))
+        drf.copy_(H.logits_view(H.dev_logits(w["draft"], spec.dtype, cuda_device), spec.V))
+        for k, x in (("tokens", 2), ("u", 3), ("v", 4), ("prefix_len", 5)):
+            plan.keep[x].copy_(H.dev(w[k], cuda_device))
+        graph.replay()
+        torch.cuda.synchronize()
+        H.compare_chain(H.to_np(plan.out), H.oracle_chain(w), False)
+
+
 def test_chain_data_errors(cuda_device):
     spec = W(S["sampling_chain_b32_g8_v32000_bf16"], B=6, gamma=4, V=3000)
     w = synth.make(spec, seed=2)
