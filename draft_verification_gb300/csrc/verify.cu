@@ -190,19 +190,22 @@ struct ChainSmem {
   int st_arg[kMaxGamma + 1];
   int tok[kMaxGamma];
   float gp[kMaxGamma], gq[kMaxGamma];
+  float u[kMaxGamma], v;  // the call's uniforms (sampling)
   int err, a;
 };
 
-// Tokens and the logits at the drafted tokens (inputs only: safe before the
-// statistics are complete).
+// Tokens, the logits at the drafted tokens and the uniforms (inputs only:
+// safe before the statistics are complete).
 template <typename T>
 __device__ void chain_inputs(const ChainParams& P, int b, ChainSmem& cs, bool sampling) {
   const int g = P.gamma, tid = threadIdx.x;
   if (tid == 0) cs.err = 0;
   __syncthreads();
+  if (sampling && tid == kThreads - 1) cs.v = P.v[b];
   if (tid < g) {
     const long long d0 = static_cast<long long>(b) * g;
     const long long t0 = static_cast<long long>(b) * (g + 1);
+    if (sampling) cs.u[tid] = P.u[d0 + tid];
     const int t = P.tokens[d0 + tid];
     cs.tok[tid] = t;
     if (t < 0 || t >= P.V) {
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
     bool keep = true;
     if (lane < g) {
       const float mq = cs.st_m[g + 1 + lane], sq = cs.st_s[g + 1 + lane];
-      keep = keeps(P.u[drow0 + lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
+      keep = keeps(cs.u[lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
       if (lead) {
         if (P.p_at) P.p_at[drow0 + lane] = prob(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], c);
         if (P.q_at) P.q_at[drow0 + lane] = prob(cs.gq[lane], mq, sq, c);
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
                             a < g ? cs.st_s[g + 1 + a] : 1.f, 1.f, c);
   int buf = 0, flag = 0;
   const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
-  const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, P.v[b]), false, ps);
+  const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps);
   if (y < 0) return;  // another CTA of the cluster holds the drawn tile
   if (ps.fault) flag |= SPEC_ERR_INTERNAL;
   if (tid == 0) {
@@ -330,6 +333,8 @@ struct CascadeSmem {
   int st_arg[3 * kMaxGamma + 1];
   int tok[kMaxGamma];
   float g1p[kMaxGamma], g1q[kMaxGamma];
+  float g2p[kMaxGamma], g2q[kMaxGamma];  // M_2 and M_1 logits at drafted token i (i < min(g1, g2))
+  float u1[kMaxGamma], u2[kMaxGamma], v1, v2;  // the call's uniforms (sampling)
   int err, a1, a2;
 };
 
@@ -356,11 +361,18 @@ struct CascadeOut {
 
 template <typename T>
 __device__ void cascade_inputs(const CascadeParams& P, int b, CascadeSmem& cs, bool sampling) {
-  const int g1 = P.g1, tid = threadIdx.x;
+  const int g1 = P.g1, g2 = P.g2, tid = threadIdx.x;
   if (tid == 0) cs.err = 0;
   __syncthreads();
+  if (sampling && tid == kThreads - 1) {
+    cs.v1 = P.v1[b];
+    cs.v2 = P.v2[b];
+  }
+  if (sampling && tid < g2) cs.u2[tid] = P.u2[static_cast<long long>(b) * g2 + tid];
   if (tid < g1) {
     const long long b0 = static_cast<long long>(b) * g1, b1 = static_cast<long long>(b) * (g1 + 1);
+    const long long b2 = static_cast<long long>(b) * g2;
+    if (sampling) cs.u1[tid] = P.u1[b0 + tid];
     const int t = P.tokens[b0 + tid];
     cs.tok[tid] = t;
     if (t < 0 || t >= P.V) {
@@ -368,6 +380,10 @@ __device__ void cascade_inputs(const CascadeParams& P, int b, CascadeSmem& cs, b
     } else if (sampling) {
       cs.g1p[tid] = load_elem(static_cast<const T*>(P.l1) + (b1 + tid) * P.ld + t);
       cs.g1q[tid] = load_elem(static_cast<const T*>(P.l0) + (b0 + tid) * P.ld + t);
+      if (tid < g2) {  // stage 2 tests drafted token i at position i while i < a1
+        cs.g2p[tid] = load_elem(static_cast<const T*>(P.l2) + (b2 + tid) * P.ld + t);
+        cs.g2q[tid] = cs.g1p[tid];
+      }
     }
   }
 }
@@ -442,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 4) cascade_walk_kernel(const StatsPa
   if (warp == 0) {
     bool keep = true;
     if (lane < g1)
-      keep = keeps(P.u1[b0 + lane], ratio(cs.g1p[lane], cs.st_m[r1 + lane], cs.st_s[r1 + lane], cs.g1q[lane],
+      keep = keeps(cs.u1[lane], ratio(cs.g1p[lane], cs.st_m[r1 + lane], cs.st_s[r1 + lane], cs.g1q[lane],
                                          cs.st_m[lane], cs.st_s[lane], c));
     const unsigned rej = __ballot_sync(0xffffffffu, lane < g1 && !keep);
     if (lane == 0) cs.a1 = rej ? __ffs(rej) - 1 : g1;
@@ -454,17 +470,17 @@ __global__ void __launch_bounds__(kThreads, 4) cascade_walk_kernel(const StatsPa
                              a1 < g1 ? cs.st_s[a1] : 1.f, 1.f, c);
   int buf = 0, flag = 0;
   const DF Z1 = pass_or_fallback(S1, G.V, c, G.ntiles, &buf, &flag, ps);
-  const int t1 = cluster_draw(S1, G.V, c, G.ntiles, buf, df_mul_f(Z1, P.v1[b]), true, ps);
+  const int t1 = cluster_draw(S1, G.V, c, G.ntiles, buf, df_mul_f(Z1, cs.v1), true, ps);
 
   // stage 2: M_2 verifies the first w2 tokens of O_1 = d[0, a1) ++ t1 against M_1
   const int w2 = min(g2, a1 + 1);
   if (warp == 0) {
     bool keep = true;
     if (lane < w2) {
-      const int o = lane < a1 ? cs.tok[lane] : t1;
-      const float xp = load_elem(L2 + (b2 + lane) * P.ld + o);
-      const float xq = load_elem(L1 + (b1 + lane) * P.ld + o);
-      keep = keeps(P.u2[b2 + lane],
+      // drafted tokens' logits were loaded with the inputs; only t1's is new
+      const float xp = lane < a1 ? cs.g2p[lane] : load_elem(L2 + (b2 + lane) * P.ld + t1);
+      const float xq = lane < a1 ? cs.g2q[lane] : load_elem(L1 + (b1 + lane) * P.ld + t1);
+      keep = keeps(cs.u2[lane],
                    ratio(xp, cs.st_m[r2 + lane], cs.st_s[r2 + lane], xq, cs.st_m[r1 + lane], cs.st_s[r1 + lane], c));
     }
     const unsigned rej = __ballot_sync(0xffffffffu, lane < w2 && !keep);
@@ -481,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 4) cascade_walk_kernel(const StatsPa
                              cs.st_m[r1 + a2], cs.st_s[r1 + a2], 1.f, c);
   buf ^= 1;
   const DF Z2 = pass_or_fallback(S2, G.V, c, G.ntiles, &buf, &flag, ps);
-  const int t2 = cluster_draw(S2, G.V, c, G.ntiles, buf, df_mul_f(Z2, P.v2[b]), false, ps);
+  const int t2 = cluster_draw(S2, G.V, c, G.ntiles, buf, df_mul_f(Z2, cs.v2), false, ps);
   if (t2 < 0) return;
   if (tid == 0) out.write(a1, t1, a2, w2, t2, 1, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0));
 }

@@ -248,8 +248,6 @@ struct PassSmem {
   float warp_excl[kWarps];
   float thr_incl[kThreads];
   float all[2][kMaxTiles];  // tile sums of a whole pass, double-buffered
-  DF slice[2][kMaxCluster]; // total of each CTA's slice of tiles, double-buffered
-  DF lane_blk[32];          // sum of each lane's block of tiles of one slice
   uint64_t bar[kStages];    // one mbarrier per stage buffer
   uint64_t xbar[2];         // tile-sum exchange between the CTAs of the cluster
   uint64_t lbar;            // loads of a resident slice
@@ -309,13 +307,47 @@ __device__ __forceinline__ void stage_load8(const unsigned char* row, int j, uin
   }
 }
 
-// Staged path: full tiles [t0, t1) of rows whose addresses are 16-byte
-// aligned.  Thread 0 streams the tiles through kStages shared-memory buffers
-// with bulk copies (one mbarrier per buffer, up to kStages in flight) while
-// all threads compute the tiles already landed.  A buffer is refilled only
-// after the barrier that ends the computation on it.
+// Elements [0, Vv) of a row come in whole 16-byte vectors: what a bulk copy
+// of an aligned row can bring; elements [Vv, V) are read one by one.
 template <typename T>
-__device__ void staged_sums(const PassSpec<T>& S, float c, int t0, int t1, float* out, PassSmem& sh) {
+__device__ __forceinline__ int vector_end(int V) {
+  constexpr int E = 16 / static_cast<int>(sizeof(T));
+  return V / E * E;
+}
+
+// This thread's 8 elements of tile `tile` of a staged row whose copy in
+// `row` (local tile j) holds its elements below vector_end(V): elements in
+// [Vv, V) are loaded from the row in global memory `g`, elements >= V are
+// -inf.  Used for a row's last, partial tile.
+template <typename T>
+__device__ __forceinline__ void stage_load8_tail(const unsigned char* row, int j, const T* g, int tile, int V,
+                                                 float* x) {
+  const int Vv = vector_end<T>(V);
+  const int e0 = tile * kTileElems + 8 * threadIdx.x;
+  const T* s = reinterpret_cast<const T*>(row) + j * kTileElems + 8 * threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int idx = e0 + e;
+    float v = -kInf;
+    if (idx < Vv) {
+      if constexpr (sizeof(T) == 2) v = __uint_as_float(static_cast<uint32_t>(s[e]) << 16);
+      else v = s[e];
+    } else if (idx < V) {
+      v = load_elem(g + idx);
+    }
+    x[e] = v;
+  }
+}
+
+// Staged path: tiles [t0, t1) of rows whose addresses are 16-byte aligned,
+// the row's last tile included even when it is partial (its whole vectors
+// come by bulk copy, the rest by plain loads).  Thread 0 streams the tiles
+// through kStages shared-memory buffers with bulk copies (one mbarrier per
+// buffer, up to kStages in flight) while all threads compute the tiles
+// already landed.  A buffer is refilled only after the barrier that ends the
+// computation on it.
+template <typename T>
+__device__ void staged_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, float* out, PassSmem& sh) {
   constexpr int TPS = kStageRowBytes / (kTileElems * static_cast<int>(sizeof(T)));  // tiles per stage
   static_assert(TPS >= 1 && TPS <= kMaxBatch, "stage geometry");
   constexpr int R = Load8<T>::kRegs;
@@ -323,12 +355,15 @@ __device__ void staged_sums(const PassSpec<T>& S, float c, int t0, int t1, float
   const bool useQ = S.cq != 0.f;
   const int nst = (t1 - t0 + TPS - 1) / TPS;
   const int g0 = sh.staged;  // global number of this pass's first stage
+  const int Vv = vector_end<T>(V);
   auto issue = [&](int k) {  // thread 0
     const int ta = t0 + k * TPS, te = min(t1, ta + TPS);
-    const unsigned bytes = static_cast<unsigned>((te - ta) * kTileElems * sizeof(T));
+    // whole vectors of tiles [ta, te): a multiple of 16 bytes, possibly 0
+    const unsigned bytes = static_cast<unsigned>((min(te * kTileElems, Vv) - ta * kTileElems) * sizeof(T));
     const int b = (g0 + k) % kStages;
     unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
     mbar_expect_tx(&sh.bar[b], useQ ? 2 * bytes : bytes);
+    if (bytes == 0) return;  // the arrival alone completes the phase
     bulk_load(buf, S.P + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
     if (useQ) bulk_load(buf + kStageRowBytes, S.Q + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
   };
@@ -350,13 +385,18 @@ __device__ void staged_sums(const PassSpec<T>& S, float c, int t0, int t1, float
 #pragma unroll
     for (int j = 0; j < TPS; ++j) {
       if (j < nb) {
-        uint32_t rp[R], rq[R];
         float xp[8], xq[8], w[8];
-        stage_load8<T>(buf, j, rp);
-        Load8<T>::get(rp, xp);
-        if (useQ) {
-          stage_load8<T>(buf + kStageRowBytes, j, rq);
-          Load8<T>::get(rq, xq);
+        if ((ta + j + 1) * kTileElems <= Vv) {
+          uint32_t rp[R], rq[R];
+          stage_load8<T>(buf, j, rp);
+          Load8<T>::get(rp, xp);
+          if (useQ) {
+            stage_load8<T>(buf + kStageRowBytes, j, rq);
+            Load8<T>::get(rq, xq);
+          }
+        } else {  // the row's last tile, partial
+          stage_load8_tail<T>(buf, j, S.P, ta + j, V, xp);
+          if (useQ) stage_load8_tail<T>(buf + kStageRowBytes, j, S.Q, ta + j, V, xq);
         }
         pass_weights(S, c, xp, xq, w);
         const float incl = warp_incl_scan(sum8(w));
@@ -529,21 +569,18 @@ __device__ void resident_sums(const PassSpec<T>& S, float c, int t0, int t1, flo
 }
 
 // Sums of tiles [t0, t1) into out[t0 .. t1) (shared memory).  All threads
-// call it; out[] is complete when it returns.  Full tiles of aligned rows go
-// through the staged path, the rest through the register path.
+// call it; out[] is complete when it returns.  Tiles of aligned rows go
+// through the staged path, tiles of misaligned rows through the register
+// path.
 template <typename T>
 __device__ void tile_sums(const PassSpec<T>& S, int V, float c, int t0, int t1, float* out, PassSmem& sh) {
   const bool useQ = S.cq != 0.f;
   const bool aligned = row_is_aligned(S.P) && (!useQ || row_is_aligned(S.Q));
-  int tb = t0;
-  if (aligned) {
-    const int tf = max(t0, min(t1, V / kTileElems));  // tiles before tf are full
-    if (tf > t0) staged_sums(S, c, t0, tf, out, sh);
-    tb = tf;
-  }
-  if (tb < t1) {
-    __syncthreads();  // the warp-total ring restarts at slot 0
-    direct_sums(S, V, c, tb, t1, out, sh);
+  if (t1 <= t0) {
+  } else if (aligned) {
+    staged_sums(S, V, c, t0, t1, out, sh);
+  } else {
+    direct_sums(S, V, c, t0, t1, out, sh);
   }
   __syncthreads();
 }
@@ -555,49 +592,42 @@ __device__ __forceinline__ void lane_block(int ntiles, int lane, int& j0, int& j
   j1 = min(ntiles, j0 + per);
 }
 
-// Tiles [j0, j1) of the slice [s0, s0 + m) handled by one lane: the slice is
-// cut into at most 32 contiguous blocks.
-__device__ __forceinline__ void lane_block(int s0, int m, int lane, int& j0, int& j1, int& nblocks) {
-  const int per = max(1, (m + 31) / 32);
-  j0 = s0 + min(m, lane * per);
-  j1 = s0 + min(m, (lane + 1) * per);
-  nblocks = (m + per - 1) / per;
-}
-
-// Double-float sum of the tile sums all[s0 .. s0 + m), one warp: each lane
-// adds its block in order and publishes it, then every lane adds the block
-// sums in order (broadcast reads).  Every lane returns the same value.
-__device__ DF slice_sum(const float* all, int s0, int m, PassSmem& sh) {
+// Inclusive double-float scan of the tile sums all[0 .. ntiles) by one warp:
+// lane l adds the tiles of its block [j0, j1) in order, the block sums are
+// scanned across the lanes by shuffles (a fixed order), and each lane gets
+// the prefix before its block in *excl.  Returns the total to every lane.
+// Every warp that runs it on the same tile sums gets the same bits.
+__device__ DF warp_tile_scan(const float* all, int ntiles, DF* excl) {
   const int lane = threadIdx.x & 31;
-  int j0, j1, nb;
-  lane_block(s0, m, lane, j0, j1, nb);
-  DF run{0.f, 0.f};
-  for (int j = j0; j < j1; ++j) run = df_add_f(run, all[j]);
-  sh.lane_blk[lane] = run;
-  __syncwarp();
-  DF acc{0.f, 0.f};
-  for (int l = 0; l < nb; ++l) acc = df_add(acc, sh.lane_blk[l]);
-  __syncwarp();  // lane_blk is reused by the next call
-  return acc;
+  int j0, j1;
+  lane_block(ntiles, lane, j0, j1);
+  DF blk{0.f, 0.f};
+  for (int j = j0; j < j1; ++j) blk = df_add_f(blk, all[j]);
+  DF incl = blk;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y = df_shfl_up(incl, o);
+    if (lane >= o) incl = df_add(y, incl);
+  }
+  const DF prev = df_shfl_up(incl, 1);
+  *excl = lane == 0 ? DF{0.f, 0.f} : prev;
+  return {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
 }
-
-__device__ __forceinline__ bool df_gt(DF a, DF b) { return df_add(a, df_neg(b)).hi > 0.f; }
 
 // One pass split over the CTAs of the cluster (from the resident slice when
 // `resident`, which then holds this CTA's tiles of the pass's rows).  CTA
-// `rank` sums its slice of the tiles (tile sums into sh.all[buf], their
-// total into sh.slice[buf][rank]) and sends both to every other CTA of the
-// cluster by asynchronous stores that count on the receiver's exchange
-// barrier (warp 0); once its own barrier has every peer's bytes, each CTA
-// holds every tile sum and slice total.
-// Returns the pass total, the slice totals added in slice order (bit-
-// identical in every CTA).  Every CTA of the cluster calls it with the same
-// pass.  Consecutive passes alternate `buf` and the exchange barrier: a CTA
-// can send into a peer's buffer or barrier again only after it has received
-// that peer's data for the next pass, which the peer sends after it has
-// finished reading this one (fault states are not double-buffered: they only
-// go from 0 to 1, so reading a later one is harmless).  A wait that gives up
-// sets the fault state instead of hanging.
+// `rank` sums its slice of the tiles into sh.all[buf] and sends the sums to
+// every other CTA of the cluster by asynchronous stores that count on the
+// receiver's exchange barrier (warp 0); once its own barrier has every
+// peer's bytes, each CTA holds every tile sum.
+// Returns the pass total, the warp_tile_scan total of all tile sums (the
+// same bits in every warp of every CTA).  Every CTA of the cluster calls it
+// with the same pass.  Consecutive passes alternate `buf` and the exchange
+// barrier: a CTA can send into a peer's buffer or barrier again only after
+// it has received that peer's data for the next pass, which the peer sends
+// after it has finished reading this one (fault states are not
+// double-buffered: they only go from 0 to 1, so reading a later one is
+// harmless).  A wait that gives up sets the fault state instead of hanging.
 template <typename T>
 __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int buf, PassSmem& sh,
                            bool resident = false) {
@@ -605,22 +635,21 @@ __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int
   const int rank = static_cast<int>(cluster_rank()), n = static_cast<int>(cluster_size());
   const int tpc = (ntiles + n - 1) / n;
   const int t0 = min(ntiles, rank * tpc), t1 = min(ntiles, t0 + tpc);
-  const int x = sh.exchanges;  // stable: updated only after the barriers below
   float* all = sh.all[buf];
   if (resident) resident_sums(S, c, t0, t1, all, sh);
   else tile_sums(S, V, c, t0, t1, all, sh);
-  if (tid < 32) {
-    const DF mine = slice_sum(all, t0, t1 - t0, sh);
-    if (n > 1) {
-      // every peer's tile sums, slice total and fault state arrive by
-      // asynchronous stores counted on this CTA's exchange barrier
+  if (n > 1) {
+    int x = 0;  // exchanges completed before this one (thread 0 keeps the count)
+    if (tid < 32) {
+      x = __shfl_sync(0xffffffffu, sh.exchanges, 0);
+      // every peer's tile sums and fault state arrive by asynchronous stores
+      // counted on this CTA's exchange barrier
       uint64_t* xb = &sh.xbar[x & 1];
       if (tid == 0) {
         unsigned expect = 0;
         for (int d = 0; d < n; ++d)
-          if (d != rank) expect += 4u * static_cast<unsigned>(min(ntiles, d * tpc + tpc) - min(ntiles, d * tpc)) + 12u;
+          if (d != rank) expect += 4u * static_cast<unsigned>(min(ntiles, d * tpc + tpc) - min(ntiles, d * tpc)) + 4u;
         mbar_expect_tx(xb, expect);
-        sh.slice[buf][rank] = mine;
         sh.flt[rank] = sh.fault;
       }
       const int nt = t1 - t0;
@@ -630,77 +659,43 @@ __device__ DF cluster_pass(const PassSpec<T>& S, int V, float c, int ntiles, int
         if (d >= rank) ++d;
         st_async_cluster(all + t0 + k, static_cast<unsigned>(d), __float_as_uint(all[t0 + k]), xb);
       }
-      if (tid < n && tid != rank) {
-        st_async_cluster(&sh.slice[buf][rank].hi, static_cast<unsigned>(tid), __float_as_uint(mine.hi), xb);
-        st_async_cluster(&sh.slice[buf][rank].lo, static_cast<unsigned>(tid), __float_as_uint(mine.lo), xb);
+      if (tid < n && tid != rank)
         st_async_cluster(&sh.flt[rank], static_cast<unsigned>(tid), static_cast<uint32_t>(sh.fault), xb);
-      }
       if (!mbar_wait_cluster(xb, (x >> 1) & 1)) sh.fault = 1;
-    } else if (tid == 0) {
-      sh.slice[buf][0] = mine;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int f = sh.fault;
+      for (int r = 0; r < n; ++r) f |= sh.flt[r];
+      sh.fault = f;
+      sh.exchanges = x + 1;
     }
   }
-  __syncthreads();
-  if (n > 1 && tid == 0) {
-    int f = sh.fault;
-    for (int r = 0; r < n; ++r) f |= sh.flt[r];
-    sh.fault = f;
-    sh.exchanges = x + 1;
-  }
-  DF z{0.f, 0.f};
-  for (int r = 0; r < n; ++r) z = df_add(z, sh.slice[buf][r]);
-  return z;
+  DF excl;
+  return warp_tile_scan(all, ntiles, &excl);
 }
 
 __device__ __forceinline__ bool pass_ok(DF z) { return z.hi > 0.f && z.hi < kInf; }
 
 // Inverse-CDF draw from a pass given as tile sums `all` (ntiles, shared
-// memory) and the totals `slices` of its n slices of tpc = ceil(ntiles / n)
-// tiles: the first index whose running sum exceeds `target`.  The prefix
-// before a tile is the slice totals before its slice plus the tile sums
-// before it in its slice (double-float, in order).  The owning slice is the
-// first slice with mass whose end passes the target (else the last slice
-// with mass); in it, with E_j the prefix before tile j and r_j = target -
-// E_j rounded to float, the drawn tile is the first tile with mass whose sum
-// exceeds r_j (else the last tile with mass), and inside the tile the first
-// element whose float running sum exceeds r_j (else its last element with
-// mass).
+// memory): the first index whose running sum exceeds `target`.  With E_j
+// the prefix before tile j (warp_tile_scan's block prefix plus the tile
+// sums before j in the block, double-float) and r_j = target - E_j rounded
+// to float, the drawn tile is the first tile with mass whose sum exceeds r_j
+// (else the last tile with mass), and inside the tile the first element
+// whose float running sum exceeds r_j (else its last element with mass).
 //
-// locate_tile finds the slice and tile (warp 0; every CTA gets the same
-// result); draw_in_tile recomputes that tile with the same code as the pass
-// and returns the index to all threads.
-__device__ void locate_tile(const float* all, const DF* slices, int n, int ntiles, DF target, PassSmem& sh) {
+// locate_tile finds the tile (warp 0; every CTA gets the same result) and
+// the CTA of the cluster (of n) whose slice holds it; draw_in_tile
+// recomputes that tile with the same code as the pass and returns the index
+// to all threads.
+__device__ void locate_tile(const float* all, int n, int ntiles, DF target, PassSmem& sh) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int tpc = (ntiles + n - 1) / n;
   if (tid < 32) {
-    // the owning slice (every lane computes the same)
-    DF E{0.f, 0.f}, Ef{0.f, 0.f}, El{0.f, 0.f};
-    int rf_ = -1, rl = -1;
-    for (int r = 0; r < n; ++r) {
-      const DF Tr = slices[r];
-      if (Tr.hi > 0.f) {
-        if (rf_ < 0 && df_gt(df_add(E, Tr), target)) {
-          rf_ = r;
-          Ef = E;
-        }
-        rl = r;
-        El = E;
-      }
-      E = df_add(E, Tr);
-    }
-    bool last_mode = rf_ < 0;
-    const int owner = last_mode ? max(rl, 0) : rf_;
-    const DF Eo = last_mode ? El : Ef;
-    // inside the slice: blocks of tiles, then the tiles of one block
-    const int s0 = min(ntiles, owner * tpc), m = min(ntiles, s0 + tpc) - s0;
-    int j0, j1, nb;
-    lane_block(s0, m, lane, j0, j1, nb);
-    DF run{0.f, 0.f};
-    for (int j = j0; j < j1; ++j) run = df_add_f(run, all[j]);
-    sh.lane_blk[lane] = run;
-    __syncwarp();
-    DF e = Eo;
-    for (int l = 0; l < min(lane, nb); ++l) e = df_add(e, sh.lane_blk[l]);
+    DF e;
+    warp_tile_scan(all, ntiles, &e);
+    int j0, j1;
+    lane_block(ntiles, lane, j0, j1);
     int first = 0x7fffffff, last = -1;
     float rf_first = 0.f, rf_last = 0.f;
     for (int j = j0; j < j1; ++j) {
@@ -716,7 +711,7 @@ __device__ void locate_tile(const float* all, const DF* slices, int n, int ntile
       }
       e = df_add_f(e, s);
     }
-    const int fmin = last_mode ? 0x7fffffff : __reduce_min_sync(0xffffffffu, first);
+    const int fmin = __reduce_min_sync(0xffffffffu, first);
     const int lmax = __reduce_max_sync(0xffffffffu, last);
     if (fmin != 0x7fffffff) {
       if (first == fmin) {
@@ -732,13 +727,14 @@ __device__ void locate_tile(const float* all, const DF* slices, int n, int ntile
         sh.last_mode = 1;
         sh.thread = -1;
       }
-    } else if (lane == 0) {
-      sh.tile = min(s0, ntiles - 1);
+    } else if (lane == 0) {  // no mass at all (the callers rule this out)
+      sh.tile = 0;
       sh.rf = 0.f;
       sh.last_mode = 1;
       sh.thread = -1;
     }
-    if (lane == 0) sh.owner = owner;
+    __syncwarp();
+    if (lane == 0) sh.owner = sh.tile / ((ntiles + n - 1) / n);
   }
   __syncthreads();
 }
@@ -793,13 +789,13 @@ __device__ int draw_in_tile(const PassSpec<T>& S, int V, float c, PassSmem& sh) 
   return sh.result;
 }
 
-// The draw from a cluster pass (sh.all[buf] / sh.slice[buf]): every CTA
+// The draw from a cluster pass (the tile sums in sh.all[buf]): every CTA
 // locates the tile; the CTA owning its slice, or every CTA when all_ctas is
 // set, recomputes the tile and returns the index; the others return -1.
 template <typename T>
 __device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, int buf, DF target,
                             bool all_ctas, PassSmem& sh) {
-  locate_tile(sh.all[buf], sh.slice[buf], static_cast<int>(cluster_size()), ntiles, target, sh);
+  locate_tile(sh.all[buf], static_cast<int>(cluster_size()), ntiles, target, sh);
   if (!all_ctas && sh.owner != static_cast<int>(cluster_rank())) return -1;
   return draw_in_tile(S, V, c, sh);
 }
