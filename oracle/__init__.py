@@ -12,10 +12,12 @@ Modules
                   written step by step in float64 NumPy, one sequence at a time.
 ``closed_forms``  the PipeSpec analytical model (expected tokens per step,
                   steady-state verification probability and its recurrence).
+``compact``       the cache compaction after a tree verification (the kept
+                  root path's rows moved to contiguous positions).
 
 Every function states the passage it follows.  Points where the pages are
 silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import closed_forms, verify  # noqa: F401
+from . import closed_forms, compact, verify  # noqa: F401
