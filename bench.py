@@ -55,7 +55,9 @@ KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification
 # the kernels of one call (statistics, then walk); greedy calls use the
 # greedy walk kernels
 KERNELS = {"chain": ["stats_kernel", "chain_walk_kernel"], "tree": ["stats_kernel", "tree_kernel"],
-           "cascade": ["stats_kernel", "cascade_walk_kernel"]}
+           "cascade": ["stats_kernel", "cascade_walk_kernel"], "compact": ["compact_kernel"]}
+COMPACT_METRIC = "cache rows compacted/sec and GB/s moved vs GB300 HBM peak (1 GPU)"
+COMPACT_SOURCES = ["draft_verification_gb300/csrc/compact.cu"]
 
 
 def parse():
@@ -142,18 +144,18 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in KERNEL_SOURCES if sources is None else sources:
         with open(os.path.join(ROOT, p), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes of one verification call (both kernels, caches flushed) from
-    the committed ncu launch-list summary, if it was taken on the current
-    kernel source; else None."""
+def profiled_traffic(workload: str, sources=None):
+    """DRAM bytes of one call (all its kernels, caches flushed) from the
+    committed ncu launch-list summary, if it was taken on the current kernel
+    source; else None."""
     path = os.path.join(ROOT, "profiles", f"launches_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -163,7 +165,7 @@ def profiled_traffic(workload: str):
             if line.startswith("- ") and " = " in line:
                 k, v = line[2:].split(" = ", 1)
                 fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_hash") != kernel_source_hash():
+    if fields.get("source_hash") != kernel_source_hash(sources):
         return None
     try:
         return int(float(fields["dram_bytes_per_call"]))
@@ -509,6 +511,195 @@ def e2e_rate(args, w, dev, stream):
             "ms_per_step": 1000.0 * el / n, "steps": n}
 
 
+# --------------------------------------------------------------------------
+# cache compaction after a tree verification (a workload of its own)
+# --------------------------------------------------------------------------
+
+def compact_rows(w) -> int:
+    """Cache rows one compaction call writes (the root and the kept nodes of
+    every sequence the verifier did not flag)."""
+    ok = w["path_nodes"][:, 0] >= 0
+    return int(np.sum(np.where(ok, w["path_len"] + 1, 0)))
+
+
+def compact_bytes(w) -> int:
+    """Algorithmic bytes of one call: every written row read once and written once."""
+    return 2 * compact_rows(w) * w["spec"].row_bytes
+
+
+def compact_oracle_rate(w, budget_s: float):
+    from oracle import compact as K  # the reference is only used on this leg
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        K.compact_tree_path(w["tree_rows"], w["cache"], w["path_nodes"], w["path_len"], w["prefix_len"])
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return compact_rows(w) * calls / el, f"{calls} whole calls ({el:.1f} s, NumPy row copies)"
+
+
+def compact_config(w) -> dict:
+    s = w["spec"]
+    return {"workload": s.name, "kind": "compact", "batch": s.B, "tree_nodes": int(len(w["parent"])),
+            "max_depth": s.max_depth, "row_bytes": s.row_bytes, "cache_rows": int(w["cache"].shape[1]),
+            "rows_per_call": compact_rows(w)}
+
+
+def run_compact(args, w):
+    import torch
+    import draft_verification_gb300 as dv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dv.build_library()
+    s = w["spec"]
+    W = s.row_bytes
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    moved = compact_bytes(w)
+    set_bytes = w["tree_rows"].nbytes + w["cache"].nbytes
+    n_sets = max(2, math.ceil(3 * l2 / max(moved, 1)) + 1)
+    n_sets = min(n_sets, max(2, int(0.5 * props.total_memory // max(set_bytes, 1))))
+    tree0 = torch.from_numpy(w["tree_rows"]).to(dev)
+    cache0 = torch.from_numpy(w["cache"]).to(dev)
+    paths = {k: torch.from_numpy(np.ascontiguousarray(w[k])).to(dev) for k in ("path_nodes", "path_len", "prefix_len")}
+    sets = [(tree0, cache0)] + [(tree0.clone(), cache0.clone()) for _ in range(n_sets - 1)]
+    stream = torch.cuda.Stream(dev)
+
+    def call(i):
+        t, c = sets[i]
+        dv.compact_tree_path(t[:, :, :W], c[:, :, :W], paths["path_nodes"], paths["path_len"],
+                             paths["prefix_len"], stream=stream)
+
+    def one_pass():
+        for i in range(n_sets):
+            call(i)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            call(i % n_sets)
+    stream.synchronize()
+    launch = "cuda_graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            one_pass()
+        stream.synchronize()
+    except Exception as exc:
+        launch = f"eager ({type(exc).__name__})"
+        graph = None
+
+    def run_steps(k):
+        full, rest = divmod(k, n_sets)
+        for _ in range(full):
+            if graph is not None:
+                graph.replay()
+            else:
+                one_pass()
+        for i in range(rest):
+            call(i)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            run_steps(n_sets * 20)
+            stream.synchronize()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end through the public call: host tree rows, cache and paths
+    # in, the cache back out, every step
+    host = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory()
+            for k in ("tree_rows", "cache", "path_nodes", "path_len", "prefix_len")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host["cache"].numel()
+    out = torch.empty_like(host["cache"]).pin_memory()
+
+    def e2e_call():
+        with torch.cuda.stream(stream):
+            d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+            dv.compact_tree_path(d["tree_rows"][:, :, :W], d["cache"][:, :, :W], d["path_nodes"], d["path_len"],
+                                 d["prefix_len"], stream=stream)
+            out.copy_(d["cache"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_call()
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        e2e_call()
+    el = time.perf_counter() - t0
+
+    rows = compact_rows(w)
+    peak, peak_src = measured_peak()
+    gbs = moved / (ms * 1e-3) / 1e9
+    return {
+        "metric": COMPACT_METRIC, "value": rows / (ms * 1e-3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded random bytes; root paths drawn on the 64-node tree)",
+        "config": dict(compact_config(w), parallelism="1 GPU", launch=launch,
+                       l2_policy=f"rotating {n_sets} copies of tree rows and cache "
+                                 f"({n_sets * moved / 2**20:.0f} MB moved per rotation > 3 x L2 {l2 / 2**20:.0f} MB)"),
+        "roofline": {"bound": "hbm", "kernel": "compact_kernel", "unit_of_work": "one compaction call",
+                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
+                     "kernel_ms": ms, "algorithmic_bytes": moved,
+                     "traffic": profiled_traffic(s.name, COMPACT_SOURCES)},
+        "e2e": {"value": rows / (el / n), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+
+
+def compact_main(args, w, rank):
+    if args.impl == "reference":
+        if rank == 0:
+            rate, desc = compact_oracle_rate(w, args.cpu_seconds)
+            print(json.dumps({
+                "impl": "reference", "metric": COMPACT_METRIC, "value": rate, "unit": "rows/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * compact_rows(w) / rate, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "u8", "data": "synthetic", "config": compact_config(w),
+                "cpu_baseline": {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc},
+                "e2e": {"value": rate, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+        return
+    if args.profile:
+        import torch
+        import draft_verification_gb300 as dv
+        dev = torch.device("cuda", 0)
+        dv.build_library()
+        W = w["spec"].row_bytes
+        tree = torch.from_numpy(w["tree_rows"]).to(dev)
+        cache = torch.from_numpy(w["cache"]).to(dev)
+        p = {k: torch.from_numpy(np.ascontiguousarray(w[k])).to(dev) for k in ("path_nodes", "path_len", "prefix_len")}
+        for _ in range(args.warmup + args.steps):
+            dv.compact_tree_path(tree[:, :, :W], cache[:, :, :W], p["path_nodes"], p["path_len"], p["prefix_len"])
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": w["spec"].name, "calls": args.warmup + args.steps}))
+        return
+    if rank != 0:
+        return  # one GPU: the other ranks of a replica launch have nothing to add
+    line = run_compact(args, w)
+    if not args.no_cpu_baseline:
+        rate, desc = compact_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
 def run_profile(args, w):
     """W + K eager calls on one input copy, nothing else (an ncu target)."""
     import torch
@@ -527,8 +718,12 @@ def main():
     from workloads import synth
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.workload in synth.COMPACT_SPECS:
+        compact_main(args, synth.make(synth.COMPACT_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
+        return
     if args.workload not in synth.SPECS:
-        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.SPECS)}")
+        raise SystemExit(f"unknown workload {args.workload}; choose from "
+                         f"{sorted(synth.SPECS) + sorted(synth.COMPACT_SPECS)}")
     w = synth.make(synth.SPECS[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":

@@ -62,6 +62,15 @@ class CascadeArgs(C.Structure):
     ]
 
 
+class CompactArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("N", C.c_int), ("max_depth", C.c_int), ("cache_rows", C.c_int),
+        ("row_bytes", C.c_longlong), ("tree_ld", C.c_longlong), ("cache_ld", C.c_longlong),
+        ("tree_rows", _vp), ("cache", _vp), ("path_nodes", _vp), ("path_len", _vp),
+        ("prefix_len", _vp), ("seq_error", _vp), ("error_word", _vp)
+    ]
+
+
 # every symbol include/spec_verify.h declares, with its ctypes signature
 SIGNATURES = {
     "spec_chain_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
@@ -71,6 +80,7 @@ SIGNATURES = {
     "spec_verify_tree": (C.c_int, [C.POINTER(TreeArgs), _vp]),
     "spec_cascade_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spec_verify_cascade": (C.c_int, [C.POINTER(CascadeArgs), _vp]),
+    "spec_compact_tree_path": (C.c_int, [C.POINTER(CompactArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
 }
 

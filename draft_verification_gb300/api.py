@@ -290,6 +290,43 @@ def verify_cascade(l0, l1, l2, tokens, u1=None, v1=None, u2=None, v2=None, base0
     return _finish(plan.run(stream), host)
 
 
+def _byte_rows(t: torch.Tensor, name: str):
+    """(rows per sequence, row bytes, row stride in bytes) of a uint8 tensor
+    [B, R, W] whose last dimension is contiguous."""
+    if t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1 or t.stride(0) != t.shape[1] * t.stride(1):
+        raise TypeError(f"{name}: expected a uint8 tensor [B, rows, W] with contiguous rows "
+                        "(row stride >= W, sequences back to back)")
+    return t.shape[1], t.shape[2], t.stride(1)
+
+
+def compact_tree_path(tree_rows, cache, path_nodes, path_len, prefix_len=None, stream=None):
+    """Move each sequence's kept tree path into its contiguous cache, in place.
+
+    tree_rows uint8 [B, N, W] (one row per tree node), cache uint8 [B, C, W]
+    (written in place), path_nodes int32 [B, max_depth+1] and path_len int32
+    [B] as returned by verify_tree, prefix_len int32 [B] or None.  Returns the
+    per-sequence error bits (int32 [B]: 0, or ERR_PARENT for a malformed path).
+    See spec_compact_tree_path.
+    """
+    lib = L.lib()
+    B = tree_rows.shape[0]
+    N, W, tree_ld = _byte_rows(tree_rows, "tree_rows")
+    Cr, W2, cache_ld = _byte_rows(cache, "cache")
+    if W2 != W or cache.shape[0] != B:
+        raise ValueError("tree_rows and cache: same batch and row size required")
+    path_nodes = _i32(path_nodes, "path_nodes")
+    seq_error = torch.empty(B, dtype=torch.int32, device=cache.device)
+    a = L.CompactArgs()
+    a.B, a.N, a.max_depth, a.cache_rows = B, N, path_nodes.shape[1] - 1, Cr
+    a.row_bytes, a.tree_ld, a.cache_ld = W, tree_ld, cache_ld
+    a.tree_rows, a.cache = _ptr(tree_rows), _ptr(cache)
+    a.path_nodes, a.path_len = _ptr(path_nodes), _ptr(_i32(path_len, "path_len"))
+    a.prefix_len = _ptr(_i32(prefix_len, "prefix_len"))
+    a.seq_error, a.error_word = _ptr(seq_error), None
+    _check(lib.spec_compact_tree_path(C.byref(a), _stream_handle(stream)), "compact_tree_path")
+    return seq_error
+
+
 def workspace_bytes(kind: str, *sizes) -> int:
     fn = {"chain": "spec_chain_workspace_size", "tree": "spec_tree_workspace_size",
           "cascade": "spec_cascade_workspace_size"}[kind]

@@ -251,6 +251,43 @@ typedef struct spec_cascade_args {
 size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V);
 spec_status spec_verify_cascade(const spec_cascade_args* args, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------- */
+/* Cache compaction after a tree verification.  Staged Speculative         */
+/* Decoding, abstract (the speculative batch is a tree); PipeSpec review,  */
+/* "What carries the argument" (a buffer keeps the verified prefix and is  */
+/* rolled back to the last verified token).  The verify pass wrote one row */
+/* of W bytes per tree node (e.g. every layer's keys and values of that    */
+/* node's token); this call copies the root's row to position prefix_len  */
+/* of the sequence's contiguous cache and the i-th kept node's row to      */
+/* position prefix_len + i.  No other byte of the cache changes.           */
+/*  - A sequence whose path_nodes[b][0] is -1 (the verifier's data-error   */
+/*    marking) is skipped and gets no error bit.                           */
+/*  - A path length outside [0, max_depth], a node outside [0, N) or a     */
+/*    destination past position C - 1 is a malformed path: the sequence    */
+/*    is skipped (nothing written) and gets SPEC_ERR_PARENT.               */
+/*  - Rows move as 16-byte vectors when W, both row strides and both base  */
+/*    addresses are multiples of 16, otherwise byte by byte.               */
+/*  - The tree rows and the cache must not overlap.  One kernel launch.    */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_compact_args {
+  int B;                       /* sequences, 1..65535                              */
+  int N;                       /* tree nodes per sequence, >= 1                    */
+  int max_depth;               /* path_nodes has max_depth + 1 columns, 0..65534  */
+  int cache_rows;              /* C: cache positions per sequence, >= 1            */
+  long long row_bytes;         /* W: bytes per row, >= 1                           */
+  long long tree_ld;           /* bytes between consecutive node rows, >= W        */
+  long long cache_ld;          /* bytes between consecutive cache positions, >= W  */
+  const void* tree_rows;       /* [B][N] rows; sequence b starts at b * N * tree_ld */
+  void* cache;                 /* in/out [B][C] rows; sequence b at b * C * cache_ld */
+  const int* path_nodes;       /* [B, max_depth+1] (spec_verify_tree's output)     */
+  const int* path_len;         /* [B] kept nodes, the root not counted             */
+  const int* prefix_len;       /* [B] positions before the window; NULL = all 0    */
+  int* seq_error;              /* out [B], optional: 0 or SPEC_ERR_PARENT          */
+  int* error_word;             /* in/out, optional: error bits OR-ed in            */
+} spec_compact_args;
+
+spec_status spec_compact_tree_path(const spec_compact_args* args, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* spec_status_string(spec_status status);
 

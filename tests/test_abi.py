@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 8, names
+    assert len(names) == 9, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -43,7 +43,7 @@ def test_struct_layout_matches_header(tmp_path):
     if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
         pytest.skip("gcc or CUDA headers missing")
     structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
-               "spec_cascade_args": _lib.CascadeArgs}
+               "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -175,3 +175,26 @@ def test_each_kind_accepts_exactly_its_workspace_size(lib):
     assert lib.spec_verify_cascade(C.byref(c), None) == _lib.SPEC_ECUDA
     c.workspace_bytes -= 1
     assert lib.spec_verify_cascade(C.byref(c), None) == -4
+
+
+def _compact(**kw):
+    from draft_verification_gb300 import _lib
+    a = _lib.CompactArgs()
+    a.B, a.N, a.max_depth, a.cache_rows = 2, 8, 3, 16
+    a.row_bytes, a.tree_ld, a.cache_ld = 64, 64, 64
+    fake = 0x10000  # never dereferenced: every case fails validation
+    for f in ("tree_rows", "cache", "path_nodes", "path_len"):
+        setattr(a, f, fake)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value", [
+    ("B", 0), ("B", 65536), ("N", 0), ("max_depth", -1), ("max_depth", 65535), ("cache_rows", 0),
+    ("row_bytes", 0), ("tree_ld", 63), ("cache_ld", 32), ("tree_rows", None), ("cache", None),
+    ("path_nodes", None), ("path_len", None),
+])
+def test_compact_argument_errors_are_reported_before_launch(lib, field, value):
+    assert lib.spec_compact_tree_path(C.byref(_compact(**{field: value})), None) == -1
+    assert lib.spec_compact_tree_path(None, None) == -1

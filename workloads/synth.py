@@ -165,6 +165,31 @@ SPECS = {
 }
 
 
+@dataclass(frozen=True)
+class CompactSpec:
+    """Cache compaction after a tree verification: B sequences, each with one
+    row of row_bytes per tree node (the tree of tree_topology) and a kept root
+    path drawn by walking from the root, keeping a random child with
+    probability `keep` at each level (at most max_depth kept nodes)."""
+    name: str
+    B: int
+    row_bytes: int
+    max_depth: int = 6
+    keep: float = 0.7
+    max_prefix: int = 64
+    branching: tuple = (4, 3, 2, 2, 1, 1)
+    n_nodes: int = 64
+    pad: int = 0          # row stride = row_bytes + pad bytes
+
+
+# Row size: the keys and values of one token in every layer of a 32-layer
+# model with 8 key-value heads of dimension 128 in bfloat16
+# (2 x 32 x 8 x 128 x 2 B = 131072 B).
+COMPACT_SPECS = {
+    "tree_kv_compact_b16_n64_d6_w131072": CompactSpec("tree_kv_compact_b16_n64_d6_w131072", B=16, row_bytes=131072),
+}
+
+
 def with_sizes(spec, **kw):
     """A copy of a spec with some fields replaced (e.g. a smaller B or V)."""
     return dataclasses.replace(spec, **kw)
@@ -307,9 +332,40 @@ def make_cascade(spec: CascadeSpec, seed: int = 0) -> dict:
                 u1=u1, v1=v1, u2=u2, v2=v2, base0=base.copy(), base1=base.copy())
 
 
+def make_compact(spec: CompactSpec, seed: int = 0) -> dict:
+    """Compaction workload: tree_rows uint8 [B, N, W+pad], cache uint8
+    [B, C, W+pad] with C = max_prefix + max_depth + 1 (random bytes),
+    path_nodes int32 [B, max_depth+1] (root first, -1 padded), path_len int32
+    [B], prefix_len int32 [B] in [0, max_prefix), parent int32 [N]."""
+    rng = _rng(seed, 7)
+    parent = tree_topology(spec.branching, spec.n_nodes)
+    N, B, D = len(parent), spec.B, spec.max_depth
+    children = [[] for _ in range(N)]
+    for n in range(1, N):
+        children[parent[n]].append(n)
+    path_nodes = -np.ones((B, D + 1), np.int32)
+    path_len = np.zeros(B, np.int32)
+    for b in range(B):
+        node, path = 0, [0]
+        while len(path) <= D and children[node] and rng.random() < spec.keep:
+            node = int(children[node][rng.integers(0, len(children[node]))])
+            path.append(node)
+        path_nodes[b, :len(path)] = path
+        path_len[b] = len(path) - 1
+    prefix_len = rng.integers(0, spec.max_prefix, B).astype(np.int32)
+    C = spec.max_prefix + D + 1
+    width = spec.row_bytes + spec.pad
+    tree_rows = rng.integers(0, 256, (B, N, width), dtype=np.uint8)
+    cache = rng.integers(0, 256, (B, C, width), dtype=np.uint8)
+    return dict(kind="compact", spec=spec, tree_rows=tree_rows, cache=cache, path_nodes=path_nodes,
+                path_len=path_len, prefix_len=prefix_len, parent=parent)
+
+
 def make(spec, seed: int = 0) -> dict:
     if isinstance(spec, str):
-        spec = SPECS[spec]
+        spec = SPECS[spec] if spec in SPECS else COMPACT_SPECS[spec]
+    if isinstance(spec, CompactSpec):
+        return make_compact(spec, seed)
     if isinstance(spec, ChainSpec):
         return make_chain(spec, seed)
     if isinstance(spec, TreeSpec):
