@@ -14,10 +14,12 @@ Modules
                   steady-state verification probability and its recurrence).
 ``compact``       the cache compaction after a tree verification (the kept
                   root path's rows moved to contiguous positions).
+``pipeline``      the k-model PipeSpec snapshot (stages 1 .. k-1, rollback of
+                  every earlier buffer, an optional final-stage bonus).
 
 Every function states the passage it follows.  Points where the pages are
 silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import closed_forms, compact, verify  # noqa: F401
+from . import closed_forms, compact, pipeline, verify  # noqa: F401
