@@ -62,6 +62,22 @@ class CascadeArgs(C.Structure):
     ]
 
 
+SPEC_MAX_MODELS = 8
+
+
+class PipelineArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("k", C.c_int), ("window", C.c_int * (SPEC_MAX_MODELS - 1)), ("final_bonus", C.c_int),
+        ("V", C.c_int), ("ld", C.c_longlong), ("dtype", C.c_int), ("mode", C.c_int),
+        ("temperature", C.c_float),
+        ("logits", _vp * SPEC_MAX_MODELS), ("draft_tokens", _vp),
+        ("u", _vp * (SPEC_MAX_MODELS - 1)), ("v", _vp * (SPEC_MAX_MODELS - 1)), ("base", _vp),
+        ("a", _vp), ("w", _vp), ("t", _vp), ("t_valid", _vp), ("r", _vp), ("committed", _vp),
+        ("seq_error", _vp), ("error_word", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+    ]
+
+
 class CompactArgs(C.Structure):
     _fields_ = [
         ("B", C.c_int), ("N", C.c_int), ("max_depth", C.c_int), ("cache_rows", C.c_int),
@@ -80,6 +96,8 @@ SIGNATURES = {
     "spec_verify_tree": (C.c_int, [C.POINTER(TreeArgs), _vp]),
     "spec_cascade_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spec_verify_cascade": (C.c_int, [C.POINTER(CascadeArgs), _vp]),
+    "spec_pipeline_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int, C.c_int]),
+    "spec_verify_pipeline": (C.c_int, [C.POINTER(PipelineArgs), _vp]),
     "spec_compact_tree_path": (C.c_int, [C.POINTER(CompactArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
 }

@@ -235,6 +235,71 @@ class CascadePlan(_Plan):
         self._call = lib.spec_verify_cascade
 
 
+class PipelinePlan(_Plan):
+    """k-model PipeSpec snapshot bound to fixed buffers.  See spec_verify_pipeline.
+
+    models: list of k logit views [B, rows_s, V] with one row stride (models[0]
+    may be None in greedy mode); windows: stage windows (windows[0] = drafted
+    tokens); us / vs: per-stage uniforms (sampling); base: int32 [k-1, B] or
+    None."""
+
+    def __init__(self, models, tokens, windows, us=None, vs=None, base=None, *, greedy=False, temperature=1.0,
+                 final_bonus=False, V=None, workspace=None):
+        k = len(models)
+        windows = [int(g) for g in windows]
+        if len(windows) != k - 1:
+            raise ValueError("windows: one per stage (k - 1)")
+        ref = models[1]
+        B = ref.shape[0]
+        V = ref.shape[2] if V is None else V
+        dev = ref.device
+        rows = [windows[0], windows[0] + 1] + [windows[s - 1] + (1 if (final_bonus and s == k - 1) else 0)
+                                               for s in range(2, k)]
+        ld = None
+        for s, m in enumerate(models):
+            if m is None:
+                if not greedy or s != 0:
+                    raise ValueError(f"models[{s}] is required")
+                continue
+            if m.dtype != ref.dtype:
+                raise ValueError("every model: the same dtype")
+            this = _rows(m, rows[s], f"models[{s}]")
+            if ld is not None and this != ld:
+                raise ValueError("every model: the same row stride")
+            ld = this
+        lib = L.lib()
+        self.keep = [models, tokens, us, vs, base]
+        i32 = lambda *shape: torch.empty(*shape, dtype=torch.int32, device=dev)
+        self.out = dict(a=i32(B, k - 1), w=i32(B, k - 1), t=i32(B, k - 1), t_valid=i32(B, k - 1), r=i32(B, k - 1),
+                        committed=i32(B), seq_error=i32(B),
+                        error_word=torch.zeros(1, dtype=torch.int32, device=dev))
+        win = (C.c_int * (L.SPEC_MAX_MODELS - 1))(*windows)
+        need = lib.spec_pipeline_workspace_size(B, k, win, int(final_bonus), V)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        a = L.PipelineArgs()
+        a.B, a.k, a.final_bonus, a.V, a.ld = B, k, int(bool(final_bonus)), V, ld
+        a.window = win
+        a.dtype = _DTYPES[ref.dtype]
+        a.mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        a.temperature = float(temperature)
+        for s, m in enumerate(models):
+            a.logits[s] = None if m is None else m.data_ptr()
+        a.draft_tokens = _i32(tokens, "tokens").data_ptr()
+        if not greedy:
+            for s in range(k - 1):
+                a.u[s] = _f32(us[s], f"us[{s}]").data_ptr()
+                a.v[s] = _f32(vs[s], f"vs[{s}]").data_ptr()
+        a.base = None if base is None else _i32(base, "base").data_ptr()
+        o = self.out
+        a.a, a.w, a.t, a.t_valid, a.r = (o[n].data_ptr() for n in ("a", "w", "t", "t_valid", "r"))
+        a.committed, a.seq_error, a.error_word = (o[n].data_ptr() for n in ("committed", "seq_error", "error_word"))
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_pipeline
+
+
 def _to_device(xs, device):
     moved = []
     for x in xs:

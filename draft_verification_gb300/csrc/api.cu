@@ -244,3 +244,90 @@ spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream)
 }
 
 }  // extern "C"
+
+namespace {
+
+// Rows per sequence of each model of a pipeline (model s at index s), their
+// total over the models the statistics read, or -1 for a bad window.
+int pipeline_rows(int k, const int* window, bool final_bonus, bool greedy, int* rows) {
+  if (k < 2 || k > kMaxSets) return -1;
+  for (int s = 0; s < k - 1; ++s)
+    if (window[s] < 1 || window[s] > 32) return -1;
+  rows[0] = window[0];
+  rows[1] = window[0] + 1;
+  for (int s = 2; s < k; ++s) rows[s] = window[s - 1] + ((final_bonus && s == k - 1) ? 1 : 0);
+  if (k == 2 && final_bonus) rows[1] = window[0] + 1;  // stage 1 always has its bonus row
+  int total = 0;
+  for (int s = greedy ? 1 : 0; s < k; ++s) total += rows[s];
+  return total;
+}
+
+}  // namespace
+
+extern "C" size_t spec_pipeline_workspace_size(int B, int k, const int* window, int final_bonus, int V) {
+  if (B < 1 || V < 1 || window == nullptr) return 0;
+  int rows[kMaxSets];
+  const int total = pipeline_rows(k, window, final_bonus != 0, false, rows);
+  if (total < 0) return 0;
+  return workspace_bytes(B, total, V);
+}
+
+extern "C" spec_status spec_verify_pipeline(const spec_pipeline_args* a, cudaStream_t stream) {
+  if (a == nullptr) return SPEC_EINVAL;
+  spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
+  if (st != SPEC_OK) return st;
+  const bool greedy = a->mode == SPEC_GREEDY;
+  const bool bf16 = a->dtype == SPEC_BF16;
+  const int k = a->k;
+  int rows[kMaxSets];
+  const int total = pipeline_rows(k, a->window, a->final_bonus != 0, greedy, rows);
+  if (total < 0) return SPEC_EINVAL;
+  if (!a->draft_tokens || !a->a || !a->w || !a->t || !a->t_valid || !a->r || !a->committed) return SPEC_EINVAL;
+  for (int s = greedy ? 1 : 0; s < k; ++s) {
+    if (!a->logits[s]) return SPEC_EINVAL;
+    if (!aligned16(a->logits[s])) return SPEC_EALIGN;
+  }
+  if (!greedy)
+    for (int s = 0; s < k - 1; ++s)
+      if (!a->u[s] || !a->v[s]) return SPEC_EINVAL;
+  if (!a->workspace || a->workspace_bytes < workspace_bytes(a->B, total, a->V) || !aligned16(a->workspace))
+    return SPEC_EWORKSPACE;
+
+  StatsParams sp;
+  if (!stats_params(sp, a->B, a->V, a->ld, bf16, greedy, a->temperature, total, a->workspace)) return SPEC_EINVAL;
+  PipelineParams pp = {};
+  pp.B = a->B;
+  pp.k = k;
+  pp.V = a->V;
+  pp.ld = a->ld;
+  pp.final_bonus = a->final_bonus != 0;
+  int off = 0;
+  sp.nsets = 0;
+  for (int s = 0; s < k; ++s) {
+    pp.rows[s] = rows[s];
+    pp.logits[s] = a->logits[s];
+    if (greedy && s == 0) {
+      pp.rowoff[0] = 0;
+      continue;
+    }
+    pp.rowoff[s] = off;
+    off += rows[s];
+    sp.set[sp.nsets++] = RowSet{a->logits[s], rows[s]};
+  }
+  for (int s = 0; s < k - 1; ++s) {
+    pp.window[s] = a->window[s];
+    pp.u[s] = greedy ? nullptr : a->u[s];
+    pp.v[s] = greedy ? nullptr : a->v[s];
+  }
+  pp.tokens = a->draft_tokens;
+  pp.base = a->base;
+  pp.a = a->a;
+  pp.w = a->w;
+  pp.t = a->t;
+  pp.t_valid = a->t_valid;
+  pp.r = a->r;
+  pp.committed = a->committed;
+  pp.seq_error = a->seq_error;
+  pp.error_word = a->error_word;
+  return run(launch_pipeline(sp, pp, bf16, greedy, stream));
+}

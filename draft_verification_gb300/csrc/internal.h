@@ -15,9 +15,12 @@ struct RowSet {
   int rows;
 };
 
+// Row sets of one call: up to one per model of a k-model pipeline.
+constexpr int kMaxSets = 8;
+
 // Everything the kernels need besides the kind-specific arguments.
 struct StatsParams {
-  RowSet set[3];
+  RowSet set[kMaxSets];
   int nsets;
   int rows_per_seq;     // sum of set[k].rows
   int B;
@@ -107,6 +110,34 @@ struct CascadeParams {
   int* seq_error;
   int* error_word;
 };
+
+// k-model pipeline.  Model s's rows of a sequence: window[0] (M_0),
+// window[0] + 1 (M_1), window[s-1] (+1 for the last model with the bonus);
+// rowoff[s] is the first statistics row of model s (greedy calls have no
+// M_0 rows: rowoff[0] is unused there).
+struct PipelineParams {
+  int B, k, V, final_bonus;
+  long long ld;
+  int window[kMaxSets - 1];
+  int rows[kMaxSets];
+  int rowoff[kMaxSets];
+  const void* logits[kMaxSets];
+  const int* tokens;
+  const float* u[kMaxSets - 1];
+  const float* v[kMaxSets - 1];
+  const int* base;
+  int* a;
+  int* w;
+  int* t;
+  int* t_valid;
+  int* r;
+  int* committed;
+  int* seq_error;
+  int* error_word;
+};
+
+cudaError_t launch_pipeline(const StatsParams& g, const PipelineParams& p, bool bf16, bool greedy,
+                            cudaStream_t s);
 
 // `grouped` allows a large call to be split into batch groups on library
 // streams (forked from and joined into s); false keeps every launch on s.

@@ -54,20 +54,13 @@ static_assert(kMaxTiles * kTileElems >= 2097152, "tile sums of the largest row f
 
 template <typename T>
 __device__ __forceinline__ const T* stats_row(const StatsParams& G, int b, int r) {
-  int i = r;
-  const void* base = G.set[0].base;
-  int rows = G.set[0].rows;
-  if (G.nsets > 1 && i >= rows) {
-    i -= rows;
-    base = G.set[1].base;
-    rows = G.set[1].rows;
-    if (G.nsets > 2 && i >= rows) {
-      i -= rows;
-      base = G.set[2].base;
-      rows = G.set[2].rows;
-    }
+  // the set holding statistics row r of a sequence, and r's row within it
+  int i = r, k = 0;
+  while (k + 1 < G.nsets && i >= G.set[k].rows) {
+    i -= G.set[k].rows;
+    ++k;
   }
-  return static_cast<const T*>(base) + (static_cast<long long>(b) * rows + i) * G.ld;
+  return static_cast<const T*>(G.set[k].base) + (static_cast<long long>(b) * G.set[k].rows + i) * G.ld;
 }
 
 // Row statistics of sequence b.  The chunk partials of a group of rows are
@@ -500,6 +493,178 @@ __global__ void __launch_bounds__(kThreads, 4) cascade_walk_kernel(const StatsPa
   const int t2 = cluster_draw(S2, G.V, c, G.ntiles, buf, df_mul_f(Z2, cs.v2), false, ps);
   if (t2 < 0) return;
   if (tid == 0) out.write(a1, t1, a2, w2, t2, 1, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0));
+}
+
+// ===========================================================================
+// 2b'. k-model pipeline (PipeSpec review, "What carries the argument")
+// Statistics rows: model s's rows start at P.rowoff[s] (sampling: M_0 first;
+// greedy: M_0 not read).
+// ===========================================================================
+constexpr int kMaxPipeRows = kMaxGamma + (kMaxSets - 1) * (kMaxGamma + 1);
+
+struct PipeSmem {
+  float st_m[kMaxPipeRows], st_s[kMaxPipeRows];
+  int st_arg[kMaxPipeRows];
+  int buf[kMaxGamma + 1];  // the buffer the current stage verifies
+  float u[kMaxSets - 1][kMaxGamma], v[kMaxSets - 1];
+  int a[kMaxSets - 1], w[kMaxSets - 1], t[kMaxSets - 1], tv[kMaxSets - 1];
+  int err, len, ra;
+};
+
+// Tokens and uniforms (inputs only: safe before the statistics are complete).
+__device__ void pipe_inputs(const PipelineParams& P, int b, PipeSmem& cs, bool sampling) {
+  const int g1 = P.window[0], tid = threadIdx.x;
+  if (tid == 0) cs.err = 0;
+  __syncthreads();
+  if (tid < g1) {
+    const int t = P.tokens[static_cast<long long>(b) * g1 + tid];
+    cs.buf[tid] = t;
+    if (t < 0 || t >= P.V) atomicOr(&cs.err, SPEC_ERR_TOKEN);
+  }
+  if (sampling) {
+    for (int i = tid; i < (P.k - 1) * kMaxGamma; i += kThreads) {
+      const int s = i / kMaxGamma, j = i - s * kMaxGamma;
+      if (j < P.window[s]) cs.u[s][j] = P.u[s][static_cast<long long>(b) * P.window[s] + j];
+    }
+    if (tid < P.k - 1) cs.v[tid] = P.v[tid][b];
+  }
+}
+
+// The outputs of sequence b (one thread).  Rollback: buffer O_j keeps
+// min(L_j, a_s of every rejecting stage s > j), L_0 = a_1, L_j = w_{j+1}.
+__device__ void pipe_write(const PipelineParams& P, int b, const PipeSmem& cs, int flag, bool error) {
+  const int k1 = P.k - 1;
+  const long long o = static_cast<long long>(b) * k1;
+  for (int s = 0; s < k1; ++s) {
+    P.a[o + s] = error ? 0 : cs.a[s];
+    P.w[o + s] = error ? 0 : cs.w[s];
+    P.t[o + s] = error ? -1 : cs.t[s];
+    P.t_valid[o + s] = error ? 0 : cs.tv[s];
+  }
+  for (int j = 0; j < k1; ++j) {
+    int keep = 0;
+    if (!error) {
+      keep = j == 0 ? cs.a[0] : cs.w[j];
+      for (int s = j; s < k1; ++s)  // stage s + 1 > j
+        if (cs.a[s] < cs.w[s]) keep = min(keep, cs.a[s]);
+    }
+    P.r[o + j] = (P.base ? P.base[static_cast<long long>(j) * P.B + b] : 0) + keep;
+  }
+  P.committed[b] = error ? 0 : cs.len;
+  if (P.seq_error) P.seq_error[b] = flag;
+  if (flag && P.error_word) atomicOr(P.error_word, flag);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) pipeline_greedy_kernel(const StatsParams G, const PipelineParams P) {
+  __shared__ PipeSmem cs;
+  __shared__ float2 stage[kStage];
+  const int b = blockIdx.x, k = P.k;
+  pipe_inputs(P, b, cs, false);
+  pdl_wait();
+  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  if (threadIdx.x != 0) return;
+  if (err) {
+    pipe_write(P, b, cs, err, true);
+    return;
+  }
+  int len = P.window[0];
+  for (int s = 1; s < k; ++s) {
+    const int* arg = cs.st_arg + P.rowoff[s];
+    const int w = s == 1 ? P.window[0] : min(P.window[s - 1], len);
+    int a = w;
+    for (int j = 0; j < w; ++j)
+      if (cs.buf[j] != arg[j]) {
+        a = j;
+        break;
+      }
+    const bool bonus = s == 1 || (P.final_bonus && s == k - 1);
+    int tok = -1, valid = 0;
+    if (a < w || bonus) {
+      tok = arg[a];  // a == w for the bonus: the row after the window
+      valid = 1;
+      cs.buf[a] = tok;
+      len = a + 1;
+    } else {
+      len = w;
+    }
+    cs.a[s - 1] = a;
+    cs.w[s - 1] = w;
+    cs.t[s - 1] = tok;
+    cs.tv[s - 1] = valid;
+  }
+  cs.len = len;
+  pipe_write(P, b, cs, 0, false);
+}
+
+// Sampling pipeline, every stage in one cluster per sequence.  Every CTA
+// draws every emitted token (the next stage tests it); the lead CTA writes.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 4) pipeline_walk_kernel(const StatsParams G, const PipelineParams P) {
+  __shared__ PipeSmem cs;
+  __shared__ PassSmem ps;
+  __shared__ float2 stage[kStage];
+  const int b = blockIdx.y, k = P.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = G.c;
+  const bool lead = cluster_rank() == 0;
+
+  pass_begin(ps);
+  cluster_enter();
+  pipe_inputs(P, b, cs, true);
+  pdl_wait();
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  cluster_ready();
+  if (err) {
+    if (lead && tid == 0) pipe_write(P, b, cs, err, true);
+    return;
+  }
+  if (tid == 0) cs.len = P.window[0];
+  __syncthreads();
+  int pbuf = 1, flag = 0;
+  for (int s = 1; s < k; ++s) {
+    const T* Ms = static_cast<const T*>(P.logits[s]) + static_cast<long long>(b) * P.rows[s] * P.ld;
+    const T* Mq = static_cast<const T*>(P.logits[s - 1]) + static_cast<long long>(b) * P.rows[s - 1] * P.ld;
+    const int ros = P.rowoff[s], roq = P.rowoff[s - 1];
+    const int w = s == 1 ? P.window[0] : min(P.window[s - 1], cs.len);
+    if (warp == 0) {
+      bool keep = true;
+      if (lane < w) {
+        const int o = cs.buf[lane];
+        const float xp = load_elem(Ms + lane * P.ld + o), xq = load_elem(Mq + lane * P.ld + o);
+        keep = keeps(cs.u[s - 1][lane],
+                     ratio(xp, cs.st_m[ros + lane], cs.st_s[ros + lane], xq, cs.st_m[roq + lane], cs.st_s[roq + lane], c));
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, lane < w && !keep);
+      if (lane == 0) cs.ra = rej ? __ffs(rej) - 1 : w;
+    }
+    __syncthreads();
+    const int a = cs.ra;
+    const bool bonus = s == 1 || (P.final_bonus && s == k - 1);
+    int tok = -1;
+    if (a < w || bonus) {
+      // the residual max(0, p_s - p_{s-1}) at position a, or M_s's row w for the bonus
+      PassSpec<T> S = make_spec(Ms + a * P.ld, cs.st_m[ros + a], cs.st_s[ros + a], a < w ? Mq + a * P.ld : nullptr,
+                                a < w ? cs.st_m[roq + a] : 0.f, a < w ? cs.st_s[roq + a] : 1.f, 1.f, c);
+      pbuf ^= 1;
+      const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &pbuf, &flag, ps);
+      tok = cluster_draw(S, G.V, c, G.ntiles, pbuf, df_mul_f(Z, cs.v[s - 1]), true, ps);
+    }
+    if (tid == 0) {
+      cs.a[s - 1] = a;
+      cs.w[s - 1] = w;
+      cs.t[s - 1] = tok;
+      cs.tv[s - 1] = tok >= 0 ? 1 : 0;
+      if (tok >= 0) {
+        cs.buf[a] = tok;
+        cs.len = a + 1;
+      } else {
+        cs.len = w;
+      }
+    }
+    __syncthreads();
+  }
+  if (lead && tid == 0) pipe_write(P, b, cs, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0), false);
 }
 
 // ===========================================================================
@@ -1099,7 +1264,19 @@ cudaError_t cascade_impl(const StatsParams& G, const CascadeParams& p, bool gree
   return cascade_one<T>(G, p, greedy, s, -1);
 }
 
+template <typename T>
+cudaError_t pipeline_impl(const StatsParams& G, const PipelineParams& p, bool greedy, cudaStream_t s) {
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
+  if (e != cudaSuccess) return e;
+  if (greedy) return launch_dependent(pipeline_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s);
+  return launch_walk(pipeline_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
+}
+
 }  // namespace
+
+cudaError_t launch_pipeline(const StatsParams& G, const PipelineParams& p, bool bf16, bool greedy, cudaStream_t s) {
+  return bf16 ? pipeline_impl<bf16_t>(G, p, greedy, s) : pipeline_impl<float>(G, p, greedy, s);
+}
 
 int stats_chunks(int V, bool bf16) {
   const int ce = bf16 ? chunk_elems<bf16_t>() : chunk_elems<float>();

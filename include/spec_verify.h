@@ -252,6 +252,63 @@ size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V);
 spec_status spec_verify_cascade(const spec_cascade_args* args, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* k-model PipeSpec snapshot (PipeSpec review, "What carries the argument": */
+/* M_0 drafts into O_0, each later M_i verifies O_{i-1} against its own      */
+/* prediction and appends the verified prefix to O_i; a mismatch rolls     */
+/* every earlier buffer back to the last verified token).  One synchronous  */
+/* snapshot; each stage's window starts at the start of the buffer below.   */
+/*  - Stage 1 is the chain rule (p = M_1, q = M_0) over the window[0]       */
+/*    drafted tokens and always emits one token: the correction at the      */
+/*    first rejection, else the bonus from M_1's row window[0].             */
+/*  - Stage s >= 2 verifies the first w_s = min(window[s-1], len(O_{s-1}))  */
+/*    tokens of O_{s-1} (p = M_s, q = M_{s-1}); it emits a correction on a   */
+/*    rejection and nothing when it keeps all w_s, except the last stage     */
+/*    when final_bonus is set: it then draws a bonus from M_{k-1}'s row w.   */
+/*  - Rollback: buffer O_j (j = 0 .. k-2) keeps min(L_j, a_s of every        */
+/*    rejecting stage s > j), L_0 = a_1, L_j = w_{j+1}; r = base + that.     */
+/*  - k = 3 without the bonus is spec_verify_cascade; k = 2 is the chain.    */
+/*  - Greedy mode compares argmaxes (corrections and bonus are argmaxes);   */
+/*    logits[0] and the uniforms are not read.                              */
+/* ---------------------------------------------------------------------- */
+#define SPEC_MAX_MODELS 8
+typedef struct spec_pipeline_args {
+  int B;                        /* sequences, >= 1                                */
+  int k;                        /* models M_0 .. M_{k-1}, 2..SPEC_MAX_MODELS      */
+  int window[SPEC_MAX_MODELS - 1]; /* window[s-1]: stage s's window, 1..32        */
+                                /* (window[0] = drafted tokens per sequence)       */
+  int final_bonus;              /* nonzero: the last stage's bonus (see above)    */
+  int V;                        /* vocabulary size, >= 1                          */
+  long long ld;                 /* row stride of every logit array (elements)     */
+  spec_dtype dtype;
+  spec_mode mode;
+  float temperature;            /* > 0 and finite in SPEC_SAMPLE                   */
+  const void* logits[SPEC_MAX_MODELS];
+                                /* logits[0]: M_0 [B, window[0], ld] (sampling);  */
+                                /* logits[1]: M_1 [B, window[0]+1, ld];            */
+                                /* logits[s], s >= 2: M_s [B, window[s-1], ld],    */
+                                /* one more row for the last model with the bonus */
+  const int* draft_tokens;      /* [B, window[0]]                                  */
+  const float* u[SPEC_MAX_MODELS - 1]; /* u[s-1]: stage s accept uniforms        */
+                                /* [B, window[s-1]] (SPEC_SAMPLE)                  */
+  const float* v[SPEC_MAX_MODELS - 1]; /* v[s-1]: stage s draw uniform [B]       */
+  const int* base;              /* [k-1, B] buffer lengths before the snapshot, or */
+                                /* NULL (all 0)                                   */
+  int* a;                       /* out [B, k-1]: tokens stage s kept              */
+  int* w;                       /* out [B, k-1]: tokens stage s tested            */
+  int* t;                       /* out [B, k-1]: token stage s emitted, or -1     */
+  int* t_valid;                 /* out [B, k-1]: 1 when stage s emitted a token   */
+  int* r;                       /* out [B, k-1]: base + kept length of O_j        */
+  int* committed;               /* out [B]: len(O_{k-1})                          */
+  int* seq_error;               /* out [B], optional                              */
+  int* error_word;              /* in/out, optional                               */
+  void* workspace;              /* 16-byte aligned, see the file comment          */
+  size_t workspace_bytes;
+} spec_pipeline_args;
+
+size_t spec_pipeline_workspace_size(int B, int k, const int* window, int final_bonus, int V);
+spec_status spec_verify_pipeline(const spec_pipeline_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Cache compaction after a tree verification.  Staged Speculative         */
 /* Decoding, abstract (the speculative batch is a tree); PipeSpec review,  */
 /* "What carries the argument" (a buffer keeps the verified prefix and is  */

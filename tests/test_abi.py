@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 9, names
+    assert len(names) == 11, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -43,7 +43,8 @@ def test_struct_layout_matches_header(tmp_path):
     if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
         pytest.skip("gcc or CUDA headers missing")
     structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
-               "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs}
+               "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs,
+               "spec_pipeline_args": _lib.PipelineArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -198,3 +199,47 @@ def _compact(**kw):
 def test_compact_argument_errors_are_reported_before_launch(lib, field, value):
     assert lib.spec_compact_tree_path(C.byref(_compact(**{field: value})), None) == -1
     assert lib.spec_compact_tree_path(None, None) == -1
+
+
+def test_pipeline_argument_errors_and_workspace(lib):
+    from draft_verification_gb300 import _lib
+    win = (C.c_int * 7)(8, 6, 4)
+    # rows M_0..M_3 = 8 + 9 + 6 + 4 (+1 with the final bonus)
+    assert lib.spec_pipeline_workspace_size(128, 4, win, 0, 128256) == 256 * ((128 * 27 * 16 * 8 + 255) // 256)
+    assert lib.spec_pipeline_workspace_size(128, 4, win, 1, 128256) == 256 * ((128 * 28 * 16 * 8 + 255) // 256)
+    assert lib.spec_pipeline_workspace_size(128, 9, win, 0, 100) == 0
+    bad = (C.c_int * 7)(8, 0, 4)
+    assert lib.spec_pipeline_workspace_size(128, 4, bad, 0, 100) == 0
+
+    def args(**kw):
+        a = _lib.PipelineArgs()
+        a.B, a.k, a.V, a.ld = 2, 4, 100, 100
+        a.window = (C.c_int * 7)(3, 2, 2)
+        a.dtype, a.mode, a.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
+        fake = 0x10000
+        for i in range(4):
+            a.logits[i] = fake
+        for i in range(3):
+            a.u[i] = fake
+            a.v[i] = fake
+        for f in ("draft_tokens", "a", "w", "t", "t_valid", "r", "committed", "workspace"):
+            setattr(a, f, fake)
+        a.workspace_bytes = 1 << 20
+        for key, v in kw.items():
+            setattr(a, key, v)
+        return a
+
+    for kw, code in [(dict(k=1), -1), (dict(k=9), -1), (dict(B=0), -1), (dict(window=(C.c_int * 7)(3, 33, 2)), -1),
+                     (dict(temperature=0.0), -1), (dict(dtype=5), -2), (dict(committed=None), -1),
+                     (dict(workspace_bytes=8), -4)]:
+        assert lib.spec_verify_pipeline(C.byref(args(**kw)), None) == code, kw
+    a = args()
+    a.logits[2] = None
+    assert lib.spec_verify_pipeline(C.byref(a), None) == -1
+    a = args()
+    a.logits[1] = 0x10002
+    assert lib.spec_verify_pipeline(C.byref(a), None) == -3
+    a = args()
+    a.u[2] = None
+    assert lib.spec_verify_pipeline(C.byref(a), None) == -1
+    assert lib.spec_verify_pipeline(None, None) == -1

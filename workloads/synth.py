@@ -166,6 +166,38 @@ SPECS = {
 
 
 @dataclass(frozen=True)
+class PipelineSpec:
+    """k-model PipeSpec snapshot: windows[s-1] is stage s's window (windows[0]
+    = drafted tokens).  Logits: M_0 ~ sigma_q N(0, 1); M_s = a[s-1] M_{s-1} +
+    s[s-1] N(0, 1) row by row (the cascade's model, one more link per stage)."""
+    name: str
+    B: int
+    windows: tuple
+    V: int
+    dtype: str
+    greedy: bool
+    temperature: float
+    sigma_q: float
+    a: tuple
+    s: tuple
+    final_bonus: bool = False
+    pad: int = 0
+
+    @property
+    def k(self) -> int:
+        return len(self.windows) + 1
+
+
+# Four models (M_0 -> M_1 -> M_2 -> M_3): the cascade's first two links, and
+# a third with the second link's scales.
+PIPELINE_SPECS = {
+    "pipeline4_b128_g8_g6_g4_v128256_bf16": PipelineSpec(
+        "pipeline4_b128_g8_g6_g4_v128256_bf16", B=128, windows=(8, 6, 4), V=128256, dtype="bf16", greedy=False,
+        temperature=1.0, sigma_q=2.0, a=(0.9, 0.9, 0.9), s=(0.465, 1.024, 1.024)),
+}
+
+
+@dataclass(frozen=True)
 class CompactSpec:
     """Cache compaction after a tree verification: B sequences, each with one
     row of row_bytes per tree node (the tree of tree_topology) and a kept root
@@ -361,9 +393,52 @@ def make_compact(spec: CompactSpec, seed: int = 0) -> dict:
                 path_len=path_len, prefix_len=prefix_len, parent=parent)
 
 
+def pipeline_rows(spec: PipelineSpec, s: int) -> int:
+    """Rows per sequence of model s."""
+    g = spec.windows
+    if s == 0:
+        return g[0]
+    if s == 1:
+        return g[0] + 1
+    return g[s - 1] + (1 if (spec.final_bonus and s == spec.k - 1) else 0)
+
+
+def make_pipeline(spec: PipelineSpec, seed: int = 0) -> dict:
+    """Pipeline workload: models = [M_0 .. M_{k-1}] logits [B, rows_s, V+pad],
+    tokens int32 [B, windows[0]] drawn from M_0, us[s-1] [B, windows[s-1]],
+    vs[s-1] [B], base int32 [k-1, B]."""
+    rng = _rng(seed, 5)
+    B, V, k = spec.B, spec.V, spec.k
+    dt = np.uint16 if spec.dtype == "bf16" else np.float32
+    rows = [pipeline_rows(spec, s) for s in range(k)]
+    depth = max(rows)
+    models = [np.empty((B, rows[s], V), dt) for s in range(k)]
+    tokens = np.empty((B, spec.windows[0]), np.int32)
+    for b in range(B):
+        m = rng.standard_normal((depth, V), dtype=np.float32) * np.float32(spec.sigma_q)
+        for s in range(k):
+            if s > 0:
+                m = np.float32(spec.a[s - 1]) * m + rng.standard_normal((depth, V), dtype=np.float32) * np.float32(
+                    spec.s[s - 1])
+            models[s][b] = _store(m[:rows[s]], spec.dtype)
+        v0 = _values(models[0][b], spec.dtype)
+        if spec.greedy:
+            tokens[b] = np.argmax(v0, axis=-1)
+        else:
+            tokens[b] = _gumbel_argmax(rng, v0 / np.float32(spec.temperature))
+    us = [rng.random((B, g), dtype=np.float32) for g in spec.windows]
+    vs = [rng.random(B, dtype=np.float32) for _ in spec.windows]
+    base = np.tile(rng.integers(0, 4096, B, dtype=np.int32), (k - 1, 1))
+    return dict(kind="pipeline", spec=spec, models=[_pad(x, spec.pad) for x in models], tokens=tokens, us=us,
+                vs=vs, base=base)
+
+
 def make(spec, seed: int = 0) -> dict:
     if isinstance(spec, str):
-        spec = SPECS[spec] if spec in SPECS else COMPACT_SPECS[spec]
+        spec = SPECS[spec] if spec in SPECS else (COMPACT_SPECS[spec] if spec in COMPACT_SPECS
+                                                  else PIPELINE_SPECS[spec])
+    if isinstance(spec, PipelineSpec):
+        return make_pipeline(spec, seed)
     if isinstance(spec, CompactSpec):
         return make_compact(spec, seed)
     if isinstance(spec, ChainSpec):
