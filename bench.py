@@ -55,7 +55,8 @@ KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification
 # the kernels of one call (statistics, then walk); greedy calls use the
 # greedy walk kernels
 KERNELS = {"chain": ["stats_kernel", "chain_walk_kernel"], "tree": ["stats_kernel", "tree_kernel"],
-           "cascade": ["stats_kernel", "cascade_walk_kernel"], "compact": ["compact_kernel"]}
+           "cascade": ["stats_kernel", "cascade_walk_kernel"], "compact": ["compact_kernel"],
+           "pipeline": ["stats_kernel", "pipeline_walk_kernel"]}
 COMPACT_METRIC = "cache rows compacted/sec and GB/s moved vs GB300 HBM peak (1 GPU)"
 COMPACT_SOURCES = ["draft_verification_gb300/csrc/compact.cu"]
 
@@ -86,6 +87,8 @@ def draft_tokens_per_call(w) -> int:
         return s.B * s.gamma
     if w["kind"] == "tree":
         return s.B * (w["parent"].shape[1] - 1)
+    if w["kind"] == "pipeline":
+        return s.B * s.windows[0]
     return s.B * (s.gamma1 + s.gamma2)
 
 
@@ -101,6 +104,8 @@ def workload_config(w) -> dict:
         cfg["nodes"] = int(w["parent"].shape[1])
         cfg["max_depth"] = w["max_depth"]
         cfg["alpha_target"] = s.alpha_target
+    elif w["kind"] == "pipeline":
+        cfg.update(models=s.k, windows=list(s.windows), final_bonus=s.final_bonus)
     else:
         cfg.update(gamma1=s.gamma1, gamma2=s.gamma2, alpha01_target=s.alpha01_target,
                    alpha12_target=s.alpha12_target)
@@ -250,6 +255,10 @@ def oracle_rate(w, budget_s: float):
         elif w["kind"] == "tree":
             V.verify_tree(w["parent"], w["tokens"], w["target"], w["draft"], w["u"], w["v"],
                           w["prefix_len"], s.temperature, s.greedy, w["max_depth"], s.dtype, V=s.V)
+        elif w["kind"] == "pipeline":
+            from oracle import pipeline as Pp
+            Pp.verify_pipeline(w["models"], w["tokens"], w["us"], w["vs"], s.temperature, s.greedy,
+                               s.final_bonus, s.dtype, V=s.V, base=w["base"])
         else:
             V.verify_cascade(w["l0"], w["l1"], w["l2"], w["tokens"], w["u1"], w["v1"], w["u2"],
                              w["v2"], w["base0"], w["base1"], s.temperature, s.greedy, s.dtype, V=s.V)
@@ -269,6 +278,10 @@ def subset(w, nseq):
     for k, v in w.items():
         if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w["spec"].B:
             out[k] = v[:nseq]
+        elif isinstance(v, list):
+            out[k] = [x[:nseq] for x in v]
+    if w["kind"] == "pipeline":
+        out["base"] = w["base"][:, :nseq]
     return out
 
 
@@ -313,6 +326,10 @@ def device_inputs(w, dev):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     out = {}
+    if w["kind"] == "pipeline":
+        out["models"] = [logits(m) for m in w["models"]]
+        out["us"] = [torch.from_numpy(u).to(dev) for u in w["us"]]
+        out["vs"] = [torch.from_numpy(v).to(dev) for v in w["vs"]]
     for k, v in w.items():
         if not isinstance(v, np.ndarray):
             continue
@@ -333,6 +350,11 @@ def make_plan(w, t, workspace=None):
         return dv.TreePlan(t["parent"], t["tokens"], t["target"], t["draft"], t["u"], t["v"],
                            t["prefix_len"], max_depth=w["max_depth"], greedy=s.greedy,
                            temperature=s.temperature, workspace=workspace)
+    if w["kind"] == "pipeline":
+        models = [None if (s.greedy and i == 0) else m[:, :, :s.V] for i, m in enumerate(t["models"])]
+        return dv.PipelinePlan(models, t["tokens"], s.windows, t["us"], t["vs"], t["base"], greedy=s.greedy,
+                               temperature=s.temperature, final_bonus=s.final_bonus, V=s.V,
+                               workspace=workspace)
     return dv.CascadePlan(t["l0"], t["l1"], t["l2"], t["tokens"], t["u1"], t["v1"], t["u2"], t["v2"],
                           t["base0"], t["base1"], greedy=s.greedy, temperature=s.temperature,
                           workspace=workspace)
@@ -353,7 +375,10 @@ def run_ours(args, w, rank, world, dist):
     n_sets = min(n_sets, max(2, int(0.5 * props.total_memory // max(bytes_per_call, 1))))
 
     base = device_inputs(w, dev)
-    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
+    def clone(v):
+        return [x.clone() for x in v] if isinstance(v, list) else v.clone()
+
+    sets = [base] + [{k: clone(v) for k, v in base.items()} for _ in range(n_sets - 1)]
     ws = torch.empty(max(16, int(plan_workspace(w))), dtype=torch.uint8, device=dev)
     plans = [make_plan(w, t, ws) for t in sets]
     stream = torch.cuda.Stream(dev)
@@ -458,6 +483,11 @@ def plan_workspace(w):
         return dv.workspace_bytes("chain", s.B, s.gamma, s.V)
     if w["kind"] == "tree":
         return dv.workspace_bytes("tree", s.B, int(w["parent"].shape[1]), s.V)
+    if w["kind"] == "pipeline":
+        import ctypes
+        from draft_verification_gb300 import _lib
+        win = (ctypes.c_int * (_lib.SPEC_MAX_MODELS - 1))(*s.windows)
+        return int(_lib.lib().spec_pipeline_workspace_size(s.B, s.k, win, int(s.final_bonus), s.V))
     return dv.workspace_bytes("cascade", s.B, s.gamma1, s.gamma2, s.V)
 
 
@@ -468,6 +498,8 @@ def e2e_rate(args, w, dev, stream):
     import torch
     import draft_verification_gb300 as dv
     s = w["spec"]
+    if w["kind"] == "pipeline":
+        return pipeline_e2e(args, w, dev, stream)
     host = {}
     for k, v in w.items():
         if isinstance(v, np.ndarray):
@@ -700,6 +732,48 @@ def compact_main(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def pipeline_e2e(args, w, dev, stream):
+    """e2e_rate for the k-model pipeline (lists of per-model inputs)."""
+    import torch
+    import draft_verification_gb300 as dv
+    s = w["spec"]
+
+    def pin(a, logits=False):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if logits and s.dtype == "bf16":
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.pin_memory()
+
+    models = [None if (s.greedy and i == 0) else pin(m[:, :, :s.V], True) for i, m in enumerate(w["models"])]
+    us = None if s.greedy else [pin(u) for u in w["us"]]
+    vs = None if s.greedy else [pin(v) for v in w["vs"]]
+    tokens, base = pin(w["tokens"]), pin(w["base"])
+    h2d = sum(m.numel() * m.element_size() for m in models if m is not None) + tokens.numel() * 4 + base.numel() * 4
+    if not s.greedy:
+        h2d += sum(u.numel() * 4 for u in us) + sum(v.numel() * 4 for v in vs)
+
+    def call():
+        with torch.cuda.stream(stream):
+            return dv.verify_pipeline(models, tokens, s.windows, us, vs, base, greedy=s.greedy,
+                                      temperature=s.temperature, final_bonus=s.final_bonus, V=s.V, device=dev,
+                                      stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    d2h = 0
+    for _ in range(n):
+        o = call()
+        stream.synchronize()
+        d2h = sum(v.numel() * v.element_size() for v in o.values())
+    el = time.perf_counter() - t0
+    return {"value": draft_tokens_per_call(w) / (el / n), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": 1000.0 * el / n, "steps": n}
+
+
 def run_profile(args, w):
     """W + K eager calls on one input copy, nothing else (an ncu target)."""
     import torch
@@ -721,10 +795,11 @@ def main():
     if args.workload in synth.COMPACT_SPECS:
         compact_main(args, synth.make(synth.COMPACT_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
         return
-    if args.workload not in synth.SPECS:
+    specs = dict(synth.SPECS, **synth.PIPELINE_SPECS)
+    if args.workload not in specs:
         raise SystemExit(f"unknown workload {args.workload}; choose from "
-                         f"{sorted(synth.SPECS) + sorted(synth.COMPACT_SPECS)}")
-    w = synth.make(synth.SPECS[args.workload], seed=replica_seed(args.seed, rank))
+                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS)}")
+    w = synth.make(specs[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":
         if rank == 0:

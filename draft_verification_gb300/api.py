@@ -392,6 +392,21 @@ def compact_tree_path(tree_rows, cache, path_nodes, path_len, prefix_len=None, s
     return seq_error
 
 
+def verify_pipeline(models, tokens, windows, us=None, vs=None, base=None, *, greedy=False, temperature=1.0,
+                    final_bonus=False, V=None, device="cuda", stream=None):
+    """One k-model PipeSpec snapshot; returns a, w, t, t_valid, r [B, k-1],
+    committed, seq_error, error_word (host tensors in, host tensors out)."""
+    host = tokens.device.type == "cpu"
+    if host:
+        models = _to_device(list(models), device)
+        tokens, base = _to_device([tokens, base], device)
+        us = None if us is None else _to_device(list(us), device)
+        vs = None if vs is None else _to_device(list(vs), device)
+    plan = PipelinePlan(models, tokens, windows, us, vs, base, greedy=greedy, temperature=temperature,
+                        final_bonus=final_bonus, V=V)
+    return _finish(plan.run(stream), host)
+
+
 def workspace_bytes(kind: str, *sizes) -> int:
     fn = {"chain": "spec_chain_workspace_size", "tree": "spec_tree_workspace_size",
           "cascade": "spec_cascade_workspace_size"}[kind]

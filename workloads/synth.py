@@ -458,6 +458,8 @@ def logit_bytes(w: dict) -> int:
         rows = spec.gamma + 1 + (0 if spec.greedy else spec.gamma)
     elif w["kind"] == "tree":
         rows = w["target"].shape[1] * (1 if spec.greedy else 2)
+    elif w["kind"] == "pipeline":
+        rows = sum(pipeline_rows(spec, s) for s in range(1 if spec.greedy else 0, spec.k))
     else:
         rows = spec.gamma1 + 1 + spec.gamma2 + (0 if spec.greedy else spec.gamma1)
     return spec.B * rows * spec.V * es
