@@ -16,10 +16,12 @@ Modules
                   root path's rows moved to contiguous positions).
 ``pipeline``      the k-model PipeSpec snapshot (stages 1 .. k-1, rollback of
                   every earlier buffer, an optional final-stage bonus).
+``consulted``     the chain rule consulting rows in position order (rows after
+                  the first rejection are never read).
 
 Every function states the passage it follows.  Points where the pages are
 silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import closed_forms, compact, pipeline, verify  # noqa: F401
+from . import closed_forms, compact, consulted, pipeline, verify  # noqa: F401
