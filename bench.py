@@ -74,6 +74,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="plain eager loop for an ncu capture: warm-up + steps calls, one input copy")
+    ap.add_argument("--consulted-only", action="store_true",
+                    help="sampling chains: read each position's rows only while no earlier position was rejected")
     return ap.parse_args()
 
 
@@ -340,12 +342,16 @@ def device_inputs(w, dev):
     return out
 
 
+CONSULTED = False  # set from --consulted-only
+
+
 def make_plan(w, t, workspace=None):
     import draft_verification_gb300 as dv
     s = w["spec"]
     if w["kind"] == "chain":
         return dv.ChainPlan(t["target"], t["draft"], t["tokens"], t["u"], t["v"], t["prefix_len"],
-                            greedy=s.greedy, temperature=s.temperature, workspace=workspace)
+                            greedy=s.greedy, temperature=s.temperature, workspace=workspace,
+                            consulted_only=CONSULTED and not s.greedy)
     if w["kind"] == "tree":
         return dv.TreePlan(t["parent"], t["tokens"], t["target"], t["draft"], t["u"], t["v"],
                            t["prefix_len"], max_depth=w["max_depth"], greedy=s.greedy,
@@ -452,6 +458,14 @@ def run_ours(args, w, rank, world, dist):
     accepted = None
     if w["kind"] == "chain":
         accepted = float((check["accept_len"].float() + 1).mean().item())
+    roof_bytes, roof_unit = bytes_per_call, "one verification call"
+    if w["kind"] == "chain" and CONSULTED and not s.greedy:
+        # the rows the rule consults: 2 (a + 1) after a rejection at a, 2 gamma + 1 otherwise
+        a = check["accept_len"].cpu().numpy().astype(np.int64)
+        rows = np.where(a < s.gamma, 2 * (a + 1), 2 * s.gamma + 1)
+        roof_bytes = int(rows.sum()) * s.V * (2 if s.dtype == "bf16" else 4)
+        roof_unit = "one verification call (consulted rows only)"
+        kernel_gbs = roof_bytes / (kernel_ms * 1e-3) / 1e9
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -459,16 +473,17 @@ def run_ours(args, w, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; shapes of the pages' model families)",
         "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       consulted_only=bool(CONSULTED and w["kind"] == "chain" and not s.greedy),
                        l2_policy=f"rotating {n_sets} input copies ({n_sets * bytes_per_call / 2**20:.0f} MB "
                                  f"> 3 x L2 {l2 / 2**20:.0f} MB)", launch=launch),
         "logits_gbs": logits_gbs,
         "logits_frac_of_peak": logits_gbs / peak,
         "accepted_tokens_per_s": None if accepted is None else accepted * s.B * world / (ms * 1e-3),
-        "roofline": {"bound": "hbm", "kernel": "+".join(KERNELS[w["kind"]]), "unit_of_work": "one verification call",
+        "roofline": {"bound": "hbm", "kernel": "+".join(KERNELS[w["kind"]]), "unit_of_work": roof_unit,
                      "achieved": kernel_gbs,
                      "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak, "peak_source": peak_src,
-                     "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_per_call,
-                     "traffic": profiled_traffic(s.name)},
+                     "kernel_ms": kernel_ms, "algorithmic_bytes": roof_bytes,
+                     "traffic": None if CONSULTED else profiled_traffic(s.name)},
         "e2e": e2e,
         "gpu_launches": args.steps * len(KERNELS[w["kind"]]),
         "clocks": clock_info,
@@ -788,7 +803,9 @@ def run_profile(args, w):
 
 
 def main():
+    global CONSULTED
     args = parse()
+    CONSULTED = args.consulted_only
     from workloads import synth
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

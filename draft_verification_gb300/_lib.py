@@ -30,7 +30,8 @@ class ChainArgs(C.Structure):
         ("accept_len", _vp), ("out_token", _vp), ("rollback_idx", _vp),
         ("p_at_draft", _vp), ("q_at_draft", _vp), ("resid_mass", _vp),
         ("seq_error", _vp), ("error_word", _vp),
-        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t),
+        ("consulted_only", C.c_int)
     ]
 
 

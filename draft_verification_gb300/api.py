@@ -79,7 +79,7 @@ class ChainPlan(_Plan):
     """Chain verification bound to fixed buffers.  See spec_verify_chain."""
 
     def __init__(self, target, draft, tokens, u=None, v=None, prefix_len=None, *,
-                 greedy=False, temperature=1.0, V=None, workspace=None, want_probs=True):
+                 greedy=False, temperature=1.0, V=None, workspace=None, want_probs=True, consulted_only=False):
         B, R, width = target.shape
         gamma = R - 1
         V = width if V is None else V
@@ -124,6 +124,7 @@ class ChainPlan(_Plan):
         a.q_at_draft = _ptr(o.get("q_at_draft"))
         a.resid_mass = _ptr(o.get("resid_mass"))
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        a.consulted_only = int(bool(consulted_only))
         self.args = a
         self._call = lib.spec_verify_chain
 

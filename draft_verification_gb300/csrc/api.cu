@@ -67,7 +67,9 @@ spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool
     return SPEC_EALIGN;
   // sampling reads the draft rows too; greedy reads the target rows only
   const int rows = greedy ? a->gamma + 1 : 2 * a->gamma + 1;
-  if (!a->workspace || a->workspace_bytes < workspace_bytes(a->B, rows, a->V) ||
+  const bool consulted = a->consulted_only != 0;
+  if (consulted && (greedy || a->gamma < 1)) return SPEC_EINVAL;
+  if (!a->workspace || a->workspace_bytes < chain_workspace_bytes(a->B, a->gamma, rows, a->V) ||
       !aligned16(a->workspace))
     return SPEC_EWORKSPACE;
 
@@ -97,6 +99,12 @@ spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool
   cp.resid = a->resid_mass;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
+  if (consulted) {
+    char* ctl = static_cast<char*>(a->workspace) + workspace_bytes(a->B, rows, a->V);
+    cp.count = reinterpret_cast<unsigned*>(ctl);
+    cp.skip = reinterpret_cast<int*>(ctl) + static_cast<size_t>(a->B) * a->gamma;
+    if (cudaMemsetAsync(ctl, 0, chain_ctl_bytes(a->B, a->gamma), stream) != cudaSuccess) return SPEC_ECUDA;
+  }
   return run(launch_chain(sp, cp, bf16, greedy, grouped, stream));
 }
 
@@ -116,7 +124,7 @@ const char* spec_status_string(spec_status status) {
 
 size_t spec_chain_workspace_size(int B, int gamma, int V) {
   if (B < 1 || gamma < 0 || V < 1) return 0;
-  return workspace_bytes(B, 2 * gamma + 1, V);
+  return chain_workspace_bytes(B, gamma, 2 * gamma + 1, V);
 }
 
 size_t spec_tree_workspace_size(int B, int N, int V) {

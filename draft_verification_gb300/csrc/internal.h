@@ -46,11 +46,22 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 inline size_t workspace_bytes(int B, int rows_per_seq, int V) {
   return align256(static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
 }
+// Chain workspace: the partials, then the consulted-only mode's counters
+// (B x gamma) and first-rejection words (B).
+inline size_t chain_ctl_bytes(int B, int gamma) { return align256(static_cast<size_t>(B) * (gamma + 1) * 4); }
+inline size_t chain_workspace_bytes(int B, int gamma, int rows_per_seq, int V) {
+  return workspace_bytes(B, rows_per_seq, V) + chain_ctl_bytes(B, gamma);
+}
 
 
 struct ChainParams {
   int B, gamma, V;
   long long ld;
+  // consulted-only mode (null otherwise): per (sequence, position) count of
+  // statistics chunks done, and per sequence gamma + 1 - (first position
+  // found rejected), 0 while none; both zeroed at the start of the call
+  unsigned* count;
+  int* skip;
   const void* target;
   const void* draft;
   const int* tokens;

@@ -49,6 +49,9 @@ namespace sv {
 namespace {
 
 constexpr int kMaxGamma = 32;
+constexpr int kMaxDecisionChunks = 256;  // statistics chunks of the longest row (2^21 float32 logits)
+
+__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 constexpr int kStage = 4 * kThreads;  // chunk partials staged per round (8 KB)
 static_assert(kMaxTiles * kTileElems >= 2097152, "tile sums of the largest row fit in shared memory");
 
@@ -175,6 +178,49 @@ __global__ void __launch_bounds__(kStatsThreads, 5) stats_kernel(const StatsPara
   stats_unit<T, kGreedy>(stats_row<T>(G, b, r), G.V, k, G.c, out, sm);
 }
 
+// Consulted-only statistics of a sampling chain (grid (2 C, B, gamma + 1):
+// chunk and row kind fastest, then the sequence, then the position, so
+// position t of every sequence comes before position t + 1 of any).  A CTA
+// of position t skips its chunk when an earlier position of its sequence has
+// been found rejected.  The CTA that completes both rows of position t
+// (the count of its 2 C chunks) merges them in chunk order and runs the
+// position's accept test exactly as the walk does; a rejection (or a row
+// that is not finite, or a token out of range, which end the consulted
+// prefix too) records gamma + 1 - t in P.skip[b] (the largest record is the
+// first position).
+template <typename T>
+__global__ void __launch_bounds__(kStatsThreads, 5) stats_consulted_kernel(const StatsParams G, const ChainParams P) {
+  pdl_launch_dependents();
+  __shared__ StatsSmem sm;
+  __shared__ float2 dpart[2][kMaxDecisionChunks];
+  const int C = G.chunks, g = P.gamma;
+  const int t = blockIdx.z, b = blockIdx.y, half = blockIdx.x / C, k = blockIdx.x - half * C;
+  if (t == g && half == 1) return;  // no draft row at the bonus position
+  if (ld_volatile(P.skip + b) > g + 1 - t) return;  // a position before t was rejected
+  const int r = half == 0 ? t : g + 1 + t;
+  float2* part = G.partials + (static_cast<long long>(b) * G.rows_per_seq) * C;
+  stats_unit<T, false>(stats_row<T>(G, b, r), G.V, k, G.c, part + static_cast<long long>(r) * C + k, sm);
+  if (t == g || threadIdx.x != 0) return;
+  __threadfence();
+  if (atomicAdd(P.count + static_cast<long long>(b) * g + t, 1u) != static_cast<unsigned>(2 * C - 1)) return;
+  __threadfence();
+  // the last chunk of position t: merge both rows and test the position
+  for (int q = 0; q < C; ++q) {
+    dpart[0][q] = __ldcg(part + static_cast<long long>(t) * C + q);
+    dpart[1][q] = __ldcg(part + static_cast<long long>(g + 1 + t) * C + q);
+  }
+  const MaxSum mp = combine_row(dpart[0], C, G.c), mq = combine_row(dpart[1], C, G.c);
+  const int tok = P.tokens[static_cast<long long>(b) * g + t];
+  bool stop = !row_stats_ok(mp) || !row_stats_ok(mq) || tok < 0 || tok >= P.V;
+  if (!stop) {
+    const T* trow = static_cast<const T*>(P.target) + (static_cast<long long>(b) * (g + 1) + t) * P.ld;
+    const T* drow = static_cast<const T*>(P.draft) + (static_cast<long long>(b) * g + t) * P.ld;
+    stop = !keeps(P.u[static_cast<long long>(b) * g + t],
+                  ratio(load_elem(trow + tok), mp.m, mp.s, load_elem(drow + tok), mq.m, mq.s, G.c));
+  }
+  if (stop) atomicMax(P.skip + b, g + 1 - t);
+}
+
 // ===========================================================================
 // 2a. chain
 // ===========================================================================
@@ -276,7 +322,24 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   cluster_enter();
   chain_inputs<T>(P, b, cs, true);
   pdl_wait();  // the statistics are complete and visible from here on
-  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  // consulted-only mode: the first rejected position was found by the
+  // statistics kernel; only rows up to it (and the bonus row when there is
+  // none) were read and are merged and checked
+  const int rec = P.skip ? ld_volatile(P.skip + b) : 0;
+  const int first = rec > 0 ? g + 1 - rec : g;
+  int err;
+  if (P.skip) {
+    merge_stats<false>(G, b, stage, [&](int r, float2 v, bool ok) {
+      const bool read = r <= g ? r <= first : r - (g + 1) <= first;
+      if (!read) return;
+      cs.st_m[r] = v.x;
+      cs.st_s[r] = v.y;
+      if (!ok) atomicOr(&cs.err, SPEC_ERR_NONFINITE);
+    });
+    err = cs.err;
+  } else {
+    err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  }
   cluster_ready();
   if (err) {  // every CTA of the cluster sees the same error; the lead reports it
     if (lead) chain_error_out(P, b, err);
@@ -284,16 +347,20 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   }
   if (warp == 0) {
     bool keep = true;
-    if (lane < g) {
+    const int tested = P.skip ? min(g, first + 1) : g;  // positions whose rows were read
+    if (lane < tested) {
       const float mq = cs.st_m[g + 1 + lane], sq = cs.st_s[g + 1 + lane];
       keep = keeps(cs.u[lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
       if (lead) {
         if (P.p_at) P.p_at[drow0 + lane] = prob(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], c);
         if (P.q_at) P.q_at[drow0 + lane] = prob(cs.gq[lane], mq, sq, c);
       }
+    } else if (lane < g && lead) {
+      if (P.p_at) P.p_at[drow0 + lane] = __int_as_float(0x7fc00000);
+      if (P.q_at) P.q_at[drow0 + lane] = __int_as_float(0x7fc00000);
     }
-    const unsigned rej = __ballot_sync(0xffffffffu, lane < g && !keep);
-    if (lane == 0) cs.a = rej ? __ffs(rej) - 1 : g;
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < tested && !keep);
+    if (lane == 0) cs.a = rej ? __ffs(rej) - 1 : (P.skip ? first : g);
   }
   __syncthreads();
   const int a = cs.a;
@@ -1223,7 +1290,20 @@ cudaError_t chain_one(const StatsParams& G, const ChainParams& p, bool greedy, c
 }
 
 template <typename T>
+cudaError_t chain_consulted(const StatsParams& G, const ChainParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * G.chunks, G.B, p.gamma + 1);
+  cfg.blockDim = dim3(kStatsThreads);
+  cfg.stream = s;
+  void* argv[] = {const_cast<StatsParams*>(&G), const_cast<ChainParams*>(&p)};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(stats_consulted_kernel<T>), argv);
+  if (e != cudaSuccess) return e;
+  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
+}
+
+template <typename T>
 cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, bool grouped, cudaStream_t s) {
+  if (p.skip) return chain_consulted<T>(G, p, s);
   const Groups gr = plan_groups(G.B, logit_bytes(G, sizeof(T)));
   if (!grouped || gr.n == 1) return chain_one<T>(G, p, greedy, s, -1);
   return run_groups(gr, s, [&](int i, cudaStream_t si) {

@@ -128,8 +128,22 @@ typedef struct spec_chain_args {
   int* error_word;             /* in/out, optional: data-error bits OR-ed in        */
   void* workspace;             /* 16-byte aligned, see the file comment             */
   size_t workspace_bytes;
+  int consulted_only;          /* SPEC_SAMPLE only: 0 = every row is read; nonzero  */
+                               /* = rows are consulted in position order (below)    */
 } spec_chain_args;
 
+/* Consulted-only mode (PipeSpec review, "What carries the argument": the  */
+/* tokens after the first mismatch are rolled back unused).  Position i's   */
+/* target and draft rows are read only while no earlier position of the    */
+/* sequence has been found rejected; the statistics run position by        */
+/* position over the batch, the last chunk of each position tests it, and  */
+/* the rows of later positions of a rejected sequence are skipped.  The     */
+/* decisions, token, rollback and resid_mass are those of the ordinary mode; */
+/* p_at_draft / q_at_draft are NaN after the first rejection, and a NaN or  */
+/* +inf row is an error only when it is read.  Which later rows are skipped */
+/* depends on timing (a row may still be read before its position's        */
+/* predecessor is decided); the outputs do not.  Greedy calls return        */
+/* SPEC_EINVAL in this mode.                                                */
 size_t spec_chain_workspace_size(int B, int gamma, int V);
 spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
 

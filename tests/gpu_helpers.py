@@ -55,7 +55,7 @@ def logits_view(t: torch.Tensor, V: int) -> torch.Tensor:
 # chain
 # --------------------------------------------------------------------------
 
-def chain_plan(w, device, greedy=None, workspace=None):
+def chain_plan(w, device, greedy=None, workspace=None, consulted_only=False):
     from draft_verification_gb300 import ChainPlan
     s = w["spec"]
     greedy = s.greedy if greedy is None else greedy
@@ -63,11 +63,11 @@ def chain_plan(w, device, greedy=None, workspace=None):
     drf = logits_view(dev_logits(w["draft"], s.dtype, device), s.V)
     return ChainPlan(tgt, drf, dev(w["tokens"], device), dev(w["u"], device), dev(w["v"], device),
                      dev(w["prefix_len"], device), greedy=greedy, temperature=s.temperature,
-                     workspace=workspace)
+                     workspace=workspace, consulted_only=consulted_only)
 
 
-def gpu_chain(w, device, greedy=None, workspace=None):
-    return to_np(chain_plan(w, device, greedy, workspace).run())
+def gpu_chain(w, device, greedy=None, workspace=None, consulted_only=False):
+    return to_np(chain_plan(w, device, greedy, workspace, consulted_only).run())
 
 
 def oracle_chain(w, greedy=None):

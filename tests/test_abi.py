@@ -80,7 +80,8 @@ def test_workspace_sizes(lib):
     def size(B, rows, V):
         return (B * rows * -(-V // 8192) * 8 + 255) // 256 * 256
 
-    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256) == 90112
+    # the chain adds its consulted-only control words: 4 B per (sequence, position + 1)
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256) + 1536 == 91648
     assert lib.spec_tree_workspace_size(16, 64, 50257) == size(16, 128, 50257)
     assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == size(128, 21, 128256)
     assert lib.spec_chain_workspace_size(0, 5, 10) == 0
@@ -111,6 +112,15 @@ def _chain(**kw):
 def test_chain_argument_errors_are_reported_before_launch(lib, field, value, code):
     a = _chain(**{field: value})
     assert lib.spec_verify_chain(C.byref(a), None) == code
+
+
+def test_consulted_only_is_sampling_only(lib):
+    from draft_verification_gb300 import _lib
+    # refused before anything touches the device (no control-word clear)
+    a = _chain(mode=_lib.SPEC_GREEDY, consulted_only=1)
+    assert lib.spec_verify_chain(C.byref(a), None) == -1
+    a = _chain(gamma=0, consulted_only=1)
+    assert lib.spec_verify_chain(C.byref(a), None) == -1
 
 
 def test_tree_and_cascade_argument_errors(lib):
