@@ -754,8 +754,9 @@ struct TreeSmem {
   float* gq;   // [N] draft logit of the same
   int* scr_a;  // [N] depth pointer jumping, then the children of the current node
   int* scr_b;  // [N] depth pointer jumping, then the kept path
+  float* u;    // [N] node i's accept uniform
 };
-constexpr int kTreeSmemPerNode = 40;
+constexpr int kTreeSmemPerNode = 44;
 constexpr int kMaxNodes = 1024;
 
 __device__ __forceinline__ TreeSmem tree_smem(char* base, int N) {
@@ -767,6 +768,7 @@ __device__ __forceinline__ TreeSmem tree_smem(char* base, int N) {
   t.gq = t.gp + N;
   t.scr_a = reinterpret_cast<int*>(t.gq + N);
   t.scr_b = t.scr_a + N;
+  t.u = reinterpret_cast<float*>(t.scr_b + N);
   return t;
 }
 
@@ -793,6 +795,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   __shared__ PassSmem ps;
   __shared__ float2 stage[kStage];
   __shared__ int err_s, nk_s, keep_s;
+  __shared__ float v_s;
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
   const int N = P.N;
@@ -852,9 +855,11 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
     if (!kGreedy && err_s == 0) {
       for (int i = tid + 1; i < N; i += kThreads) {
         const long long off = (row0 + ts.par[i]) * P.ld + ts.tk[i];
+        ts.u[i] = P.u[row0 + i];
         ts.gp[i] = load_elem(static_cast<const T*>(P.target) + off);
         ts.gq[i] = load_elem(static_cast<const T*>(P.draft) + off);
       }
+      if (tid == 0) v_s = P.v[b];
     }
   }
   pdl_wait();
@@ -945,7 +950,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
           const double pt = prob(ts.gp[ch], sp.x, sp.y, c);
           const double qt = prob(ts.gq[ch], sq.x, sq.y, c);
           const double num = fmax(0.0, pt - cc * qt);
-          keep_s = static_cast<double>(P.u[row0 + ch]) * W * qt < num;
+          keep_s = static_cast<double>(ts.u[ch]) * W * qt < num;
         }
         __syncthreads();
         if (keep_s) {
@@ -986,7 +991,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         }
         Z = cluster_pass(S, P.V, c, G.ntiles, buf, ps, res_ok);
       }
-      token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, P.v[b]), false, ps);
+      token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, v_s), false, ps);
       writer = token >= 0;
       break;
     }
