@@ -1,6 +1,6 @@
 // Batched draft verification kernels and their launch sequence.
 //
-// Every call is two kernels on the caller's stream; the second is launched
+// A call is two kernels on the caller's stream; the second is launched
 // with programmatic dependent launch, so it is resident and has read its own
 // inputs by the time the first finishes:
 //
@@ -17,8 +17,15 @@
 //                    shared memory (walk.cuh); the CTA holding the drawn
 //                    index's tile writes the result.  Greedy calls use one
 //                    CTA per sequence.  The cascade runs both of its stages
-//                    in the same cluster; a tree runs its serial walk in
-//                    every CTA of its cluster and splits each pass.
+//                    in the same cluster, the k-model pipeline its k - 1
+//                    stages; a tree runs its serial walk in every CTA of its
+//                    cluster and splits each pass.
+//
+// Variants: large sampling chains run as batch groups (several statistics
+// and walk launches on forked library streams); the consulted-only chain
+// mode replaces the statistics kernel by stats_consulted_kernel (positions
+// in order, later positions of a rejected sequence skipped) after clearing
+// its control words with one memset.
 //
 // Rules (pages: the Pith review of PipeSpec, "What carries the argument" and
 // the acceptance rule of Leviathan et al. its Circularity Check cites; Staged
@@ -27,7 +34,8 @@
 //    first rejection, from the bonus row when all are kept; greedy keeps
 //    drafts equal to the target argmax;
 //  * cascade: stage 1 (M_1 verifies M_0's drafts), then stage 2 (M_2 verifies
-//    the first tokens of stage 1's output);
+//    the first tokens of stage 1's output); the pipeline generalises it to k
+//    models with an optional final-stage bonus;
 //  * tree: a serial walk from the root (each rejected sibling changes the
 //    distribution the next sibling is tested against).
 //

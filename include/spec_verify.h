@@ -54,8 +54,12 @@
  *    walk) per batch group; large sampling chain calls are split into
  *    groups that run on library streams forked from `stream` and joined
  *    back into it, so the call is ordered on `stream` like any other work.
+ *    A consulted-only chain call adds one memset of its control words;
+ *    spec_compact_tree_path is one kernel.
  *  - The workspace holds the row statistics passed from the first kernel of
- *    a call to the second (8 bytes per sequence, row and 8192-element chunk).
+ *    a call to the second (8 bytes per sequence, row and 8192-element chunk;
+ *    a chain's also 4 bytes per sequence and position for its consulted-only
+ *    control words, cleared by the call that uses them).
  *    Size it with the matching *_workspace_size function; it needs no
  *    initialisation and nothing in it outlives a call.  Two calls that can
  *    run at the same time (other streams) need two workspaces.  Results are
