@@ -18,10 +18,12 @@ Modules
                   every earlier buffer, an optional final-stage bonus).
 ``consulted``     the chain rule consulting rows in position order (rows after
                   the first rejection are never read).
+``clasp``         the CLaSp layer-selection dynamic program and its
+                  backtracking, on synthetic residual layers.
 
 Every function states the passage it follows.  Points where the pages are
 silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import closed_forms, compact, consulted, pipeline, verify  # noqa: F401
+from . import clasp, closed_forms, compact, consulted, pipeline, verify  # noqa: F401
