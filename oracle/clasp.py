@@ -18,9 +18,12 @@ Readings (R16 in the design notes):
   * Both branches: the one with the larger cosine wins; a tie keeps the layer.
   * Backtracking follows the stored decisions from (L, M).
   * The layer functions of the synthetic workload are residual linear maps
-    f_l(x) = x + W_l x with bfloat16 weights; the product W_l x is formed from
-    x rounded to bfloat16 (the precision the GPU's tensor-core product takes
-    its operands in), accumulated here in float64.
+    f_l(x) = x + W_l x with bfloat16 weights and the product taken at full
+    precision (float64 here).  Rounding x to bfloat16 before the product was
+    rejected: the rounding of each layer's input is then decided by noise far
+    below the bfloat16 step, and a float32 and a float64 run of the same
+    skip path drift apart by about 5e-3 relative after 32 layers, so no two
+    implementations would agree on the decisions.
 """
 
 from __future__ import annotations
@@ -29,7 +32,8 @@ import numpy as np
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
-    """float64 -> float32 -> nearest bfloat16 (ties to even), as float64."""
+    """float64 -> float32 -> nearest bfloat16 (ties to even), as float64
+    (used to make bfloat16 weights in tests)."""
     f = np.asarray(x, np.float64).astype(np.float32)
     bits = f.view(np.uint32)
     rounding = np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))
@@ -42,7 +46,7 @@ def cosine(a: np.ndarray, b: np.ndarray) -> float:
 
 def layer(W: np.ndarray, x: np.ndarray) -> np.ndarray:
     """f(x) = x + W x, W float64 values of bfloat16 weights [d, d] (out, in)."""
-    return x + W @ bf16_round(x)
+    return x + W @ x
 
 
 def clasp_dp(h, Ws, M):
@@ -55,10 +59,11 @@ def clasp_dp(h, Ws, M):
     choice = {}
     gap = {}
     for i in range(1, L + 1):
+        W = np.asarray(Ws[i - 1], np.float64)
         for j in range(0, min(i, M) + 1):
             cands = []
             if j <= i - 1:  # keep layer i - 1
-                k = layer(Ws[i - 1], g[(i - 1, j)])
+                k = layer(W, g[(i - 1, j)])
                 cands.append((cosine(h[i], k), 0, k))
             if j >= 1:      # skip layer i - 1
                 s = g[(i - 1, j - 1)]
@@ -93,13 +98,13 @@ def apply_skips(h0, Ws, mask):
 
 
 def clasp_batch(h, Ws, M):
-    """h [B, L+1, d]; Ws [L, d, d] (float values of the bf16 weights).
+    """h [B, L+1, d]; Ws [L, d, d] (float values of the bf16 weights; each
+    layer is taken to float64 as the DP reaches it).
     Returns mask [B, L], score [B], margin [B]."""
     B, L = h.shape[0], len(Ws)
-    Wl = [np.asarray(W, np.float64) for W in Ws]
     mask = np.zeros((B, L), np.int64)
     score = np.zeros(B)
     margin = np.zeros(B)
     for b in range(B):
-        mask[b], score[b], margin[b] = clasp_dp(np.asarray(h[b], np.float64), Wl, M)
+        mask[b], score[b], margin[b] = clasp_dp(np.asarray(h[b], np.float64), Ws, M)
     return mask, score, margin
