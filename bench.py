@@ -56,9 +56,13 @@ KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification
 # greedy walk kernels
 KERNELS = {"chain": ["stats_kernel", "chain_walk_kernel"], "tree": ["stats_kernel", "tree_kernel"],
            "cascade": ["stats_kernel", "cascade_walk_kernel"], "compact": ["compact_kernel"],
-           "pipeline": ["stats_kernel", "pipeline_walk_kernel"]}
+           "pipeline": ["stats_kernel", "pipeline_walk_kernel"],
+           "clasp": ["clasp_init_kernel", "clasp_step_kernel", "clasp_backtrack_kernel"]}
 COMPACT_METRIC = "cache rows compacted/sec and GB/s moved vs GB300 HBM peak (1 GPU)"
 COMPACT_SOURCES = ["draft_verification_gb300/csrc/compact.cu"]
+CLASP_METRIC = "CLaSp layer selections/sec and weight GB/s vs GB300 HBM and bf16 tensor peaks (1 GPU)"
+CLASP_SOURCES = ["draft_verification_gb300/csrc/clasp.cu"]
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -149,6 +153,19 @@ def measured_peak():
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def measured_tensor_peak(sustained: bool):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as fh:
+            mp = json.load(fh)
+        if key in mp:
+            return float(mp[key]), f"measured (MEASURED_PEAKS.json {key})"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16, no MEASURED_PEAKS.json)"
 
 
 def kernel_source_hash(sources=None) -> str:
@@ -747,6 +764,200 @@ def compact_main(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# CLaSp layer selection (a workload of its own)
+# --------------------------------------------------------------------------
+
+def clasp_columns(spec) -> int:
+    """GEMM columns of one call: two bfloat16 terms of every state that may
+    keep its layer and can still reach (L, M), summed over the layers."""
+    L, M = spec.L, spec.M
+    n = 0
+    for i in range(1, L + 1):
+        lo, last_keep = max(0, M - (L - i)), min(i - 1, M)
+        n += max(0, last_keep - lo + 1)
+    return 2 * spec.B * n
+
+
+def clasp_bytes(spec) -> int:
+    """Algorithmic HBM bytes of one call: every weight read once, the hidden
+    states read once (the DP's states and products stay in L2)."""
+    return spec.L * spec.d * spec.d * 2 + spec.B * (spec.L + 1) * spec.d * 4
+
+
+def clasp_flops(spec) -> int:
+    return 2 * spec.d * spec.d * clasp_columns(spec)
+
+
+def clasp_oracle_rate(w, budget_s: float):
+    """Selections/s of the oracle on whole sequences until the budget is
+    spent; cores = process CPU time over wall time (NumPy's BLAS may use
+    several threads for the matrix-vector products)."""
+    from oracle import clasp as K  # the reference is only used on this leg
+    from workloads import synth
+    s = w["spec"]
+    Wv = synth.clasp_weight_values(w)
+    t0, c0 = time.perf_counter(), time.process_time()
+    n = 0
+    while True:
+        K.clasp_dp(w["hidden"][n % s.B].astype(np.float64), Wv, s.M)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    cores = (time.process_time() - c0) / el
+    return n / el, f"{n} whole sequences ({el:.1f} s; NumPy float64, BLAS matrix-vector products)", round(cores, 1)
+
+
+def clasp_config(w) -> dict:
+    s = w["spec"]
+    return {"workload": s.name, "kind": "clasp", "batch": s.B, "layers": s.L, "width": s.d, "skips": s.M,
+            "layer": "x + W x, W bf16 ~ N(0, %.2f^2/d)" % s.scale, "gemm_columns_per_call": clasp_columns(s)}
+
+
+def run_clasp(args, w):
+    import torch
+    import draft_verification_gb300 as dv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dv.build_library()
+    s = w["spec"]
+    hidden = torch.from_numpy(w["hidden"]).to(dev)
+    weights = torch.from_numpy(w["weights"].view(np.int16)).to(dev).view(torch.bfloat16)
+    stream = torch.cuda.Stream(dev)
+    plan = dv.ClaspPlan(hidden, weights, s.M)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            plan.run(stream)
+    stream.synchronize()
+    launch = "cuda_graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            plan.run(stream)
+        stream.synchronize()
+    except Exception as exc:
+        launch = f"eager ({type(exc).__name__})"
+        graph = None
+
+    def run_steps(k):
+        for _ in range(k):
+            if graph is not None:
+                graph.replay()
+            else:
+                plan.run(stream)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            run_steps(50)
+            stream.synchronize()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end through the public call: the hidden states from pinned host
+    # memory every step, the skip masks and scores back; the weights are the
+    # model's parameters and stay resident
+    host_h = torch.from_numpy(w["hidden"]).pin_memory()
+    h2d = host_h.numel() * 4
+
+    def e2e_call():
+        with torch.cuda.stream(stream):
+            o = dv.clasp_layer_select(host_h, weights, s.M, device=dev, stream=stream)
+        stream.synchronize()
+        return o
+
+    for _ in range(2):
+        e2e_call()
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        o = e2e_call()
+    el = time.perf_counter() - t0
+    d2h = sum(v.numel() * v.element_size() for v in o.values())
+
+    hbm_peak, hbm_src = measured_peak()
+    tc_peak, tc_src = measured_tensor_peak(sustained=False)
+    gbs = clasp_bytes(s) / (ms * 1e-3) / 1e9
+    tfs = clasp_flops(s) / (ms * 1e-3) / 1e12
+    hbm_frac, tc_frac = gbs / hbm_peak, tfs / tc_peak
+    # the roofline bound is the resource the call would saturate first
+    t_hbm = clasp_bytes(s) / (hbm_peak * 1e9)
+    t_tc = clasp_flops(s) / (tc_peak * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_frac,
+                "peak_source": hbm_src, "algorithmic_bytes": clasp_bytes(s)}
+    else:
+        roof = {"bound": "tensor", "achieved": tfs, "peak": tc_peak, "unit": "TFLOP/s", "frac": tc_frac,
+                "peak_source": tc_src, "algorithmic_flops": clasp_flops(s)}
+    roof.update({"kernel": "whole call: per layer one cuBLAS bf16 GEMM + clasp_step_kernel",
+                 "unit_of_work": "one layer-selection call", "kernel_ms": ms,
+                 "other": {"hbm_GBps": gbs, "hbm_frac": hbm_frac, "tensor_TFLOPs": tfs, "tensor_frac": tc_frac},
+                 "traffic": profiled_traffic(s.name, CLASP_SOURCES)})
+    return {
+        "metric": CLASP_METRIC, "value": s.B / (ms * 1e-3), "unit": "selections/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x2 split, f32 accumulate",
+        "data": "synthetic (seeded bf16 residual layers; hidden states of the full stack plus noise)",
+        "config": dict(clasp_config(w), parallelism="1 GPU", launch=launch,
+                       l2_policy=f"weights {clasp_bytes(s) / 2**20:.0f} MB per call > L2: every call streams them"),
+        "roofline": roof,
+        "e2e": {"value": s.B / (el / n), "unit": "selections/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n,
+                "note": "hidden states host to device each step; weights resident"},
+        "gpu_launches": args.steps * (s.L + 2),
+        "clocks": clock_info,
+    }
+
+
+def clasp_main(args, w, rank):
+    s = w["spec"]
+    if args.impl == "reference":
+        if rank == 0:
+            rate, desc, cores = clasp_oracle_rate(w, args.cpu_seconds)
+            print(json.dumps({
+                "impl": "reference", "metric": CLASP_METRIC, "value": rate, "unit": "selections/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * s.B / rate, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": clasp_config(w),
+                "cpu_baseline": {"value": rate, "unit": "selections/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": rate, "unit": "selections/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+        return
+    if args.profile:
+        import torch
+        import draft_verification_gb300 as dv
+        dev = torch.device("cuda", 0)
+        dv.build_library()
+        hidden = torch.from_numpy(w["hidden"]).to(dev)
+        weights = torch.from_numpy(w["weights"].view(np.int16)).to(dev).view(torch.bfloat16)
+        plan = dv.ClaspPlan(hidden, weights, s.M)
+        for _ in range(args.warmup + args.steps):
+            plan.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": s.name, "calls": args.warmup + args.steps}))
+        return
+    if rank != 0:
+        return  # one GPU: the other ranks of a replica launch have nothing to add
+    line = run_clasp(args, w)
+    if not args.no_cpu_baseline:
+        rate, desc, cores = clasp_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "selections/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
 def pipeline_e2e(args, w, dev, stream):
     """e2e_rate for the k-model pipeline (lists of per-model inputs)."""
     import torch
@@ -812,10 +1023,13 @@ def main():
     if args.workload in synth.COMPACT_SPECS:
         compact_main(args, synth.make(synth.COMPACT_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
         return
+    if args.workload in synth.CLASP_SPECS:
+        clasp_main(args, synth.make(synth.CLASP_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
+        return
     specs = dict(synth.SPECS, **synth.PIPELINE_SPECS)
     if args.workload not in specs:
         raise SystemExit(f"unknown workload {args.workload}; choose from "
-                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS)}")
+                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS) + sorted(synth.CLASP_SPECS)}")
     w = synth.make(specs[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":

@@ -88,6 +88,14 @@ class CompactArgs(C.Structure):
     ]
 
 
+class ClaspArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("L", C.c_int), ("d", C.c_int), ("M", C.c_int),
+        ("hidden", _vp), ("weights", _vp), ("skip_mask", _vp), ("score", _vp), ("choice", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+    ]
+
+
 # every symbol include/spec_verify.h declares, with its ctypes signature
 SIGNATURES = {
     "spec_chain_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
@@ -100,6 +108,8 @@ SIGNATURES = {
     "spec_pipeline_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int, C.c_int]),
     "spec_verify_pipeline": (C.c_int, [C.POINTER(PipelineArgs), _vp]),
     "spec_compact_tree_path": (C.c_int, [C.POINTER(CompactArgs), _vp]),
+    "spec_clasp_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spec_clasp_layer_select": (C.c_int, [C.POINTER(ClaspArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
 }
 

@@ -408,7 +408,55 @@ def verify_pipeline(models, tokens, windows, us=None, vs=None, base=None, *, gre
     return _finish(plan.run(stream), host)
 
 
+class ClaspPlan(_Plan):
+    """CLaSp layer selection bound to fixed buffers.  See spec_clasp_layer_select.
+
+    hidden float32 [B, L+1, d] (h_0 .. h_L), weights bfloat16 [L, d, d]
+    (W_l[out][in]), M layers to skip.  ``run()`` returns skip_mask int32
+    [B, L], score float32 [B] and, with ``choices=True``, choice uint8
+    [B, L, M+1] (1 skip, 0 keep, 255 not evaluated).
+    """
+
+    def __init__(self, hidden, weights, M, *, choices=False, workspace=None):
+        lib = L.lib()
+        if hidden.dtype != torch.float32 or not hidden.is_contiguous() or hidden.dim() != 3:
+            raise TypeError("hidden: expected a contiguous float32 tensor [B, L+1, d]")
+        B, L1, d = hidden.shape
+        if weights.dtype != torch.bfloat16 or not weights.is_contiguous() or tuple(weights.shape) != (L1 - 1, d, d):
+            raise TypeError(f"weights: expected a contiguous bfloat16 tensor [{L1 - 1}, {d}, {d}]")
+        dev = hidden.device
+        need = int(lib.spec_clasp_workspace_size(B, L1 - 1, d, int(M)))
+        if need == 0:
+            raise ValueError(f"CLaSp sizes out of range: B={B} L={L1 - 1} d={d} M={M}")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        self.out = {"skip_mask": torch.empty((B, L1 - 1), dtype=torch.int32, device=dev),
+                    "score": torch.empty(B, dtype=torch.float32, device=dev)}
+        if choices:
+            self.out["choice"] = torch.empty((B, L1 - 1, int(M) + 1), dtype=torch.uint8, device=dev)
+        self._keep = (hidden, weights)
+        a = L.ClaspArgs()
+        a.B, a.L, a.d, a.M = B, L1 - 1, d, int(M)
+        a.hidden, a.weights = _ptr(hidden), _ptr(weights)
+        a.skip_mask, a.score = _ptr(self.out["skip_mask"]), _ptr(self.out["score"])
+        a.choice = _ptr(self.out.get("choice"))
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        self.args = a
+        self._call = lib.spec_clasp_layer_select
+
+
+def clasp_layer_select(hidden, weights, M, *, choices=False, device="cuda", stream=None):
+    """One CLaSp layer selection (host tensors in, host tensors out; device
+    tensors stay on the device).  See ClaspPlan."""
+    host = hidden.device.type == "cpu"
+    if host:
+        hidden, weights = _to_device([hidden, weights], device)
+    plan = ClaspPlan(hidden, weights, M, choices=choices)
+    return _finish(plan.run(stream), host)
+
+
 def workspace_bytes(kind: str, *sizes) -> int:
     fn = {"chain": "spec_chain_workspace_size", "tree": "spec_tree_workspace_size",
-          "cascade": "spec_cascade_workspace_size"}[kind]
+          "cascade": "spec_cascade_workspace_size", "clasp": "spec_clasp_workspace_size"}[kind]
     return int(getattr(L.lib(), fn)(*sizes))

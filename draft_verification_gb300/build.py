@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libspecverify.so"
-SOURCES = ["verify.cu", "api.cu", "noalloc.cu", "compact.cu"]
+SOURCES = ["verify.cu", "api.cu", "noalloc.cu", "compact.cu", "clasp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v"]
 
@@ -78,7 +78,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 sys.stderr.write(f"[build] {name}\n{r.stderr}")
     lib = lib_path()
     if force or jobs or not os.path.exists(lib):
-        cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart", "-lcublas"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

@@ -33,8 +33,9 @@
  *
  * Conventions for every entry point.
  *  - All array pointers are DEVICE pointers, row-major, caller-owned.  The
- *    library never allocates, frees or synchronises; every call is
- *    asynchronous on `stream`.  Inputs are only read; outputs are written
+ *    library never allocates device memory, frees or synchronises (the one
+ *    exception: spec_clasp_layer_select creates a cuBLAS handle on its first
+ *    call on a device); every call is asynchronous on `stream`.  Inputs are only read; outputs are written
  *    completely (including on a data error).
  *  - Logit arrays hold float32 (SPEC_F32) or bfloat16 (SPEC_BF16) values.
  *    Row r of a logit array starts at element r * ld; only the first V
@@ -55,7 +56,8 @@
  *    groups that run on library streams forked from `stream` and joined
  *    back into it, so the call is ordered on `stream` like any other work.
  *    A consulted-only chain call adds one memset of its control words;
- *    spec_compact_tree_path is one kernel.
+ *    spec_compact_tree_path is one kernel; spec_clasp_layer_select is
+ *    L + 2 kernels and L cuBLAS GEMMs (see its section).
  *  - The workspace holds the row statistics passed from the first kernel of
  *    a call to the second (8 bytes per sequence, row and 8192-element chunk;
  *    a chain's also 4 bytes per sequence and position for its consulted-only
@@ -362,6 +364,64 @@ typedef struct spec_compact_args {
 } spec_compact_args;
 
 spec_status spec_compact_tree_path(const spec_compact_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* CLaSp layer selection.  Pith review of "CLaSp: In-Context Layer Skip    */
+/* for Self-Speculative Decoding" (arXiv 2505.24196), "What carries the    */
+/* argument", and its referee report, minor comments 1 and 4.  For each    */
+/* sequence, given the full model's hidden states h_0 .. h_L, choose which */
+/* M of the L layers the draft skips: g(0, 0) = h_0; for i = 1 .. L and    */
+/* each number of skips j, g(i, j) is the candidate with the larger cosine */
+/* to h_i among f_{i-1}(g(i-1, j)) (keep layer i-1, when j <= i-1) and     */
+/* g(i-1, j-1) (skip it, when j >= 1); a tie keeps the layer.  The skip    */
+/* set is read back from (L, M) through the stored decisions.              */
+/*  - Layer functions: f_l(x) = x + W_l x, W_l bfloat16 [d, d] row-major   */
+/*    (out, in).  States are float32; the product splits x into two        */
+/*    bfloat16 terms (hi = bf16(x), lo = bf16(x - hi)) and runs on the     */
+/*    tensor cores with float32 accumulation, so it carries about 16       */
+/*    significant bits of x.  The cosines come from float32 partial sums   */
+/*    combined in double.                                                  */
+/*  - Only states that can still reach (L, M) are evaluated,               */
+/*    max(0, M - (L - i)) <= j <= min(i, M); others never feed g(L, M).    */
+/*  - Per layer: one cuBLAS bf16 GEMM over both terms of the batch's      */
+/*    states (the weights are streamed once per layer for the whole        */
+/*    batch), then one DP-step kernel; an initial and a final              */
+/*    (backtracking) kernel.                                               */
+/*  - cuBLAS: the first call on a device creates one cuBLAS handle for the */
+/*    device (cuBLAS allocates its own small state then); do not make that */
+/*    first call inside a stream capture.  Calls set the handle's stream   */
+/*    and point its workspace into `workspace`; calls from several host    */
+/*    threads are serialised while they enqueue.                           */
+/*  - Non-finite values are not checked: a NaN cosine never wins, so a     */
+/*    decision involving one keeps the layer when it can.                  */
+/*  - Results are deterministic for the same inputs on the same GPU.       */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_clasp_args {
+  int B;                       /* sequences, 1..65535                              */
+  int L;                       /* layers, 1..4096                                  */
+  int d;                       /* hidden width, a multiple of 8, 8..65536          */
+  int M;                       /* layers to skip, 0..L                             */
+  const float* hidden;         /* [B, L+1, d]: h_0 .. h_L; 16-byte aligned         */
+  const void* weights;         /* [L, d, d] bfloat16 W_l[out][in]; 16-byte aligned */
+  int* skip_mask;              /* out [B, L]: 1 where layer l is skipped, else 0   */
+  float* score;                /* out [B]: D(L, M) = cos(h_L, g(L, M))             */
+  unsigned char* choice;       /* out [B, L, M+1], optional: decision of state     */
+                               /* (i = l+1, j) at [b, l, j]: 1 skip, 0 keep, 255   */
+                               /* for states not evaluated                         */
+  void* workspace;             /* 256-byte aligned, spec_clasp_workspace_size bytes */
+  size_t workspace_bytes;
+} spec_clasp_args;
+
+/* Workspace for spec_clasp_layer_select: 2 (M+1) B d float32 states,        */
+/* 2 (M+1) B d float32 products, 2 (M+1) B d bfloat16 split terms,           */
+/* L (M+1) B decision bytes and 32 MiB for cuBLAS (each part rounded up to   */
+/* 256 bytes).  0 for sizes outside the limits above.                        */
+size_t spec_clasp_workspace_size(int B, int L, int d, int M);
+/* SPEC_EINVAL: a size outside the limits or a NULL required pointer;        */
+/* SPEC_EALIGN: hidden or weights not 16-byte aligned; SPEC_EWORKSPACE:      */
+/* workspace NULL, short or not 256-byte aligned; SPEC_ECUDA: a launch or a  */
+/* cuBLAS call failed (or the cuBLAS handle could not be created).           */
+spec_status spec_clasp_layer_select(const spec_clasp_args* args, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* spec_status_string(spec_status status);

@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -44,7 +44,7 @@ def test_struct_layout_matches_header(tmp_path):
         pytest.skip("gcc or CUDA headers missing")
     structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
                "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs,
-               "spec_pipeline_args": _lib.PipelineArgs}
+               "spec_pipeline_args": _lib.PipelineArgs, "spec_clasp_args": _lib.ClaspArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -253,3 +253,54 @@ def test_pipeline_argument_errors_and_workspace(lib):
     a.u[2] = None
     assert lib.spec_verify_pipeline(C.byref(a), None) == -1
     assert lib.spec_verify_pipeline(None, None) == -1
+
+
+def _clasp(**kw):
+    from draft_verification_gb300 import _lib
+    a = _lib.ClaspArgs()
+    a.B, a.L, a.d, a.M = 2, 4, 64, 2
+    fake = 0x10000  # 256-byte aligned, never dereferenced
+    for f in ("hidden", "weights", "skip_mask", "score", "workspace"):
+        setattr(a, f, fake)
+    a.workspace_bytes = 1 << 30
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_clasp_workspace_size(lib):
+    B, L, d, M = 16, 32, 4096, 12
+    cells = (M + 1) * B * d
+
+    def r(x):
+        return 256 * ((x + 255) // 256)
+    want = 2 * r(4 * cells) + r(2 * 2 * cells) + r(2 * 4 * cells) + r(L * (M + 1) * B) + (32 << 20)
+    assert lib.spec_clasp_workspace_size(B, L, d, M) == want
+    for bad in [(0, 4, 64, 2), (65536, 4, 64, 2), (2, 0, 64, 2), (2, 4097, 64, 2), (2, 4, 60, 2), (2, 4, 0, 2),
+                (2, 4, 65544, 2), (2, 4, 64, -1), (2, 4, 64, 5)]:
+        assert lib.spec_clasp_workspace_size(*bad) == 0, bad
+    assert lib.spec_clasp_workspace_size(2, 4, 64, 4) > 0  # M = L: skip every layer
+    assert lib.spec_clasp_workspace_size(2, 4, 64, 0) > 0  # M = 0: keep every layer
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), -1), (dict(L=0), -1), (dict(d=12), -1), (dict(M=5), -1), (dict(M=-1), -1),
+    (dict(hidden=None), -1), (dict(weights=None), -1), (dict(skip_mask=None), -1), (dict(score=None), -1),
+    (dict(hidden=0x10004), -3), (dict(weights=0x10008), -3),
+    (dict(workspace=None), -4), (dict(workspace_bytes=1024), -4), (dict(workspace=0x10010), -4),
+])
+def test_clasp_argument_errors_are_reported_before_launch(lib, kw, code):
+    assert lib.spec_clasp_layer_select(C.byref(_clasp(**kw)), None) == code
+    assert lib.spec_clasp_layer_select(None, None) == -1
+
+
+def test_clasp_accepts_exactly_its_workspace_size(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on placeholder pointers")
+    from draft_verification_gb300 import _lib
+    a = _clasp()
+    a.workspace_bytes = lib.spec_clasp_workspace_size(a.B, a.L, a.d, a.M)
+    assert lib.spec_clasp_layer_select(C.byref(a), None) == _lib.SPEC_ECUDA  # no GPU here
+    a.workspace_bytes -= 1
+    assert lib.spec_clasp_layer_select(C.byref(a), None) == -4

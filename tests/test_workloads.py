@@ -70,3 +70,16 @@ def test_tree_topology_reading():
         depth[i] = depth[parent[i]] + 1
     assert list(np.bincount(depth)) == [1, 4, 9, 11, 13, 13, 13]
     assert int((np.bincount(parent[1:], minlength=64) == 0).sum()) == 18
+
+
+def test_clasp_workload_is_seeded_and_shaped():
+    spec = synth.with_sizes(synth.CLASP_SPECS["clasp_b16_l32_d4096_m12_bf16"], B=3, L=5, d=64, M=2)
+    a, b, c = synth.make(spec, seed=1), synth.make(spec, seed=1), synth.make(spec, seed=2)
+    assert a["weights"].shape == (5, 64, 64) and a["weights"].dtype == np.uint16
+    assert a["hidden"].shape == (3, 6, 64) and a["hidden"].dtype == np.float32
+    assert np.array_equal(a["weights"], b["weights"]) and np.array_equal(a["hidden"], b["hidden"])
+    assert not np.array_equal(a["hidden"], c["hidden"])
+    assert np.isfinite(a["hidden"]).all()
+    # weights are bf16 values of N(0, scale^2 / d): sample sd near scale / sqrt(d)
+    wv = synth.clasp_weight_values(a)
+    assert abs(wv.std() * np.sqrt(64) / spec.scale - 1) < 0.05

@@ -222,6 +222,30 @@ COMPACT_SPECS = {
 }
 
 
+@dataclass(frozen=True)
+class ClaspSpec:
+    """CLaSp layer selection: B sequences, an L-layer stack of width d whose
+    layers are residual linear maps with bfloat16 weights W_l ~ N(0, scale^2
+    / d), and M layers to skip.  The full model's hidden states h_0 .. h_L
+    come from h_0 ~ N(0, 1) and h_{l+1} = h_l + W_l h_l + N(0, tau^2) in
+    float64 (unrounded inputs plus per-layer noise: the full model is not
+    exactly the stack the draft's layers compute), stored as float32."""
+    name: str
+    B: int
+    L: int
+    d: int
+    M: int
+    scale: float = 0.3
+    tau: float = 0.1
+
+
+# LLaMA-3-8B's depth and width (32 layers, d = 4096) with 12 of 32 layers
+# skipped, the setting of the CLaSp page's DP versus brute-force comparison.
+CLASP_SPECS = {
+    "clasp_b16_l32_d4096_m12_bf16": ClaspSpec("clasp_b16_l32_d4096_m12_bf16", B=16, L=32, d=4096, M=12),
+}
+
+
 def with_sizes(spec, **kw):
     """A copy of a spec with some fields replaced (e.g. a smaller B or V)."""
     return dataclasses.replace(spec, **kw)
@@ -393,6 +417,30 @@ def make_compact(spec: CompactSpec, seed: int = 0) -> dict:
                 path_len=path_len, prefix_len=prefix_len, parent=parent)
 
 
+def make_clasp(spec: ClaspSpec, seed: int = 0) -> dict:
+    """CLaSp workload: weights uint16 [L, d, d] (bfloat16 bits of W_l[out][in]),
+    hidden float32 [B, L+1, d] (h_0 .. h_L of the full model)."""
+    rng = _rng(seed, 9)
+    B, L, d = spec.B, spec.L, spec.d
+    weights = np.empty((L, d, d), np.uint16)
+    sd = np.float32(spec.scale / np.sqrt(d))
+    for l in range(L):
+        weights[l] = bf16_from_float32(rng.standard_normal((d, d), dtype=np.float32) * sd)
+    hidden = np.empty((B, L + 1, d), np.float32)
+    x = rng.standard_normal((B, d))
+    hidden[:, 0] = x
+    for l in range(L):
+        Wl = float32_from_bf16(weights[l]).astype(np.float64)
+        x = x + x @ Wl.T + spec.tau * rng.standard_normal((B, d))
+        hidden[:, l + 1] = x
+    return dict(kind="clasp", spec=spec, weights=weights, hidden=hidden)
+
+
+def clasp_weight_values(w: dict) -> np.ndarray:
+    """The workload's weights as float32 values [L, d, d] (exact)."""
+    return float32_from_bf16(w["weights"])
+
+
 def pipeline_rows(spec: PipelineSpec, s: int) -> int:
     """Rows per sequence of model s."""
     g = spec.windows
@@ -435,10 +483,11 @@ def make_pipeline(spec: PipelineSpec, seed: int = 0) -> dict:
 
 def make(spec, seed: int = 0) -> dict:
     if isinstance(spec, str):
-        spec = SPECS[spec] if spec in SPECS else (COMPACT_SPECS[spec] if spec in COMPACT_SPECS
-                                                  else PIPELINE_SPECS[spec])
+        spec = {**SPECS, **COMPACT_SPECS, **PIPELINE_SPECS, **CLASP_SPECS}[spec]
     if isinstance(spec, PipelineSpec):
         return make_pipeline(spec, seed)
+    if isinstance(spec, ClaspSpec):
+        return make_clasp(spec, seed)
     if isinstance(spec, CompactSpec):
         return make_compact(spec, seed)
     if isinstance(spec, ChainSpec):
