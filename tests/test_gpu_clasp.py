@@ -115,6 +115,7 @@ CASES = [
     synth.with_sizes(BASE, name="b3_l1_d8_m0", B=3, L=1, d=8, M=0),
     synth.with_sizes(BASE, name="b3_l1_d8_m1", B=3, L=1, d=8, M=1),
     synth.with_sizes(BASE, name="b130_l6_d32_m2_two_blocks", B=130, L=6, d=32, M=2),
+    synth.with_sizes(BASE, name="b4_l6_d272_m2_two_ksplits", B=4, L=6, d=272, M=2),
     synth.with_sizes(BASE, name="b8_l16_d1024_m6_scale05", B=8, L=16, d=1024, M=6, scale=0.5, tau=0.2),
 ]
 
