@@ -20,14 +20,12 @@
 // One call, per layer i = 1 .. L (the layer applied is l = i - 1):
 //   1. the products Y = W_l [hi lo] for every state that can still reach
 //      (L, M) and may keep layer l: one cuBLAS bf16 GEMM (m = d, n = 2 x B x
-//      states, k = d) that streams W_l from HBM once for the whole batch.
-//      With few columns the GEMM is split S ways along k (a strided batch of
-//      S GEMMs writing S partial products) so that enough CTAs stream the
-//      weights; the step kernel adds the partials in a fixed order;
-//   2. clasp_step_kernel, one CTA per (sequence, state j): the cosines of
-//      both candidates with h_i (float32 sums, the warps' totals combined in
-//      double by one thread), the decision, and the chosen state written as
-//      the next g(i, j) in float32 and as its two bfloat16 terms.
+//      states, k = d) that streams W_l from HBM once for the whole batch;
+//   2. clasp_step_kernel, one CTA per (sequence, state j), launched with
+//      programmatic dependent launch so that its launch overlaps the GEMM's
+//      tail (every memory access waits for the GEMM): the cosines of both
+//      candidates with h_i (float32 sums), the decision, and the chosen state
+//      written as the next g(i, j) in float32 and as its two bfloat16 terms.
 // Then clasp_backtrack_kernel, one warp per sequence, stages the sequence's
 // decisions in shared memory and walks them back from (L, M).
 //
@@ -35,10 +33,15 @@
 // state with fewer skips can no longer reach M skips by layer L, so it never
 // feeds g(L, M).  This changes no decision that the backtracking visits.
 //
+// Precision: the sums of the five products are float32 (per-thread partials
+// of at most d / 2048 float4 groups, then shuffle trees), relative error
+// about 1e-6 at d = 4096, far inside the margin a decision needs to be
+// reproducible against a float64 evaluation (1e-5 and more on the cosines).
+//
 // Workspace (every part 256-byte aligned):
 //   G0, G1  float32 [M+1][B][d]        states g(i-1, .) and g(i, .), ping-pong
 //   X       bfloat16 [M+1][2][B][d]    the states' hi and lo terms
-//   Y       float32 [S][M+1][2][B][d]  W_l X, one partial per k-split
+//   Y       float32 [M+1][2][B][d]     W_l X
 //   table   uint8 [B][L][M+1]          decisions (1 = skip)
 //   blas    32 MiB                     cuBLAS workspace (no cuBLAS allocation)
 #include <cublas_v2.h>
@@ -58,21 +61,18 @@ namespace {
 
 constexpr int kStepThreads = 512;
 constexpr int kStepWarps = kStepThreads / 32;
+constexpr int kCached = 2;                            // float4 groups per thread kept in registers
 constexpr size_t kBlasWorkspace = size_t(32) << 20;
 constexpr int kMaxLayers = 4096;
 constexpr int kMaxWidth = 65536;
-constexpr int kMaxSplit = 4;                          // k-splits of the product
-constexpr size_t kSplitBytes = size_t(48) << 20;      // partial products kept within L2
 constexpr int kBacktrackSmem = 48 * 1024;             // decisions staged per sequence
 
 struct ClaspParams {
   int B, L, d, M;
-  int split;                   // S
   const float* h;              // [B][L+1][d]
   float* G[2];                 // [M+1][B][d]
   __nv_bfloat16* X;            // [M+1][2][B][d]
-  const float* Y;              // [S][M+1][2][B][d]
-  size_t ystride;              // elements between the partials of two k-splits
+  const float* Y;              // [M+1][2][B][d]
   unsigned char* table;        // [B][L][M+1]
   int* mask;                   // [B][L]
   float* score;                // [B]
@@ -132,19 +132,16 @@ __global__ void __launch_bounds__(kStepThreads) clasp_init_kernel(ClaspParams p)
   }
 }
 
-// W_l x at element group e of a state: the hi and lo partials of every
-// k-split, added in a fixed order.
-__device__ inline float4 product4(const float4* yh, size_t half4, size_t split4, int S, int e) {
-  float4 y = add4(yh[e], yh[e + half4]);
-  for (int s = 1; s < S; ++s) y = add4(y, add4(yh[e + s * split4], yh[e + s * split4 + half4]));
-  return y;
-}
+// The five partial sums of one float4 group (see clasp_step_kernel).
+struct Sums {
+  float hh = 0.f, hk = 0.f, kk = 0.f, hs = 0.f, ss = 0.f;
+};
 
 // One DP step: state (layer i, j) of sequence b, j = state_lo(i) + blockIdx.y.
 __global__ void __launch_bounds__(kStepThreads) clasp_step_kernel(ClaspParams p, int i, int prev) {
   const int b = blockIdx.x;
   const int j = state_lo(i, p.L, p.M) + blockIdx.y;
-  const int B = p.B, S = p.split;
+  const int B = p.B;
   const size_t d = p.d;
   const int n4 = p.d / 4;
   const bool can_keep = j <= i - 1;  // g(i-1, j) exists
@@ -153,58 +150,82 @@ __global__ void __launch_bounds__(kStepThreads) clasp_step_kernel(ClaspParams p,
   const float4* hv = reinterpret_cast<const float4*>(p.h + (static_cast<size_t>(b) * (p.L + 1) + i) * d);
   const float4* gk = reinterpret_cast<const float4*>(Gp + (static_cast<size_t>(j) * B + b) * d);
   const float4* yh = reinterpret_cast<const float4*>(p.Y + (static_cast<size_t>(j) * 2 * B + b) * d);
-  const size_t half4 = static_cast<size_t>(B) * d / 4;  // hi partial -> lo partial
-  const size_t split4 = p.ystride / 4;                   // one k-split -> the next
+  const float4* yl = yh + static_cast<size_t>(B) * d / 4;
   const float4* gs = can_skip ? reinterpret_cast<const float4*>(Gp + (static_cast<size_t>(j - 1) * B + b) * d)
                               : nullptr;
+  // the products of this layer (and, through stream order, everything
+  // before them) are complete past this point
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // <h, h>, <h, k>, <k, k>, <h, s>, <s, s> with k = g(i-1, j) + W g(i-1, j)
-  // the kept candidate and s = g(i-1, j-1) the skipped one
-  float part[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-  for (int e = threadIdx.x; e < n4; e += kStepThreads) {
+  // the kept candidate and s = g(i-1, j-1) the skipped one; the first
+  // kCached groups of each candidate stay in registers for the write-back
+  Sums t;
+  float4 kc[kCached], sc[kCached];
+#pragma unroll
+  for (int c = 0; c < kCached; ++c) {
+    const int e = threadIdx.x + c * kStepThreads;
+    kc[c] = sc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e < n4) {
+      const float4 x = hv[e];
+      t.hh = dot4(x, x, t.hh);
+      if (can_keep) {
+        kc[c] = add4(gk[e], add4(yh[e], yl[e]));
+        t.hk = dot4(x, kc[c], t.hk);
+        t.kk = dot4(kc[c], kc[c], t.kk);
+      }
+      if (can_skip) {
+        sc[c] = gs[e];
+        t.hs = dot4(x, sc[c], t.hs);
+        t.ss = dot4(sc[c], sc[c], t.ss);
+      }
+    }
+  }
+  for (int e = threadIdx.x + kCached * kStepThreads; e < n4; e += kStepThreads) {
     const float4 x = hv[e];
-    part[0] = dot4(x, x, part[0]);
+    t.hh = dot4(x, x, t.hh);
     if (can_keep) {
-      const float4 k = add4(gk[e], product4(yh, half4, split4, S, e));
-      part[1] = dot4(x, k, part[1]);
-      part[2] = dot4(k, k, part[2]);
+      const float4 k = add4(gk[e], add4(yh[e], yl[e]));
+      t.hk = dot4(x, k, t.hk);
+      t.kk = dot4(k, k, t.kk);
     }
     if (can_skip) {
       const float4 s = gs[e];
-      part[3] = dot4(x, s, part[3]);
-      part[4] = dot4(s, s, part[4]);
+      t.hs = dot4(x, s, t.hs);
+      t.ss = dot4(s, s, t.ss);
     }
   }
-  __shared__ float red[kStepWarps][5];
+  float v[5] = {t.hh, t.hk, t.kk, t.hs, t.ss};
+#pragma unroll
+  for (int q = 0; q < 5; ++q)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+  __shared__ float red[5][kStepWarps];
   __shared__ int decided;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
 #pragma unroll
-  for (int q = 0; q < 5; ++q) {
-    float v = part[q];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    part[q] = v;
-  }
-  const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-    for (int q = 0; q < 5; ++q) red[warp][q] = part[q];
+    for (int q = 0; q < 5; ++q) red[q][warp] = v[q];
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double sum[5];
+  if (warp == 0) {
+#pragma unroll
     for (int q = 0; q < 5; ++q) {
-      double v = 0.0;
-      for (int w = 0; w < kStepWarps; ++w) v += red[w][q];
-      sum[q] = v;
+      float a = lane < kStepWarps ? red[q][lane] : 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+      v[q] = a;
     }
-    const double cos_keep = sum[1] / (sqrt(sum[0]) * sqrt(sum[2]));
-    const double cos_skip = sum[3] / (sqrt(sum[0]) * sqrt(sum[4]));
-    // the larger cosine wins; a tie (or a NaN comparison) keeps the layer
-    const bool skip = !can_keep || (can_skip && cos_skip > cos_keep);
-    decided = skip;
-    p.table[(static_cast<size_t>(b) * p.L + (i - 1)) * (p.M + 1) + j] = skip ? 1 : 0;
-    if (i == p.L) p.score[b] = static_cast<float>(skip ? cos_skip : cos_keep);
+    if (lane == 0) {
+      const float nh = sqrtf(v[0]);
+      const float cos_keep = v[1] / (nh * sqrtf(v[2]));
+      const float cos_skip = v[3] / (nh * sqrtf(v[4]));
+      // the larger cosine wins; a tie (or a NaN comparison) keeps the layer
+      const bool skip = !can_keep || (can_skip && cos_skip > cos_keep);
+      decided = skip;
+      p.table[(static_cast<size_t>(b) * p.L + (i - 1)) * (p.M + 1) + j] = skip ? 1 : 0;
+      if (i == p.L) p.score[b] = skip ? cos_skip : cos_keep;
+    }
   }
   if (i == p.L) return;  // g(L, M) itself is not needed, only its score
   __syncthreads();
@@ -213,11 +234,19 @@ __global__ void __launch_bounds__(kStepThreads) clasp_step_kernel(ClaspParams p,
   float4* gc = reinterpret_cast<float4*>(p.G[prev ^ 1] + (static_cast<size_t>(j) * B + b) * d);
   __nv_bfloat16* xh = p.X + (static_cast<size_t>(j) * 2 * B + b) * d;
   __nv_bfloat16* xl = xh + static_cast<size_t>(B) * d;
-#pragma unroll 2
-  for (int e = threadIdx.x; e < n4; e += kStepThreads) {
-    const float4 v = skip ? gs[e] : add4(gk[e], product4(yh, half4, split4, S, e));
-    gc[e] = v;
-    store_split4(xh + 4 * e, xl + 4 * e, v);
+#pragma unroll
+  for (int c = 0; c < kCached; ++c) {
+    const int e = threadIdx.x + c * kStepThreads;
+    if (e < n4) {
+      const float4 w = skip ? sc[c] : kc[c];
+      gc[e] = w;
+      store_split4(xh + 4 * e, xl + 4 * e, w);
+    }
+  }
+  for (int e = threadIdx.x + kCached * kStepThreads; e < n4; e += kStepThreads) {
+    const float4 w = skip ? gs[e] : add4(gk[e], add4(yh[e], yl[e]));
+    gc[e] = w;
+    store_split4(xh + 4 * e, xl + 4 * e, w);
   }
 }
 
@@ -266,28 +295,16 @@ cublasHandle_t blas_handle_locked() {
   return h;
 }
 
-// k-splits of the product: as many as kMaxSplit while d splits into pieces
-// of whole 16-byte groups and the partial products stay within kSplitBytes.
-int split_of(int B, int d, int M) {
-  const size_t partial = static_cast<size_t>(M + 1) * 2 * B * d * sizeof(float);
-  int S = kMaxSplit;
-  while (S > 1 && (d % (8 * S) != 0 || S * partial > kSplitBytes)) S /= 2;
-  return S;
-}
-
 struct Layout {
-  int split;
-  size_t states, x, y, ystride, table, total;
+  size_t states, x, y, table, total;
 };
 
 Layout layout(int B, int L, int d, int M) {
   const size_t cells = static_cast<size_t>(M + 1) * B * d;
   Layout w;
-  w.split = split_of(B, d, M);
   w.states = align256(cells * sizeof(float));
   w.x = align256(2 * cells * sizeof(__nv_bfloat16));
-  w.ystride = 2 * cells;  // elements; 2 * cells * 4 bytes is a multiple of 256 (d % 8 == 0)
-  w.y = align256(w.split * w.ystride * sizeof(float));
+  w.y = align256(2 * cells * sizeof(float));
   w.table = align256(static_cast<size_t>(L) * (M + 1) * B);
   w.total = 2 * w.states + w.x + w.y + w.table + kBlasWorkspace;
   return w;
@@ -296,6 +313,21 @@ Layout layout(int B, int L, int d, int M) {
 bool sizes_ok(int B, int L, int d, int M) {
   return B >= 1 && B <= kMaxSeq && L >= 1 && L <= kMaxLayers && d >= 8 && d <= kMaxWidth && d % 8 == 0 &&
          M >= 0 && M <= L;
+}
+
+// The step kernel of layer i, launched so that it may start while the
+// layer's GEMM drains (it waits for the GEMM before any memory access).
+cudaError_t launch_step(const ClaspParams& p, int i, int prev, cudaStream_t s) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.B, state_hi(i, p.M) - state_lo(i, p.L, p.M) + 1);
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, clasp_step_kernel, p, i, prev);
 }
 
 cudaError_t launch_clasp(const ClaspParams& p, const __nv_bfloat16* W, cublasHandle_t blas, void* blas_ws,
@@ -307,7 +339,6 @@ cudaError_t launch_clasp(const ClaspParams& p, const __nv_bfloat16* W, cublasHan
   if (e != cudaSuccess) return e;
   const float one = 1.f, zero = 0.f;
   const size_t d = p.d;
-  const int kpart = p.d / p.split;
   int prev = 0;
   for (int i = 1; i <= p.L; ++i) {
     const int lo = state_lo(i, p.L, p.M);
@@ -315,25 +346,15 @@ cudaError_t launch_clasp(const ClaspParams& p, const __nv_bfloat16* W, cublasHan
     if (lo <= last_keep) {
       const size_t off = static_cast<size_t>(lo) * 2 * p.B * d;
       const int n = (last_keep - lo + 1) * 2 * p.B;
-      const __nv_bfloat16* Wl = W + static_cast<size_t>(i - 1) * d * d;
-      float* Y = const_cast<float*>(p.Y) + off;
       // Y[:, cols] = W_{i-1} X[:, cols] (hi and lo columns of each state);
       // column-major views: W_{i-1} stored [out][in] row-major is its
-      // transpose with leading dimension d.  Split s takes the input
-      // features [s d / S, (s + 1) d / S) and writes partial s.
-      const cublasStatus_t st =
-          p.split == 1
-              ? cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, p.d, n, p.d, &one, Wl, CUDA_R_16BF, p.d, p.X + off,
-                             CUDA_R_16BF, p.d, &zero, Y, CUDA_R_32F, p.d, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT)
-              : cublasGemmStridedBatchedEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, p.d, n, kpart, &one, Wl, CUDA_R_16BF,
-                                           p.d, kpart, p.X + off, CUDA_R_16BF, p.d, kpart, &zero, Y, CUDA_R_32F,
-                                           p.d, static_cast<long long>(p.ystride), p.split, CUBLAS_COMPUTE_32F,
-                                           CUBLAS_GEMM_DEFAULT);
-      if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+      // transpose with leading dimension d
+      if (cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, p.d, n, p.d, &one, W + static_cast<size_t>(i - 1) * d * d,
+                       CUDA_R_16BF, p.d, p.X + off, CUDA_R_16BF, p.d, &zero, const_cast<float*>(p.Y) + off,
+                       CUDA_R_32F, p.d, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+        return cudaErrorUnknown;
     }
-    const dim3 grid(p.B, state_hi(i, p.M) - lo + 1);
-    clasp_step_kernel<<<grid, kStepThreads, 0, s>>>(p, i, prev);
-    e = cudaGetLastError();
+    e = launch_step(p, i, prev, s);
     if (e != cudaSuccess) return e;
     prev ^= 1;
   }
@@ -374,8 +395,6 @@ extern "C" spec_status spec_clasp_layer_select(const spec_clasp_args* a, cudaStr
   p.G[1] = reinterpret_cast<float*>(ws + w.states);
   p.X = reinterpret_cast<__nv_bfloat16*>(ws + 2 * w.states);
   p.Y = reinterpret_cast<const float*>(ws + 2 * w.states + w.x);
-  p.ystride = w.ystride;
-  p.split = w.split;
   p.table = reinterpret_cast<unsigned char*>(ws + 2 * w.states + w.x + w.y);
   void* blas_ws = ws + 2 * w.states + w.x + w.y + w.table;
   p.mask = a->skip_mask;
