@@ -20,10 +20,13 @@ Modules
                   the first rejection are never read).
 ``clasp``         the CLaSp layer-selection dynamic program and its
                   backtracking, on synthetic residual layers.
+``pipeline_async`` the PipeSpec stages at independent buffer offsets (each
+                  stage a chain verification of its own window, then the
+                  rollbacks).
 
 Every function states the passage it follows.  Points where the pages are
 silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import clasp, closed_forms, compact, consulted, pipeline, verify  # noqa: F401
+from . import clasp, closed_forms, compact, consulted, pipeline, pipeline_async, verify  # noqa: F401
