@@ -18,7 +18,8 @@ tokens of O_{s-1} that follow what O_s already holds:
   * buffer lengths before the snapshot are l_0 .. l_{k-1}; stage s reads the
     window O_{s-1}[l_s : l_s + w_s], which must already be there
     (l_{s-1} >= l_s + w_s, the full-window assumption; otherwise the
-    sequence is malformed: ERR_WINDOW and no change);
+    sequence is malformed: ERR_WINDOW and no change, the stages' own data
+    errors reported beside it);
   * stage s is the chain rule with p = M_s and q = M_{s-1} at the window's
     positions (``oracle.verify.verify_chain_sequence``, M_s passing w_s + 1
     rows: the window's and the one after it);
@@ -67,18 +68,17 @@ def verify_pipeline_async_sequence(targets, drafts, windows, us, vs, lengths, te
     k = len(lengths)
     out = dict(a=[0] * (k - 1), t=[-1] * (k - 1), t_valid=[0] * (k - 1), r=list(lengths), committed=lengths[-1],
                error=0, margin_u=math.inf, margin_v=math.inf)
-    if any(l < 0 for l in lengths) or any(lengths[s - 1] < lengths[s] + len(windows[s - 1]) for s in range(1, k)):
-        out["error"] = ERR_WINDOW
-        return out
+    malformed = any(l < 0 for l in lengths) or any(
+        lengths[s - 1] < lengths[s] + len(windows[s - 1]) for s in range(1, k))
     stages = []
-    error = 0
-    for s in range(1, k):
+    error = ERR_WINDOW if malformed else 0
+    for s in range(1, k):  # every stage is verified; its data errors are reported either way
         c = verify_chain_sequence(targets[s - 1], None if greedy else drafts[s - 1], windows[s - 1],
                                   None if greedy else us[s - 1], None if greedy else vs[s - 1], temperature,
                                   greedy)
         error |= c["error"]
         stages.append(c)
-    if error & (ERR_TOKEN | ERR_NONFINITE):
+    if error & (ERR_TOKEN | ERR_NONFINITE | ERR_WINDOW):
         out["error"] = error
         return out
     new = [lengths[0]]
