@@ -958,6 +958,223 @@ def clasp_main(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# PipeSpec stages at independent buffer offsets (asynchronous snapshot)
+# --------------------------------------------------------------------------
+
+def async_rows(spec) -> int:
+    """Logit rows of one call per sequence: each stage's M_s rows (window + 1)
+    and, sampling, its M_{s-1} rows (window)."""
+    return sum(w + 1 + (0 if spec.greedy else w) for w in spec.windows)
+
+
+def async_bytes(spec) -> int:
+    return spec.B * async_rows(spec) * spec.V * (2 if spec.dtype == "bf16" else 4)
+
+
+def async_tokens(spec) -> int:
+    return spec.B * sum(spec.windows)
+
+
+def async_config(w) -> dict:
+    s = w["spec"]
+    return {"workload": s.name, "kind": "pipeline_async", "batch": s.B, "models": s.k, "windows": list(s.windows),
+            "vocab": s.V, "dtype": s.dtype, "temperature": s.temperature, "final_bonus": s.final_bonus,
+            "greedy": s.greedy, "logit_bytes_per_call": async_bytes(s)}
+
+
+def async_oracle_rate(w, budget_s: float):
+    from oracle import pipeline_async as A  # the reference is only used on this leg
+    s = w["spec"]
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        b = n % s.B
+        sub = lambda xs: [x[b:b + 1] for x in xs]
+        A.verify_pipeline_async(sub(w["targets"]), None if s.greedy else sub(w["drafts"]), sub(w["tokens"]),
+                                sub(w["us"]), sub(w["vs"]), w["length"][:, b:b + 1], s.temperature, s.greedy,
+                                s.final_bonus, s.dtype, V=s.V)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return n * sum(s.windows) / el, f"{n} whole sequences ({el:.1f} s, float64 NumPy)"
+
+
+def run_pipeline_async(args, w):
+    import torch
+    import draft_verification_gb300 as dv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dv.build_library()
+    s = w["spec"]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    nbytes = async_bytes(s)
+    n_sets = max(2, math.ceil(3 * l2 / nbytes) + 1)
+
+    def logits(a):
+        t = torch.from_numpy(a).to(dev)
+        return (t.view(torch.bfloat16) if s.dtype == "bf16" else t)[:, :, :s.V]
+
+    small = dict(tokens=[torch.from_numpy(t).to(dev) for t in w["tokens"]],
+                 length=torch.from_numpy(w["length"]).to(dev),
+                 us=[torch.from_numpy(u).to(dev) for u in w["us"]], vs=[torch.from_numpy(v).to(dev) for v in w["vs"]])
+    base_t = [logits(x.view(np.int16) if s.dtype == "bf16" else x) for x in w["targets"]]
+    base_d = [logits(x.view(np.int16) if s.dtype == "bf16" else x) for x in w["drafts"]]
+    sets = [(base_t, base_d)] + [([t.clone() for t in base_t], [d.clone() for d in base_d]) for _ in range(n_sets - 1)]
+    plans = [dv.PipelineAsyncPlan(t, None if s.greedy else d, small["tokens"], small["length"],
+                                  None if s.greedy else small["us"], None if s.greedy else small["vs"],
+                                  greedy=s.greedy, temperature=s.temperature, final_bonus=s.final_bonus)
+             for t, d in sets]
+    stream = torch.cuda.Stream(dev)
+
+    def one_pass():
+        for p in plans:
+            p.run(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            plans[i % n_sets].run(stream)
+    stream.synchronize()
+    launch = "cuda_graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            one_pass()
+        stream.synchronize()
+    except Exception as exc:
+        launch = f"eager ({type(exc).__name__})"
+        graph = None
+
+    def run_steps(k):
+        full, rest = divmod(k, n_sets)
+        for _ in range(full):
+            if graph is not None:
+                graph.replay()
+            else:
+                one_pass()
+        for i in range(rest):
+            plans[i].run(stream)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            run_steps(n_sets * 10)
+            stream.synchronize()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end through the public call: host logits, tokens, uniforms and
+    # lengths in, the outputs back, every step
+    def pin(a, is_logits=False):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if is_logits and s.dtype == "bf16":
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.pin_memory()
+
+    host_t = [pin(x[:, :, :s.V], True) for x in w["targets"]]
+    host_d = None if s.greedy else [pin(x[:, :, :s.V], True) for x in w["drafts"]]
+    host_tok = [pin(t) for t in w["tokens"]]
+    host_len = pin(w["length"])
+    host_u = None if s.greedy else [pin(u) for u in w["us"]]
+    host_v = None if s.greedy else [pin(v) for v in w["vs"]]
+    h2d = sum(t.numel() * t.element_size() for t in host_t + (host_d or []) + host_tok + (host_u or []) +
+              (host_v or [])) + host_len.numel() * 4
+
+    def e2e_call():
+        with torch.cuda.stream(stream):
+            o = dv.verify_pipeline_async(host_t, host_d, host_tok, host_len, host_u, host_v, greedy=s.greedy,
+                                         temperature=s.temperature, final_bonus=s.final_bonus, V=s.V, device=dev,
+                                         stream=stream)
+        stream.synchronize()
+        return o
+
+    for _ in range(2):
+        e2e_call()
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        o = e2e_call()
+    el = time.perf_counter() - t0
+    d2h = sum(v.numel() * v.element_size() for v in o.values())
+
+    peak, peak_src = measured_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": async_tokens(s) / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
+        "data": "synthetic (seeded logits; windows drawn from the drafter's softmax)",
+        "config": dict(async_config(w), parallelism="1 GPU", launch=launch,
+                       l2_policy=f"rotating {n_sets} copies of the logits "
+                                 f"({n_sets * nbytes / 2**20:.0f} MB > 3 x L2 {l2 / 2**20:.0f} MB)"),
+        "roofline": {"bound": "hbm", "kernel": "whole call: per stage stats_kernel + chain_walk_kernel, then "
+                                               "pipeline_async_combine_kernel",
+                     "unit_of_work": "one asynchronous snapshot", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": peak_src, "kernel_ms": ms, "algorithmic_bytes": nbytes,
+                     "traffic": None},
+        "e2e": {"value": async_tokens(s) / (el / n), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n},
+        "gpu_launches": args.steps * (2 * (s.k - 1) + 1),
+        "clocks": clock_info,
+    }
+
+
+def pipeline_async_main(args, w, rank):
+    s = w["spec"]
+    if args.impl == "reference":
+        if rank == 0:
+            rate, desc = async_oracle_rate(w, args.cpu_seconds)
+            print(json.dumps({
+                "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * async_tokens(s) / rate,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": async_config(w),
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+        return
+    if args.profile:
+        import torch
+        import draft_verification_gb300 as dv
+        dev = torch.device("cuda", 0)
+        dv.build_library()
+
+        def logits(a):
+            t = torch.from_numpy(a.view(np.int16) if s.dtype == "bf16" else a).to(dev)
+            return (t.view(torch.bfloat16) if s.dtype == "bf16" else t)[:, :, :s.V]
+
+        d = lambda xs: [torch.from_numpy(x).to(dev) for x in xs]
+        plan = dv.PipelineAsyncPlan([logits(x) for x in w["targets"]],
+                                    None if s.greedy else [logits(x) for x in w["drafts"]], d(w["tokens"]),
+                                    torch.from_numpy(w["length"]).to(dev), None if s.greedy else d(w["us"]),
+                                    None if s.greedy else d(w["vs"]), greedy=s.greedy, temperature=s.temperature,
+                                    final_bonus=s.final_bonus)
+        for _ in range(args.warmup + args.steps):
+            plan.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": s.name, "calls": args.warmup + args.steps}))
+        return
+    if rank != 0:
+        return  # one GPU: the other ranks of a replica launch have nothing to add
+    line = run_pipeline_async(args, w)
+    if not args.no_cpu_baseline:
+        rate, desc = async_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
 def pipeline_e2e(args, w, dev, stream):
     """e2e_rate for the k-model pipeline (lists of per-model inputs)."""
     import torch
@@ -1023,13 +1240,17 @@ def main():
     if args.workload in synth.COMPACT_SPECS:
         compact_main(args, synth.make(synth.COMPACT_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
         return
+    if args.workload in synth.PIPELINE_ASYNC_SPECS:
+        pipeline_async_main(args, synth.make(synth.PIPELINE_ASYNC_SPECS[args.workload],
+                                             seed=replica_seed(args.seed, rank)), rank)
+        return
     if args.workload in synth.CLASP_SPECS:
         clasp_main(args, synth.make(synth.CLASP_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
         return
     specs = dict(synth.SPECS, **synth.PIPELINE_SPECS)
     if args.workload not in specs:
         raise SystemExit(f"unknown workload {args.workload}; choose from "
-                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS) + sorted(synth.CLASP_SPECS)}")
+                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS) + sorted(synth.CLASP_SPECS) + sorted(synth.PIPELINE_ASYNC_SPECS)}")
     w = synth.make(specs[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":

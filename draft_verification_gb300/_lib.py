@@ -16,7 +16,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EALIGN, SPEC_EWORKSPACE, SPEC_ECUDA = 0,
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_GREEDY, SPEC_SAMPLE = 0, 1
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
-ERR_TOKEN, ERR_PARENT, ERR_NONFINITE, ERR_ZERO_MASS, ERR_INTERNAL = 1, 2, 4, 8, 16
+ERR_TOKEN, ERR_PARENT, ERR_NONFINITE, ERR_ZERO_MASS, ERR_INTERNAL, ERR_WINDOW = 1, 2, 4, 8, 16, 32
 
 _vp = C.c_void_p
 
@@ -79,6 +79,20 @@ class PipelineArgs(C.Structure):
     ]
 
 
+class PipelineAsyncArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("k", C.c_int), ("window", C.c_int * (SPEC_MAX_MODELS - 1)), ("final_bonus", C.c_int),
+        ("V", C.c_int), ("ld", C.c_longlong), ("dtype", C.c_int), ("mode", C.c_int),
+        ("temperature", C.c_float),
+        ("target", _vp * (SPEC_MAX_MODELS - 1)), ("draft", _vp * (SPEC_MAX_MODELS - 1)),
+        ("tokens", _vp * (SPEC_MAX_MODELS - 1)), ("u", _vp * (SPEC_MAX_MODELS - 1)),
+        ("v", _vp * (SPEC_MAX_MODELS - 1)), ("length", _vp),
+        ("a", _vp), ("t", _vp), ("t_valid", _vp), ("r", _vp), ("committed", _vp),
+        ("seq_error", _vp), ("error_word", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+    ]
+
+
 class CompactArgs(C.Structure):
     _fields_ = [
         ("B", C.c_int), ("N", C.c_int), ("max_depth", C.c_int), ("cache_rows", C.c_int),
@@ -108,6 +122,8 @@ SIGNATURES = {
     "spec_pipeline_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int, C.c_int]),
     "spec_verify_pipeline": (C.c_int, [C.POINTER(PipelineArgs), _vp]),
     "spec_compact_tree_path": (C.c_int, [C.POINTER(CompactArgs), _vp]),
+    "spec_pipeline_async_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int]),
+    "spec_verify_pipeline_async": (C.c_int, [C.POINTER(PipelineAsyncArgs), _vp]),
     "spec_clasp_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spec_clasp_layer_select": (C.c_int, [C.POINTER(ClaspArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),

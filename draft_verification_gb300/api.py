@@ -301,6 +301,80 @@ class PipelinePlan(_Plan):
         self._call = lib.spec_verify_pipeline
 
 
+class PipelineAsyncPlan(_Plan):
+    """PipeSpec stages at independent buffer offsets, bound to fixed buffers.
+    See spec_verify_pipeline_async.
+
+    targets: per stage s = 1 .. k-1 the logit view [B, w_s + 1, V] of M_s;
+    drafts: per stage [B, w_s, V] of M_{s-1} (None in greedy mode); tokens:
+    per stage int32 [B, w_s] (the window); us / vs: per stage uniforms
+    (sampling); length: int32 [k, B] buffer lengths before the snapshot.
+    ``run()`` returns a, t, t_valid, r [B, k-1], committed, seq_error and
+    error_word."""
+
+    def __init__(self, targets, drafts, tokens, length, us=None, vs=None, *, greedy=False, temperature=1.0,
+                 final_bonus=False, V=None, workspace=None):
+        S = len(targets)
+        k = S + 1
+        if not 1 <= S <= L.SPEC_MAX_MODELS - 1 or len(tokens) != S:
+            raise ValueError("targets and tokens: one per stage, 1 .. 7 stages")
+        windows = [int(t.shape[1]) for t in tokens]
+        ref = targets[0]
+        B = ref.shape[0]
+        V = ref.shape[2] if V is None else V
+        dev = ref.device
+        ld = None
+
+        def stride(m, rows, name):
+            nonlocal ld
+            if m.dtype != ref.dtype:
+                raise ValueError("every logit view: the same dtype")
+            this = _rows(m, rows, name)
+            if ld is not None and this != ld:
+                raise ValueError("every logit view: the same row stride")
+            ld = this
+
+        for s in range(S):
+            stride(targets[s], windows[s] + 1, f"targets[{s}]")
+            if not greedy:
+                stride(drafts[s], windows[s], f"drafts[{s}]")
+        length = _i32(length, "length")
+        if tuple(length.shape) != (k, B):
+            raise ValueError(f"length: expected [{k}, {B}]")
+        lib = L.lib()
+        self.keep = [targets, drafts, tokens, length, us, vs]
+        i32 = lambda *shape: torch.empty(*shape, dtype=torch.int32, device=dev)
+        self.out = dict(a=i32(B, S), t=i32(B, S), t_valid=i32(B, S), r=i32(B, S), committed=i32(B),
+                        seq_error=i32(B), error_word=torch.zeros(1, dtype=torch.int32, device=dev))
+        win = (C.c_int * (L.SPEC_MAX_MODELS - 1))(*windows)
+        need = lib.spec_pipeline_async_workspace_size(B, k, win, V)
+        if need == 0:
+            raise ValueError(f"asynchronous snapshot sizes out of range: B={B} k={k} windows={windows} V={V}")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        a = L.PipelineAsyncArgs()
+        a.B, a.k, a.final_bonus, a.V, a.ld = B, k, int(bool(final_bonus)), V, ld
+        a.window = win
+        a.dtype = _DTYPES[ref.dtype]
+        a.mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        a.temperature = float(temperature)
+        for s in range(S):
+            a.target[s] = targets[s].data_ptr()
+            a.tokens[s] = _i32(tokens[s], f"tokens[{s}]").data_ptr()
+            if not greedy:
+                a.draft[s] = drafts[s].data_ptr()
+                a.u[s] = _f32(us[s], f"us[{s}]").data_ptr()
+                a.v[s] = _f32(vs[s], f"vs[{s}]").data_ptr()
+        a.length = length.data_ptr()
+        o = self.out
+        a.a, a.t, a.t_valid, a.r = (o[n].data_ptr() for n in ("a", "t", "t_valid", "r"))
+        a.committed, a.seq_error, a.error_word = (o[n].data_ptr() for n in ("committed", "seq_error", "error_word"))
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_pipeline_async
+
+
 def _to_device(xs, device):
     moved = []
     for x in xs:
@@ -453,6 +527,23 @@ def clasp_layer_select(hidden, weights, M, *, choices=False, device="cuda", stre
     if host:
         hidden, weights = _to_device([hidden, weights], device)
     plan = ClaspPlan(hidden, weights, M, choices=choices)
+    return _finish(plan.run(stream), host)
+
+
+def verify_pipeline_async(targets, drafts, tokens, length, us=None, vs=None, *, greedy=False, temperature=1.0,
+                          final_bonus=False, V=None, device="cuda", stream=None):
+    """One asynchronous PipeSpec snapshot (host tensors in, host tensors out;
+    device tensors stay on the device).  See PipelineAsyncPlan."""
+    host = length.device.type == "cpu"
+    if host:
+        targets = _to_device(list(targets), device)
+        drafts = None if drafts is None else _to_device(list(drafts), device)
+        tokens = _to_device(list(tokens), device)
+        (length,) = _to_device([length], device)
+        us = None if us is None else _to_device(list(us), device)
+        vs = None if vs is None else _to_device(list(vs), device)
+    plan = PipelineAsyncPlan(targets, drafts, tokens, length, us, vs, greedy=greedy, temperature=temperature,
+                             final_bonus=final_bonus, V=V)
     return _finish(plan.run(stream), host)
 
 

@@ -57,7 +57,8 @@
  *    back into it, so the call is ordered on `stream` like any other work.
  *    A consulted-only chain call adds one memset of its control words;
  *    spec_compact_tree_path is one kernel; spec_clasp_layer_select is
- *    L + 2 kernels and L cuBLAS GEMMs (see its section).
+ *    L + 2 kernels and L cuBLAS GEMMs; spec_verify_pipeline_async is one
+ *    chain verification per stage and a combine kernel (see their sections).
  *  - The workspace holds the row statistics passed from the first kernel of
  *    a call to the second (8 bytes per sequence, row and 8192-element chunk;
  *    a chain's also 4 bytes per sequence and position for its consulted-only
@@ -100,6 +101,9 @@ typedef enum spec_mode { SPEC_GREEDY = 0, SPEC_SAMPLE = 1 } spec_mode;
 #define SPEC_ERR_INTERNAL 16  /* a bulk copy of logits into shared memory did not
                                  complete in time; this sequence's outputs are
                                  not valid (never expected; reported, not hung) */
+#define SPEC_ERR_WINDOW 32    /* asynchronous pipeline: a negative buffer length,
+                                 or a stage window that does not fit in the
+                                 buffer below it                                 */
 
 /* ---------------------------------------------------------------------- */
 /* Chain verification: B sequences, each with a gamma-token draft.         */
@@ -327,6 +331,65 @@ typedef struct spec_pipeline_args {
 
 size_t spec_pipeline_workspace_size(int B, int k, const int* window, int final_bonus, int V);
 spec_status spec_verify_pipeline(const spec_pipeline_args* args, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* PipeSpec stages at independent buffer offsets: one asynchronous         */
+/* snapshot.  PipeSpec review, "What carries the argument" (the models run */
+/* without global synchronisation; each M_s verifies O_{s-1}, appends the  */
+/* longest matching prefix, and a mismatch rolls every earlier buffer      */
+/* back) and "What would settle it" (a verifier finds a full window).      */
+/* Buffer O_j holds length[j][b] tokens before the snapshot.  Every stage  */
+/* s = 1 .. k-1 verifies, independently of the others, the w_s tokens      */
+/* O_{s-1}[l_s, l_s + w_s) with the chain rule (p = M_s, q = M_{s-1}):     */
+/*  - a window must fit, l_{s-1} >= l_s + w_s (and every l_j >= 0); else   */
+/*    the sequence gets SPEC_ERR_WINDOW and empty outputs;                 */
+/*  - a rejection at window position a emits the correction and cuts every */
+/*    earlier buffer to at most P_s = l_s + a;                             */
+/*  - when every token is kept, stage 1 and (final_bonus) the last stage   */
+/*    emit the bonus from M_s's row w_s, but only if position l_s + w_s is */
+/*    still empty in the buffer below after that buffer's own appends in   */
+/*    this snapshot (O_0 does not grow); middle stages emit nothing;       */
+/*  - O_s grows to l_s + a_s (+1 when it emits); r_j = min(that, P_s over  */
+/*    every rejecting stage s > j); committed = the last buffer's length.  */
+/* Every stage passes w_s + 1 rows of M_s (the window's and the one after  */
+/* it; the last is read even where no bonus can be emitted).  A sequence   */
+/* with bit 1, 4, 16 or 32 gets empty outputs: a = 0, t = -1, t_valid = 0, */
+/* r_j = l_j, committed = l_{k-1}.  Launches: one chain verification per   */
+/* stage (each as spec_verify_chain), then one combine kernel.             */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_pipeline_async_args {
+  int B;                        /* sequences, 1..65535                            */
+  int k;                        /* models M_0 .. M_{k-1}, 2..SPEC_MAX_MODELS      */
+  int window[SPEC_MAX_MODELS - 1]; /* window[s-1] = w_s, 1..32                    */
+  int final_bonus;              /* nonzero: the last stage may emit a bonus       */
+  int V;                        /* vocabulary size, >= 1                          */
+  long long ld;                 /* row stride of every logit array (elements)     */
+  spec_dtype dtype;
+  spec_mode mode;
+  float temperature;            /* sampling mode, > 0                             */
+  const void* target[SPEC_MAX_MODELS - 1]; /* stage s: M_s rows [B, w_s + 1]      */
+  const void* draft[SPEC_MAX_MODELS - 1];  /* stage s: M_{s-1} rows [B, w_s]      */
+                                /* (sampling; unused in greedy mode)               */
+  const int* tokens[SPEC_MAX_MODELS - 1];  /* stage s: the window [B, w_s]        */
+  const float* u[SPEC_MAX_MODELS - 1];     /* stage s: [B, w_s] (sampling)        */
+  const float* v[SPEC_MAX_MODELS - 1];     /* stage s: [B] (sampling)             */
+  const int* length;            /* [k, B]: l_j of sequence b at j * B + b         */
+  int* a;                       /* out [B, k-1]: kept window tokens per stage     */
+  int* t;                       /* out [B, k-1]: emitted token, -1 if none        */
+  int* t_valid;                 /* out [B, k-1]: 1 when the stage emitted         */
+  int* r;                       /* out [B, k-1]: new lengths of O_0 .. O_{k-2}    */
+  int* committed;               /* out [B]: new length of O_{k-1}                 */
+  int* seq_error;               /* out [B], optional                              */
+  int* error_word;              /* in/out, optional                               */
+  void* workspace;              /* 16-byte aligned                                */
+  size_t workspace_bytes;
+} spec_pipeline_async_args;
+
+/* The largest stage's chain workspace (stages run one after another on     */
+/* `stream` and share it) plus 16 bytes per (stage, sequence) of stage       */
+/* results.  0 for sizes outside the limits above.                           */
+size_t spec_pipeline_async_workspace_size(int B, int k, const int* window, int V);
+spec_status spec_verify_pipeline_async(const spec_pipeline_async_args* args, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* Cache compaction after a tree verification.  Staged Speculative         */

@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -44,7 +44,8 @@ def test_struct_layout_matches_header(tmp_path):
         pytest.skip("gcc or CUDA headers missing")
     structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
                "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs,
-               "spec_pipeline_args": _lib.PipelineArgs, "spec_clasp_args": _lib.ClaspArgs}
+               "spec_pipeline_args": _lib.PipelineArgs, "spec_clasp_args": _lib.ClaspArgs,
+               "spec_pipeline_async_args": _lib.PipelineAsyncArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -304,3 +305,49 @@ def test_clasp_accepts_exactly_its_workspace_size(lib):
     assert lib.spec_clasp_layer_select(C.byref(a), None) == _lib.SPEC_ECUDA  # no GPU here
     a.workspace_bytes -= 1
     assert lib.spec_clasp_layer_select(C.byref(a), None) == -4
+
+
+def _async(**kw):
+    from draft_verification_gb300 import _lib
+    a = _lib.PipelineAsyncArgs()
+    a.B, a.k, a.V, a.ld = 2, 4, 100, 100
+    a.window = (C.c_int * 7)(3, 2, 2)
+    a.dtype, a.mode, a.temperature = _lib.SPEC_BF16, _lib.SPEC_SAMPLE, 1.0
+    fake = 0x10000  # never dereferenced: every case fails validation
+    for i in range(3):
+        for arr in (a.target, a.draft, a.tokens, a.u, a.v):
+            arr[i] = fake
+    for f in ("length", "a", "t", "t_valid", "r", "committed", "workspace"):
+        setattr(a, f, fake)
+    a.workspace_bytes = 1 << 20
+    for key, v in kw.items():
+        setattr(a, key, v)
+    return a
+
+
+def test_pipeline_async_workspace_and_argument_errors(lib):
+    from draft_verification_gb300 import _lib
+    win = (C.c_int * 7)(8, 6, 4)
+    chain = lib.spec_chain_workspace_size(128, 8, 128256)  # the largest stage's chain workspace
+    scratch = 256 * ((3 * 3 * 128 * 4 + 255) // 256)
+    assert lib.spec_pipeline_async_workspace_size(128, 4, win, 128256) == 256 * ((chain + 255) // 256) + scratch
+    assert lib.spec_pipeline_async_workspace_size(128, 9, win, 100) == 0
+    assert lib.spec_pipeline_async_workspace_size(128, 1, win, 100) == 0
+    assert lib.spec_pipeline_async_workspace_size(0, 4, win, 100) == 0
+    assert lib.spec_pipeline_async_workspace_size(128, 4, (C.c_int * 7)(8, 0, 4), 100) == 0
+    assert lib.spec_pipeline_async_workspace_size(128, 4, (C.c_int * 7)(8, 33, 4), 100) == 0
+    for kw, code in [(dict(k=1), -1), (dict(k=9), -1), (dict(B=0), -1), (dict(window=(C.c_int * 7)(3, 33, 2)), -1),
+                     (dict(dtype=5), -2), (dict(mode=3), -2), (dict(committed=None), -1), (dict(length=None), -1),
+                     (dict(workspace_bytes=8), -4), (dict(workspace=0x10008), -4)]:
+        assert lib.spec_verify_pipeline_async(C.byref(_async(**kw)), None) == code, kw
+    for field in ("target", "tokens", "draft", "u", "v"):
+        a = _async()
+        getattr(a, field)[2] = None
+        assert lib.spec_verify_pipeline_async(C.byref(a), None) == -1, field
+    # greedy mode needs no draft rows or uniforms
+    a = _async(mode=_lib.SPEC_GREEDY)
+    for i in range(3):
+        a.draft[i] = a.u[i] = a.v[i] = None
+    a.workspace_bytes = 8
+    assert lib.spec_verify_pipeline_async(C.byref(a), None) == -4
+    assert lib.spec_verify_pipeline_async(None, None) == -1

@@ -198,6 +198,43 @@ PIPELINE_SPECS = {
 
 
 @dataclass(frozen=True)
+class PipelineAsyncSpec:
+    """PipeSpec stages at independent buffer offsets: stage s verifies w_s =
+    windows[s-1] tokens of O_{s-1} after the l_s tokens O_s already holds.
+    Buffer lengths: l_{k-1} uniform in [0, max_base), l_{s-1} = l_s + w_s +
+    a gap uniform in [0, extra] (a gap of 0: the window ends the buffer
+    below).  Per stage and sequence: M_{s-1} rows Q ~ sigma_q N(0, 1) at the
+    window's positions and the one after, M_s rows a[s-1] Q + s[s-1] N(0, 1)
+    (the pipeline's model), the window tokens drawn from M_{s-1}'s softmax
+    at the temperature (greedy: its argmax); the windows of different stages
+    cover disjoint positions, so they are drawn independently."""
+    name: str
+    B: int
+    windows: tuple
+    V: int
+    dtype: str = "bf16"
+    greedy: bool = False
+    temperature: float = 1.0
+    sigma_q: float = 2.0
+    a: tuple = (0.9, 0.9, 0.9)
+    s: tuple = (0.465, 1.024, 1.024)
+    final_bonus: bool = False
+    extra: int = 2
+    max_base: int = 64
+    pad: int = 0
+
+    @property
+    def k(self) -> int:
+        return len(self.windows) + 1
+
+
+PIPELINE_ASYNC_SPECS = {
+    "pipeline4_async_b128_g8_g6_g4_v128256_bf16": PipelineAsyncSpec(
+        "pipeline4_async_b128_g8_g6_g4_v128256_bf16", B=128, windows=(8, 6, 4), V=128256),
+}
+
+
+@dataclass(frozen=True)
 class CompactSpec:
     """Cache compaction after a tree verification: B sequences, each with one
     row of row_bytes per tree node (the tree of tree_topology) and a kept root
@@ -481,11 +518,47 @@ def make_pipeline(spec: PipelineSpec, seed: int = 0) -> dict:
                 vs=vs, base=base)
 
 
+def make_pipeline_async(spec: PipelineAsyncSpec, seed: int = 0) -> dict:
+    """Asynchronous snapshot workload: per stage targets [B, w_s + 1, V+pad]
+    (M_s), drafts [B, w_s, V+pad] (M_{s-1}), tokens int32 [B, w_s], us
+    float32 [B, w_s], vs float32 [B]; length int32 [k, B]."""
+    rng = _rng(seed, 11)
+    B, V, k = spec.B, spec.V, spec.k
+    dt = np.uint16 if spec.dtype == "bf16" else np.float32
+    length = np.zeros((k, B), np.int32)
+    length[k - 1] = rng.integers(0, spec.max_base, B)
+    for s in range(k - 1, 0, -1):
+        length[s - 1] = length[s] + spec.windows[s - 1] + rng.integers(0, spec.extra + 1, B)
+    targets, drafts, tokens = [], [], []
+    for s in range(1, k):
+        w = spec.windows[s - 1]
+        tg = np.empty((B, w + 1, V), dt)
+        dr = np.empty((B, w, V), dt)
+        tk = np.empty((B, w), np.int32)
+        for b in range(B):
+            q = rng.standard_normal((w + 1, V), dtype=np.float32) * np.float32(spec.sigma_q)
+            p = np.float32(spec.a[s - 1]) * q + rng.standard_normal((w + 1, V), dtype=np.float32) * np.float32(
+                spec.s[s - 1])
+            dr[b] = _store(q[:w], spec.dtype)
+            tg[b] = _store(p, spec.dtype)
+            qv = _values(dr[b], spec.dtype)
+            tk[b] = np.argmax(qv, axis=-1) if spec.greedy else _gumbel_argmax(rng, qv / np.float32(spec.temperature))
+        targets.append(_pad(tg, spec.pad))
+        drafts.append(_pad(dr, spec.pad))
+        tokens.append(tk)
+    us = [rng.random((B, w), dtype=np.float32) for w in spec.windows]
+    vs = [rng.random(B, dtype=np.float32) for _ in spec.windows]
+    return dict(kind="pipeline_async", spec=spec, targets=targets, drafts=drafts, tokens=tokens, us=us, vs=vs,
+                length=length)
+
+
 def make(spec, seed: int = 0) -> dict:
     if isinstance(spec, str):
-        spec = {**SPECS, **COMPACT_SPECS, **PIPELINE_SPECS, **CLASP_SPECS}[spec]
+        spec = {**SPECS, **COMPACT_SPECS, **PIPELINE_SPECS, **PIPELINE_ASYNC_SPECS, **CLASP_SPECS}[spec]
     if isinstance(spec, PipelineSpec):
         return make_pipeline(spec, seed)
+    if isinstance(spec, PipelineAsyncSpec):
+        return make_pipeline_async(spec, seed)
     if isinstance(spec, ClaspSpec):
         return make_clasp(spec, seed)
     if isinstance(spec, CompactSpec):
