@@ -60,6 +60,7 @@ KERNELS = {"chain": ["stats_kernel", "chain_walk_kernel"], "tree": ["stats_kerne
            "clasp": ["clasp_init_kernel", "clasp_step_kernel", "clasp_backtrack_kernel"]}
 COMPACT_METRIC = "cache rows compacted/sec and GB/s moved vs GB300 HBM peak (1 GPU)"
 COMPACT_SOURCES = ["draft_verification_gb300/csrc/compact.cu"]
+ASYNC_SOURCES = KERNEL_SOURCES + ["draft_verification_gb300/csrc/pipeline_async.cu"]
 CLASP_METRIC = "CLaSp layer selections/sec and weight GB/s vs GB300 HBM and bf16 tensor peaks (1 GPU)"
 CLASP_SOURCES = ["draft_verification_gb300/csrc/clasp.cu"]
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -1123,7 +1124,7 @@ def run_pipeline_async(args, w):
                                                "pipeline_async_combine_kernel",
                      "unit_of_work": "one asynchronous snapshot", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_source": peak_src, "kernel_ms": ms, "algorithmic_bytes": nbytes,
-                     "traffic": None},
+                     "traffic": profiled_traffic(s.name, ASYNC_SOURCES)},
         "e2e": {"value": async_tokens(s) / (el / n), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n},
         "gpu_launches": args.steps * (2 * (s.k - 1) + 1),
