@@ -53,7 +53,7 @@ bool stats_params(StatsParams& sp, int B, int V, long long ld, bool bf16, bool g
 
 using namespace sv;
 
-spec_status sv::chain_setup(const spec_chain_args* a, StatsParams* spp, ChainParams* cpp) {
+spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool grouped) {
   if (a == nullptr) return SPEC_EINVAL;
   spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
   if (st != SPEC_OK) return st;
@@ -73,15 +73,14 @@ spec_status sv::chain_setup(const spec_chain_args* a, StatsParams* spp, ChainPar
       !aligned16(a->workspace))
     return SPEC_EWORKSPACE;
 
-  StatsParams& sp = *spp;
+  StatsParams sp;
   if (!stats_params(sp, a->B, a->V, a->ld, bf16, greedy, a->temperature, rows, a->workspace))
     return SPEC_EINVAL;
   sp.set[0] = RowSet{a->target_logits, a->gamma + 1};
   sp.set[1] = RowSet{a->draft_logits, a->gamma};
   sp.nsets = (greedy || a->gamma == 0) ? 1 : 2;
 
-  ChainParams& cp = *cpp;
-  cp = ChainParams{};
+  ChainParams cp = {};
   cp.B = a->B;
   cp.gamma = a->gamma;
   cp.V = a->V;
@@ -100,18 +99,7 @@ spec_status sv::chain_setup(const spec_chain_args* a, StatsParams* spp, ChainPar
   cp.resid = a->resid_mass;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
-  return SPEC_OK;
-}
-
-spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool grouped) {
-  StatsParams sp;
-  ChainParams cp;
-  const spec_status st = chain_setup(a, &sp, &cp);
-  if (st != SPEC_OK) return st;
-  const bool greedy = a->mode == SPEC_GREEDY;
-  const bool bf16 = a->dtype == SPEC_BF16;
-  if (a->consulted_only != 0) {
-    const int rows = 2 * a->gamma + 1;
+  if (consulted) {
     char* ctl = static_cast<char*>(a->workspace) + workspace_bytes(a->B, rows, a->V);
     cp.count = reinterpret_cast<unsigned*>(ctl);
     cp.skip = reinterpret_cast<int*>(ctl) + static_cast<size_t>(a->B) * a->gamma;

@@ -154,11 +154,6 @@ cudaError_t launch_pipeline(const StatsParams& g, const PipelineParams& p, bool 
 // streams (forked from and joined into s); false keeps every launch on s.
 cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, bool greedy, bool grouped,
                          cudaStream_t s);
-// Several independent chain verifications (the stages of an asynchronous
-// pipeline snapshot) as one set of batch groups on the library streams:
-// one fork from s and one join into s for all of them.
-cudaError_t launch_chains(const StatsParams* g, const ChainParams* p, int n, bool bf16, bool greedy,
-                          cudaStream_t s);
 cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
 cudaError_t launch_cascade(const StatsParams& g, const CascadeParams& p, bool bf16, bool greedy,
                            cudaStream_t s);
@@ -169,7 +164,4 @@ namespace sv {
 // spec_verify_chain with batch groups allowed or not (the no-allocation
 // entry point runs everything on the caller's stream).
 spec_status verify_chain(const spec_chain_args* a, cudaStream_t stream, bool grouped);
-// The argument checks of spec_verify_chain and the launch parameters they
-// give (no launch; the consulted-only control words are not set up).
-spec_status chain_setup(const spec_chain_args* a, StatsParams* sp, ChainParams* cp);
 }  // namespace sv

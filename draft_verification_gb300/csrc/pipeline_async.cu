@@ -10,12 +10,11 @@
 // The stages of an asynchronous snapshot do not feed one another: stage s
 // reads the window O_{s-1}[l_s, l_s + w_s) that was in place before the
 // snapshot.  So each stage is one chain verification of its own window (the
-// same statistics and walk kernels as spec_verify_chain), and the stages'
-// batch groups all run side by side on the library's group streams (one
-// fork and one join for the call; every stage has its own workspace part),
-// so one stage's walks overlap the next stage's statistics.
-// pipeline_async_combine_kernel then applies the emission and rollback
-// rules per sequence:
+// same statistics and walk kernels as spec_verify_chain, with the stage's
+// buffer length as the prefix, so that the chain's rollback index is the
+// absolute rejection position), and the stages run one after another on the
+// caller's stream sharing one workspace.  pipeline_async_combine_kernel then
+// applies the emission and rollback rules per sequence:
 //   - a window that does not fit (l_{s-1} < l_s + w_s) or a negative length
 //     makes the sequence malformed (SPEC_ERR_WINDOW, empty outputs);
 //   - a rejection emits the correction and cuts every earlier buffer to at
@@ -28,6 +27,7 @@
 //     every rejecting stage s > j).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -115,21 +115,19 @@ __global__ void __launch_bounds__(kCombineThreads) pipeline_async_combine_kernel
 }
 
 struct AsyncLayout {
-  size_t stage_off[kMaxStages + 1];  // stage s's chain workspace at [off[s], off[s + 1])
-  size_t scratch, total;
+  size_t chain, scratch, total;
 };
 
 bool async_layout(int B, int k, const int* window, int V, AsyncLayout* out) {
   if (B < 1 || B > kMaxSeq || k < 2 || k > SPEC_MAX_MODELS || window == nullptr || V < 1) return false;
-  size_t off = 0;
+  size_t chain = 0;
   for (int s = 0; s < k - 1; ++s) {
     if (window[s] < 1 || window[s] > 32) return false;
-    out->stage_off[s] = off;
-    off += align256(chain_workspace_bytes(B, window[s], 2 * window[s] + 1, V));
+    chain = std::max(chain, chain_workspace_bytes(B, window[s], 2 * window[s] + 1, V));
   }
-  out->stage_off[k - 1] = off;
+  out->chain = align256(chain);
   out->scratch = align256(static_cast<size_t>(3) * (k - 1) * B * sizeof(int));
-  out->total = off + out->scratch;
+  out->total = out->chain + out->scratch;
   return true;
 }
 
@@ -158,13 +156,12 @@ extern "C" spec_status spec_verify_pipeline_async(const spec_pipeline_async_args
   if (!a->workspace || a->workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(a->workspace) & 15u))
     return SPEC_EWORKSPACE;
   char* ws = static_cast<char*>(a->workspace);
-  int* accept = reinterpret_cast<int*>(ws + w.stage_off[S]);
+  int* accept = reinterpret_cast<int*>(ws + w.chain);
   int* token = accept + static_cast<size_t>(S) * a->B;
   int* stage_err = token + static_cast<size_t>(S) * a->B;
 
-  // one chain verification per stage, each with its own workspace part
-  StatsParams G[kMaxStages];
-  ChainParams P[kMaxStages];
+  // one chain verification per stage; the chain's rollback index (prefix +
+  // accept length) is not needed, the combine recomputes the cuts
   for (int s = 0; s < S; ++s) {
     spec_chain_args c{};
     c.B = a->B;
@@ -179,16 +176,16 @@ extern "C" spec_status spec_verify_pipeline_async(const spec_pipeline_async_args
     c.draft_tokens = a->tokens[s];
     c.u = greedy ? nullptr : a->u[s];
     c.v = greedy ? nullptr : a->v[s];
+    c.prefix_len = nullptr;
     c.accept_len = accept + static_cast<size_t>(s) * a->B;
     c.out_token = token + static_cast<size_t>(s) * a->B;
     c.seq_error = stage_err + static_cast<size_t>(s) * a->B;
     c.error_word = a->error_word;
-    c.workspace = ws + w.stage_off[s];
-    c.workspace_bytes = w.stage_off[s + 1] - w.stage_off[s];
-    const spec_status st = chain_setup(&c, &G[s], &P[s]);
+    c.workspace = a->workspace;
+    c.workspace_bytes = w.chain;
+    const spec_status st = verify_chain(&c, stream, true);
     if (st != SPEC_OK) return st;
   }
-  if (launch_chains(G, P, S, a->dtype == SPEC_BF16, greedy, stream) != cudaSuccess) return SPEC_ECUDA;
   AsyncParams p{};
   p.B = a->B;
   p.k = a->k;

@@ -1325,59 +1325,6 @@ cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, 
   });
 }
 
-// Several independent chain verifications (the stages of an asynchronous
-// pipeline snapshot) as one set of batch groups: each call is split into its
-// own groups and every (call, group) unit is placed on the library's group
-// streams in turn, all forked from s once and joined back once.  One call's
-// walks then run beside the next call's statistics, as the groups of one
-// call already do; statistics priorities fall with the unit's position
-// (clamped at the device's least), walks keep the greatest.  The calls'
-// workspaces must be disjoint.
-template <typename T>
-cudaError_t chains_impl(const StatsParams* G, const ChainParams* P, int n, bool greedy, cudaStream_t s) {
-  cudaStream_t side[kMaxGroups];
-  cudaError_t e = group_streams(side);
-  if (e != cudaSuccess) return e;
-  cudaEvent_t fork;
-  e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-  if (e != cudaSuccess) return e;
-  cudaError_t first = cudaEventRecord(fork, s);
-  bool forked[kMaxGroups] = {};
-  int unit = 0;
-  for (int c = 0; c < n && first == cudaSuccess; ++c) {
-    const Groups gr = plan_groups(G[c].B, logit_bytes(G[c], sizeof(T)));
-    for (int i = 0; i < gr.n && first == cudaSuccess; ++i, ++unit) {
-      const int q = unit % kMaxGroups;
-      if (!forked[q]) {
-        e = cudaStreamWaitEvent(side[q], fork, 0);
-        if (e != cudaSuccess) {
-          first = e;
-          break;
-        }
-        forked[q] = true;
-      }
-      const int b0 = gr.b0[i], nb = gr.b0[i + 1] - b0;
-      e = chain_one<T>(stats_group<T>(G[c], b0, nb), chain_group<T>(P[c], b0, nb), greedy, side[q], unit);
-      if (e != cudaSuccess) first = e;
-    }
-  }
-  // the join is recorded even when a launch failed, so s never runs ahead
-  // of work that was enqueued
-  for (int q = 0; q < kMaxGroups; ++q) {
-    if (!forked[q]) continue;
-    cudaEvent_t done;
-    if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess) {
-      if (cudaEventRecord(done, side[q]) == cudaSuccess) {
-        e = cudaStreamWaitEvent(s, done, 0);
-        if (e != cudaSuccess && first == cudaSuccess) first = e;
-      }
-      cudaEventDestroy(done);
-    }
-  }
-  cudaEventDestroy(fork);
-  return first;
-}
-
 template <typename T>
 cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, cudaStream_t s) {
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
@@ -1434,11 +1381,6 @@ int pass_tiles(int V) { return (V + kTileElems - 1) / kTileElems; }
 cudaError_t launch_chain(const StatsParams& G, const ChainParams& p, bool bf16, bool greedy, bool grouped,
                          cudaStream_t s) {
   return bf16 ? chain_impl<bf16_t>(G, p, greedy, grouped, s) : chain_impl<float>(G, p, greedy, grouped, s);
-}
-
-cudaError_t launch_chains(const StatsParams* G, const ChainParams* P, int n, bool bf16, bool greedy,
-                          cudaStream_t s) {
-  return bf16 ? chains_impl<bf16_t>(G, P, n, greedy, s) : chains_impl<float>(G, P, n, greedy, s);
 }
 
 cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s) {

@@ -355,8 +355,7 @@ spec_status spec_verify_pipeline(const spec_pipeline_args* args, cudaStream_t st
 /* it; the last is read even where no bonus can be emitted).  A sequence   */
 /* with bit 1, 4, 16 or 32 gets empty outputs: a = 0, t = -1, t_valid = 0, */
 /* r_j = l_j, committed = l_{k-1}.  Launches: one chain verification per   */
-/* stage (statistics and walk per batch group, all stages' groups side by  */
-/* side on library streams forked from `stream`), then one combine kernel. */
+/* stage (each as spec_verify_chain), then one combine kernel.             */
 /* ---------------------------------------------------------------------- */
 typedef struct spec_pipeline_async_args {
   int B;                        /* sequences, 1..65535                            */
@@ -386,9 +385,9 @@ typedef struct spec_pipeline_async_args {
   size_t workspace_bytes;
 } spec_pipeline_async_args;
 
-/* Every stage's chain workspace (spec_chain_workspace_size of its window,  */
-/* rounded up to 256 bytes; the stages run side by side) plus 12 bytes per   */
-/* (stage, sequence) of stage results.  0 for sizes outside the limits.      */
+/* The largest stage's chain workspace (stages run one after another on     */
+/* `stream` and share it) plus 16 bytes per (stage, sequence) of stage       */
+/* results.  0 for sizes outside the limits above.                           */
 size_t spec_pipeline_async_workspace_size(int B, int k, const int* window, int V);
 spec_status spec_verify_pipeline_async(const spec_pipeline_async_args* args, cudaStream_t stream);
 

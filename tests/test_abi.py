@@ -328,10 +328,9 @@ def _async(**kw):
 def test_pipeline_async_workspace_and_argument_errors(lib):
     from draft_verification_gb300 import _lib
     win = (C.c_int * 7)(8, 6, 4)
-    # every stage's chain workspace, then the stage results
-    chains = sum(256 * ((lib.spec_chain_workspace_size(128, g, 128256) + 255) // 256) for g in (8, 6, 4))
+    chain = lib.spec_chain_workspace_size(128, 8, 128256)  # the largest stage's chain workspace
     scratch = 256 * ((3 * 3 * 128 * 4 + 255) // 256)
-    assert lib.spec_pipeline_async_workspace_size(128, 4, win, 128256) == chains + scratch
+    assert lib.spec_pipeline_async_workspace_size(128, 4, win, 128256) == 256 * ((chain + 255) // 256) + scratch
     assert lib.spec_pipeline_async_workspace_size(128, 9, win, 100) == 0
     assert lib.spec_pipeline_async_workspace_size(128, 1, win, 100) == 0
     assert lib.spec_pipeline_async_workspace_size(0, 4, win, 100) == 0
