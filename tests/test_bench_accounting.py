@@ -1,0 +1,75 @@
+"""bench.py's work accounting on the CPU: the units and algorithmic bytes
+(or flops) that every reported rate and roofline fraction divides by."""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import bench
+from workloads import synth
+
+
+def _reachable_keep_states(L, M):
+    """States (i - 1, j) whose layer i - 1 is applied in the DP, counted by
+    brute force: j keeps layer i - 1 (j <= i - 1) and (i, j) can still end at
+    (L, M) with at most one skip per remaining layer (M - j <= L - i)."""
+    n = 0
+    for i in range(1, L + 1):
+        for j in range(0, min(i, M) + 1):
+            if j <= i - 1 and M - j <= L - i:
+                n += 1
+    return n
+
+
+@pytest.mark.parametrize("L,M", [(32, 12), (8, 0), (8, 8), (5, 2), (1, 0), (1, 1), (12, 11)])
+def test_clasp_columns_count_the_reachable_kept_states(L, M):
+    spec = synth.with_sizes(synth.CLASP_SPECS["clasp_b16_l32_d4096_m12_bf16"], B=3, L=L, M=M)
+    assert bench.clasp_columns(spec) == 2 * 3 * _reachable_keep_states(L, M)
+
+
+def test_clasp_columns_and_bytes_of_the_workload():
+    spec = synth.CLASP_SPECS["clasp_b16_l32_d4096_m12_bf16"]
+    assert bench.clasp_columns(spec) == 8320
+    assert bench.clasp_bytes(spec) == 32 * 4096 * 4096 * 2 + 16 * 33 * 4096 * 4
+    assert bench.clasp_flops(spec) == 2 * 4096 * 4096 * 8320
+
+
+def test_clasp_band_matches_brute_force_reachability():
+    # the kernels evaluate max(0, M - (L - i)) <= j <= min(i, M); brute force
+    # over skip sets: (i, j) lies on some path that ends at (L, M)
+    for L, M in [(6, 2), (7, 7), (5, 0), (9, 4)]:
+        reach = set()
+        for S in itertools.combinations(range(L), M):
+            j = 0
+            reach.add((0, 0))
+            for i in range(1, L + 1):
+                j += (i - 1) in S
+                reach.add((i, j))
+        for i in range(L + 1):
+            band = {j for j in range(max(0, M - (L - i)), min(i, M) + 1)}
+            assert band == {j for (ii, j) in reach if ii == i}, (L, M, i)
+
+
+def test_async_bytes_and_tokens():
+    spec = synth.PIPELINE_ASYNC_SPECS["pipeline4_async_b128_g8_g6_g4_v128256_bf16"]
+    assert bench.async_rows(spec) == (9 + 8) + (7 + 6) + (5 + 4)
+    assert bench.async_bytes(spec) == 128 * 39 * 128256 * 2
+    assert bench.async_tokens(spec) == 128 * 18
+    g = synth.with_sizes(spec, greedy=True, dtype="f32")
+    assert bench.async_bytes(g) == 128 * (9 + 7 + 5) * 128256 * 4
+
+
+def test_async_workload_layout_is_consistent():
+    spec = synth.with_sizes(synth.PIPELINE_ASYNC_SPECS["pipeline4_async_b128_g8_g6_g4_v128256_bf16"], B=5, V=300)
+    w = synth.make(spec, seed=4)
+    L = w["length"]
+    assert L.shape == (4, 5) and (L >= 0).all()
+    for s in range(1, 4):
+        gap = L[s - 1] - L[s] - spec.windows[s - 1]
+        assert (gap >= 0).all() and (gap <= spec.extra).all()
+        assert w["targets"][s - 1].shape == (5, spec.windows[s - 1] + 1, 300)
+        assert w["drafts"][s - 1].shape == (5, spec.windows[s - 1], 300)
+        assert ((w["tokens"][s - 1] >= 0) & (w["tokens"][s - 1] < 300)).all()
+    again = synth.make(spec, seed=4)
+    assert all(np.array_equal(a, b) for a, b in zip(w["tokens"], again["tokens"]))
