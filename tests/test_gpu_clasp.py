@@ -158,3 +158,27 @@ def test_clasp_is_deterministic_and_choice_is_optional(cuda_device):
         assert a[k].tobytes() == b[k].tobytes() == c[k].tobytes(), k
     assert a["choice"].tobytes() == b["choice"].tobytes()
     assert "choice" not in c
+
+
+def test_clasp_graph_replays(cuda_device):
+    # one call captured in a CUDA graph (cuBLAS products included) and
+    # replayed on new hidden states copied into the same buffer
+    from draft_verification_gb300 import ClaspPlan
+    spec = synth.with_sizes(BASE, B=5, L=10, d=512, M=4)
+    ws = [synth.make(spec, seed=30 + i) for i in range(3)]
+    w0 = ws[0]
+    hidden = torch.from_numpy(w0["hidden"]).to(cuda_device)
+    weights = torch.from_numpy(w0["weights"].view(np.int16)).to(cuda_device).view(torch.bfloat16)
+    plan = ClaspPlan(hidden, weights, spec.M, choices=True)
+    stream = torch.cuda.Stream(cuda_device)
+    plan.run(stream)  # the first call on the device creates the cuBLAS handle: outside the capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.run(stream)
+    for w in ws[1:] + ws[:1]:
+        w = dict(w, weights=w0["weights"])  # the weights stay bound; only the hidden states change
+        hidden.copy_(torch.from_numpy(w["hidden"]).to(cuda_device))
+        graph.replay()
+        torch.cuda.synchronize()
+        check(w, {k: v.cpu().numpy() for k, v in plan.out.items()})

@@ -123,3 +123,38 @@ def test_two_models_equal_the_chain_entry(cuda_device, greedy):
     assert np.array_equal(g["a"][:, 0], c["accept_len"])
     assert np.array_equal(g["t"][:, 0], c["out_token"])
     assert np.array_equal(g["committed"], c["rollback_idx"] + 1)
+
+
+def test_pipeline_async_graph_replays(cuda_device):
+    # one call (per-stage chains with their batch-group streams, then the
+    # combine) captured in a CUDA graph and replayed on new inputs
+    import torch
+    from draft_verification_gb300 import PipelineAsyncPlan
+    spec = synth.with_sizes(BASE, B=40, V=9000, final_bonus=True, extra=1)
+    ws = [synth.make(spec, seed=40 + i) for i in range(3)]
+    w0 = ws[0]
+    tg = [H.logits_view(H.dev_logits(x, spec.dtype, cuda_device), spec.V) for x in w0["targets"]]
+    dr = [H.logits_view(H.dev_logits(x, spec.dtype, cuda_device), spec.V) for x in w0["drafts"]]
+    tok = [H.dev(t, cuda_device) for t in w0["tokens"]]
+    us = [H.dev(u, cuda_device) for u in w0["us"]]
+    vs = [H.dev(v, cuda_device) for v in w0["vs"]]
+    length = H.dev(w0["length"], cuda_device)
+    plan = PipelineAsyncPlan(tg, dr, tok, length, us, vs, temperature=spec.temperature, final_bonus=True)
+    stream = torch.cuda.Stream(cuda_device)
+    plan.run(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.run(stream)
+    for w in ws[1:] + ws[:1]:
+        for dst, src in zip(tg, w["targets"]):
+            dst.copy_(H.logits_view(H.dev_logits(src, spec.dtype, cuda_device), spec.V))
+        for dst, src in zip(dr, w["drafts"]):
+            dst.copy_(H.logits_view(H.dev_logits(src, spec.dtype, cuda_device), spec.V))
+        for dst, src in zip(tok + us + vs, w["tokens"] + w["us"] + w["vs"]):
+            dst.copy_(H.dev(src, cuda_device))
+        length.copy_(H.dev(w["length"], cuda_device))
+        plan.out["error_word"].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        compare(H.to_np(plan.out), oracle_async(w), False)
