@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "internal.h"
@@ -38,6 +39,7 @@ namespace sv {
 namespace {
 
 constexpr int kMaxStages = SPEC_MAX_MODELS - 1;
+constexpr int kMaxVocab = 2097152;  // the chain call's limit
 constexpr int kCombineThreads = 128;
 constexpr int kHardErrors = SPEC_ERR_TOKEN | SPEC_ERR_NONFINITE | SPEC_ERR_INTERNAL | SPEC_ERR_WINDOW;
 
@@ -131,6 +133,8 @@ bool async_layout(int B, int k, const int* window, int V, AsyncLayout* out) {
   return true;
 }
 
+bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
 }  // namespace
 }  // namespace sv
 
@@ -147,12 +151,18 @@ extern "C" spec_status spec_verify_pipeline_async(const spec_pipeline_async_args
   if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_EDTYPE;
   if (a->mode != SPEC_GREEDY && a->mode != SPEC_SAMPLE) return SPEC_EDTYPE;
   const bool greedy = a->mode == SPEC_GREEDY;
+  // every check a stage's chain call makes is made here first, so that an
+  // argument error is reported before any stage has been launched
+  if (a->V > kMaxVocab || a->ld < a->V || a->ld > (1LL << 40)) return SPEC_EINVAL;
+  if (!greedy && !(a->temperature > 0.f && std::isfinite(a->temperature))) return SPEC_EINVAL;
   if (!a->length || !a->a || !a->t || !a->t_valid || !a->r || !a->committed) return SPEC_EINVAL;
   const int S = a->k - 1;
   for (int s = 0; s < S; ++s) {
     if (!a->target[s] || !a->tokens[s]) return SPEC_EINVAL;
     if (!greedy && (!a->draft[s] || !a->u[s] || !a->v[s])) return SPEC_EINVAL;
   }
+  for (int s = 0; s < S; ++s)
+    if (!aligned16(a->target[s]) || (!greedy && !aligned16(a->draft[s]))) return SPEC_EALIGN;
   if (!a->workspace || a->workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(a->workspace) & 15u))
     return SPEC_EWORKSPACE;
   char* ws = static_cast<char*>(a->workspace);

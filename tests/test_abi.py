@@ -340,6 +340,14 @@ def test_pipeline_async_workspace_and_argument_errors(lib):
                      (dict(dtype=5), -2), (dict(mode=3), -2), (dict(committed=None), -1), (dict(length=None), -1),
                      (dict(workspace_bytes=8), -4), (dict(workspace=0x10008), -4)]:
         assert lib.spec_verify_pipeline_async(C.byref(_async(**kw)), None) == code, kw
+    # checks every stage's chain call would make, made before any launch
+    for kw, code in [(dict(V=2097153, ld=2097153), -1), (dict(ld=99), -1), (dict(temperature=0.0), -1),
+                     (dict(temperature=float("inf")), -1)]:
+        assert lib.spec_verify_pipeline_async(C.byref(_async(**kw)), None) == code, kw
+    for field in ("target", "draft"):
+        a = _async()
+        getattr(a, field)[2] = 0x10008  # the last stage's rows misaligned
+        assert lib.spec_verify_pipeline_async(C.byref(a), None) == -3, field
     for field in ("target", "tokens", "draft", "u", "v"):
         a = _async()
         getattr(a, field)[2] = None
