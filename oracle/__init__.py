@@ -20,6 +20,8 @@ Modules
                   the first rejection are never read).
 ``clasp``         the CLaSp layer-selection dynamic program and its
                   backtracking, on synthetic residual layers.
+``consulted_tree`` the tree walk consulting only the rows of the nodes it
+                  visits (rows off the path are never read).
 ``pipeline_async`` the PipeSpec stages at independent buffer offsets (each
                   stage a chain verification of its own window, then the
                   rollbacks).
@@ -29,4 +31,4 @@ silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import clasp, closed_forms, compact, consulted, pipeline, pipeline_async, verify  # noqa: F401
+from . import clasp, closed_forms, compact, consulted, consulted_tree, pipeline, pipeline_async, verify  # noqa: F401
