@@ -20,6 +20,8 @@ Modules
                   the first rejection are never read).
 ``clasp``         the CLaSp layer-selection dynamic program and its
                   backtracking, on synthetic residual layers.
+``lm_head``       chain verification from the final hidden states and the
+                  LM-head weights (the logits as exact products).
 ``consulted_tree`` the tree walk consulting only the rows of the nodes it
                   visits (rows off the path are never read).
 ``pipeline_async`` the PipeSpec stages at independent buffer offsets (each
@@ -31,4 +33,5 @@ silent or ambiguous follow the readings listed in the design notes; each is
 repeated in the docstring that depends on it.
 """
 
-from . import clasp, closed_forms, compact, consulted, consulted_tree, pipeline, pipeline_async, verify  # noqa: F401
+from . import (clasp, closed_forms, compact, consulted, consulted_tree, lm_head, pipeline,  # noqa: F401
+               pipeline_async, verify)
