@@ -99,6 +99,23 @@ def draft_tokens_per_call(w) -> int:
     return s.B * (s.gamma1 + s.gamma2)
 
 
+def chain_groups(B: int, rows: int, V: int, elt: int) -> int:
+    """Batch groups of one chain call, as the library plans them: at most 4,
+    each with at least 16 sequences and 40 MB of logits."""
+    return max(1, min(4, B // 16, int(B * rows * V * elt / 40e6)))
+
+
+def launches_per_call(w) -> int:
+    """Kernels of the library launched by one verification call: statistics
+    and walk per batch group for chains (one group in consulted-only mode),
+    statistics and walk for the other kinds."""
+    s = w["spec"]
+    if w["kind"] == "chain" and not (CONSULTED and not s.greedy):
+        rows = s.gamma + 1 if s.greedy else 2 * s.gamma + 1
+        return 2 * chain_groups(s.B, rows, s.V, 2 if s.dtype == "bf16" else 4)
+    return 2
+
+
 def workload_config(w) -> dict:
     s = w["spec"]
     cfg = {"workload": s.name, "kind": w["kind"], "batch": s.B, "vocab": s.V,
@@ -503,7 +520,7 @@ def run_ours(args, w, rank, world, dist):
                      "kernel_ms": kernel_ms, "algorithmic_bytes": roof_bytes,
                      "traffic": None if CONSULTED else profiled_traffic(s.name)},
         "e2e": e2e,
-        "gpu_launches": args.steps * len(KERNELS[w["kind"]]),
+        "gpu_launches": args.steps * launches_per_call(w),
         "clocks": clock_info,
     }
     return line
@@ -977,6 +994,14 @@ def async_tokens(spec) -> int:
     return spec.B * sum(spec.windows)
 
 
+def async_launches_per_call(spec) -> int:
+    """One chain verification per stage (statistics and walk per batch
+    group), then the combine kernel."""
+    elt = 2 if spec.dtype == "bf16" else 4
+    return 1 + sum(2 * chain_groups(spec.B, w + 1 if spec.greedy else 2 * w + 1, spec.V, elt)
+                   for w in spec.windows)
+
+
 def async_config(w) -> dict:
     s = w["spec"]
     return {"workload": s.name, "kind": "pipeline_async", "batch": s.B, "models": s.k, "windows": list(s.windows),
@@ -1127,7 +1152,7 @@ def run_pipeline_async(args, w):
                      "traffic": profiled_traffic(s.name, ASYNC_SOURCES)},
         "e2e": {"value": async_tokens(s) / (el / n), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n},
-        "gpu_launches": args.steps * (2 * (s.k - 1) + 1),
+        "gpu_launches": args.steps * async_launches_per_call(s),
         "clocks": clock_info,
     }
 

@@ -73,3 +73,31 @@ def test_async_workload_layout_is_consistent():
         assert ((w["tokens"][s - 1] >= 0) & (w["tokens"][s - 1] < 300)).all()
     again = synth.make(spec, seed=4)
     assert all(np.array_equal(a, b) for a, b in zip(w["tokens"], again["tokens"]))
+
+
+def _stats_launches_per_call(name, calls):
+    """Statistics-kernel launches per call in a committed ncu launch list."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles",
+                        f"launches_{name}.md")
+    for line in open(path):
+        if line.startswith("| stats_kernel"):
+            return int(line.split("|")[2]) // calls
+    raise AssertionError(name)
+
+
+@pytest.mark.parametrize("name,per_call", [("sampling_chain_b32_g8_v32000_bf16", 2),
+                                           ("sampling_chain_b64_g5_v128256_bf16_a60", 8),
+                                           ("greedy_chain_b4_g4_v1000_f32", 2)])
+def test_chain_launches_per_call_match_the_launch_lists(name, per_call):
+    spec = synth.SPECS[name]
+    w = dict(kind="chain", spec=spec)
+    assert bench.launches_per_call(w) == per_call
+    # the launch lists (5 calls each) saw one statistics kernel per group
+    assert 2 * _stats_launches_per_call(name, 5) == per_call
+
+
+def test_async_launches_per_call_match_the_launch_list():
+    spec = synth.PIPELINE_ASYNC_SPECS["pipeline4_async_b128_g8_g6_g4_v128256_bf16"]
+    assert bench.async_launches_per_call(spec) == 3 * 8 + 1
+    assert 2 * _stats_launches_per_call(spec.name, 5) + 1 == bench.async_launches_per_call(spec)
