@@ -6,9 +6,11 @@ One step = one verification call over one batch of the workload: two kernels
 on one stream, the row-statistics kernel (streams every logit once) and the
 walk kernel (one thread-block cluster per sequence: accept tests, residual
 or bonus pass, inverse-CDF draw), chained with programmatic dependent launch.
-The default workload is the sampling chain B=32, gamma=8, V=32000, bf16,
-T=1.0, mean acceptance ~0.7; --workload selects any of
-workloads.synth.SPECS.  Inputs are synthetic and seeded.
+The default workload is the largest one, the three-model PipeSpec cascade
+B=128, gamma1=8, gamma2=4, V=128256, bf16, T=1.0 (one 689.5 MB call: the
+M_0, M_1 and M_2 logit rows); --workload selects any of
+workloads.synth.SPECS (e.g. the 128256-vocabulary sampling chain
+sampling_chain_b64_g5_v128256_bf16_a60).  Inputs are synthetic and seeded.
 
 Timing: W warm-up steps, then a loaded soak of about one second (clocks are
 sampled over it and the timed region), then exactly K steps between CUDA
@@ -47,7 +49,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "sampling_chain_b32_g8_v32000_bf16"
+DEFAULT_WORKLOAD = "cascade_b128_g8_g4_v128256_bf16"
 METRIC = "verified draft tokens/sec and logits GB/s vs GB300 HBM peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["draft_verification_gb300/csrc/verify.cu", "draft_verification_gb300/csrc/stats.cuh",
@@ -114,6 +116,12 @@ def launches_per_call(w) -> int:
         rows = s.gamma + 1 if s.greedy else 2 * s.gamma + 1
         return 2 * chain_groups(s.B, rows, s.V, 2 if s.dtype == "bf16" else 4)
     return 2
+
+
+def compute_dtype(logit_dtype: str) -> str:
+    """Arithmetic of the verification path: float32 throughout, on logits
+    stored as bfloat16 or float32."""
+    return "bf16 in, f32 accumulate" if logit_dtype == "bf16" else "f32"
 
 
 def workload_config(w) -> dict:
@@ -506,7 +514,7 @@ def run_ours(args, w, rank, world, dist):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded; shapes of the pages' model families)",
+        "dtype": compute_dtype(s.dtype), "data": "synthetic (seeded; shapes of the pages' model families)",
         "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        consulted_only=bool(CONSULTED and w["kind"] == "chain" and not s.greedy),
                        l2_policy=f"rotating {n_sets} input copies ({n_sets * bytes_per_call / 2**20:.0f} MB "
@@ -1140,7 +1148,7 @@ def run_pipeline_async(args, w):
     return {
         "metric": METRIC, "value": async_tokens(s) / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype(s.dtype),
         "data": "synthetic (seeded logits; windows drawn from the drafter's softmax)",
         "config": dict(async_config(w), parallelism="1 GPU", launch=launch,
                        l2_policy=f"rotating {n_sets} copies of the logits "

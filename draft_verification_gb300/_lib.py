@@ -127,6 +127,7 @@ SIGNATURES = {
     "spec_clasp_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spec_clasp_layer_select": (C.c_int, [C.POINTER(ClaspArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
+    "spec_test_inject_copy_timeout": (C.c_int, [C.c_int]),
 }
 
 _LIB = None

@@ -138,10 +138,12 @@ size_t spec_cascade_workspace_size(int B, int gamma1, int gamma2, int V) {
 }
 
 spec_status spec_verify_chain(const spec_chain_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_chain");
   return sv::verify_chain(a, stream, true);
 }
 
 spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_tree");
   if (a == nullptr) return SPEC_EINVAL;
   spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
   if (st != SPEC_OK) return st;
@@ -189,6 +191,7 @@ spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
 }
 
 spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_cascade");
   if (a == nullptr) return SPEC_EINVAL;
   spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
   if (st != SPEC_OK) return st;
@@ -281,6 +284,7 @@ extern "C" size_t spec_pipeline_workspace_size(int B, int k, const int* window, 
 }
 
 extern "C" spec_status spec_verify_pipeline(const spec_pipeline_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_pipeline");
   if (a == nullptr) return SPEC_EINVAL;
   spec_status st = check_common(a->B, a->V, a->ld, a->dtype, a->mode, a->temperature);
   if (st != SPEC_OK) return st;

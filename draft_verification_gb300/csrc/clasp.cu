@@ -375,6 +375,7 @@ extern "C" size_t spec_clasp_workspace_size(int B, int L, int d, int M) {
 }
 
 extern "C" spec_status spec_clasp_layer_select(const spec_clasp_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_clasp_layer_select");
   using namespace sv;
   if (a == nullptr) return SPEC_EINVAL;
   if (!sizes_ok(a->B, a->L, a->d, a->M)) return SPEC_EINVAL;

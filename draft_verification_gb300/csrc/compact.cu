@@ -103,6 +103,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace sv;
 
 extern "C" spec_status spec_compact_tree_path(const spec_compact_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_compact_tree_path");
   if (a == nullptr) return SPEC_EINVAL;
   if (a->B < 1 || a->B > 65535 || a->N < 1 || a->max_depth < 0 || a->max_depth > 65534 || a->cache_rows < 1)
     return SPEC_EINVAL;

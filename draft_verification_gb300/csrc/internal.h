@@ -7,7 +7,18 @@
 
 #include "spec_verify.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace sv {
+
+// NVTX range around one entry-point call (the call's launches nest inside
+// it on a profiler's timeline; costs nothing when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Logit rows of one tensor: row (b, i) starts at base + (b * rows + i) * ld.
 struct RowSet {

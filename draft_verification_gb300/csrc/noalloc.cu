@@ -54,6 +54,7 @@ cudaError_t scratch_address(void** out) {
 }  // namespace
 
 extern "C" spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_chain_noalloc");
   if (args == nullptr) return SPEC_EINVAL;
   // Refuse calls whose scratch would not fit before touching the device.
   if (args->B < 1 || args->B > 65535 || args->gamma < 0 || args->gamma > 32 || args->V < 1) return SPEC_EINVAL;
@@ -61,8 +62,10 @@ extern "C" spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cu
     return SPEC_EWORKSPACE;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return SPEC_ECUDA;
-  // The scratch holds only values a call writes before it reads them, so
-  // nothing has to be cleared between calls.
+  // The statistics partials in the scratch are written before they are
+  // read; the consulted-only mode's control words, which must start at zero,
+  // are cleared by the call itself (one memset on `stream`), so nothing a
+  // previous call left behind is ever read.
   spec_chain_args a = *args;
   a.workspace = scratch;
   a.workspace_bytes = SPEC_NOALLOC_SCRATCH_BYTES;

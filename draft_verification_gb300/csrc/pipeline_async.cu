@@ -10,11 +10,12 @@
 // The stages of an asynchronous snapshot do not feed one another: stage s
 // reads the window O_{s-1}[l_s, l_s + w_s) that was in place before the
 // snapshot.  So each stage is one chain verification of its own window (the
-// same statistics and walk kernels as spec_verify_chain, with the stage's
-// buffer length as the prefix, so that the chain's rollback index is the
-// absolute rejection position), and the stages run one after another on the
-// caller's stream sharing one workspace.  pipeline_async_combine_kernel then
-// applies the emission and rollback rules per sequence:
+// same statistics and walk kernels as spec_verify_chain, with no prefix: the
+// chain reports only the stage's accept length a_s, token and error bits),
+// and the stages run one after another on the caller's stream sharing one
+// workspace.  pipeline_async_combine_kernel then forms each rejection
+// position P_s = l_s + a_s from the buffer lengths and applies the emission
+// and rollback rules per sequence:
 //   - a window that does not fit (l_{s-1} < l_s + w_s) or a negative length
 //     makes the sequence malformed (SPEC_ERR_WINDOW, empty outputs);
 //   - a rejection emits the correction and cuts every earlier buffer to at
@@ -144,6 +145,7 @@ extern "C" size_t spec_pipeline_async_workspace_size(int B, int k, const int* wi
 }
 
 extern "C" spec_status spec_verify_pipeline_async(const spec_pipeline_async_args* a, cudaStream_t stream) {
+  sv::NvtxRange nvtx_range("spec_verify_pipeline_async");
   using namespace sv;
   if (a == nullptr) return SPEC_EINVAL;
   AsyncLayout w;

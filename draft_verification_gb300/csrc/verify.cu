@@ -60,6 +60,11 @@ constexpr int kMaxGamma = 32;
 constexpr int kMaxDecisionChunks = 256;  // statistics chunks of the longest row (2^21 float32 logits)
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+// Test hook (spec_test_inject_copy_timeout): nonzero makes every bulk-copy
+// stage of a residual pass expect 16 bytes that never come, so that its
+// bounded wait gives up.  Zero in normal operation.
+__device__ int g_copy_timeout_test = 0;
 constexpr int kStage = 4 * kThreads;  // chunk partials staged per round (8 KB)
 static_assert(kMaxTiles * kTileElems >= 2097152, "tile sums of the largest row fit in shared memory");
 
@@ -153,7 +158,7 @@ __device__ __forceinline__ PassSpec<T> make_spec(const T* P, float mP, float sP,
   S.MQ = Q ? scaled_max(mQ, c) : 0.f;
   S.invSQ = Q ? __fdiv_rn(1.f, sQ) : 0.f;
   S.cq = Q ? cq : 0.f;
-  S.pad = 0;
+  S.extra_tx = g_copy_timeout_test ? 16u : 0u;
   return S;
 }
 
@@ -380,7 +385,18 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
   const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps);
   if (y < 0) return;  // another CTA of the cluster holds the drawn tile
-  if (ps.fault) flag |= SPEC_ERR_INTERNAL;
+  if (ps.fault) {  // a bounded wait gave up: the draw is not trusted
+    flag |= SPEC_ERR_INTERNAL;
+    if (tid == 0) {
+      P.accept_len[b] = 0;
+      P.out_token[b] = -1;
+      if (P.rollback) P.rollback[b] = P.prefix ? P.prefix[b] : 0;
+      if (P.resid) P.resid[b] = 0.f;
+      if (P.seq_error) P.seq_error[b] = flag;
+      if (P.error_word) atomicOr(P.error_word, flag);
+    }
+    return;
+  }
   if (tid == 0) {
     P.accept_len[b] = a;
     P.out_token[b] = y;
@@ -410,6 +426,14 @@ struct CascadeOut {
   const CascadeParams& P;
   int b;
   __device__ void write(int a1, int t1, int a2, int w2, int t2, int t2v, int flag) const {
+    if (flag & SPEC_ERR_INTERNAL) {  // a bounded wait gave up: empty outputs
+      a1 = 0;
+      t1 = -1;
+      a2 = 0;
+      w2 = 0;
+      t2 = -1;
+      t2v = 0;
+    }
     const bool rej = a2 < w2;
     const int base0 = P.base0 ? P.base0[b] : 0;
     const int base1 = P.base1 ? P.base1[b] : 0;
@@ -739,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 4) pipeline_walk_kernel(const StatsP
     }
     __syncthreads();
   }
-  if (lead && tid == 0) pipe_write(P, b, cs, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0), false);
+  if (lead && tid == 0) pipe_write(P, b, cs, flag | (ps.fault ? SPEC_ERR_INTERNAL : 0), ps.fault != 0);
 }
 
 // ===========================================================================
@@ -1006,7 +1030,11 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   }
   __syncthreads();
   if (!writer) return;
-  if (ps.fault) flag |= SPEC_ERR_INTERNAL;
+  if (ps.fault) {  // a bounded wait gave up: empty outputs
+    flag |= SPEC_ERR_INTERNAL;
+    token = -1;
+    plen = 0;
+  }
   if (tid == 0) {
     P.out_token[b] = token;
     P.path_len[b] = plen;
@@ -1014,7 +1042,8 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
     if (P.seq_error) P.seq_error[b] = flag;
     if (flag && P.error_word) atomicOr(P.error_word, flag);
   }
-  for (int q = tid; q < pn; q += kThreads) pnodes[q] = q == 0 ? 0 : (q <= plen ? path[q - 1] : -1);
+  for (int q = tid; q < pn; q += kThreads)
+    pnodes[q] = ps.fault ? -1 : (q == 0 ? 0 : (q <= plen ? path[q - 1] : -1));
 }
 
 // ---------------------------------------------------------------------------
@@ -1198,23 +1227,54 @@ Groups plan_groups(int B, double bytes) {
   return g;
 }
 
-cudaError_t group_streams(cudaStream_t* out) {
-  static std::mutex mu;
-  static std::map<int, std::array<cudaStream_t, kMaxGroups>> cache;
+// Library streams and events of the calling host thread on the current
+// device: one side stream per group, the fork event and one join event per
+// group.  They are created on the thread's first grouped call on the device
+// and reused by its later calls, so a call creates nothing; keeping them per
+// thread means that calls from different host threads never share a side
+// stream (one thread capturing a call into a graph cannot pull another
+// thread's eager call into its capture).  They are released when the thread
+// exits.
+struct GroupResources {
+  cudaStream_t side[kMaxGroups];
+  cudaEvent_t fork;
+  cudaEvent_t join[kMaxGroups];
+};
+
+struct ThreadGroupResources {
+  std::map<int, GroupResources> per_device;
+  ~ThreadGroupResources() {
+    for (auto& kv : per_device) {
+      int cur = 0;
+      if (cudaGetDevice(&cur) != cudaSuccess) return;  // the runtime is already gone
+      if (cudaSetDevice(kv.first) != cudaSuccess) continue;
+      for (int i = 0; i < kMaxGroups; ++i) {
+        cudaStreamDestroy(kv.second.side[i]);
+        cudaEventDestroy(kv.second.join[i]);
+      }
+      cudaEventDestroy(kv.second.fork);
+      cudaSetDevice(cur);
+    }
+  }
+};
+
+cudaError_t group_resources(GroupResources** out) {
+  thread_local ThreadGroupResources mine;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(dev);
-  if (it == cache.end()) {
-    std::array<cudaStream_t, kMaxGroups> st{};
-    for (int i = 0; i < kMaxGroups; ++i) {
-      e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
-      if (e != cudaSuccess) return e;
+  auto it = mine.per_device.find(dev);
+  if (it == mine.per_device.end()) {
+    GroupResources r{};
+    for (int i = 0; i < kMaxGroups && e == cudaSuccess; ++i) {
+      e = cudaStreamCreateWithFlags(&r.side[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.join[i], cudaEventDisableTiming);
     }
-    it = cache.emplace(dev, st).first;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;  // (a partial set is not kept)
+    it = mine.per_device.emplace(dev, r).first;
   }
-  for (int i = 0; i < kMaxGroups; ++i) out[i] = it->second[i];
+  *out = &it->second;
   return cudaSuccess;
 }
 
@@ -1224,28 +1284,20 @@ cudaError_t group_streams(cudaStream_t* out) {
 // that was enqueued.
 template <typename F>
 cudaError_t run_groups(const Groups& gr, cudaStream_t s, F launch_group) {
-  cudaStream_t side[kMaxGroups];
-  cudaError_t e = group_streams(side);
+  GroupResources* r = nullptr;
+  cudaError_t e = group_resources(&r);
   if (e != cudaSuccess) return e;
-  cudaEvent_t fork;
-  e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-  if (e != cudaSuccess) return e;
-  e = cudaEventRecord(fork, s);
+  e = cudaEventRecord(r->fork, s);
   cudaError_t first = e;
   for (int i = 0; i < gr.n && first == cudaSuccess; ++i) {
-    cudaEvent_t done;
-    e = cudaStreamWaitEvent(side[i], fork, 0);
-    if (e == cudaSuccess) e = launch_group(i, side[i]);
+    e = cudaStreamWaitEvent(r->side[i], r->fork, 0);
+    if (e == cudaSuccess) e = launch_group(i, r->side[i]);
     if (e != cudaSuccess) first = e;
-    if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess) {
-      if (cudaEventRecord(done, side[i]) == cudaSuccess) {
-        e = cudaStreamWaitEvent(s, done, 0);
-        if (e != cudaSuccess && first == cudaSuccess) first = e;
-      }
-      cudaEventDestroy(done);
+    if (cudaEventRecord(r->join[i], r->side[i]) == cudaSuccess) {
+      e = cudaStreamWaitEvent(s, r->join[i], 0);
+      if (e != cudaSuccess && first == cudaSuccess) first = e;
     }
   }
-  cudaEventDestroy(fork);
   return first;
 }
 
@@ -1392,3 +1444,8 @@ cudaError_t launch_cascade(const StatsParams& G, const CascadeParams& p, bool bf
 }
 
 }  // namespace sv
+
+extern "C" spec_status spec_test_inject_copy_timeout(int enable) {
+  const int v = enable ? 1 : 0;
+  return cudaMemcpyToSymbol(sv::g_copy_timeout_test, &v, sizeof(v)) == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}

@@ -39,7 +39,8 @@ struct PassSpec {
   float MP, invSP;  // scaled max and 1/sum of the target row
   float MQ, invSQ;
   float cq;         // coefficient of q
-  int pad;
+  unsigned extra_tx;  // bytes each bulk-copy stage expects beyond its copies:
+                      // 0, or 16 under the copy-timeout test hook
 };
 
 // ---------------------------------------------------------------------------
@@ -362,7 +363,7 @@ __device__ void staged_sums(const PassSpec<T>& S, int V, float c, int t0, int t1
     const unsigned bytes = static_cast<unsigned>((min(te * kTileElems, Vv) - ta * kTileElems) * sizeof(T));
     const int b = (g0 + k) % kStages;
     unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
-    mbar_expect_tx(&sh.bar[b], useQ ? 2 * bytes : bytes);
+    mbar_expect_tx(&sh.bar[b], (useQ ? 2 * bytes : bytes) + S.extra_tx);
     if (bytes == 0) return;  // the arrival alone completes the phase
     bulk_load(buf, S.P + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
     if (useQ) bulk_load(buf + kStageRowBytes, S.Q + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);

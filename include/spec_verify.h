@@ -49,12 +49,18 @@
  *    returns SPEC_ECUDA.
  *  - Data errors found on the device never trap: they set bits in the
  *    optional per-sequence `seq_error` array and are OR-ed into the optional
- *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2 or 4 gets
- *    empty outputs: accept length 0, tokens -1, rollback = prefix length.
+ *    `*error_word` (caller zeroes it).  A sequence with bit 1, 2, 4 or 16
+ *    gets empty outputs: accept length 0, tokens -1, rollback = prefix length.
  *  - Each call is two kernel launches (row statistics, then the per-sequence
  *    walk) per batch group; large sampling chain calls are split into
  *    groups that run on library streams forked from `stream` and joined
  *    back into it, so the call is ordered on `stream` like any other work.
+ *    Those streams and their fork / join events belong to the calling host
+ *    thread (created on its first grouped call on a device, reused after,
+ *    released when the thread exits), so calls from different threads never
+ *    share them; within one thread, do not enqueue a grouped call eagerly
+ *    while another of the thread's calls is being captured into a graph
+ *    under the global capture mode.
  *    A consulted-only chain call adds one memset of its control words;
  *    spec_compact_tree_path is one kernel; spec_clasp_layer_select is
  *    L + 2 kernels and L cuBLAS GEMMs; spec_verify_pipeline_async is one
@@ -98,9 +104,10 @@ typedef enum spec_mode { SPEC_GREEDY = 0, SPEC_SAMPLE = 1 } spec_mode;
 #define SPEC_ERR_NONFINITE 4  /* a logit row with NaN or +inf, or no finite entry */
 #define SPEC_ERR_ZERO_MASS 8  /* residual mass 0 after a rejection: the token was
                                  drawn from p instead (outputs stay valid)       */
-#define SPEC_ERR_INTERNAL 16  /* a bulk copy of logits into shared memory did not
-                                 complete in time; this sequence's outputs are
-                                 not valid (never expected; reported, not hung) */
+#define SPEC_ERR_INTERNAL 16  /* a bounded wait (a bulk copy of logits into shared
+                                 memory, or a peer's exchange) gave up after
+                                 about 65 ms; the sequence gets empty outputs
+                                 (never expected; reported, not hung)          */
 #define SPEC_ERR_WINDOW 32    /* asynchronous pipeline: a negative buffer length,
                                  or a stage window that does not fit in the
                                  buffer below it                                 */
@@ -176,6 +183,10 @@ spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
 /*    on the GPU (other streams, other host threads) race on it and give    */
 /*    wrong results.  Serialise them, or use spec_verify_chain with one     */
 /*    workspace per stream.                                                 */
+/*  - The array keeps what the last call left in it.  A call reads only     */
+/*    statistics it wrote itself; in consulted-only mode the control words  */
+/*    that must start at zero are cleared by the call (one memset on        */
+/*    `stream`).                                                            */
 /* ---------------------------------------------------------------------- */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
 spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cudaStream_t stream);
@@ -488,6 +499,20 @@ spec_status spec_clasp_layer_select(const spec_clasp_args* args, cudaStream_t st
 
 /* Human-readable name of a status code (static string). */
 const char* spec_status_string(spec_status status);
+
+/* ---------------------------------------------------------------------- */
+/* Test hook for the bounded waits (no counterpart on the pages).  While   */
+/* enabled on the current device, every bulk-copy stage of a sampling      */
+/* walk's residual or bonus pass expects 16 bytes more than it copies, so  */
+/* its wait gives up after about 65 ms instead of completing: the sequence */
+/* reports SPEC_ERR_INTERNAL with empty outputs and the GPU stays usable.   */
+/* Nothing faults and nothing is left in flight (the copies themselves     */
+/* complete).  Synchronous (one small copy to the device); affects calls   */
+/* launched after it returns.  For tests of the give-up path only: leave   */
+/* it disabled (the default) in any other use.                             */
+/* SPEC_ECUDA if the copy fails.                                           */
+/* ---------------------------------------------------------------------- */
+spec_status spec_test_inject_copy_timeout(int enable);
 
 #ifdef __cplusplus
 }

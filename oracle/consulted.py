@@ -38,7 +38,7 @@ def verify_chain_consulted_sequence(target, draft, tokens, u, v, temperature):
     gamma = len(tokens)
     V = target.shape[1]
     out = dict(accept_len=0, out_token=-1, error=0, p_at_draft=np.zeros(gamma), q_at_draft=np.zeros(gamma),
-               resid_mass=0.0, margin_u=math.inf, margin_v=math.inf, rows_read=0)
+               resid_mass=0.0, margin_u=math.inf, margin_v=math.inf, rows_read=0, min_mass=math.inf)
     if any(t < 0 or t >= V for t in tokens):
         out["error"] = ERR_TOKEN
         return out
@@ -61,6 +61,7 @@ def verify_chain_consulted_sequence(target, draft, tokens, u, v, temperature):
     error = 0
     if a < gamma:
         weights = residual(p, q)
+        out["min_mass"] = float(np.sum(weights))
         if not np.sum(weights) > 0.0:
             error |= ERR_ZERO_MASS
             weights = p
@@ -85,7 +86,8 @@ def verify_chain_consulted(target, draft, tokens, u, v, prefix_len, temperature,
     res = dict(accept_len=np.zeros(B, np.int64), out_token=np.zeros(B, np.int64),
                rollback_idx=np.zeros(B, np.int64), error=np.zeros(B, np.int64),
                p_at_draft=np.zeros((B, gamma)), q_at_draft=np.zeros((B, gamma)), resid_mass=np.zeros(B),
-               margin_u=np.zeros(B), margin_v=np.zeros(B), rows_read=np.zeros(B, np.int64))
+               margin_u=np.zeros(B), margin_v=np.zeros(B), rows_read=np.zeros(B, np.int64),
+               min_mass=np.zeros(B))
 
     class Rows:  # converts a row when it is read
         def __init__(self, arr, n):
@@ -101,7 +103,8 @@ def verify_chain_consulted(target, draft, tokens, u, v, prefix_len, temperature,
     for b in range(B):
         r = verify_chain_consulted_sequence(Rows(target[b], gamma + 1), Rows(draft[b], gamma),
                                             [int(t) for t in tokens[b]], u[b], v[b], temperature)
-        for k in ("accept_len", "out_token", "error", "resid_mass", "margin_u", "margin_v", "rows_read"):
+        for k in ("accept_len", "out_token", "error", "resid_mass", "margin_u", "margin_v", "rows_read",
+                  "min_mass"):
             res[k][b] = r[k]
         res["p_at_draft"][b] = r["p_at_draft"]
         res["q_at_draft"][b] = r["q_at_draft"]

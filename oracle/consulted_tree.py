@@ -38,9 +38,10 @@ from .verify import (ERR_NONFINITE, ERR_PARENT, ERR_TOKEN, ERR_ZERO_MASS, accept
 def verify_tree_consulted_sequence(parent, tokens, target, draft, u, v, temperature, greedy, max_depth):
     """One tree (arguments as ``oracle.verify.verify_tree_sequence``; target
     and draft may be lazy row sources: only rows[i] and .shape are used).
-    Returns dict(path, out_token, error, margin_u, margin_v, rows_read)."""
+    Returns dict(path, out_token, error, margin_u, margin_v, rows_read, min_mass)."""
     N, V = target.shape
-    out = dict(path=[], out_token=-1, error=0, margin_u=math.inf, margin_v=math.inf, rows_read=0)
+    out = dict(path=[], out_token=-1, error=0, margin_u=math.inf, margin_v=math.inf, rows_read=0,
+               min_mass=math.inf)
     error = 0
     depth = tree_depths([int(x) for x in parent])
     if depth is None or max(depth) > max_depth:
@@ -91,6 +92,7 @@ def verify_tree_consulted_sequence(parent, tokens, target, draft, u, v, temperat
                     break
                 nxt = residual(p, q)
                 mass = float(np.sum(nxt))
+                out["min_mass"] = min(out["min_mass"], mass)
                 if not mass > 0.0:
                     zero_mass = True
                     break
@@ -116,7 +118,7 @@ def verify_tree_consulted(parent, tokens, target, draft, u, v, prefix_len, tempe
     res = dict(path_len=np.zeros(B, np.int64), path_nodes=-np.ones((B, max_depth + 1), np.int64),
                out_token=np.zeros(B, np.int64), rollback_idx=np.zeros(B, np.int64),
                error=np.zeros(B, np.int64), margin_u=np.zeros(B), margin_v=np.zeros(B),
-               rows_read=np.zeros(B, np.int64))
+               rows_read=np.zeros(B, np.int64), min_mass=np.zeros(B))
 
     class Rows:  # converts a row when it is read
         def __init__(self, arr):
@@ -133,7 +135,7 @@ def verify_tree_consulted(parent, tokens, target, draft, u, v, prefix_len, tempe
         r = verify_tree_consulted_sequence(parent[b], tokens[b], Rows(target[b]),
                                            None if greedy else Rows(draft[b]), None if greedy else u[b],
                                            None if greedy else v[b], temperature, greedy, max_depth)
-        for k in ("out_token", "error", "margin_u", "margin_v", "rows_read"):
+        for k in ("out_token", "error", "margin_u", "margin_v", "rows_read", "min_mass"):
             res[k][b] = r[k]
         res["path_len"][b] = len(r["path"])
         if r["error"] & (ERR_TOKEN | ERR_PARENT | ERR_NONFINITE) == 0:

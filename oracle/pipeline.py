@@ -53,14 +53,14 @@ def verify_pipeline_sequence(models, tokens, us, vs, temperature, greedy, final_
     us      list of k - 1 arrays: us[s-1] holds stage s's accept uniforms
     vs      list of k - 1 draw uniforms
     Returns dict(a, w, t, t_valid: lists over stages 1..k-1; r: list over
-    buffers 0..k-2; committed, error, margin_u, margin_v).
+    buffers 0..k-2; committed, error, margin_u, margin_v, min_mass).
     """
     k = len(models)
     g1 = len(tokens)
     V = models[1].shape[1]
     gs = [g1] + [models[s].shape[0] - (1 if (final_bonus and s == k - 1) else 0) for s in range(2, k)]
     out = dict(a=[0] * (k - 1), w=[0] * (k - 1), t=[-1] * (k - 1), t_valid=[0] * (k - 1), r=[0] * (k - 1),
-               committed=0, error=0, margin_u=math.inf, margin_v=math.inf)
+               committed=0, error=0, margin_u=math.inf, margin_v=math.inf, min_mass=math.inf)
     error = 0
     if any(t < 0 or t >= V for t in tokens):
         error |= ERR_TOKEN
@@ -76,6 +76,8 @@ def verify_pipeline_sequence(models, tokens, us, vs, temperature, greedy, final_
 
     def draw(weights, v, fallback):
         nonlocal error
+        if weights is not fallback:  # a residual, formed after a rejection
+            out["min_mass"] = min(out["min_mass"], float(np.sum(weights)))
         if not np.sum(weights) > 0.0:
             error |= ERR_ZERO_MASS
             weights = fallback
@@ -126,13 +128,13 @@ def verify_pipeline(models, tokens, us, vs, temperature, greedy, final_bonus, dt
     arrays [B, rows]; vs: list of k - 1 arrays [B]; base [k - 1, B] or None:
     buffer lengths before the snapshot, added to the rollback lengths (on a
     data error r_j = base_j).  Returns arrays a, w, t, t_valid [B, k-1], r
-    [B, k-1], committed [B], error [B], margin_u, margin_v [B]."""
+    [B, k-1], committed [B], error [B], margin_u, margin_v, min_mass [B]."""
     k = len(models)
     B = tokens.shape[0]
     V = models[1].shape[2] if V is None else V
     res = {n: np.zeros((B, k - 1), np.int64) for n in ("a", "w", "t", "t_valid", "r")}
     res.update(committed=np.zeros(B, np.int64), error=np.zeros(B, np.int64), margin_u=np.zeros(B),
-               margin_v=np.zeros(B))
+               margin_v=np.zeros(B), min_mass=np.zeros(B))
     for b in range(B):
         ms = [None if (greedy and s == 0) else
               np.stack([row_to_float64(models[s][b, i, :V], dtype) for i in range(models[s].shape[1])])
@@ -142,7 +144,7 @@ def verify_pipeline(models, tokens, us, vs, temperature, greedy, final_bonus, dt
                                      None if greedy else [v[b] for v in vs], temperature, greedy, final_bonus)
         for n in ("a", "w", "t", "t_valid", "r"):
             res[n][b] = r[n]
-        for n in ("committed", "error", "margin_u", "margin_v"):
+        for n in ("committed", "error", "margin_u", "margin_v", "min_mass"):
             res[n][b] = r[n]
         if base is not None:
             res["r"][b] += np.asarray([int(base[j][b]) for j in range(k - 1)])

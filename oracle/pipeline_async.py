@@ -63,11 +63,11 @@ def verify_pipeline_async_sequence(targets, drafts, windows, us, vs, lengths, te
     us, vs   per stage: accept uniforms [w_s] and the draw uniform
     lengths  l_0 .. l_{k-1}
     Returns dict(a, t, t_valid over stages; r over buffers 0 .. k-1 (r[k-1]
-    is committed); committed, error, margin_u, margin_v).
+    is committed); committed, error, margin_u, margin_v, min_mass).
     """
     k = len(lengths)
     out = dict(a=[0] * (k - 1), t=[-1] * (k - 1), t_valid=[0] * (k - 1), r=list(lengths), committed=lengths[-1],
-               error=0, margin_u=math.inf, margin_v=math.inf)
+               error=0, margin_u=math.inf, margin_v=math.inf, min_mass=math.inf)
     malformed = any(l < 0 for l in lengths) or any(
         lengths[s - 1] < lengths[s] + len(windows[s - 1]) for s in range(1, k))
     stages = []
@@ -95,6 +95,7 @@ def verify_pipeline_async_sequence(targets, drafts, windows, us, vs, lengths, te
         if a < w:
             cuts.append((s, lengths[s] + a))
         out["margin_u"] = min(out["margin_u"], c["margin_u"])
+        out["min_mass"] = min(out["min_mass"], c["min_mass"])
         if emits:
             out["margin_v"] = min(out["margin_v"], c["margin_v"])
     out["r"] = [min([new[j]] + [P for s, P in cuts if s > j]) for j in range(k)]
@@ -109,13 +110,13 @@ def verify_pipeline_async(targets, drafts, windows, us, vs, lengths, temperature
     [B, w_s + 1, ld] / [B, w_s, ld] (drafts may be None when greedy);
     windows: per stage int arrays [B, w_s]; us: per stage [B, w_s]; vs: per
     stage [B]; lengths [k, B].  Returns a, t, t_valid [B, k-1], r [B, k-1]
-    (buffers 0 .. k-2), committed, error, margin_u, margin_v [B]."""
+    (buffers 0 .. k-2), committed, error, margin_u, margin_v, min_mass [B]."""
     k = len(targets) + 1
     B = windows[0].shape[0]
     V = targets[0].shape[2] if V is None else V
     res = {n: np.zeros((B, k - 1), np.int64) for n in ("a", "t", "t_valid", "r")}
     res.update(committed=np.zeros(B, np.int64), error=np.zeros(B, np.int64), margin_u=np.zeros(B),
-               margin_v=np.zeros(B))
+               margin_v=np.zeros(B), min_mass=np.zeros(B))
 
     def rows(arr, b):
         return np.stack([row_to_float64(arr[b, i, :V], dtype) for i in range(arr.shape[1])])
@@ -129,6 +130,6 @@ def verify_pipeline_async(targets, drafts, windows, us, vs, lengths, temperature
         for n in ("a", "t", "t_valid"):
             res[n][b] = r[n]
         res["r"][b] = r["r"][:k - 1]
-        for n in ("committed", "error", "margin_u", "margin_v"):
+        for n in ("committed", "error", "margin_u", "margin_v", "min_mass"):
             res[n][b] = r[n]
     return res

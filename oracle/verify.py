@@ -51,7 +51,12 @@ Every accept test and every inverse-CDF draw also records how close it came to
 flipping (``margin_u`` = |u - r|; ``margin_v`` = distance of v*Z to the
 nearest bracketing running sum, divided by Z) so that parity tests can set
 aside decisions a faithful float32 implementation may legitimately take the
-other way.
+other way.  ``min_mass`` is the smallest mass of a residual distribution
+max(0, p - q) formed after a rejection (inf when no rejection forms one): it
+is exactly 0 when reading R3 applies, and a small positive value means the
+residual is the difference of two nearly equal distributions, which a
+float32 implementation resolves only to its rounding (the zero-mass fallback
+and the draw may then go either way).
 """
 
 from __future__ import annotations
@@ -173,13 +178,14 @@ def verify_chain_sequence(target, draft, tokens, u, v, temperature, greedy):
     v       float                 uniform for the one draw (sampling only)
 
     Returns a dict: accept_len, out_token, error, p_at_draft, q_at_draft,
-    resid_mass, margin_u, margin_v.
+    resid_mass, margin_u, margin_v, min_mass.
     """
     gamma = len(tokens)
     V = target.shape[1]
     out = dict(accept_len=0, out_token=-1, error=0,
                p_at_draft=np.zeros(gamma), q_at_draft=np.zeros(gamma),
-               resid_mass=0.0, margin_u=math.inf, margin_v=math.inf)
+               resid_mass=0.0, margin_u=math.inf, margin_v=math.inf,
+               min_mass=math.inf)
     error = 0
     if any(t < 0 or t >= V for t in tokens):
         error |= ERR_TOKEN
@@ -218,6 +224,7 @@ def verify_chain_sequence(target, draft, tokens, u, v, temperature, greedy):
             break
     if a < gamma:
         weights = residual(p_rows[a], q_rows[a])
+        out["min_mass"] = float(np.sum(weights))
         if not np.sum(weights) > 0.0:  # reading R3
             error |= ERR_ZERO_MASS
             weights = p_rows[a]
@@ -245,7 +252,8 @@ def verify_chain(target, draft, tokens, u, v, prefix_len, temperature,
     res = dict(accept_len=np.zeros(B, np.int64), out_token=np.zeros(B, np.int64),
                rollback_idx=np.zeros(B, np.int64), error=np.zeros(B, np.int64),
                p_at_draft=np.zeros((B, gamma)), q_at_draft=np.zeros((B, gamma)),
-               resid_mass=np.zeros(B), margin_u=np.zeros(B), margin_v=np.zeros(B))
+               resid_mass=np.zeros(B), margin_u=np.zeros(B), margin_v=np.zeros(B),
+               min_mass=np.zeros(B))
     for b in range(B):
         tgt = np.stack([row_to_float64(target[b, i, :V], dtype) for i in range(gamma + 1)])
         drf = None
@@ -256,7 +264,7 @@ def verify_chain(target, draft, tokens, u, v, prefix_len, temperature,
                                   None if greedy else u[b],
                                   None if greedy else v[b], temperature, greedy)
         for k in ("accept_len", "out_token", "error", "resid_mass",
-                  "margin_u", "margin_v"):
+                  "margin_u", "margin_v", "min_mass"):
             res[k][b] = r[k]
         res["p_at_draft"][b] = r["p_at_draft"]
         res["q_at_draft"][b] = r["q_at_draft"]
@@ -306,7 +314,7 @@ def verify_tree_sequence(parent, tokens, target, draft, u, v, temperature,
     """
     N, V = target.shape
     out = dict(path=[], out_token=-1, error=0, margin_u=math.inf,
-               margin_v=math.inf)
+               margin_v=math.inf, min_mass=math.inf)
     error = 0
     depth = tree_depths([int(x) for x in parent])
     if depth is None or max(depth) > max_depth:
@@ -354,6 +362,7 @@ def verify_tree_sequence(parent, tokens, target, draft, u, v, temperature,
                 break
             nxt = residual(p, q)
             mass = float(np.sum(nxt))
+            out["min_mass"] = min(out["min_mass"], mass)
             if not mass > 0.0:  # reading R3
                 zero_mass = True
                 break
@@ -376,7 +385,7 @@ def verify_tree(parent, tokens, target, draft, u, v, prefix_len, temperature,
 
     Returns path_len [B], path_nodes [B, max_depth+1] (root first, then the
     kept nodes, -1 padded; all -1 on a data error), out_token, rollback_idx
-    (= prefix_len + path_len), error, margin_u, margin_v.
+    (= prefix_len + path_len), error, margin_u, margin_v, min_mass.
     """
     B, N, width = target.shape
     V = width if V is None else V
@@ -384,7 +393,7 @@ def verify_tree(parent, tokens, target, draft, u, v, prefix_len, temperature,
                path_nodes=-np.ones((B, max_depth + 1), np.int64),
                out_token=np.zeros(B, np.int64), rollback_idx=np.zeros(B, np.int64),
                error=np.zeros(B, np.int64), margin_u=np.zeros(B),
-               margin_v=np.zeros(B))
+               margin_v=np.zeros(B), min_mass=np.zeros(B))
     for b in range(B):
         tgt = np.stack([row_to_float64(target[b, i, :V], dtype) for i in range(N)])
         drf = None if greedy else np.stack(
@@ -397,6 +406,7 @@ def verify_tree(parent, tokens, target, draft, u, v, prefix_len, temperature,
         res["out_token"][b] = r["out_token"]
         res["margin_u"][b] = r["margin_u"]
         res["margin_v"][b] = r["margin_v"]
+        res["min_mass"][b] = r["min_mass"]
         res["path_len"][b] = len(r["path"])
         if r["error"] & (ERR_TOKEN | ERR_PARENT | ERR_NONFINITE) == 0:
             nodes = [0] + list(r["path"])
@@ -431,7 +441,8 @@ def verify_cascade_sequence(l0, l1, l2, tokens, u1, v1, u2, v2, temperature,
     g2 = l2.shape[0]
     V = l1.shape[1]
     out = dict(a1=0, t1=-1, a2=0, w2=0, t2=-1, t2_valid=0, r0=0, r1=0,
-               committed=0, error=0, margin_u=math.inf, margin_v=math.inf)
+               committed=0, error=0, margin_u=math.inf, margin_v=math.inf,
+               min_mass=math.inf)
     error = 0
     if any(t < 0 or t >= V for t in tokens):
         error |= ERR_TOKEN
@@ -475,6 +486,8 @@ def verify_cascade_sequence(l0, l1, l2, tokens, u1, v1, u2, v2, temperature,
                 a1 = j
                 break
         weights = residual(p1[a1], p0[a1]) if a1 < g1 else p1[g1]
+        if a1 < g1:
+            out["min_mass"] = float(np.sum(weights))
         if not np.sum(weights) > 0.0:
             error |= ERR_ZERO_MASS
             weights = p1[a1]
@@ -492,6 +505,7 @@ def verify_cascade_sequence(l0, l1, l2, tokens, u1, v1, u2, v2, temperature,
                 break
         if a2 < w2:
             weights = residual(p2[a2], p1[a2])
+            out["min_mass"] = min(out["min_mass"], float(np.sum(weights)))
             if not np.sum(weights) > 0.0:
                 error |= ERR_ZERO_MASS
                 weights = p2[a2]
@@ -522,6 +536,7 @@ def verify_cascade(l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1,
     res = {k: np.zeros(B, np.int64) for k in keys}
     res["margin_u"] = np.zeros(B)
     res["margin_v"] = np.zeros(B)
+    res["min_mass"] = np.zeros(B)
     for b in range(B):
         m1 = np.stack([row_to_float64(l1[b, i, :V], dtype) for i in range(g1 + 1)])
         m2 = np.stack([row_to_float64(l2[b, i, :V], dtype) for i in range(g2)])
@@ -536,6 +551,7 @@ def verify_cascade(l0, l1, l2, tokens, u1, v1, u2, v2, base0, base1,
             res[k][b] = r[k]
         res["margin_u"][b] = r["margin_u"]
         res["margin_v"][b] = r["margin_v"]
+        res["min_mass"][b] = r["min_mass"]
         res["r0"][b] += int(base0[b])
         res["r1"][b] += int(base1[b])
     return res

@@ -10,6 +10,17 @@ Parity rules (the tolerances are written here and used by every GPU test):
     sums that bracket the drawn index.  The float32 kernels compute p/q and
     the running sums with relative errors of a few 1e-7, so decisions inside
     these bands may legitimately go either way;
+  * a residual distribution max(0, p - q) formed after a rejection whose
+    float64 mass is positive but below Z_MIN is also set aside: float32
+    weights carry a relative error of up to about 1e-6 that is common to a
+    whole row (its rounded 1/s), so a residual of two nearly equal
+    distributions is known only to about 1e-6 in absolute terms; below Z_MIN
+    neither the zero-mass fallback (reading R3) nor the draw from the
+    residual is decided by the inputs alone.  An exactly zero mass (R3
+    proper) is not set aside: both sides must take the fallback;
+  * error words are compared whole (the zero-mass bit 8 included) on every
+    sequence not set aside; on every sequence the data-error bits must agree,
+    and no sequence may carry bit 16 (a bounded wait that gave up);
   * float outputs (p(d), q(d), residual mass) within REL_F of the float64
     oracle, or within ABS_F in absolute terms for values below 1e-30
     (float32 flushes subnormal probabilities to zero).
@@ -27,6 +38,31 @@ TOL_V = 1e-6
 REL_F = 1e-5
 ABS_F = 1e-30
 MAX_FLAGGED = 0.25  # a parity run that sets aside more than this is not a test
+Z_MIN = 1e-3
+ERR_INTERNAL = 16
+
+
+def set_aside(o, greedy):
+    """Sequences whose outputs a faithful float32 implementation may take
+    either way: near ties of an accept test or a draw, and residuals whose
+    mass is positive but below Z_MIN (greedy decisions are exact)."""
+    B = len(o["error"])
+    if greedy:
+        return np.zeros(B, bool)
+    thin = (o["min_mass"] > 0.0) & (o["min_mass"] < Z_MIN)
+    return (o["margin_u"] < TOL_U) | (o["margin_v"] < TOL_V) | thin
+
+
+def compare_errors(g_err, o_err, flagged, hard):
+    """Error words: the data-error bits `hard` on every sequence, the whole
+    word on every sequence not set aside, and never bit 16."""
+    g_err = np.asarray(g_err, np.int64)
+    o_err = np.asarray(o_err, np.int64)
+    assert not (g_err & ERR_INTERNAL).any(), f"a bounded wait gave up: {np.flatnonzero(g_err & ERR_INTERNAL)}"
+    assert np.array_equal(g_err & hard, o_err & hard), (g_err, o_err)
+    keep = ~flagged
+    bad = np.flatnonzero(keep & (g_err != o_err))
+    assert bad.size == 0, f"error words differ at {bad[:8]}: gpu {g_err[bad[:8]]} oracle {o_err[bad[:8]]}"
 
 
 def dev_logits(arr: np.ndarray, dtype: str, device) -> torch.Tensor:
@@ -87,7 +123,7 @@ def close(a, b):
 
 def compare_chain(g, o, greedy):
     B = len(o["accept_len"])
-    flagged = np.zeros(B, bool) if greedy else ((o["margin_u"] < TOL_U) | (o["margin_v"] < TOL_V))
+    flagged = set_aside(o, greedy)
     ok = ~flagged
     assert flagged.mean() <= MAX_FLAGGED, f"{flagged.sum()} of {B} sequences set aside"
     bad = np.flatnonzero(ok & ((g["accept_len"] != o["accept_len"]) | (g["out_token"] != o["out_token"])
@@ -96,8 +132,7 @@ def compare_chain(g, o, greedy):
         f"mismatch at {bad[:8]}: gpu a={g['accept_len'][bad[:8]]} t={g['out_token'][bad[:8]]}, "
         f"oracle a={o['accept_len'][bad[:8]]} t={o['out_token'][bad[:8]]} "
         f"margins u={o['margin_u'][bad[:8]]} v={o['margin_v'][bad[:8]]}")
-    hard = o["error"] & (V.ERR_TOKEN | V.ERR_NONFINITE)
-    assert np.array_equal(g["seq_error"] & 7, hard), (g["seq_error"], o["error"])
+    compare_errors(g["seq_error"], o["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
     if not greedy:
         valid = hard == 0
         assert close(g["p_at_draft"][valid], o["p_at_draft"][valid]).all()
@@ -134,7 +169,7 @@ def oracle_tree(w, greedy=None):
 
 def compare_tree(g, o, greedy):
     B = len(o["path_len"])
-    flagged = np.zeros(B, bool) if greedy else ((o["margin_u"] < TOL_U) | (o["margin_v"] < TOL_V))
+    flagged = set_aside(o, greedy)
     ok = ~flagged
     assert flagged.mean() <= MAX_FLAGGED, f"{flagged.sum()} of {B} sequences set aside"
     bad = np.flatnonzero(ok & ((g["path_len"] != o["path_len"]) | (g["out_token"] != o["out_token"])
@@ -142,8 +177,7 @@ def compare_tree(g, o, greedy):
                                | (g["path_nodes"] != o["path_nodes"]).any(axis=1)))
     assert bad.size == 0, (f"mismatch at {bad[:8]}: gpu {g['path_nodes'][bad[:4]]} {g['out_token'][bad[:4]]}"
                            f" oracle {o['path_nodes'][bad[:4]]} {o['out_token'][bad[:4]]}")
-    hard = o["error"] & (V.ERR_TOKEN | V.ERR_PARENT | V.ERR_NONFINITE)
-    assert np.array_equal(g["seq_error"] & 7, hard), (g["seq_error"], o["error"])
+    compare_errors(g["seq_error"], o["error"], flagged, V.ERR_TOKEN | V.ERR_PARENT | V.ERR_NONFINITE)
     return flagged
 
 
@@ -177,12 +211,11 @@ def oracle_cascade(w, greedy=None):
 
 def compare_cascade(g, o, greedy):
     B = len(o["a1"])
-    flagged = np.zeros(B, bool) if greedy else ((o["margin_u"] < TOL_U) | (o["margin_v"] < TOL_V))
+    flagged = set_aside(o, greedy)
     ok = ~flagged
     assert flagged.mean() <= MAX_FLAGGED, f"{flagged.sum()} of {B} sequences set aside"
     for k in CASCADE_KEYS:
         bad = np.flatnonzero(ok & (g[k] != o[k]))
         assert bad.size == 0, f"{k} mismatch at {bad[:8]}: gpu {g[k][bad[:8]]} oracle {o[k][bad[:8]]}"
-    hard = o["error"] & (V.ERR_TOKEN | V.ERR_NONFINITE)
-    assert np.array_equal(g["seq_error"] & 7, hard)
+    compare_errors(g["seq_error"], o["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
     return flagged

@@ -92,6 +92,8 @@ def pin_hand_examples(V):
         assert list(r["path"]) == e["expect"]["path"], f"hand example {e['name']}: path {r['path']}"
         assert r["out_token"] == e["expect"]["out_token"], \
             f"hand example {e['name']}: token {r['out_token']}"
+        if "error" in e["expect"]:
+            assert r["error"] == e["expect"]["error"], f"hand example {e['name']}: error {r['error']}"
     for e in ex["cascade"]:
         r = V.verify_cascade_sequence(_arr(e["l0"]), _arr(e["l1"]), _arr(e["l2"]),
                                       e["tokens"], e["u1"], e["v1"], e["u2"],

@@ -22,13 +22,13 @@ def oracle(w):
 
 def compare(g, o):
     B = len(o["accept_len"])
-    flagged = (o["margin_u"] < H.TOL_U) | (o["margin_v"] < H.TOL_V)
+    flagged = H.set_aside(o, False)
     ok = ~flagged
     assert flagged.mean() <= H.MAX_FLAGGED
     for k in ("accept_len", "out_token", "rollback_idx"):
         bad = np.flatnonzero(ok & (g[k] != o[k]))
         assert bad.size == 0, (k, bad[:8], g[k][bad[:4]], o[k][bad[:4]])
-    assert np.array_equal(g["seq_error"] & 7, o["error"] & 7)
+    H.compare_errors(g["seq_error"], o["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
     fine = ok & (o["error"] == 0)
     for k in ("p_at_draft", "q_at_draft"):
         gn, on = np.isnan(g[k][fine]), np.isnan(o[k][fine])

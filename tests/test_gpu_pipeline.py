@@ -43,7 +43,7 @@ def oracle_pipeline(w, greedy=None):
 
 def compare(g, o, greedy):
     B = len(o["committed"])
-    flagged = np.zeros(B, bool) if greedy else ((o["margin_u"] < H.TOL_U) | (o["margin_v"] < H.TOL_V))
+    flagged = H.set_aside(o, greedy)
     ok = ~flagged
     assert flagged.mean() <= H.MAX_FLAGGED, f"{flagged.sum()} of {B} sequences set aside"
     for k in KEYS:
@@ -51,8 +51,7 @@ def compare(g, o, greedy):
         diff = (gk != ok_k) if gk.ndim == 1 else (gk != ok_k).any(axis=1)
         bad = np.flatnonzero(ok & diff)
         assert bad.size == 0, f"{k} mismatch at {bad[:8]}: gpu {gk[bad[:4]]} oracle {ok_k[bad[:4]]}"
-    hard = o["error"] & (V.ERR_TOKEN | V.ERR_NONFINITE)
-    assert np.array_equal(g["seq_error"] & 7, hard)
+    H.compare_errors(g["seq_error"], o["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
 
 
 CASES = [

@@ -49,6 +49,8 @@ MUTANTS = {
     # the tree keeps testing siblings against the unchanged p
     "tree_no_residual_update": ("residual", lambda p, q: p.copy(),
                                 [lambda: pins.pin_hand_examples(V), lambda: pins.pin_tree_lossless(V, n=4000)]),
+    # reading R3's fallback loses its error bit (the draw still comes from p)
+    "zero_mass_bit_dropped": ("ERR_ZERO_MASS", 0, [lambda: pins.pin_hand_examples(V)]),
     # +inf logits silently accepted
     "inf_not_flagged": ("row_is_nonfinite", lambda l: bool(np.isnan(l).any()),
                         [lambda: pins.pin_nonfinite_rows(V)]),

@@ -59,6 +59,25 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls(cuda_device, spec)
         assert want["error_word"][0] == 0
 
 
+def test_noalloc_consulted_only_on_consecutive_calls(cuda_device):
+    # consulted-only mode keeps its control words (chunk counters, first
+    # rejections) in the shared scratch and must find them cleared on every
+    # call, whatever the previous call left there: two calls in a row on each
+    # of two input sets, against the workspace entry point in the same mode
+    from draft_verification_gb300 import ChainPlan, ChainPlanNoAlloc
+    spec = synth.with_sizes(synth.SPECS["sampling_chain_b64_g5_v128256_bf16_a30"], B=24)
+    kw = dict(greedy=False, temperature=spec.temperature, consulted_only=True)
+    for seed in (13, 14):
+        args = _inputs(spec, seed, cuda_device)
+        want = _np(ChainPlan(*args, **kw).run())
+        plan = ChainPlanNoAlloc(*args, **kw)
+        first = _np(plan.run())
+        second = _np(plan.run())
+        _same(first, want)
+        _same(second, want)
+        assert (want["accept_len"] < spec.gamma).any()  # some rows after a rejection were skipped
+
+
 def test_noalloc_runs_allocate_no_device_memory(cuda_device):
     from draft_verification_gb300 import ChainPlanNoAlloc
     spec = synth.with_sizes(synth.SPECS["sampling_chain_b32_g8_v32000_bf16"], B=8)
