@@ -526,7 +526,9 @@ def run_ours(args, w, rank, world, dist):
                      "achieved": kernel_gbs,
                      "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak, "peak_source": peak_src,
                      "kernel_ms": kernel_ms, "algorithmic_bytes": roof_bytes,
-                     "traffic": None if CONSULTED else profiled_traffic(s.name)},
+                     "traffic": None if CONSULTED else profiled_traffic(s.name),
+                     "traffic_note": "DRAM read + write bytes of one call from the committed ncu capture, "
+                                     "caches flushed before each launch (an upper bound for re-reads)"},
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_call(w),
         "clocks": clock_info,
