@@ -1266,6 +1266,229 @@ def run_profile(args, w):
     print(json.dumps({"profile_run": w["spec"].name, "calls": args.warmup + args.steps}))
 
 
+# --------------------------------------------------------------------------
+# LM head folded into the verification (spec_verify_chain_lm_head)
+# --------------------------------------------------------------------------
+LM_HEAD_SOURCES = ["draft_verification_gb300/csrc/lm_head.cu", "draft_verification_gb300/csrc/tc.cuh"] + \
+    KERNEL_SOURCES
+
+
+def lm_head_flops(spec) -> int:
+    """2 * rows * d * V per head: the products the head kernels compute."""
+    rows_t = spec.B * (spec.gamma + 1)
+    rows_d = 0 if spec.greedy else spec.B * spec.gamma
+    return 2 * spec.V * (rows_t * spec.d_target + rows_d * spec.d_draft)
+
+
+def lm_head_bytes(spec) -> int:
+    """Algorithmic HBM bytes: each head's weights once and the hidden states."""
+    heads = spec.V * spec.d_target * 2 + (0 if spec.greedy or spec.gamma == 0 else spec.V * spec.d_draft * 2)
+    hidden = spec.B * ((spec.gamma + 1) * spec.d_target + (0 if spec.greedy else spec.gamma * spec.d_draft)) * 2
+    return heads + hidden
+
+
+def lm_head_config(w) -> dict:
+    s = w["spec"]
+    return {"workload": s.name, "kind": "lm_head", "batch": s.B, "gamma": s.gamma, "vocab": s.V,
+            "d_target": s.d_target, "d_draft": s.d_draft, "shared_head": s.d_target == s.d_draft,
+            "mode": "greedy" if s.greedy else "sampling", "temperature": s.temperature,
+            "alpha_target": s.alpha_target}
+
+
+def lm_head_device(w, dev):
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    wt = bf(w["w_target"])
+    wd = wt if w["w_draft"] is w["w_target"] else bf(w["w_draft"])
+    return dict(h_target=bf(w["h_target"]), h_draft=bf(w["h_draft"]), w_target=wt, w_draft=wd,
+                tokens=torch.from_numpy(w["tokens"]).to(dev), u=torch.from_numpy(w["u"]).to(dev),
+                v=torch.from_numpy(w["v"]).to(dev), prefix_len=torch.from_numpy(w["prefix_len"]).to(dev))
+
+
+def lm_head_plan(w, t):
+    import draft_verification_gb300 as dv
+    s = w["spec"]
+    return dv.LmHeadChainPlan(t["h_target"], t["h_draft"], t["w_target"], t["w_draft"], t["tokens"], t["u"],
+                              t["v"], t["prefix_len"], greedy=s.greedy, temperature=s.temperature)
+
+
+def lm_head_oracle_rate(w, budget_s: float):
+    """Verified draft tokens/s of the oracle on whole sequences (exact
+    float64 products, then the chain rule) until the budget is spent."""
+    from oracle import lm_head as LH  # the reference is only used on this leg
+    s = w["spec"]
+    wt = LH.bf16_values(w["w_target"])
+    wd = wt if w["w_draft"] is w["w_target"] else LH.bf16_values(w["w_draft"])
+    t0, c0 = time.perf_counter(), time.process_time()
+    n = 0
+    while True:
+        b = n % s.B
+        LH.verify_chain_from_hidden(LH.bf16_values(w["h_target"][b:b + 1]), LH.bf16_values(w["h_draft"][b:b + 1]),
+                                    wt, wd, w["tokens"][b:b + 1], w["u"][b:b + 1], w["v"][b:b + 1],
+                                    w["prefix_len"][b:b + 1], s.temperature, s.greedy)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    cores = (time.process_time() - c0) / el
+    return n * s.gamma / el, (f"{n} whole sequences ({el:.1f} s; NumPy float64 products and chain rule)",
+                              round(cores, 1))
+
+
+def run_lm_head(args, w):
+    import torch
+    import draft_verification_gb300 as dv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dv.build_library()
+    s = w["spec"]
+    t = lm_head_device(w, dev)
+    plan = lm_head_plan(w, t)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            plan.run(stream)
+    stream.synchronize()
+    launch = "cuda_graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            plan.run(stream)
+        stream.synchronize()
+    except Exception as exc:
+        launch = f"eager ({type(exc).__name__})"
+        graph = None
+
+    def run_steps(k):
+        for _ in range(k):
+            if graph is not None:
+                graph.replay()
+            else:
+                plan.run(stream)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            run_steps(20)
+            stream.synchronize()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end: the hidden states from pinned host memory every step, the
+    # outputs back; the heads are model parameters and stay resident
+    host = {k: torch.from_numpy(np.ascontiguousarray(w[k]).view(np.int16)).pin_memory()
+            for k in ("h_target", "h_draft")}
+    host.update({k: torch.from_numpy(w[k]).pin_memory() for k in ("tokens", "u", "v", "prefix_len")})
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    dev_in = {k: torch.empty_like(x, device=dev) for k, x in host.items()}
+    e2e_plan = dv.LmHeadChainPlan(dev_in["h_target"].view(torch.bfloat16), dev_in["h_draft"].view(torch.bfloat16),
+                                  t["w_target"], t["w_draft"], dev_in["tokens"], dev_in["u"], dev_in["v"],
+                                  dev_in["prefix_len"], greedy=s.greedy, temperature=s.temperature,
+                                  workspace=plan.workspace)
+    outs_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in e2e_plan.out.items()}
+    d2h = sum(x.numel() * x.element_size() for x in outs_host.values())
+
+    def e2e_call():
+        with torch.cuda.stream(stream):
+            for k in host:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            e2e_plan.run(stream)
+            for k, x in e2e_plan.out.items():
+                outs_host[k].copy_(x, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_call()
+    n = max(3, args.e2e_steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        e2e_call()
+    el = time.perf_counter() - t0
+
+    hbm_peak, hbm_src = measured_peak()
+    tc_peak, tc_src = measured_tensor_peak(sustained=True)
+    flops, nbytes = lm_head_flops(s), lm_head_bytes(s)
+    tfs = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    if flops / (tc_peak * 1e12) >= nbytes / (hbm_peak * 1e9):
+        roof = {"bound": "tensor", "achieved": tfs, "peak": tc_peak, "unit": "TFLOP/s", "frac": tfs / tc_peak,
+                "peak_source": tc_src, "algorithmic_flops": flops}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                "peak_source": hbm_src, "algorithmic_bytes": nbytes}
+    launches = 2 if (s.greedy or s.gamma == 0) else 3
+    roof.update({"kernel": "whole call: lm_head_kernel per head + chain walk", "unit_of_work": "one call",
+                 "kernel_ms": ms,
+                 "other": {"tensor_TFLOPs": tfs, "tensor_frac": tfs / tc_peak, "weights_GBps": gbs,
+                           "hbm_frac": gbs / hbm_peak},
+                 "traffic": profiled_traffic(s.name, LM_HEAD_SOURCES)})
+    tokens = s.B * s.gamma
+    return {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, f32 accumulate (tcgen05)",
+        "data": "synthetic (seeded bf16 hidden states and LM heads)",
+        "config": dict(lm_head_config(w), parallelism="1 GPU", launch=launch,
+                       l2_policy=f"heads {nbytes / 2**20:.0f} MB per call > L2: every call streams them"),
+        "roofline": roof,
+        "e2e": {"value": tokens / (el / n), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / n, "steps": n,
+                "note": "hidden states, tokens and uniforms host to device each step; heads resident"},
+        "gpu_launches": args.steps * launches,
+        "clocks": clock_info,
+    }
+
+
+def lm_head_main(args, w, rank):
+    s = w["spec"]
+    if args.impl == "reference":
+        if rank == 0:
+            rate, (desc, cores) = lm_head_oracle_rate(w, args.cpu_seconds)
+            print(json.dumps({
+                "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * s.B * s.gamma / rate, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": lm_head_config(w),
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                flush=True)
+        return
+    if args.profile:
+        import torch
+        import draft_verification_gb300 as dv
+        dev = torch.device("cuda", 0)
+        dv.build_library()
+        plan = lm_head_plan(w, lm_head_device(w, dev))
+        for _ in range(args.warmup + args.steps):
+            plan.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": s.name, "calls": args.warmup + args.steps}))
+        return
+    if rank != 0:
+        return
+    line = run_lm_head(args, w)
+    if not args.no_cpu_baseline:
+        rate, (desc, cores) = lm_head_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     global CONSULTED
     args = parse()
@@ -1283,10 +1506,13 @@ def main():
     if args.workload in synth.CLASP_SPECS:
         clasp_main(args, synth.make(synth.CLASP_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
         return
+    if args.workload in synth.LM_HEAD_SPECS:
+        lm_head_main(args, synth.make(synth.LM_HEAD_SPECS[args.workload], seed=replica_seed(args.seed, rank)), rank)
+        return
     specs = dict(synth.SPECS, **synth.PIPELINE_SPECS)
     if args.workload not in specs:
         raise SystemExit(f"unknown workload {args.workload}; choose from "
-                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS) + sorted(synth.CLASP_SPECS) + sorted(synth.PIPELINE_ASYNC_SPECS)}")
+                         f"{sorted(specs) + sorted(synth.COMPACT_SPECS) + sorted(synth.CLASP_SPECS) + sorted(synth.PIPELINE_ASYNC_SPECS) + sorted(synth.LM_HEAD_SPECS)}")
     w = synth.make(specs[args.workload], seed=replica_seed(args.seed, rank))
 
     if args.impl == "reference":

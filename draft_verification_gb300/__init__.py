@@ -5,7 +5,8 @@ include/spec_verify.h); this package only builds it and marshals arguments.
 """
 
 from .api import (  # noqa: F401
-    CascadePlan, ChainPlan, ChainPlanNoAlloc, ClaspPlan, PipelineAsyncPlan, PipelinePlan, TreePlan,
+    CascadePlan, ChainPlan, ChainPlanNoAlloc, ClaspPlan, LmHeadChainPlan, PipelineAsyncPlan, PipelinePlan,
+    TreePlan,
     clasp_layer_select, compact_tree_path, verify_cascade, verify_chain, verify_pipeline, verify_pipeline_async,
     verify_tree, workspace_bytes,
 )

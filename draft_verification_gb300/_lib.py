@@ -93,6 +93,19 @@ class PipelineAsyncArgs(C.Structure):
     ]
 
 
+class LmHeadChainArgs(C.Structure):
+    _fields_ = [
+        ("B", C.c_int), ("gamma", C.c_int), ("V", C.c_int), ("d_target", C.c_int), ("d_draft", C.c_int),
+        ("mode", C.c_int), ("temperature", C.c_float),
+        ("h_target", _vp), ("h_draft", _vp), ("w_target", _vp), ("w_draft", _vp),
+        ("draft_tokens", _vp), ("u", _vp), ("v", _vp), ("prefix_len", _vp),
+        ("accept_len", _vp), ("out_token", _vp), ("rollback_idx", _vp),
+        ("p_at_draft", _vp), ("q_at_draft", _vp), ("resid_mass", _vp),
+        ("seq_error", _vp), ("error_word", _vp),
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+    ]
+
+
 class CompactArgs(C.Structure):
     _fields_ = [
         ("B", C.c_int), ("N", C.c_int), ("max_depth", C.c_int), ("cache_rows", C.c_int),
@@ -128,6 +141,8 @@ SIGNATURES = {
     "spec_clasp_layer_select": (C.c_int, [C.POINTER(ClaspArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
     "spec_test_inject_copy_timeout": (C.c_int, [C.c_int]),
+    "spec_lm_head_chain_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spec_verify_chain_lm_head": (C.c_int, [C.POINTER(LmHeadChainArgs), _vp]),
 }
 
 _LIB = None

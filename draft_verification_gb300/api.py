@@ -145,6 +145,96 @@ class ChainPlanNoAlloc(ChainPlan):
         self._call = L.lib().spec_verify_chain_noalloc
 
 
+class LmHeadChainPlan(_Plan):
+    """Chain verification from final hidden states and LM-head weights,
+    bound to fixed buffers.  See spec_verify_chain_lm_head.
+
+    h_target [B, gamma+1, d_t] and h_draft [B, gamma, d_d] bfloat16 hidden
+    states, w_target [V, d_t] and w_draft [V, d_d] bfloat16 heads (the draft
+    ones are not read in greedy mode and may be None).  The workspace holds
+    the chunk partials and, in sampling mode, the float32 logits of every row
+    (``target_logits()`` / ``draft_logits()`` view them after a run)."""
+
+    def __init__(self, h_target, h_draft, w_target, w_draft, tokens, u=None, v=None, prefix_len=None, *,
+                 greedy=False, temperature=1.0, workspace=None):
+        B, R, d_t = h_target.shape
+        gamma = R - 1
+        V = w_target.shape[0]
+        dev = h_target.device
+        for name, t in (("h_target", h_target), ("w_target", w_target)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name}: contiguous bfloat16 required")
+        d_d = 0
+        if not greedy and gamma > 0:
+            for name, t in (("h_draft", h_draft), ("w_draft", w_draft)):
+                if t is None or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                    raise ValueError(f"{name}: contiguous bfloat16 required")
+            d_d = h_draft.shape[2]
+            if tuple(h_draft.shape[:2]) != (B, gamma) or tuple(w_draft.shape) != (V, d_d):
+                raise ValueError("h_draft [B, gamma, d_draft] and w_draft [V, d_draft] required")
+        if w_target.shape[1] != d_t:
+            raise ValueError("w_target [V, d_target] required")
+        lib = L.lib()
+        self.B, self.gamma, self.V = B, gamma, V
+        self.keep = [h_target, h_draft, w_target, w_draft, tokens, u, v, prefix_len]
+        self.out = dict(
+            accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+            out_token=torch.empty(B, dtype=torch.int32, device=dev),
+            rollback_idx=torch.empty(B, dtype=torch.int32, device=dev),
+            seq_error=torch.empty(B, dtype=torch.int32, device=dev),
+            error_word=torch.zeros(1, dtype=torch.int32, device=dev),
+            p_at_draft=torch.empty(B, gamma, dtype=torch.float32, device=dev),
+            q_at_draft=torch.empty(B, gamma, dtype=torch.float32, device=dev),
+            resid_mass=torch.empty(B, dtype=torch.float32, device=dev),
+        )
+        mode = L.SPEC_GREEDY if greedy else L.SPEC_SAMPLE
+        need = lib.spec_lm_head_chain_workspace_size(B, gamma, V, mode)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        self.greedy = greedy
+        a = L.LmHeadChainArgs()
+        a.B, a.gamma, a.V, a.d_target, a.d_draft = B, gamma, V, d_t, d_d
+        a.mode = mode
+        a.temperature = float(temperature)
+        a.h_target, a.w_target = _ptr(h_target), _ptr(w_target)
+        a.h_draft = _ptr(h_draft) if d_d else None
+        a.w_draft = _ptr(w_draft) if d_d else None
+        a.draft_tokens = _ptr(_i32(tokens, "tokens"))
+        a.u = _ptr(_f32(u, "u")) if not greedy else None
+        a.v = _ptr(_f32(v, "v")) if not greedy else None
+        a.prefix_len = _ptr(_i32(prefix_len, "prefix_len"))
+        o = self.out
+        a.accept_len, a.out_token = _ptr(o["accept_len"]), _ptr(o["out_token"])
+        a.rollback_idx, a.seq_error = _ptr(o["rollback_idx"]), _ptr(o["seq_error"])
+        a.error_word = _ptr(o["error_word"])
+        a.p_at_draft, a.q_at_draft = _ptr(o["p_at_draft"]), _ptr(o["q_at_draft"])
+        a.resid_mass = _ptr(o["resid_mass"])
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        self.args = a
+        self._call = lib.spec_verify_chain_lm_head
+
+    def _logits(self, first_row, rows):
+        # the workspace layout of spec_lm_head_chain_workspace_size: the
+        # partials, then the target rows, then the draft rows (each part
+        # rounded up to 256 bytes), row stride V rounded up to 4
+        if self.greedy:
+            raise ValueError("greedy calls store no logits")
+        ldl = (self.V + 3) // 4 * 4
+        chunks = min((self.V + 127) // 128, 256)
+        part = -(-self.B * (2 * self.gamma + 1) * chunks * 8 // 256) * 256
+        tbytes = -(-self.B * (self.gamma + 1) * ldl * 4 // 256) * 256
+        off = part + (0 if first_row == 0 else tbytes)
+        f = self.workspace[off: off + rows * ldl * 4].view(torch.float32)
+        return f.view(rows, ldl)[:, :self.V]
+
+    def target_logits(self):
+        return self._logits(0, self.B * (self.gamma + 1)).view(self.B, self.gamma + 1, self.V)
+
+    def draft_logits(self):
+        return self._logits(1, self.B * self.gamma).view(self.B, self.gamma, self.V)
+
+
 class TreePlan(_Plan):
     """Tree verification bound to fixed buffers.  See spec_verify_tree."""
 
@@ -549,5 +639,6 @@ def verify_pipeline_async(targets, drafts, tokens, length, us=None, vs=None, *, 
 
 def workspace_bytes(kind: str, *sizes) -> int:
     fn = {"chain": "spec_chain_workspace_size", "tree": "spec_tree_workspace_size",
-          "cascade": "spec_cascade_workspace_size", "clasp": "spec_clasp_workspace_size"}[kind]
+          "cascade": "spec_cascade_workspace_size", "clasp": "spec_clasp_workspace_size",
+          "lm_head": "spec_lm_head_chain_workspace_size"}[kind]
     return int(getattr(L.lib(), fn)(*sizes))

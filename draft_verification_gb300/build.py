@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libspecverify.so"
-SOURCES = ["verify.cu", "api.cu", "noalloc.cu", "compact.cu", "clasp.cu", "pipeline_async.cu"]
+SOURCES = ["verify.cu", "api.cu", "noalloc.cu", "compact.cu", "clasp.cu", "pipeline_async.cu", "lm_head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v"]
 

@@ -168,6 +168,9 @@ cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, 
 cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
 cudaError_t launch_cascade(const StatsParams& g, const CascadeParams& p, bool bf16, bool greedy,
                            cudaStream_t s);
+// The chain walk alone over float32 logit rows whose chunk partials a
+// preceding kernel on s wrote (the LM-head path); plain stream order.
+cudaError_t launch_chain_walk_f32(const StatsParams& g, const ChainParams& p, bool greedy, cudaStream_t s);
 
 }  // namespace sv
 

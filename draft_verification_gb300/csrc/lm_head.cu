@@ -1,0 +1,509 @@
+// Chain verification from the models' final hidden states: the LM head and
+// the row statistics in one tensor-core kernel per head, then the chain walk.
+//
+// Source: "Accelerating LLM Inference with Staged Speculative Decoding"
+// (arXiv 2308.04623), abstract: small-batch inference has low arithmetic
+// intensity, so the step is bound by the bytes it moves, and the logits the
+// verification reads are what the LM head writes just before it.  Folding
+// the row statistics into the head's epilogue removes the statistics pass
+// over the vocabulary-wide rows.  The rule applied afterwards is the one of
+// spec_verify_chain (PipeSpec review, Circularity Check).
+//
+// lm_head_kernel: logits L = X W^T for one head, X [R, d] (bfloat16 hidden
+// states, one row per position), W [V, d] (bfloat16 LM-head weights), float32
+// accumulation in tensor memory.  One persistent CTA per SM owns a
+// contiguous slab of 128-entry vocabulary tiles.  Per tile and per block of
+// at most 512 hidden rows, the CTA streams K in 64-element steps:
+//   warp 4  (one thread)  TMA copies of the W tile [128 x 64] and the X tiles
+//                         [128 x 64] of the row block into a ring of stages;
+//   warp 5  (one thread)  tcgen05.mma, M = 128 rows, N = 128 vocabulary
+//                         entries, K = 16, one accumulator of 128 columns per
+//                         row tile (at most 4 tiles: all 512 TMEM columns);
+//                         a commit frees each stage, another hands the tile's
+//                         accumulators to the epilogue;
+//   warps 0-3             the epilogue: thread t of warp w owns TMEM lane
+//                         32 w + t, i.e. one hidden row of every row tile, and
+//                         folds the tile's 128 logits into that row's running
+//                         (max, sum of 2^(x c - M)) (sampling) or (max, first
+//                         index) (greedy), in ascending vocabulary order, and
+//                         in sampling mode stores the float32 logits for the
+//                         walk's residual or bonus draw.
+// After its slab the CTA writes one partial per row in the statistics
+// kernel's format, so the chain walk merges them exactly like the partials of
+// stored logits.  Greedy calls store no logits at all: the walk needs only
+// the argmaxes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "spec_verify.h"
+#include "tc.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzled row
+constexpr int kBV = 128;           // vocabulary entries per tile (MMA N)
+constexpr int kBR = 128;           // hidden rows per row tile (MMA M)
+constexpr int kMaxRowTiles = 4;    // 4 accumulators of 128 float32 columns: all of TMEM
+constexpr int kRowBlock = kBR * kMaxRowTiles;
+constexpr int kTileBytes = kBR * kBK * 2;  // 16 KB, also a W tile (kBV == kBR)
+constexpr int kMaxStages = 6;
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kLmThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
+
+struct LmParams {
+  int R, V, d;
+  int ntv;            // vocabulary tiles
+  int nkb;            // K steps of 64
+  int rt_max;         // row tiles of the largest row block
+  int stages;
+  int per;            // hidden rows per sequence of this head
+  int rows_seq;       // statistics rows per sequence
+  int row_off;        // this head's first statistics row
+  int chunks;         // CTAs of the launch
+  int greedy;
+  float c;            // log2(e) / T (sampling)
+  float2* partials;   // [B][rows_seq][chunks]
+  float* logits;      // [R][ldl] (sampling) or null
+  long long ldl;
+  int* error_word;    // optional: SPEC_ERR_INTERNAL when a wait gives up
+};
+
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, unsigned parity, volatile int* fault) {
+  for (int i = 0; i < kMaxPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*fault) return false;
+  }
+  *fault = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lm_head_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const LmParams P) {
+  extern __shared__ __align__(1024) unsigned char lm_dyn[];
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], tfull, tempty, drain;
+  __shared__ uint32_t tmem_s;
+  __shared__ int fault_s;
+  __shared__ int issued_s;  // stages the producer issued
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(lm_dyn) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const int stage_bytes = kTileBytes * (1 + P.rt_max);
+  const int G = P.chunks, cta = blockIdx.x;
+  const int v_t0 = static_cast<int>((static_cast<long long>(cta) * P.ntv) / G);
+  const int v_t1 = static_cast<int>((static_cast<long long>(cta + 1) * P.ntv) / G);
+  const int nrb = (P.R + kRowBlock - 1) / kRowBlock;
+  volatile int* fault = &fault_s;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull, 1);
+    mbar_init(&tempty, 4);
+    mbar_init(&drain, 1);
+    fault_s = 0;
+    issued_s = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_s, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      int it = 0;
+      for (int rb = 0; rb < nrb && !*fault; ++rb) {
+        const int rows = min(kRowBlock, P.R - rb * kRowBlock);
+        const int rt = (rows + kBR - 1) / kBR;
+        for (int vt = v_t0; vt < v_t1 && !*fault; ++vt) {
+          for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+            const int s = it % P.stages;
+            const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
+            if (!lm_wait(&empty[s], ph ^ 1u, fault)) break;
+            unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+            mbar_expect_tx(&full[s], static_cast<unsigned>(kTileBytes * (1 + rt)));
+            tma_load_2d(st, &tm_w, kb * kBK, vt * kBV, &full[s]);
+            for (int t = 0; t < rt; ++t)
+              tma_load_2d(st + kTileBytes * (1 + t), &tm_x, kb * kBK, rb * kRowBlock + t * kBR, &full[s]);
+            issued_s = it + 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(kBR, kBV);
+      int it = 0, acc = 0;
+      for (int rb = 0; rb < nrb && !*fault; ++rb) {
+        const int rows = min(kRowBlock, P.R - rb * kRowBlock);
+        const int rt = (rows + kBR - 1) / kBR;
+        for (int vt = v_t0; vt < v_t1 && !*fault; ++vt, ++acc) {
+          if (!lm_wait(&tempty, (static_cast<unsigned>(acc) & 1u) ^ 1u, fault)) break;
+          tc_fence_after();
+          for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+            const int s = it % P.stages;
+            const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
+            if (!lm_wait(&full[s], ph, fault)) break;
+            tc_fence_after();
+            const uint32_t st = smem_addr(ring + static_cast<size_t>(s) * stage_bytes);
+            for (int t = 0; t < rt; ++t) {
+              const uint32_t xa = st + kTileBytes * (1 + t);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16(tmem + static_cast<uint32_t>(t * kBV), umma_desc_sw128(xa + 32u * k),
+                          umma_desc_sw128(st + 32u * k), idesc, kb > 0 || k > 0);
+            }
+            umma_commit(&empty[s]);  // the stage is free once these MMAs are done
+          }
+          if (*fault) break;
+          umma_commit(&tfull);  // the tile's accumulators are complete
+        }
+      }
+      // every MMA issued has completed before TMEM is released
+      umma_commit(&drain);
+      mbar_wait(&drain, 0);
+    }
+  } else {
+    // ---------------- epilogue (warps 0-3) ----------------
+    const float c = P.c;
+    int acc = 0;
+    for (int rb = 0; rb < nrb; ++rb) {
+      const int rows = min(kRowBlock, P.R - rb * kRowBlock);
+      const int rt = (rows + kBR - 1) / kBR;
+      float m[kMaxRowTiles], s[kMaxRowTiles];
+      int bi[kMaxRowTiles];
+      bool bad[kMaxRowTiles];
+#pragma unroll
+      for (int t = 0; t < kMaxRowTiles; ++t) {
+        m[t] = -kInf;
+        s[t] = 0.f;
+        bi[t] = -1;
+        bad[t] = false;
+      }
+      for (int vt = v_t0; vt < v_t1; ++vt, ++acc) {
+        // the warp decides together: the TMEM loads below are warp-wide
+        const bool ready = __all_sync(0xffffffffu, lm_wait(&tfull, static_cast<unsigned>(acc) & 1u, fault));
+        if (!ready) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < kMaxRowTiles; ++t) {
+          if (t >= rt) break;
+          const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
+          float* dst = (P.logits && row < P.R) ? P.logits + static_cast<long long>(row) * P.ldl : nullptr;
+#pragma unroll 1
+          for (int cc = 0; cc < kBV / 32; ++cc) {
+            float v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * kBV + cc * 32),
+                      v);
+            const int v0 = vt * kBV + cc * 32;
+            const int nv = min(32, P.V - v0);  // >= 1: a tile starts below V
+            if (P.greedy) {
+              // ascending order with a strict comparison: ties keep the lowest
+              // index; -inf never wins (a row of -inf has no argmax)
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (j < nv) {
+                  bad[t] |= !(v[j] < kInf);
+                  if (v[j] > m[t]) {
+                    m[t] = v[j];
+                    bi[t] = v0 + j;
+                  }
+                }
+              }
+            } else {
+              float cm = -kInf;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nv) cm = fmax_nan(cm, v[j]);
+              const float mn = fmax_nan(m[t], cm);
+              if (mn != -kInf) {
+                const float Mn = scaled_max(mn, c);
+                const float scale = (m[t] == -kInf) ? 0.f : ex2(scaled_max(m[t], c) - Mn);
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < nv) sum = __fadd_rn(sum, weight(v[j], c, Mn));
+                s[t] = __fadd_rn(__fmul_rn(s[t], scale), sum);
+                m[t] = mn;
+              }
+              if (dst) {
+                if (nv == 32) {
+                  float4* d4 = reinterpret_cast<float4*>(dst + v0);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (j < nv) dst[v0 + j] = v[j];
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty);
+      }
+      // one partial per row of the block for this CTA's slab
+#pragma unroll
+      for (int t = 0; t < kMaxRowTiles; ++t) {
+        if (t >= rt) break;
+        const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
+        if (row >= P.R) continue;
+        const long long prow = static_cast<long long>(row / P.per) * P.rows_seq + P.row_off + row % P.per;
+        float2 out;
+        if (*fault) out = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+        else if (P.greedy) out = make_float2(bad[t] ? __int_as_float(0x7fc00000) : m[t], __int_as_float(bi[t]));
+        else out = make_float2(m[t], s[t]);
+        P.partials[prow * P.chunks + cta] = out;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*fault && threadIdx.x == 0) {
+    // copies still in flight land before the CTA exits: wait (bounded) for
+    // the last phase of every stage the producer issued
+    const int issued = issued_s;
+    for (int k = max(0, issued - P.stages); k < issued; ++k)
+      mbar_wait(&full[k % P.stages], static_cast<unsigned>(k / P.stages) & 1u);
+    if (P.error_word) atomicOr(P.error_word, SPEC_ERR_INTERNAL);
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a row-major bfloat16 matrix [rows, cols] (cols contiguous,
+// row stride cols elements): boxes of 128 rows x 64 columns, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* map, const void* base, long long rows, int cols) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {kBK, kBR};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = n;
+  return n;
+}
+
+// The kernel's dynamic shared memory limit, raised once per device.
+cudaError_t smem_attribute() {
+  static std::mutex mu;
+  static std::map<int, bool> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(dev)) return cudaSuccess;
+  e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 1024);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+int lm_chunks(int V) {
+  const int ntv = (V + kBV - 1) / kBV;
+  return ntv < kMaxChunks ? ntv : kMaxChunks;
+}
+
+long long logit_ld(int V) { return (static_cast<long long>(V) + 3) / 4 * 4; }
+
+struct LmLayout {
+  size_t partials, tlogits, dlogits, total;
+};
+
+LmLayout lm_layout(int B, int gamma, int V, bool greedy) {
+  LmLayout L{};
+  const int rows = greedy ? gamma + 1 : 2 * gamma + 1;
+  L.partials = align256(static_cast<size_t>(B) * rows * lm_chunks(V) * sizeof(float2));
+  if (!greedy) {
+    L.tlogits = align256(static_cast<size_t>(B) * (gamma + 1) * logit_ld(V) * sizeof(float));
+    L.dlogits = align256(static_cast<size_t>(B) * gamma * logit_ld(V) * sizeof(float));
+  }
+  L.total = L.partials + L.tlogits + L.dlogits;
+  return L;
+}
+
+cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V, const LmParams& proto,
+                        cudaStream_t s) {
+  CUtensorMap tx, tw;
+  if (!make_map(&tx, x, R, d) || !make_map(&tw, w, V, d)) return cudaErrorInvalidValue;
+  LmParams P = proto;
+  P.R = static_cast<int>(R);
+  P.V = V;
+  P.d = d;
+  P.ntv = (V + kBV - 1) / kBV;
+  P.nkb = (d + kBK - 1) / kBK;
+  const long long row_tiles = (R + kBR - 1) / kBR;
+  P.rt_max = static_cast<int>(row_tiles < kMaxRowTiles ? row_tiles : kMaxRowTiles);
+  const int stage_bytes = kTileBytes * (1 + P.rt_max);
+  P.stages = min(kMaxStages, kSmemBudget / stage_bytes);
+  const int dyn = P.stages * stage_bytes + 1024;
+  cudaError_t e = smem_attribute();
+  if (e != cudaSuccess) return e;
+  lm_head_kernel<<<P.chunks, kLmThreads, dyn, s>>>(tx, tw, P);
+  return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t spec_lm_head_chain_workspace_size(int B, int gamma, int V, spec_mode mode) {
+  if (B < 1 || gamma < 0 || gamma > 32 || V < 1) return 0;
+  return sv::lm_layout(B, gamma, V, mode == SPEC_GREEDY).total;
+}
+
+extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* a, cudaStream_t stream) {
+  using namespace sv;
+  NvtxRange nvtx_range("spec_verify_chain_lm_head");
+  if (a == nullptr) return SPEC_EINVAL;
+  if (a->mode != SPEC_GREEDY && a->mode != SPEC_SAMPLE) return SPEC_EDTYPE;
+  const bool greedy = a->mode == SPEC_GREEDY;
+  if (a->B < 1 || a->B > kMaxSeq || a->gamma < 0 || a->gamma > 32) return SPEC_EINVAL;
+  if (a->V < 1 || a->V > 2097152) return SPEC_EINVAL;
+  if (a->d_target < 8 || a->d_target > 65536 || a->d_target % 8) return SPEC_EINVAL;
+  if (!greedy && a->gamma > 0 && (a->d_draft < 8 || a->d_draft > 65536 || a->d_draft % 8)) return SPEC_EINVAL;
+  if (!greedy && !(a->temperature > 0.f && std::isfinite(a->temperature))) return SPEC_EINVAL;
+  if (!a->h_target || !a->w_target || !a->accept_len || !a->out_token) return SPEC_EINVAL;
+  if (a->gamma > 0 && !a->draft_tokens) return SPEC_EINVAL;
+  if (!greedy && (!a->v || (a->gamma > 0 && (!a->h_draft || !a->w_draft || !a->u)))) return SPEC_EINVAL;
+  if (!aligned16(a->h_target) || !aligned16(a->w_target)) return SPEC_EALIGN;
+  if (!greedy && a->gamma > 0 && (!aligned16(a->h_draft) || !aligned16(a->w_draft))) return SPEC_EALIGN;
+  const LmLayout L = lm_layout(a->B, a->gamma, a->V, greedy);
+  if (!a->workspace || a->workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
+    return SPEC_EWORKSPACE;
+  const int nsm = sm_count();
+  if (nsm < 1) return SPEC_ECUDA;
+
+  char* ws = static_cast<char*>(a->workspace);
+  const int gamma = a->gamma;
+  const int rows_seq = greedy ? gamma + 1 : 2 * gamma + 1;
+  const int chunks = min(lm_chunks(a->V), nsm);
+  const long long ldl = logit_ld(a->V);
+  float* tlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials);
+  float* dlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials + L.tlogits);
+
+  LmParams proto{};
+  proto.rows_seq = rows_seq;
+  proto.chunks = chunks;
+  proto.greedy = greedy ? 1 : 0;
+  proto.c = greedy ? 1.f : static_cast<float>(1.4426950408889634073599 / static_cast<double>(a->temperature));
+  proto.partials = reinterpret_cast<float2*>(ws);
+  proto.ldl = ldl;
+  proto.error_word = a->error_word;
+
+  // target head: rows (b, i), i <= gamma, statistics rows 0 .. gamma
+  LmParams pt = proto;
+  pt.per = gamma + 1;
+  pt.row_off = 0;
+  pt.logits = tlog;
+  cudaError_t e = launch_head(a->h_target, static_cast<long long>(a->B) * (gamma + 1), a->d_target, a->w_target,
+                              a->V, pt, stream);
+  if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
+  if (!greedy && gamma > 0) {
+    // draft head: rows (b, i), i < gamma, statistics rows gamma + 1 ..
+    LmParams pd = proto;
+    pd.per = gamma;
+    pd.row_off = gamma + 1;
+    pd.logits = dlog;
+    e = launch_head(a->h_draft, static_cast<long long>(a->B) * gamma, a->d_draft, a->w_draft, a->V, pd, stream);
+    if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
+  }
+
+  // the chain walk over the partials (and, sampling, the stored logits)
+  StatsParams sp{};
+  sp.set[0] = RowSet{tlog, gamma + 1};
+  sp.set[1] = RowSet{dlog, gamma};
+  sp.nsets = (greedy || gamma == 0) ? 1 : 2;
+  sp.rows_per_seq = rows_seq;
+  sp.B = a->B;
+  sp.V = a->V;
+  sp.ld = ldl;
+  sp.chunks = chunks;
+  sp.ntiles = pass_tiles(a->V);
+  sp.c = proto.c;
+  sp.partials = proto.partials;
+  ChainParams cp{};
+  cp.B = a->B;
+  cp.gamma = gamma;
+  cp.V = a->V;
+  cp.ld = ldl;
+  cp.target = tlog;
+  cp.draft = dlog;
+  cp.tokens = a->draft_tokens;
+  cp.u = a->u;
+  cp.v = a->v;
+  cp.prefix = a->prefix_len;
+  cp.accept_len = a->accept_len;
+  cp.out_token = a->out_token;
+  cp.rollback = a->rollback_idx;
+  cp.p_at = a->p_at_draft;
+  cp.q_at = a->q_at_draft;
+  cp.resid = a->resid_mass;
+  cp.seq_error = a->seq_error;
+  cp.error_word = a->error_word;
+  return launch_chain_walk_f32(sp, cp, greedy, stream) == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}

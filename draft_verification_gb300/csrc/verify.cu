@@ -1136,9 +1136,11 @@ int cluster_for(const std::array<int, 4>& resident, int B, int ntiles) {
 // its predecessor drains; it reads the predecessor's results only after
 // griddepcontrol.wait.  cluster > 0 launches clusters of that many CTAs
 // along x.
+// With pdl false the kernel is launched in plain stream order instead (its
+// predecessor's results are then visible from its first instruction).
 template <typename K, typename A>
 cudaError_t launch_dependent(K kernel, dim3 grid, int cluster, size_t dyn, const StatsParams& G, const A& args,
-                             cudaStream_t s, int rank = -1) {
+                             cudaStream_t s, int rank = -1, bool pdl = true) {
   const void* fn = reinterpret_cast<const void*>(kernel);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -1147,7 +1149,7 @@ cudaError_t launch_dependent(K kernel, dim3 grid, int cluster, size_t dyn, const
   cfg.stream = s;
   cudaLaunchAttribute at[3];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   int na = 1;
   if (cluster > 0) {
     at[na].id = cudaLaunchAttributeClusterDimension;
@@ -1187,7 +1189,7 @@ cudaError_t smem_limit(const void* fn, int bytes) {
 // the dynamic shared memory the cluster size is chosen for (at least dyn).
 template <typename K, typename A>
 cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsParams& G, const A& args,
-                        cudaStream_t s, int rank = -1) {
+                        cudaStream_t s, int rank = -1, bool pdl = true) {
   const void* fn = reinterpret_cast<const void*>(kernel);
   cudaError_t e = smem_limit(fn, static_cast<int>(occupancy_dyn));
   if (e != cudaSuccess) return e;
@@ -1195,7 +1197,7 @@ cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsP
   e = resident_clusters(fn, occupancy_dyn, &resident);
   if (e != cudaSuccess) return e;
   const int S = cluster_for(resident, G.B, G.ntiles);
-  return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s, rank);
+  return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s, rank, pdl);
 }
 
 // ---------------------------------------------------------------------------
@@ -1441,6 +1443,13 @@ cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bo
 
 cudaError_t launch_cascade(const StatsParams& G, const CascadeParams& p, bool bf16, bool greedy, cudaStream_t s) {
   return bf16 ? cascade_impl<bf16_t>(G, p, greedy, s) : cascade_impl<float>(G, p, greedy, s);
+}
+
+cudaError_t launch_chain_walk_f32(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s) {
+  // plain stream order: the walk reads the logits at the drafted tokens
+  // before it waits, and here those logits come from the preceding kernel
+  if (greedy) return launch_dependent(chain_greedy_kernel<float>, dim3(G.B), 0, 0, G, p, s, -1, false);
+  return launch_walk(chain_walk_kernel<float>, kStageBytes, kStageBytes, G, p, s, -1, false);
 }
 
 }  // namespace sv

@@ -497,6 +497,70 @@ size_t spec_clasp_workspace_size(int B, int L, int d, int M);
 /* cuBLAS call failed (or the cuBLAS handle could not be created).           */
 spec_status spec_clasp_layer_select(const spec_clasp_args* args, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------- */
+/* Chain verification from the models' final hidden states: the LM heads    */
+/* and the row statistics in one tensor-core pass.  "Accelerating LLM       */
+/* Inference with Staged Speculative Decoding" (arXiv 2308.04623),         */
+/* abstract: small-batch inference has low arithmetic intensity, so the    */
+/* step is bound by the bytes it moves; the logits the verification reads  */
+/* are what the LM head writes just before.  The rule is spec_verify_chain's.*/
+/*  - Target logits at the gamma + 1 positions are H_t W_t^T, draft logits   */
+/*    at the gamma positions H_d W_d^T: bfloat16 hidden states and weights,  */
+/*    float32 accumulation on the tensor cores (so a logit differs from the  */
+/*    exact product by float32 rounding of a d-term sum).                    */
+/*  - Each head is one persistent kernel (one CTA per SM, a slab of the      */
+/*    vocabulary each) whose epilogue folds every 128-entry tile of logits   */
+/*    into per-row (max, sum of exponentials) (sampling) or argmax (greedy)  */
+/*    partials, the format the chain walk merges; then the chain walk.       */
+/*  - Greedy mode writes no logits anywhere.  Sampling mode stores the       */
+/*    float32 logits of every row in the workspace, because the residual or */
+/*    bonus draw reads one or two rows per sequence chosen only after the    */
+/*    accept tests; the walk reads just those rows.                          */
+/*  - Same outputs, data-error bits and rules as spec_verify_chain (outputs  */
+/*    as in spec_chain_args).  A bounded wait in the head kernel that gives  */
+/*    up marks its rows non-finite (bit 4 on the affected sequences) and     */
+/*    sets SPEC_ERR_INTERNAL in *error_word.                                 */
+/*  - Launches: one head kernel per head (the draft head only in sampling    */
+/*    mode with gamma > 0), then one walk kernel.                            */
+/* ---------------------------------------------------------------------- */
+typedef struct spec_lm_head_chain_args {
+  int B;                       /* sequences, 1..65535                              */
+  int gamma;                   /* drafted tokens per sequence, 0..32               */
+  int V;                       /* vocabulary size, 1..2,097,152                    */
+  int d_target;                /* target hidden width, a multiple of 8, 8..65536   */
+  int d_draft;                 /* draft hidden width (sampling), same limits       */
+  spec_mode mode;
+  float temperature;           /* > 0 and finite in SPEC_SAMPLE                     */
+  const void* h_target;        /* [B, gamma+1, d_target] bfloat16, 16-byte aligned */
+  const void* h_draft;         /* [B, gamma, d_draft] bfloat16 (sampling)          */
+  const void* w_target;        /* [V, d_target] bfloat16 target LM head            */
+  const void* w_draft;         /* [V, d_draft] bfloat16 draft LM head (sampling)   */
+  const int* draft_tokens;     /* [B, gamma]                                        */
+  const float* u;              /* [B, gamma] (sampling)                             */
+  const float* v;              /* [B] (sampling)                                    */
+  const int* prefix_len;       /* [B] or NULL                                       */
+  int* accept_len;             /* out [B]                                           */
+  int* out_token;              /* out [B]                                           */
+  int* rollback_idx;           /* out [B], optional                                 */
+  float* p_at_draft;           /* out [B, gamma], optional                          */
+  float* q_at_draft;           /* out [B, gamma], optional                          */
+  float* resid_mass;           /* out [B], optional                                 */
+  int* seq_error;              /* out [B], optional                                 */
+  int* error_word;             /* in/out, optional                                  */
+  void* workspace;             /* 256-byte aligned                                  */
+  size_t workspace_bytes;
+} spec_lm_head_chain_args;
+
+/* Partials: 8 bytes per (sequence, statistics row, vocabulary slab), at most */
+/* 256 slabs; sampling adds the float32 logits of every row (row stride V    */
+/* rounded up to a multiple of 4).  0 for sizes outside the limits.          */
+size_t spec_lm_head_chain_workspace_size(int B, int gamma, int V, spec_mode mode);
+/* SPEC_EINVAL: a size outside the limits or a NULL required pointer;         */
+/* SPEC_EALIGN: a hidden-state or weight base not 16-byte aligned;            */
+/* SPEC_EWORKSPACE: workspace NULL, short or not 256-byte aligned;            */
+/* SPEC_ECUDA: a launch failed.                                               */
+spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* args, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* spec_status_string(spec_status status);
 

@@ -34,17 +34,22 @@ def verify_chain_from_hidden(h_target, h_draft, w_target, w_draft, tokens, u, v,
     """Batch: h_target [B, gamma+1, d], h_draft [B, gamma, d], w_target
     [V, d], w_draft [V, d] (float64 values of bfloat16 numbers), tokens int
     [B, gamma], u [B, gamma], v [B], prefix_len [B].  Returns accept_len,
-    out_token, rollback_idx, error, margin_u, margin_v [B]."""
+    out_token, rollback_idx, error, margin_u, margin_v [B], and the chain
+    oracle's diagnostics p_at_draft, q_at_draft [B, gamma], resid_mass,
+    min_mass [B]."""
     B, gamma = tokens.shape
     res = {k: np.zeros(B, np.int64) for k in ("accept_len", "out_token", "rollback_idx", "error")}
-    res.update(margin_u=np.zeros(B), margin_v=np.zeros(B))
+    res.update(margin_u=np.zeros(B), margin_v=np.zeros(B), resid_mass=np.zeros(B), min_mass=np.zeros(B),
+               p_at_draft=np.zeros((B, gamma)), q_at_draft=np.zeros((B, gamma)))
     for b in range(B):
         target = head_logits(h_target[b], w_target)
         draft = None if greedy else head_logits(h_draft[b], w_draft)
         r = verify_chain_sequence(target, draft, [int(t) for t in tokens[b]], None if greedy else u[b],
                                   None if greedy else float(v[b]), temperature, greedy)
-        for k in ("accept_len", "out_token", "error", "margin_u", "margin_v"):
+        for k in ("accept_len", "out_token", "error", "margin_u", "margin_v", "resid_mass", "min_mass"):
             res[k][b] = r[k]
+        res["p_at_draft"][b] = r["p_at_draft"]
+        res["q_at_draft"][b] = r["q_at_draft"]
         res["rollback_idx"][b] = int(prefix_len[b]) + r["accept_len"]
     return res
 

@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 16, names
+    assert len(names) == 18, names
     for n in names:
         assert hasattr(lib, n), n
     from draft_verification_gb300 import _lib
@@ -45,7 +45,7 @@ def test_struct_layout_matches_header(tmp_path):
     structs = {"spec_chain_args": _lib.ChainArgs, "spec_tree_args": _lib.TreeArgs,
                "spec_cascade_args": _lib.CascadeArgs, "spec_compact_args": _lib.CompactArgs,
                "spec_pipeline_args": _lib.PipelineArgs, "spec_clasp_args": _lib.ClaspArgs,
-               "spec_pipeline_async_args": _lib.PipelineAsyncArgs}
+               "spec_pipeline_async_args": _lib.PipelineAsyncArgs, "spec_lm_head_chain_args": _lib.LmHeadChainArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spec_verify.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -359,3 +359,36 @@ def test_pipeline_async_workspace_and_argument_errors(lib):
     a.workspace_bytes = 8
     assert lib.spec_verify_pipeline_async(C.byref(a), None) == -4
     assert lib.spec_verify_pipeline_async(None, None) == -1
+
+
+def test_lm_head_argument_errors_and_workspace(lib):
+    from draft_verification_gb300 import _lib
+    sampling = lib.spec_lm_head_chain_workspace_size(64, 5, 128256, _lib.SPEC_SAMPLE)
+    greedy = lib.spec_lm_head_chain_workspace_size(64, 5, 128256, _lib.SPEC_GREEDY)
+    ldl = 128256
+    part = 64 * 11 * 256 * 8
+    assert sampling == part + 64 * 6 * ldl * 4 + 64 * 5 * ldl * 4  # every part already 256-aligned
+    assert greedy == -(-64 * 6 * 256 * 8 // 256) * 256
+    assert lib.spec_lm_head_chain_workspace_size(0, 5, 100, _lib.SPEC_SAMPLE) == 0
+    assert lib.spec_lm_head_chain_workspace_size(4, 33, 100, _lib.SPEC_SAMPLE) == 0
+
+    def args(**kw):
+        a = _lib.LmHeadChainArgs()
+        a.B, a.gamma, a.V, a.d_target, a.d_draft = 2, 3, 1000, 64, 64
+        a.mode, a.temperature = _lib.SPEC_SAMPLE, 1.0
+        for name in ("h_target", "h_draft", "w_target", "w_draft", "draft_tokens", "u", "v", "accept_len",
+                     "out_token", "workspace"):
+            setattr(a, name, 4096)
+        a.workspace_bytes = 1 << 30
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    cases = [(dict(d_target=60), _lib.SPEC_EINVAL), (dict(d_draft=0), _lib.SPEC_EINVAL),
+             (dict(V=0), _lib.SPEC_EINVAL), (dict(gamma=33), _lib.SPEC_EINVAL),
+             (dict(temperature=0.0), _lib.SPEC_EINVAL), (dict(w_target=None), _lib.SPEC_EINVAL),
+             (dict(h_draft=None), _lib.SPEC_EINVAL), (dict(mode=7), _lib.SPEC_EDTYPE),
+             (dict(h_target=4097), _lib.SPEC_EALIGN), (dict(w_draft=4104), _lib.SPEC_EALIGN),
+             (dict(workspace_bytes=16), _lib.SPEC_EWORKSPACE), (dict(workspace=4096 + 128), _lib.SPEC_EWORKSPACE)]
+    for kw, code in cases:
+        assert lib.spec_verify_chain_lm_head(C.byref(args(**kw)), None) == code, kw

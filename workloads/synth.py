@@ -283,6 +283,42 @@ CLASP_SPECS = {
 }
 
 
+@dataclass(frozen=True)
+class LmHeadSpec:
+    """Chain verification from final hidden states and LM-head weights (the
+    LM head folded into the verification).  Target head W_t [V, d_t] ~
+    N(0, sigma_logit^2 / d_t) rounded to bfloat16, target hidden states
+    h_t ~ N(0, 1) rounded to bfloat16, so target logits have standard
+    deviation about sigma_logit.  The draft reads the first d_d hidden
+    coordinates: W_d = bf16(W_t[:, :d_d] * sqrt(d_t / d_d)) (W_d = W_t when
+    d_d = d_t: one shared head, as in self-speculative decoding) and
+    h_d = bf16(h_t[:, :gamma, :d_d] + s N(0, 1)), so draft logits are the
+    target's plus noise of scale about s * sigma_logit; s is chosen for the
+    named mean acceptance.  Drafted tokens are drawn from the draft softmax
+    with the Gumbel-max trick (its argmax in greedy mode)."""
+    name: str
+    B: int
+    gamma: int
+    V: int
+    d_target: int
+    d_draft: int
+    greedy: bool
+    temperature: float
+    sigma_logit: float = 2.0
+    s: float = 0.35
+    alpha_target: float | None = None
+
+
+# The 128256-vocabulary sampling chain's verification shape (B = 64,
+# gamma = 5, T = 0.7) with the LM head that produces its logits: LLaMA-3-8B's
+# width d = 4096, one head shared by target and draft.
+LM_HEAD_SPECS = {
+    "lm_head_chain_b64_g5_v128256_d4096_bf16": LmHeadSpec(
+        "lm_head_chain_b64_g5_v128256_d4096_bf16", B=64, gamma=5, V=128256, d_target=4096, d_draft=4096,
+        greedy=False, temperature=0.7, alpha_target=0.6),
+}
+
+
 def with_sizes(spec, **kw):
     """A copy of a spec with some fields replaced (e.g. a smaller B or V)."""
     return dataclasses.replace(spec, **kw)
@@ -552,9 +588,42 @@ def make_pipeline_async(spec: PipelineAsyncSpec, seed: int = 0) -> dict:
                 length=length)
 
 
+def make_lm_head(spec: LmHeadSpec, seed: int = 0) -> dict:
+    """LM-head workload (bfloat16 bit patterns as uint16): h_target [B,
+    gamma+1, d_t], h_draft [B, gamma, d_d], w_target [V, d_t], w_draft [V,
+    d_d], tokens int32 [B, gamma], u float32 [B, gamma], v float32 [B],
+    prefix_len int32 [B]."""
+    rng = _rng(seed, 7)
+    B, g, V, dt, dd = spec.B, spec.gamma, spec.V, spec.d_target, spec.d_draft
+    w_t = bf16_from_float32(rng.standard_normal((V, dt), dtype=np.float32) * np.float32(spec.sigma_logit / np.sqrt(dt)))
+    h_t = bf16_from_float32(rng.standard_normal((B, g + 1, dt), dtype=np.float32))
+    if dd == dt:
+        w_d = w_t
+    else:
+        w_d = bf16_from_float32(float32_from_bf16(w_t[:, :dd]) * np.float32(np.sqrt(dt / dd)))
+    noise = rng.standard_normal((B, g, dd), dtype=np.float32) * np.float32(spec.s)
+    h_d = bf16_from_float32(float32_from_bf16(h_t[:, :g, :dd]) + noise)
+    tokens = np.empty((B, g), np.int32)
+    wd_f = float32_from_bf16(w_d)
+    for b in range(B):  # the draft logits of one sequence at a time
+        logits = float32_from_bf16(h_d[b]) @ wd_f.T
+        if spec.greedy:
+            tokens[b] = np.argmax(logits, axis=-1)
+        else:
+            tokens[b] = _gumbel_argmax(rng, logits / np.float32(spec.temperature))
+    u = rng.random((B, g), dtype=np.float32)
+    v = rng.random(B, dtype=np.float32)
+    prefix = rng.integers(0, 4096, B, dtype=np.int32)
+    return dict(kind="lm_head", spec=spec, h_target=h_t, h_draft=h_d, w_target=w_t, w_draft=w_d,
+                tokens=tokens, u=u, v=v, prefix_len=prefix)
+
+
 def make(spec, seed: int = 0) -> dict:
     if isinstance(spec, str):
-        spec = {**SPECS, **COMPACT_SPECS, **PIPELINE_SPECS, **PIPELINE_ASYNC_SPECS, **CLASP_SPECS}[spec]
+        spec = {**SPECS, **COMPACT_SPECS, **PIPELINE_SPECS, **PIPELINE_ASYNC_SPECS, **CLASP_SPECS,
+                **LM_HEAD_SPECS}[spec]
+    if isinstance(spec, LmHeadSpec):
+        return make_lm_head(spec, seed)
     if isinstance(spec, PipelineSpec):
         return make_pipeline(spec, seed)
     if isinstance(spec, PipelineAsyncSpec):
