@@ -2,21 +2,21 @@
 the float64 oracle of oracle/lm_head.py.
 
 The kernel's logits are float32 sums of d bfloat16 products formed on the
-tensor cores, so each differs from the exact product by rounding: at most
-about d * 2^-24 * sum_k |h_k w_k| (the worst case of a d-term float32 sum),
-in practice far less.  The tests measure that error on the logits the kernel
-stores (sampling mode keeps them for the draw) and check it against the
-worst-case bound; decisions are then compared exactly except where the
-measured error could flip them:
-  * an accept test with |u - r| below TOL_U + 4 e / T * max(1, r): the
-    ratio r = p / q moves by at most 4 e / T in log space (two logits and two
-    row sums, each off by at most e);
-  * a draw whose v * Z lies within TOL_V + 8 e / (T Z) of a running sum, or
-    a residual thinner than 16 e / T (its mass is then mostly rounding);
-  * in greedy mode a tested row whose two largest exact logits are closer
-    than 4 e.
-e is the measured maximum logit error of the call; the same rules as the
-stored-logit parity tests otherwise (tests/gpu_helpers.py).
+tensor cores, so each differs from the exact product by rounding.  The
+tests check that in two steps:
+  1. the logits the kernel stores (sampling mode keeps them for the draw)
+     are within the worst-case error of a d-term float32 sum,
+     d * 2^-24 * sum_k |h_k w_k|, of the exact products;
+  2. the verification on those logits is the oracle's: the float64 oracle
+     run on the kernel's own float32 logits must give the GPU's decisions,
+     tokens and error words, with the stored-logit tests' near-tie rules
+     (tests/gpu_helpers.py), and the oracle on the exact products must give
+     the same wherever the two oracles agree.  Where they differ, the
+     rounding of the products itself moved a decision; such sequences are
+     set aside, and they must stay rare.
+Greedy calls store no logits; their GEMM is the same launch geometry as the
+sampling call's, so its logits are the same bits, and the greedy result must
+equal the argmax rule on the stored logits exactly.
 """
 
 import numpy as np
@@ -88,45 +88,45 @@ def oracle(w, seqs, greedy):
                                        w["prefix_len"][seqs], s.temperature, greedy)
 
 
-def compare_sampling(g, o, seqs, err, T):
-    r = np.where(o["q_at_draft"] > 0, o["p_at_draft"] / np.maximum(o["q_at_draft"], 1e-300), np.inf)
-    rmax = np.maximum(1.0, np.nan_to_num(r, posinf=1e30).max(axis=1)) if r.shape[1] else np.ones(len(seqs))
-    Z = np.where(o["resid_mass"] > 0, o["resid_mass"], 1.0)
-    flagged = ((o["margin_u"] < H.TOL_U + 4 * err / T * rmax)
-               | (o["margin_v"] < H.TOL_V + 8 * err / (T * Z))
-               | ((o["min_mass"] > 0) & (o["min_mass"] < max(H.Z_MIN, 16 * err / T))))
-    assert flagged.mean() <= H.MAX_FLAGGED, f"{flagged.sum()} of {len(seqs)} set aside (e = {err:.3g})"
-    ok = ~flagged
-    for k in ("accept_len", "out_token", "rollback_idx"):
-        bad = np.flatnonzero(ok & (g[k][seqs] != o[k]))
-        assert bad.size == 0, (k, seqs[bad[:8]], g[k][seqs][bad[:8]], o[k][bad[:8]])
-    H.compare_errors(g["seq_error"][seqs], o["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
-    tol = H.REL_F + 4 * err / T
-    valid = o["error"] == 0
-    for k in ("p_at_draft", "q_at_draft"):
-        a, b = g[k][seqs][valid], o[k][valid]
-        assert (np.abs(a - b) <= tol * np.abs(b) + H.ABS_F).all(), k
-    same = ok & valid & (g["accept_len"][seqs] == o["accept_len"])
-    a, b = g["resid_mass"][seqs][same], o["resid_mass"][same]
-    # each weight p or q is off by at most 2 e / T relative, so a mass built
-    # from at most two unit-mass distributions by at most 4 e / T absolute
-    assert (np.abs(a - b) <= H.REL_F * np.abs(b) + 4 * err / T + H.ABS_F).all()
-    return flagged
+def oracle_on_kernel_logits(w, logits, seqs, greedy):
+    """The chain oracle on the kernel's float32 logits (converted exactly)."""
+    s = w["spec"]
+    tgt = np.ascontiguousarray(logits[0][seqs], np.float32)
+    drf = (np.ascontiguousarray(logits[1][seqs], np.float32) if logits[1] is not None
+           else np.zeros((len(seqs), 0, s.V), np.float32))
+    return V.verify_chain(tgt, drf, w["tokens"][seqs], w["u"][seqs], w["v"][seqs], w["prefix_len"][seqs],
+                          s.temperature, greedy, "f32")
 
 
-def compare_greedy(g, o, w, seqs, err):
-    ht, _, wt, _ = exact(w, seqs)
-    flagged = np.zeros(len(seqs), bool)
-    for i in range(len(seqs)):
-        a = int(o["accept_len"][i])
-        ex = ht[i][: a + 1] @ wt.T
-        top2 = np.sort(ex, axis=1)[:, -2:]
-        flagged[i] = (top2[:, 1] - top2[:, 0] < 4 * err).any()
+DECISIONS = ("accept_len", "out_token", "rollback_idx")
+
+
+def compare(g, w, logits, seqs, greedy, err):
+    s = w["spec"]
+    o_exact = oracle(w, seqs, greedy)
+    o_kern = oracle_on_kernel_logits(w, logits, seqs, greedy)
+    moved = np.zeros(len(seqs), bool)
+    for k in DECISIONS:
+        moved |= o_exact[k] != o_kern[k]
+    assert moved.mean() <= H.MAX_FLAGGED, f"rounding of the products moved {moved.sum()} of {len(seqs)}"
+    flagged = H.set_aside(o_kern, greedy) | moved
+    assert flagged.mean() <= H.MAX_FLAGGED, f"{flagged.sum()} of {len(seqs)} set aside"
     ok = ~flagged
-    for k in ("accept_len", "out_token", "rollback_idx"):
-        bad = np.flatnonzero(ok & (g[k][seqs] != o[k]))
-        assert bad.size == 0, (k, seqs[bad[:8]], g[k][seqs][bad[:8]], o[k][bad[:8]])
-    assert (g["seq_error"][seqs] == 0).all()
+    for k in DECISIONS:
+        bad = np.flatnonzero(ok & (g[k][seqs] != o_kern[k]))
+        assert bad.size == 0, (k, seqs[bad[:8]], g[k][seqs][bad[:8]], o_kern[k][bad[:8]])
+        assert np.array_equal(o_kern[k][ok], o_exact[k][ok])
+    H.compare_errors(g["seq_error"][seqs], o_kern["error"], flagged, V.ERR_TOKEN | V.ERR_NONFINITE)
+    if not greedy:
+        valid = o_kern["error"] == 0
+        for k in ("p_at_draft", "q_at_draft"):
+            assert H.close(g[k][seqs][valid], o_kern[k][valid]).all(), k
+            # and against the exact products, within what e moves a probability
+            a, b = g[k][seqs][valid], o_exact[k][valid]
+            assert (np.abs(a - b) <= (H.REL_F + 4 * err / s.temperature) * np.abs(b) + H.ABS_F).all(), k
+        same = ok & valid
+        assert H.close(g["resid_mass"][seqs][same], o_kern["resid_mass"][same]).all()
+    return flagged, moved
 
 
 CASES = [
@@ -139,32 +139,32 @@ CASES = [
 ]
 
 
+def check(w, device, seqs):
+    g, logits = run(w, device)
+    err, bound = logit_error(w, logits, seqs)
+    assert err <= bound, (err, bound)
+    compare(g, w, logits, seqs, False, err)
+    # greedy on the same inputs: the same GEMM, argmaxes only, no logits stored
+    gg, _ = run(w, device, greedy=True)
+    _, moved = compare(gg, w, logits, seqs, True, err)
+    o_kern = oracle_on_kernel_logits(w, logits, seqs, True)
+    for k in DECISIONS:  # argmaxes of the same float32 values: exact
+        assert np.array_equal(gg[k][seqs], o_kern[k]), k
+    return g
+
+
 @pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
 def test_lm_head_chain_small(cuda_device, spec):
     w = synth.make(spec, seed=3)
-    g, logits = run(w, cuda_device)
-    seqs = np.arange(spec.B)
-    err, bound = logit_error(w, logits, seqs)
-    assert err <= bound, (err, bound)
-    compare_sampling(g, oracle(w, seqs, False), seqs, err, spec.temperature)
-    # greedy on the same inputs: the same GEMM, argmaxes only, no logits stored
-    gg, _ = run(w, cuda_device, greedy=True)
-    compare_greedy(gg, oracle(w, seqs, True), w, seqs, err)
+    check(w, cuda_device, np.arange(spec.B))
 
 
 def test_lm_head_chain_full_size_sampled(cuda_device):
     # the measured workload (B = 64, gamma = 5, V = 128256, d = 4096) in its
     # launch configuration; every output of 8 sampled sequences is checked
     w = synth.make(BASE, seed=0)
-    g, logits = run(w, cuda_device)
-    seqs = np.array([0, 9, 17, 26, 35, 44, 53, 63])
-    err, bound = logit_error(w, logits, seqs)
-    assert err <= bound, (err, bound)
-    flagged = compare_sampling(g, oracle(w, seqs, False), seqs, err, BASE.temperature)
-    assert not flagged.all()
+    g = check(w, cuda_device, np.array([0, 9, 17, 26, 35, 44, 53, 63]))
     assert (g["seq_error"] == 0).all() and g["error_word"][0] == 0
-    gg, _ = run(w, cuda_device, greedy=True)
-    compare_greedy(gg, oracle(w, seqs, True), w, seqs, err)
 
 
 def test_lm_head_matches_stored_logit_path(cuda_device):
