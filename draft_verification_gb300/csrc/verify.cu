@@ -45,6 +45,7 @@
 #include <array>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "common.cuh"
@@ -316,7 +317,12 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParam
 }
 
 // Sampling chain: one cluster per sequence (grid (S, B), cluster (S, 1, 1)).
-template <typename T>
+// kResident: every CTA loads its whole slice of the chosen row pair into
+// dynamic shared memory at once (one bulk-copy round trip instead of a ring
+// of stages) and the drawing CTA finds the element there; used where the
+// walk runs after the statistics have been read (the last batch group), so
+// its larger shared memory does not crowd the statistics kernel.
+template <typename T, bool kResident>
 __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsParams G, const ChainParams P) {
   __shared__ ChainSmem cs;
   __shared__ PassSmem ps;
@@ -382,8 +388,26 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
                             a < g ? draft + (drow0 + a) * P.ld : nullptr, a < g ? cs.st_m[g + 1 + a] : 0.f,
                             a < g ? cs.st_s[g + 1 + a] : 1.f, 1.f, c);
   int buf = 0, flag = 0;
-  const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
-  const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps);
+  DF Z;
+  int y;
+  if constexpr (kResident) {
+    const int ncl = static_cast<int>(cluster_size());
+    const int tpc = (G.ntiles + ncl - 1) / ncl;
+    const int t0 = min(G.ntiles, static_cast<int>(cluster_rank()) * tpc), t1 = min(G.ntiles, t0 + tpc);
+    slice_load(S, a < g, G.V, t0, t1, ps);
+    Z = cluster_pass(S, G.V, c, G.ntiles, buf, ps, true);
+    if (!pass_ok(Z)) {  // reading R3: the target row alone, already resident
+      flag |= SPEC_ERR_ZERO_MASS;
+      S.cq = 0.f;
+      S.Q = nullptr;
+      buf ^= 1;
+      Z = cluster_pass(S, G.V, c, G.ntiles, buf, ps, true);
+    }
+    y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps, true);
+  } else {
+    Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
+    y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps);
+  }
   if (y < 0) return;  // another CTA of the cluster holds the drawn tile
   if (ps.fault) {  // a bounded wait gave up: the draw is not trusted
     flag |= SPEC_ERR_INTERNAL;
@@ -1023,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
         }
         Z = cluster_pass(S, P.V, c, G.ntiles, buf, ps, res_ok);
       }
-      token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, v_s), false, ps);
+      token = cluster_draw(S, P.V, c, G.ntiles, buf, df_mul_f(Z, v_s), false, ps, res_ok);
       writer = token >= 0;
       break;
     }
@@ -1200,6 +1224,58 @@ cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsP
   return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s, rank, pdl);
 }
 
+// The resident-slice chain walk: the largest cluster S <= 8 (at most one
+// CTA per tile) whose slices fit in kMaxResidentBytes and for which all B
+// clusters fit in 7/8 of the resident clusters at that slice size; the staged
+// walk when none does.
+constexpr size_t kMaxResidentBytes = 96 * 1024;
+
+template <typename T>
+cudaError_t launch_chain_walk_resident(const StatsParams& G, const ChainParams& args, cudaStream_t s, int rank) {
+  const void* fn = reinterpret_cast<const void*>(chain_walk_kernel<T, true>);
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, int> fits;  // (fn, dev, S, dyn) -> clusters
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  for (int S = 8; S >= 1; S >>= 1) {
+    if (S > G.ntiles) continue;
+    const int tpc = (G.ntiles + S - 1) / S;
+    const size_t dyn = slice_bytes<T>(tpc);
+    if (tpc > kResidentTiles || dyn > kMaxResidentBytes) break;  // smaller clusters only need more
+    e = smem_limit(fn, static_cast<int>(kMaxResidentBytes));
+    if (e != cudaSuccess) return e;
+    int count = 0;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      auto key = std::make_tuple(fn, dev, S, static_cast<int>(dyn));
+      auto it = fits.find(key);
+      if (it != fits.end()) {
+        count = it->second;
+      } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(S, 1, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = dyn;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = S;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&count, fn, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          count = 0;
+        }
+        fits[key] = count;
+      }
+    }
+    if (8 * G.B <= 7 * count) return launch_dependent(chain_walk_kernel<T, true>, dim3(S, G.B), S, dyn, G, args, s, rank);
+  }
+  return launch_walk(chain_walk_kernel<T, false>, kStageBytes, kStageBytes, G, args, s, rank);
+}
+
 // ---------------------------------------------------------------------------
 // batch groups: large calls are split into up to kMaxGroups groups of
 // sequences, each verified by its own statistics kernel and walk on a
@@ -1347,13 +1423,17 @@ double logit_bytes(const StatsParams& G, size_t elt) {
 // carry priorities: every walk above every statistics kernel, and the
 // statistics of earlier groups above later ones, so that groups finish
 // their statistics in order and each walk starts as soon as it can.
+// `last`: no statistics kernel of this call runs after this group's, so its
+// walk takes the resident-slice form.
 template <typename T>
-cudaError_t chain_one(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s, int group) {
+cudaError_t chain_one(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s, int group,
+                      bool last) {
   const int sr = group < 0 ? -1 : 1 + group, wr = group < 0 ? -1 : 0;
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s, sr) : launch_stats(stats_kernel<T, false>, G, s, sr);
   if (e != cudaSuccess) return e;
   if (greedy) return launch_dependent(chain_greedy_kernel<T>, dim3(G.B), 0, 0, G, p, s, wr);
-  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s, wr);
+  if (last) return launch_chain_walk_resident<T>(G, p, s, wr);
+  return launch_walk(chain_walk_kernel<T, false>, kStageBytes, kStageBytes, G, p, s, wr);
 }
 
 template <typename T>
@@ -1365,17 +1445,17 @@ cudaError_t chain_consulted(const StatsParams& G, const ChainParams& p, cudaStre
   void* argv[] = {const_cast<StatsParams*>(&G), const_cast<ChainParams*>(&p)};
   cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(stats_consulted_kernel<T>), argv);
   if (e != cudaSuccess) return e;
-  return launch_walk(chain_walk_kernel<T>, kStageBytes, kStageBytes, G, p, s);
+  return launch_walk(chain_walk_kernel<T, false>, kStageBytes, kStageBytes, G, p, s);
 }
 
 template <typename T>
 cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, bool grouped, cudaStream_t s) {
   if (p.skip) return chain_consulted<T>(G, p, s);
   const Groups gr = plan_groups(G.B, logit_bytes(G, sizeof(T)));
-  if (!grouped || gr.n == 1) return chain_one<T>(G, p, greedy, s, -1);
+  if (!grouped || gr.n == 1) return chain_one<T>(G, p, greedy, s, -1, true);
   return run_groups(gr, s, [&](int i, cudaStream_t si) {
     const int b0 = gr.b0[i], nb = gr.b0[i + 1] - b0;
-    return chain_one<T>(stats_group<T>(G, b0, nb), chain_group<T>(p, b0, nb), greedy, si, i);
+    return chain_one<T>(stats_group<T>(G, b0, nb), chain_group<T>(p, b0, nb), greedy, si, i, i == gr.n - 1);
   });
 }
 
@@ -1449,7 +1529,7 @@ cudaError_t launch_chain_walk_f32(const StatsParams& G, const ChainParams& p, bo
   // plain stream order: the walk reads the logits at the drafted tokens
   // before it waits, and here those logits come from the preceding kernel
   if (greedy) return launch_dependent(chain_greedy_kernel<float>, dim3(G.B), 0, 0, G, p, s, -1, false);
-  return launch_walk(chain_walk_kernel<float>, kStageBytes, kStageBytes, G, p, s, -1, false);
+  return launch_walk(chain_walk_kernel<float, false>, kStageBytes, kStageBytes, G, p, s, -1, false);
 }
 
 }  // namespace sv

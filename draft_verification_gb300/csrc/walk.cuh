@@ -240,7 +240,7 @@ constexpr int kStageRowBytes = 8192;
 constexpr int kStages = 2;
 constexpr int kStageBytes = kStages * 2 * kStageRowBytes;
 constexpr int kMaxCluster = 8;
-constexpr int kResidentTiles = kStageBytes / (2 * kTileElems * 2);  // bf16 tiles of both rows
+constexpr int kResidentTiles = 16;  // tiles of a resident slice (two bf16 rows of 16 tiles: 128 KB)
 extern __shared__ __align__(128) unsigned char dyn_smem[];
 
 struct PassSmem {
@@ -474,10 +474,17 @@ __device__ void direct_sums(const PassSpec<T>& S, int V, float c, int t0, int t1
 // in the stage region of shared memory, so that several passes over the same
 // rows (the sibling passes at one tree node) read the logits once
 // ---------------------------------------------------------------------------
-// Whether `nt` tiles of both rows fit in the stage region.
+// Bytes of a resident slice of `nt` tiles of both rows.
 template <typename T>
-__device__ __forceinline__ bool slice_fits(int nt) {
-  return 2 * static_cast<size_t>(nt) * kTileElems * sizeof(T) <= static_cast<size_t>(kStageBytes);
+__host__ __device__ constexpr size_t slice_bytes(int nt) {
+  return 2 * static_cast<size_t>(nt) * kTileElems * sizeof(T);
+}
+
+// Whether `nt` tiles of both rows fit in `region` bytes of dynamic shared
+// memory (by default the stage region every walk kernel has).
+template <typename T>
+__device__ __forceinline__ bool slice_fits(int nt, size_t region = kStageBytes) {
+  return nt <= kResidentTiles && slice_bytes<T>(nt) <= region;
 }
 
 // This thread's 8 elements of local tile j of a resident row as floats.
@@ -740,12 +747,23 @@ __device__ void locate_tile(const float* all, int n, int ntiles, DF target, Pass
   __syncthreads();
 }
 
+// With `res_t0` >= 0 the drawing CTA's resident slice (first tile res_t0,
+// res_nt tiles, laid out as slice_load leaves it) holds the tile, and its
+// elements come from shared memory instead of global memory.
 template <typename T>
-__device__ int draw_in_tile(const PassSpec<T>& S, int V, float c, PassSmem& sh) {
+__device__ int draw_in_tile(const PassSpec<T>& S, int V, float c, PassSmem& sh, int res_t0 = -1, int res_nt = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = sh.tile;
   float w[8];
-  tile_weights(S, V, c, tile, w);
+  if (res_t0 >= 0) {
+    float xp[8], xq[8];
+    const int j = tile - res_t0;
+    slice_get8<T>(dyn_smem, j, xp);
+    if (S.cq != 0.f) slice_get8<T>(dyn_smem + static_cast<size_t>(res_nt) * kTileElems * sizeof(T), j, xq);
+    pass_weights(S, c, xp, xq, w);
+  } else {
+    tile_weights(S, V, c, tile, w);
+  }
   const float mine = sum8(w);
   const float incl_w = warp_incl_scan(mine);
   if (lane == 31) sh.warp_tot[0][0][warp] = incl_w;
@@ -795,9 +813,15 @@ __device__ int draw_in_tile(const PassSpec<T>& S, int V, float c, PassSmem& sh) 
 // set, recomputes the tile and returns the index; the others return -1.
 template <typename T>
 __device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, int buf, DF target,
-                            bool all_ctas, PassSmem& sh) {
-  locate_tile(sh.all[buf], static_cast<int>(cluster_size()), ntiles, target, sh);
-  if (!all_ctas && sh.owner != static_cast<int>(cluster_rank())) return -1;
+                            bool all_ctas, PassSmem& sh, bool resident = false) {
+  const int n = static_cast<int>(cluster_size()), rank = static_cast<int>(cluster_rank());
+  locate_tile(sh.all[buf], n, ntiles, target, sh);
+  if (!all_ctas && sh.owner != rank) return -1;
+  if (resident && sh.owner == rank) {
+    const int tpc = (ntiles + n - 1) / n;
+    const int t0 = min(ntiles, rank * tpc), t1 = min(ntiles, t0 + tpc);
+    return draw_in_tile(S, V, c, sh, t0, t1 - t0);
+  }
   return draw_in_tile(S, V, c, sh);
 }
 
