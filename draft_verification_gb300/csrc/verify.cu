@@ -63,8 +63,9 @@ constexpr int kMaxDecisionChunks = 256;  // statistics chunks of the longest row
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
 // Test hook (spec_test_inject_copy_timeout): nonzero makes every bulk-copy
-// stage of a residual pass expect 16 bytes that never come, so that its
-// bounded wait gives up.  Zero in normal operation.
+// wait of a residual or bonus pass (ring stage or resident slice) expect 16
+// bytes that never come, so that its bounded wait gives up.  Zero in normal
+// operation.
 __device__ int g_copy_timeout_test = 0;
 constexpr int kStage = 4 * kThreads;  // chunk partials staged per round (8 KB)
 static_assert(kMaxTiles * kTileElems >= 2097152, "tile sums of the largest row fit in shared memory");

@@ -39,8 +39,9 @@ struct PassSpec {
   float MP, invSP;  // scaled max and 1/sum of the target row
   float MQ, invSQ;
   float cq;         // coefficient of q
-  unsigned extra_tx;  // bytes each bulk-copy stage expects beyond its copies:
-                      // 0, or 16 under the copy-timeout test hook
+  unsigned extra_tx;  // bytes each bulk-copy wait (a ring stage or a resident
+                      // slice) expects beyond its copies: 0, or 16 under the
+                      // copy-timeout test hook
 };
 
 // ---------------------------------------------------------------------------
@@ -546,7 +547,7 @@ __device__ void slice_load(const PassSpec<T>& S, bool with_q, int V, int t0, int
   unsigned bytes = slice_issue(S.P, V, t0, t1, pbuf, &sh.lbar);
   if (with_q) bytes += slice_issue(S.Q, V, t0, t1, qbuf, &sh.lbar);
   const int phase = sh.loads;
-  if (threadIdx.x == 0) mbar_expect_tx(&sh.lbar, bytes);
+  if (threadIdx.x == 0) mbar_expect_tx(&sh.lbar, bytes + S.extra_tx);
   __syncthreads();  // armed and issued before anyone waits; plain stores visible
   if (!mbar_wait(&sh.lbar, phase & 1)) sh.fault = 1;
   __syncthreads();

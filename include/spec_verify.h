@@ -566,9 +566,10 @@ const char* spec_status_string(spec_status status);
 
 /* ---------------------------------------------------------------------- */
 /* Test hook for the bounded waits (no counterpart on the pages).  While   */
-/* enabled on the current device, every bulk-copy stage of a sampling      */
-/* walk's residual or bonus pass expects 16 bytes more than it copies, so  */
-/* its wait gives up after about 65 ms instead of completing: the sequence */
+/* enabled on the current device, every bulk-copy wait of a sampling      */
+/* walk's residual or bonus pass (a ring stage or a resident slice) expects */
+/* 16 bytes more than it copies, so it gives up after about 65 ms instead  */
+/* of completing: the sequence                                             */
 /* reports SPEC_ERR_INTERNAL with empty outputs and the GPU stays usable.   */
 /* Nothing faults and nothing is left in flight (the copies themselves     */
 /* complete).  Synchronous (one small copy to the device); affects calls   */
