@@ -109,10 +109,12 @@ def chain_groups(B: int, rows: int, V: int, elt: int) -> int:
 
 def launches_per_call(w) -> int:
     """Kernels of the library launched by one verification call: statistics
-    and walk per batch group for chains (one group in consulted-only mode),
-    statistics and walk for the other kinds."""
+    and walk per batch group for chains, statistics and walk for the other
+    kinds, one walk kernel in consulted-only mode."""
     s = w["spec"]
-    if w["kind"] == "chain" and not (CONSULTED and not s.greedy):
+    if CONSULTED and (w["kind"] == "tree" or (w["kind"] == "chain" and not s.greedy)):
+        return 1  # the consulted-only walk computes its own statistics
+    if w["kind"] == "chain":
         rows = s.gamma + 1 if s.greedy else 2 * s.gamma + 1
         return 2 * chain_groups(s.B, rows, s.V, 2 if s.dtype == "bf16" else 4)
     return 2
@@ -398,7 +400,7 @@ def make_plan(w, t, workspace=None):
     if w["kind"] == "tree":
         return dv.TreePlan(t["parent"], t["tokens"], t["target"], t["draft"], t["u"], t["v"],
                            t["prefix_len"], max_depth=w["max_depth"], greedy=s.greedy,
-                           temperature=s.temperature, workspace=workspace)
+                           temperature=s.temperature, workspace=workspace, consulted_only=CONSULTED)
     if w["kind"] == "pipeline":
         models = [None if (s.greedy and i == 0) else m[:, :, :s.V] for i, m in enumerate(t["models"])]
         return dv.PipelinePlan(models, t["tokens"], s.windows, t["us"], t["vs"], t["base"], greedy=s.greedy,
@@ -509,6 +511,21 @@ def run_ours(args, w, rank, world, dist):
         roof_bytes = int(rows.sum()) * s.V * (2 if s.dtype == "bf16" else 4)
         roof_unit = "one verification call (consulted rows only)"
         kernel_gbs = roof_bytes / (kernel_ms * 1e-3) / 1e9
+    if w["kind"] == "tree" and CONSULTED:
+        # the rows the walk reads: at every node it stands at, the target row,
+        # and (sampling) the draft row when the node has children
+        nodes = check["path_nodes"].cpu().numpy()
+        has_kids = np.zeros(w["parent"].shape, bool)
+        for b in range(s.B):
+            has_kids[b, np.unique(w["parent"][b, 1:])] = True
+        rows = 0
+        for b in range(s.B):
+            for n in nodes[b]:
+                if n >= 0:
+                    rows += 1 + (0 if s.greedy else int(has_kids[b, n]))
+        roof_bytes = rows * s.V * (2 if s.dtype == "bf16" else 4)
+        roof_unit = "one verification call (consulted rows only)"
+        kernel_gbs = roof_bytes / (kernel_ms * 1e-3) / 1e9
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -516,7 +533,8 @@ def run_ours(args, w, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": compute_dtype(s.dtype), "data": "synthetic (seeded; shapes of the pages' model families)",
         "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                       consulted_only=bool(CONSULTED and w["kind"] == "chain" and not s.greedy),
+                       consulted_only=bool(CONSULTED and (w["kind"] == "tree" or
+                                                           (w["kind"] == "chain" and not s.greedy))),
                        l2_policy=f"rotating {n_sets} input copies ({n_sets * bytes_per_call / 2**20:.0f} MB "
                                  f"> 3 x L2 {l2 / 2**20:.0f} MB)", launch=launch),
         "logits_gbs": logits_gbs,
@@ -575,11 +593,13 @@ def e2e_rate(args, w, dev, stream):
             if w["kind"] == "chain":
                 o = dv.verify_chain(host["target"], None if s.greedy else host["draft"], host["tokens"],
                                     host["u"], host["v"], host["prefix_len"], greedy=s.greedy,
-                                    temperature=s.temperature, device=dev, stream=stream)
+                                    temperature=s.temperature, device=dev, stream=stream,
+                                    consulted_only=CONSULTED and not s.greedy)
             elif w["kind"] == "tree":
                 o = dv.verify_tree(host["parent"], host["tokens"], host["target"], host["draft"],
                                    host["u"], host["v"], host["prefix_len"], max_depth=w["max_depth"],
-                                   greedy=s.greedy, temperature=s.temperature, device=dev, stream=stream)
+                                   greedy=s.greedy, temperature=s.temperature, device=dev, stream=stream,
+                                   consulted_only=CONSULTED)
             else:
                 o = dv.verify_cascade(host["l0"], host["l1"], host["l2"], host["tokens"], host["u1"],
                                       host["v1"], host["u2"], host["v2"], host["base0"], host["base1"],

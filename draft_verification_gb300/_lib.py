@@ -44,7 +44,8 @@ class TreeArgs(C.Structure):
         ("draft_logits", _vp), ("u", _vp), ("v", _vp), ("prefix_len", _vp),
         ("path_len", _vp), ("path_nodes", _vp), ("out_token", _vp),
         ("rollback_idx", _vp), ("seq_error", _vp), ("error_word", _vp),
-        ("workspace", _vp), ("workspace_bytes", C.c_size_t)
+        ("workspace", _vp), ("workspace_bytes", C.c_size_t),
+        ("consulted_only", C.c_int)
     ]
 
 

@@ -239,7 +239,7 @@ class TreePlan(_Plan):
     """Tree verification bound to fixed buffers.  See spec_verify_tree."""
 
     def __init__(self, parent, tokens, target, draft, u=None, v=None, prefix_len=None, *,
-                 max_depth, greedy=False, temperature=1.0, V=None, workspace=None):
+                 max_depth, greedy=False, temperature=1.0, V=None, workspace=None, consulted_only=False):
         B, N, width = target.shape
         V = width if V is None else V
         dev = target.device
@@ -278,6 +278,7 @@ class TreePlan(_Plan):
         a.out_token, a.rollback_idx = _ptr(o["out_token"]), _ptr(o["rollback_idx"])
         a.seq_error, a.error_word = _ptr(o["seq_error"]), _ptr(o["error_word"])
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        a.consulted_only = int(bool(consulted_only))
         self.args = a
         self._call = lib.spec_verify_tree
 
@@ -481,7 +482,7 @@ def _finish(out, host):
 
 
 def verify_chain(target, draft, tokens, u=None, v=None, prefix_len=None, *, greedy=False,
-                 temperature=1.0, V=None, device="cuda", stream=None):
+                 temperature=1.0, V=None, device="cuda", stream=None, consulted_only=False):
     """Verify B draft chains; returns accept_len, out_token, rollback_idx,
     p_at_draft, q_at_draft, resid_mass, seq_error, error_word."""
     host = target.device.type == "cpu"
@@ -489,12 +490,12 @@ def verify_chain(target, draft, tokens, u=None, v=None, prefix_len=None, *, gree
         target, draft, tokens, u, v, prefix_len = _to_device(
             [target, draft, tokens, u, v, prefix_len], device)
     plan = ChainPlan(target, draft, tokens, u, v, prefix_len, greedy=greedy,
-                     temperature=temperature, V=V)
+                     temperature=temperature, V=V, consulted_only=consulted_only)
     return _finish(plan.run(stream), host)
 
 
 def verify_tree(parent, tokens, target, draft, u=None, v=None, prefix_len=None, *, max_depth,
-                greedy=False, temperature=1.0, V=None, device="cuda", stream=None):
+                greedy=False, temperature=1.0, V=None, device="cuda", stream=None, consulted_only=False):
     """Walk B draft trees; returns path_len, path_nodes, out_token,
     rollback_idx, seq_error, error_word."""
     host = target.device.type == "cpu"
@@ -502,7 +503,7 @@ def verify_tree(parent, tokens, target, draft, u=None, v=None, prefix_len=None, 
         parent, tokens, target, draft, u, v, prefix_len = _to_device(
             [parent, tokens, target, draft, u, v, prefix_len], device)
     plan = TreePlan(parent, tokens, target, draft, u, v, prefix_len, max_depth=max_depth,
-                    greedy=greedy, temperature=temperature, V=V)
+                    greedy=greedy, temperature=temperature, V=V, consulted_only=consulted_only)
     return _finish(plan.run(stream), host)
 
 

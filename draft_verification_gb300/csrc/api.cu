@@ -99,13 +99,7 @@ spec_status sv::verify_chain(const spec_chain_args* a, cudaStream_t stream, bool
   cp.resid = a->resid_mass;
   cp.seq_error = a->seq_error;
   cp.error_word = a->error_word;
-  if (consulted) {
-    char* ctl = static_cast<char*>(a->workspace) + workspace_bytes(a->B, rows, a->V);
-    cp.count = reinterpret_cast<unsigned*>(ctl);
-    cp.skip = reinterpret_cast<int*>(ctl) + static_cast<size_t>(a->B) * a->gamma;
-    if (cudaMemsetAsync(ctl, 0, chain_ctl_bytes(a->B, a->gamma), stream) != cudaSuccess) return SPEC_ECUDA;
-  }
-  return run(launch_chain(sp, cp, bf16, greedy, grouped, stream));
+  return run(launch_chain(sp, cp, bf16, greedy, grouped, consulted, stream));
 }
 
 extern "C" {
@@ -187,7 +181,7 @@ spec_status spec_verify_tree(const spec_tree_args* a, cudaStream_t stream) {
   tp.rollback = a->rollback_idx;
   tp.seq_error = a->seq_error;
   tp.error_word = a->error_word;
-  return run(launch_tree(sp, tp, bf16, greedy, stream));
+  return run(launch_tree(sp, tp, bf16, greedy, a->consulted_only != 0, stream));
 }
 
 spec_status spec_verify_cascade(const spec_cascade_args* a, cudaStream_t stream) {

@@ -57,22 +57,16 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 inline size_t workspace_bytes(int B, int rows_per_seq, int V) {
   return align256(static_cast<size_t>(B) * rows_per_seq * stats_chunks(V, false) * 8);
 }
-// Chain workspace: the partials, then the consulted-only mode's counters
-// (B x gamma) and first-rejection words (B).
-inline size_t chain_ctl_bytes(int B, int gamma) { return align256(static_cast<size_t>(B) * (gamma + 1) * 4); }
+// Chain workspace: the partials (the consulted-only mode uses none).
 inline size_t chain_workspace_bytes(int B, int gamma, int rows_per_seq, int V) {
-  return workspace_bytes(B, rows_per_seq, V) + chain_ctl_bytes(B, gamma);
+  (void)gamma;
+  return workspace_bytes(B, rows_per_seq, V);
 }
 
 
 struct ChainParams {
   int B, gamma, V;
   long long ld;
-  // consulted-only mode (null otherwise): per (sequence, position) count of
-  // statistics chunks done, and per sequence gamma + 1 - (first position
-  // found rejected), 0 while none; both zeroed at the start of the call
-  unsigned* count;
-  int* skip;
   const void* target;
   const void* draft;
   const int* tokens;
@@ -163,9 +157,12 @@ cudaError_t launch_pipeline(const StatsParams& g, const PipelineParams& p, bool 
 
 // `grouped` allows a large call to be split into batch groups on library
 // streams (forked from and joined into s); false keeps every launch on s.
+// `consulted` runs the consulted-only walk (no statistics kernel).
 cudaError_t launch_chain(const StatsParams& g, const ChainParams& p, bool bf16, bool greedy, bool grouped,
-                         cudaStream_t s);
-cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s);
+                         bool consulted, cudaStream_t s);
+// `consulted` runs the consulted-only tree walk (no statistics kernel).
+cudaError_t launch_tree(const StatsParams& g, const TreeParams& p, bool bf16, bool greedy, bool consulted,
+                        cudaStream_t s);
 cudaError_t launch_cascade(const StatsParams& g, const CascadeParams& p, bool bf16, bool greedy,
                            cudaStream_t s);
 // The chain walk alone over float32 logit rows whose chunk partials a

@@ -62,10 +62,9 @@ extern "C" spec_status spec_verify_chain_noalloc(const spec_chain_args* args, cu
     return SPEC_EWORKSPACE;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return SPEC_ECUDA;
-  // The statistics partials in the scratch are written before they are
-  // read; the consulted-only mode's control words, which must start at zero,
-  // are cleared by the call itself (one memset on `stream`), so nothing a
-  // previous call left behind is ever read.
+  // The scratch holds only the statistics partials, which a call writes
+  // before it reads them (the consulted-only mode uses none), so nothing a
+  // previous call left behind is ever read and nothing needs clearing.
   spec_chain_args a = *args;
   a.workspace = scratch;
   a.workspace_bytes = SPEC_NOALLOC_SCRATCH_BYTES;

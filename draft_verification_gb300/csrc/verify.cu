@@ -23,9 +23,9 @@
 //
 // Variants: large sampling chains run as batch groups (several statistics
 // and walk launches on forked library streams); the consulted-only chain
-// mode replaces the statistics kernel by stats_consulted_kernel (positions
-// in order, later positions of a rejected sequence skipped) after clearing
-// its control words with one memset.
+// mode is one kernel, chain_consulted_kernel, whose clusters compute the
+// statistics of each position's rows themselves, in position order, and stop
+// at the first rejection.
 //
 // Rules (pages: the Pith review of PipeSpec, "What carries the argument" and
 // the acceptance rule of Leviathan et al. its Circularity Check cites; Staged
@@ -58,9 +58,7 @@ namespace sv {
 namespace {
 
 constexpr int kMaxGamma = 32;
-constexpr int kMaxDecisionChunks = 256;  // statistics chunks of the longest row (2^21 float32 logits)
 
-__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
 // Test hook (spec_test_inject_copy_timeout): nonzero makes every bulk-copy
 // wait of a residual or bonus pass (ring stage or resident slice) expect 16
@@ -193,49 +191,6 @@ __global__ void __launch_bounds__(kStatsThreads, 5) stats_kernel(const StatsPara
   stats_unit<T, kGreedy>(stats_row<T>(G, b, r), G.V, k, G.c, out, sm);
 }
 
-// Consulted-only statistics of a sampling chain (grid (2 C, B, gamma + 1):
-// chunk and row kind fastest, then the sequence, then the position, so
-// position t of every sequence comes before position t + 1 of any).  A CTA
-// of position t skips its chunk when an earlier position of its sequence has
-// been found rejected.  The CTA that completes both rows of position t
-// (the count of its 2 C chunks) merges them in chunk order and runs the
-// position's accept test exactly as the walk does; a rejection (or a row
-// that is not finite, or a token out of range, which end the consulted
-// prefix too) records gamma + 1 - t in P.skip[b] (the largest record is the
-// first position).
-template <typename T>
-__global__ void __launch_bounds__(kStatsThreads, 5) stats_consulted_kernel(const StatsParams G, const ChainParams P) {
-  pdl_launch_dependents();
-  __shared__ StatsSmem sm;
-  __shared__ float2 dpart[2][kMaxDecisionChunks];
-  const int C = G.chunks, g = P.gamma;
-  const int t = blockIdx.z, b = blockIdx.y, half = blockIdx.x / C, k = blockIdx.x - half * C;
-  if (t == g && half == 1) return;  // no draft row at the bonus position
-  if (ld_volatile(P.skip + b) > g + 1 - t) return;  // a position before t was rejected
-  const int r = half == 0 ? t : g + 1 + t;
-  float2* part = G.partials + (static_cast<long long>(b) * G.rows_per_seq) * C;
-  stats_unit<T, false>(stats_row<T>(G, b, r), G.V, k, G.c, part + static_cast<long long>(r) * C + k, sm);
-  if (t == g || threadIdx.x != 0) return;
-  __threadfence();
-  if (atomicAdd(P.count + static_cast<long long>(b) * g + t, 1u) != static_cast<unsigned>(2 * C - 1)) return;
-  __threadfence();
-  // the last chunk of position t: merge both rows and test the position
-  for (int q = 0; q < C; ++q) {
-    dpart[0][q] = __ldcg(part + static_cast<long long>(t) * C + q);
-    dpart[1][q] = __ldcg(part + static_cast<long long>(g + 1 + t) * C + q);
-  }
-  const MaxSum mp = combine_row(dpart[0], C, G.c), mq = combine_row(dpart[1], C, G.c);
-  const int tok = P.tokens[static_cast<long long>(b) * g + t];
-  bool stop = !row_stats_ok(mp) || !row_stats_ok(mq) || tok < 0 || tok >= P.V;
-  if (!stop) {
-    const T* trow = static_cast<const T*>(P.target) + (static_cast<long long>(b) * (g + 1) + t) * P.ld;
-    const T* drow = static_cast<const T*>(P.draft) + (static_cast<long long>(b) * g + t) * P.ld;
-    stop = !keeps(P.u[static_cast<long long>(b) * g + t],
-                  ratio(load_elem(trow + tok), mp.m, mp.s, load_elem(drow + tok), mq.m, mq.s, G.c));
-  }
-  if (stop) atomicMax(P.skip + b, g + 1 - t);
-}
-
 // ===========================================================================
 // 2a. chain
 // ===========================================================================
@@ -342,24 +297,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   cluster_enter();
   chain_inputs<T>(P, b, cs, true);
   pdl_wait();  // the statistics are complete and visible from here on
-  // consulted-only mode: the first rejected position was found by the
-  // statistics kernel; only rows up to it (and the bonus row when there is
-  // none) were read and are merged and checked
-  const int rec = P.skip ? ld_volatile(P.skip + b) : 0;
-  const int first = rec > 0 ? g + 1 - rec : g;
-  int err;
-  if (P.skip) {
-    merge_stats<false>(G, b, stage, [&](int r, float2 v, bool ok) {
-      const bool read = r <= g ? r <= first : r - (g + 1) <= first;
-      if (!read) return;
-      cs.st_m[r] = v.x;
-      cs.st_s[r] = v.y;
-      if (!ok) atomicOr(&cs.err, SPEC_ERR_NONFINITE);
-    });
-    err = cs.err;
-  } else {
-    err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
-  }
+  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
   cluster_ready();
   if (err) {  // every CTA of the cluster sees the same error; the lead reports it
     if (lead) chain_error_out(P, b, err);
@@ -367,20 +305,16 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   }
   if (warp == 0) {
     bool keep = true;
-    const int tested = P.skip ? min(g, first + 1) : g;  // positions whose rows were read
-    if (lane < tested) {
+    if (lane < g) {
       const float mq = cs.st_m[g + 1 + lane], sq = cs.st_s[g + 1 + lane];
       keep = keeps(cs.u[lane], ratio(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], cs.gq[lane], mq, sq, c));
       if (lead) {
         if (P.p_at) P.p_at[drow0 + lane] = prob(cs.gp[lane], cs.st_m[lane], cs.st_s[lane], c);
         if (P.q_at) P.q_at[drow0 + lane] = prob(cs.gq[lane], mq, sq, c);
       }
-    } else if (lane < g && lead) {
-      if (P.p_at) P.p_at[drow0 + lane] = __int_as_float(0x7fc00000);
-      if (P.q_at) P.q_at[drow0 + lane] = __int_as_float(0x7fc00000);
     }
-    const unsigned rej = __ballot_sync(0xffffffffu, lane < tested && !keep);
-    if (lane == 0) cs.a = rej ? __ffs(rej) - 1 : (P.skip ? first : g);
+    const unsigned rej = __ballot_sync(0xffffffffu, lane < g && !keep);
+    if (lane == 0) cs.a = rej ? __ffs(rej) - 1 : g;
   }
   __syncthreads();
   const int a = cs.a;
@@ -429,6 +363,90 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
     if (P.resid) P.resid[b] = df_float(Z);
     if (P.seq_error) P.seq_error[b] = flag;
     if (flag && P.error_word) atomicOr(P.error_word, flag);
+  }
+}
+
+// Consulted-only sampling chain (PipeSpec review, "What carries the
+// argument": the tokens after the first mismatch are rolled back unused):
+// one cluster per sequence walks the positions in order and computes each
+// position's row statistics itself, so rows after the first rejection are
+// never read.  At position i every CTA streams its slice of target row i and
+// draft row i, the cluster shares the (max, sum) partials and merges them in
+// rank order, and the accept test runs on the merged statistics; a
+// rejection is followed by the residual pass over the same two rows and the
+// draw; when every draft is kept, the bonus row gamma gets its statistics
+// and the draw.  No statistics kernel and no workspace.  Grid (S, B).
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 4) chain_consulted_kernel(const StatsParams G, const ChainParams P) {
+  __shared__ ChainSmem cs;
+  __shared__ PassSmem ps;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int g = P.gamma;
+  const float c = G.c;
+  const bool lead = cluster_rank() == 0;
+  const T* target = static_cast<const T*>(P.target);
+  const T* draft = static_cast<const T*>(P.draft);
+  const long long trow0 = static_cast<long long>(b) * (g + 1);
+  const long long drow0 = static_cast<long long>(b) * g;
+  const int ncl = static_cast<int>(cluster_size());
+  const int tpc = (G.ntiles + ncl - 1) / ncl;
+  const int t0 = min(G.ntiles, static_cast<int>(cluster_rank()) * tpc), t1 = min(G.ntiles, t0 + tpc);
+
+  pass_begin(ps);
+  cluster_enter();
+  chain_inputs<T>(P, b, cs, true);
+  cluster_ready();
+  __syncthreads();
+  if (cs.err) {  // a drafted token out of range: nothing is consulted
+    if (lead) chain_error_out(P, b, cs.err);
+    return;
+  }
+  for (int i = 0;; ++i) {
+    const bool bonus = i == g;
+    const T* prow = target + (trow0 + i) * P.ld;
+    const T* qrow = bonus ? nullptr : draft + (drow0 + i) * P.ld;
+    MaxSum part[2];
+    streamed_row_stats<T>(prow, qrow, G.V, c, t0, t1, ps, part);
+    const int xb = cluster_share4(part[0].m, part[0].s, part[1].m, part[1].s, ps);
+    MaxSum st[2];
+    merge_shared_ms2(xb, c, ps, st);
+    const bool bad = !row_stats_ok(st[0]) || (!bonus && !row_stats_ok(st[1]));
+    if (bad) {
+      if (lead) chain_error_out(P, b, SPEC_ERR_NONFINITE);
+      return;
+    }
+    bool keep = true;
+    if (!bonus) {
+      keep = keeps(cs.u[i], ratio(cs.gp[i], st[0].m, st[0].s, cs.gq[i], st[1].m, st[1].s, c));
+      if (lead && tid == 0) {
+        if (P.p_at) P.p_at[drow0 + i] = prob(cs.gp[i], st[0].m, st[0].s, c);
+        if (P.q_at) P.q_at[drow0 + i] = prob(cs.gq[i], st[1].m, st[1].s, c);
+      }
+    }
+    if (!bonus && keep) continue;
+    // position i: the residual after a rejection, or the bonus row
+    const int a = i;
+    if (lead && tid < g && tid > a) {  // positions never consulted
+      if (P.p_at) P.p_at[drow0 + tid] = __int_as_float(0x7fc00000);
+      if (P.q_at) P.q_at[drow0 + tid] = __int_as_float(0x7fc00000);
+    }
+    PassSpec<T> S = make_spec(prow, st[0].m, st[0].s, qrow, bonus ? 0.f : st[1].m, bonus ? 1.f : st[1].s, 1.f, c);
+    int buf = 0, flag = 0;
+    const DF Z = pass_or_fallback(S, G.V, c, G.ntiles, &buf, &flag, ps);
+    const int y = cluster_draw(S, G.V, c, G.ntiles, buf, df_mul_f(Z, cs.v), false, ps);
+    if (y < 0) return;  // another CTA of the cluster holds the drawn tile
+    if (ps.fault) flag |= SPEC_ERR_INTERNAL;
+    if (tid == 0) {
+      const bool ok = !(flag & SPEC_ERR_INTERNAL);
+      P.accept_len[b] = ok ? a : 0;
+      P.out_token[b] = ok ? y : -1;
+      if (P.rollback) P.rollback[b] = (P.prefix ? P.prefix[b] : 0) + (ok ? a : 0);
+      if (P.resid) P.resid[b] = ok ? df_float(Z) : 0.f;
+      if (P.seq_error) P.seq_error[b] = flag;
+      if (flag && P.error_word) atomicOr(P.error_word, flag);
+    }
+    return;
   }
 }
 
@@ -847,10 +865,17 @@ __device__ int list_children(const int* par, int N, int node, int* kids, int* co
   return *count_s;
 }
 
-template <typename T, bool kGreedy>
+// kConsulted (Staged Speculative Decoding, abstract: the walk keeps one
+// child per level; PipeSpec review, "What carries the argument": tokens after
+// the first mismatch are never used): no statistics kernel; the cluster
+// computes the statistics of node n's rows when the walk stands at n (the
+// target row, and in sampling mode the draft row when n has children), so
+// rows of nodes off the walked path are never read.  Sampling and greedy
+// both run as clusters with the stage region.
+template <typename T, bool kGreedy, bool kConsulted>
 __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, const TreeParams P) {
   __shared__ PassSmem ps;
-  __shared__ float2 stage[kStage];
+  __shared__ float2 stage[kConsulted ? 1 : kStage];
   __shared__ int err_s, nk_s, keep_s;
   __shared__ float v_s;
   const int b = blockIdx.y;
@@ -858,7 +883,8 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   const int N = P.N;
   const float c = G.c;
   const bool lead = cluster_rank() == 0;
-  TreeSmem ts = tree_smem(reinterpret_cast<char*>(dyn_smem + (kGreedy ? 0 : kStageBytes)), N);
+  constexpr bool kStageRegion = !kGreedy || kConsulted;
+  TreeSmem ts = tree_smem(reinterpret_cast<char*>(dyn_smem + (kStageRegion ? kStageBytes : 0)), N);
   const long long row0 = static_cast<long long>(b) * N;
 
   pass_begin(ps);
@@ -919,11 +945,16 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
       if (tid == 0) v_s = P.v[b];
     }
   }
-  pdl_wait();
-  merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
-    ts.st[r] = v;
-    if (!ok) atomicOr(&err_s, SPEC_ERR_NONFINITE);
-  });
+  if constexpr (!kConsulted) {
+    pdl_wait();
+    merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
+      ts.st[r] = v;
+      if (!ok) atomicOr(&err_s, SPEC_ERR_NONFINITE);
+    });
+  } else {
+    (void)stage;
+    __syncthreads();
+  }
   cluster_ready();
 
   const int err = err_s;
@@ -956,11 +987,74 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   const int tpc = (G.ntiles + ncl - 1) / ncl;
   const int t0 = min(G.ntiles, static_cast<int>(cluster_rank()) * tpc), t1 = min(G.ntiles, t0 + tpc);
   const bool res_ok = !kGreedy && slice_fits<T>(tpc);
+  // greedy consulted: the target row alone is resident when it fits
+  const bool res_one = kGreedy && kConsulted && static_cast<size_t>(tpc) * kTileElems * sizeof(T) <= kStageBytes &&
+                       tpc <= kResidentTiles;
   while (true) {
     const int nk = list_children(ts.par, N, node, kids, &nk_s);
-    if (!kGreedy && res_ok && tid < nk) {
+    // the statistics of node's rows: from the statistics kernel, or computed
+    // here (consulted-only) for the rows the walk reads at this node
+    float2 sp_node{0.f, 0.f}, sq_node{0.f, 0.f};
+    int best_node = -1;
+    bool resident_entry = false;
+    if constexpr (kConsulted) {
+      const T* prow = static_cast<const T*>(P.target) + (row0 + node) * P.ld;
+      const T* qrow = static_cast<const T*>(P.draft) + (row0 + node) * P.ld;
+      bool bad = false;
+      if constexpr (kGreedy) {
+        ArgMax am;
+        bool lbad = false;
+        if (res_one) {
+          PassSpec<T> L = make_spec(prow, 0.f, 1.f, static_cast<const T*>(nullptr), 0.f, 1.f, 0.f, 1.f);
+          slice_load(L, false, P.V, t0, t1, ps);
+          am = resident_row_argmax<T>(t0, t1 - t0, ps, &lbad);
+        } else {
+          am = direct_row_argmax<T>(prow, P.V, t0, t1, ps, &lbad);
+        }
+        const int xb = cluster_share4(am.v, __int_as_float(am.i), lbad ? 1.f : 0.f, 0.f, ps);
+        const ArgMax all = merge_shared_argmax(xb, ps, &bad);
+        bad |= all.i < 0;
+        best_node = all.i;
+      } else {
+        const bool with_q = nk > 0;
+        MaxSum part[2];
+        if (res_ok) {
+          PassSpec<T> L = make_spec(prow, 0.f, 1.f, with_q ? qrow : static_cast<const T*>(nullptr), 0.f, 1.f, 1.f, c);
+          slice_load(L, with_q, P.V, t0, t1, ps);
+          resident_entry = true;
+          resident_row_stats<T>(with_q, t1 - t0, c, ps, part);
+        } else {
+          streamed_row_stats<T>(prow, with_q ? qrow : nullptr, P.V, c, t0, t1, ps, part);
+        }
+        const int xb = cluster_share4(part[0].m, part[0].s, part[1].m, part[1].s, ps);
+        MaxSum st2[2];
+        merge_shared_ms2(xb, c, ps, st2);
+        bad = !row_stats_ok(st2[0]) || (with_q && !row_stats_ok(st2[1]));
+        sp_node = make_float2(st2[0].m, st2[0].s);
+        sq_node = make_float2(st2[1].m, st2[1].s);
+      }
+      if (bad) {  // a row the walk reads is not finite: empty outputs
+        if (lead) {
+          if (tid == 0) {
+            P.path_len[b] = 0;
+            P.out_token[b] = -1;
+            if (P.rollback) P.rollback[b] = prefix;
+            if (P.seq_error) P.seq_error[b] = SPEC_ERR_NONFINITE;
+            if (P.error_word) atomicOr(P.error_word, SPEC_ERR_NONFINITE);
+          }
+          for (int q = tid; q < pn; q += kThreads) pnodes[q] = -1;
+        }
+        return;
+      }
+    } else {
+      sp_node = ts.st[node];
+      sq_node = ts.st[N + node];
+      best_node = __float_as_int(ts.st[node].y);
+    }
+    if (!kGreedy && !kConsulted && res_ok && tid < nk) {
       // whichever child is kept next, its rows' slice of this CTA will come
       // from L2: hint the bulk-copy engine to bring every child's in now
+      // (not in consulted-only mode, which reads no row off the path)
       const int ch = kids[tid];
       const T* cp = target + (row0 + ch) * P.ld;
       const T* cq = draft + (row0 + ch) * P.ld;
@@ -972,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
       }
     }
     if constexpr (kGreedy) {
-      const int best = __float_as_int(ts.st[node].y);
+      const int best = best_node;
       int kept = -1;
       for (int q = 0; q < nk; ++q)
         if (ts.tk[kids[q]] == best) {
@@ -988,15 +1082,15 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
       ++plen;
       node = kept;
     } else {
-      const float2 sp = ts.st[node];
-      const float2 sq = ts.st[N + node];
+      const float2 sp = sp_node;
+      const float2 sq = sq_node;
       PassSpec<T> S = make_spec(target + (row0 + node) * P.ld, sp.x, sp.y, draft + (row0 + node) * P.ld, sq.x,
                                 sq.y, 1.f, c);
       S.cq = 0.f;
       double cc = 0.0, W = 1.0;
       DF Wdf{1.f, 0.f};
       int kept = -1;
-      bool zero_mass = false, resident = false;
+      bool zero_mass = false, resident = resident_entry;
       for (int q = 0; q < nk; ++q) {
         const int ch = kids[q];
         if (tid == 0) {
@@ -1225,55 +1319,26 @@ cudaError_t launch_walk(K kernel, size_t dyn, size_t occupancy_dyn, const StatsP
   return launch_dependent(kernel, dim3(S, G.B), S, dyn, G, args, s, rank, pdl);
 }
 
-// The resident-slice chain walk: the largest cluster S <= 8 (at most one
-// CTA per tile) whose slices fit in kMaxResidentBytes and for which all B
-// clusters fit in 7/8 of the resident clusters at that slice size; the staged
-// walk when none does.
-constexpr size_t kMaxResidentBytes = 96 * 1024;
+// The resident-slice chain walk, used when the cluster the staged walk would
+// get (same occupancy rule, same dynamic shared memory) holds its slices in
+// the stage region; otherwise the staged walk.  A larger resident region was
+// measured: alone, a 64 KB slice per CTA (V = 128256, clusters of 8) made the
+// walk faster (18.3 against 21.6 us), but as the last of four batch groups
+// the call took 54.7 instead of 44.6 us: clusters of CTAs that large are
+// placed late beside the other groups' statistics and walks.
 
 template <typename T>
 cudaError_t launch_chain_walk_resident(const StatsParams& G, const ChainParams& args, cudaStream_t s, int rank) {
   const void* fn = reinterpret_cast<const void*>(chain_walk_kernel<T, true>);
-  static std::mutex mu;
-  static std::map<std::tuple<const void*, int, int, int>, int> fits;  // (fn, dev, S, dyn) -> clusters
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_limit(fn, kStageBytes);
   if (e != cudaSuccess) return e;
-  for (int S = 8; S >= 1; S >>= 1) {
-    if (S > G.ntiles) continue;
-    const int tpc = (G.ntiles + S - 1) / S;
-    const size_t dyn = slice_bytes<T>(tpc);
-    if (tpc > kResidentTiles || dyn > kMaxResidentBytes) break;  // smaller clusters only need more
-    e = smem_limit(fn, static_cast<int>(kMaxResidentBytes));
-    if (e != cudaSuccess) return e;
-    int count = 0;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      auto key = std::make_tuple(fn, dev, S, static_cast<int>(dyn));
-      auto it = fits.find(key);
-      if (it != fits.end()) {
-        count = it->second;
-      } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(S, 1, 1);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = dyn;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = S;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&count, fn, &cfg) != cudaSuccess) {
-          cudaGetLastError();
-          count = 0;
-        }
-        fits[key] = count;
-      }
-    }
-    if (8 * G.B <= 7 * count) return launch_dependent(chain_walk_kernel<T, true>, dim3(S, G.B), S, dyn, G, args, s, rank);
-  }
+  std::array<int, 4> resident;
+  e = resident_clusters(fn, kStageBytes, &resident);
+  if (e != cudaSuccess) return e;
+  const int S = cluster_for(resident, G.B, G.ntiles);
+  if (slice_bytes<T>((G.ntiles + S - 1) / S) <= static_cast<size_t>(kStageBytes) &&
+      (G.ntiles + S - 1) / S <= kResidentTiles)
+    return launch_dependent(chain_walk_kernel<T, true>, dim3(S, G.B), S, kStageBytes, G, args, s, rank);
   return launch_walk(chain_walk_kernel<T, false>, kStageBytes, kStageBytes, G, args, s, rank);
 }
 
@@ -1439,19 +1504,13 @@ cudaError_t chain_one(const StatsParams& G, const ChainParams& p, bool greedy, c
 
 template <typename T>
 cudaError_t chain_consulted(const StatsParams& G, const ChainParams& p, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * G.chunks, G.B, p.gamma + 1);
-  cfg.blockDim = dim3(kStatsThreads);
-  cfg.stream = s;
-  void* argv[] = {const_cast<StatsParams*>(&G), const_cast<ChainParams*>(&p)};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(stats_consulted_kernel<T>), argv);
-  if (e != cudaSuccess) return e;
-  return launch_walk(chain_walk_kernel<T, false>, kStageBytes, kStageBytes, G, p, s);
+  return launch_walk(chain_consulted_kernel<T>, kStageBytes, kStageBytes, G, p, s);
 }
 
 template <typename T>
-cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, bool grouped, cudaStream_t s) {
-  if (p.skip) return chain_consulted<T>(G, p, s);
+cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, bool grouped, bool consulted,
+                       cudaStream_t s) {
+  if (consulted) return chain_consulted<T>(G, p, s);
   const Groups gr = plan_groups(G.B, logit_bytes(G, sizeof(T)));
   if (!grouped || gr.n == 1) return chain_one<T>(G, p, greedy, s, -1, true);
   return run_groups(gr, s, [&](int i, cudaStream_t si) {
@@ -1461,18 +1520,22 @@ cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, 
 }
 
 template <typename T>
-cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, cudaStream_t s) {
+cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, bool consulted, cudaStream_t s) {
+  const size_t nodes = static_cast<size_t>(kTreeSmemPerNode) * p.N;
+  // occupancy is evaluated once, at the largest tree's shared memory
+  const size_t most = static_cast<size_t>(kStageBytes) + static_cast<size_t>(kTreeSmemPerNode) * kMaxNodes;
+  if (consulted) {  // one kernel: the walk computes the statistics it reads
+    if (greedy) return launch_walk(tree_kernel<T, true, true>, kStageBytes + nodes, most, G, p, s);
+    return launch_walk(tree_kernel<T, false, true>, kStageBytes + nodes, most, G, p, s);
+  }
   cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
   if (e != cudaSuccess) return e;
-  const size_t nodes = static_cast<size_t>(kTreeSmemPerNode) * p.N;
   if (greedy) {
-    e = smem_limit(reinterpret_cast<const void*>(tree_kernel<T, true>), kTreeSmemPerNode * kMaxNodes);
+    e = smem_limit(reinterpret_cast<const void*>(tree_kernel<T, true, false>), kTreeSmemPerNode * kMaxNodes);
     if (e != cudaSuccess) return e;
-    return launch_dependent(tree_kernel<T, true>, dim3(1, G.B), 0, nodes, G, p, s);
+    return launch_dependent(tree_kernel<T, true, false>, dim3(1, G.B), 0, nodes, G, p, s);
   }
-  // occupancy is evaluated once, at the largest tree's shared memory
-  return launch_walk(tree_kernel<T, false>, kStageBytes + nodes,
-                     static_cast<size_t>(kStageBytes) + static_cast<size_t>(kTreeSmemPerNode) * kMaxNodes, G, p, s);
+  return launch_walk(tree_kernel<T, false, false>, kStageBytes + nodes, most, G, p, s);
 }
 
 template <typename T>
@@ -1514,12 +1577,14 @@ int stats_chunks(int V, bool bf16) {
 int pass_tiles(int V) { return (V + kTileElems - 1) / kTileElems; }
 
 cudaError_t launch_chain(const StatsParams& G, const ChainParams& p, bool bf16, bool greedy, bool grouped,
-                         cudaStream_t s) {
-  return bf16 ? chain_impl<bf16_t>(G, p, greedy, grouped, s) : chain_impl<float>(G, p, greedy, grouped, s);
+                         bool consulted, cudaStream_t s) {
+  return bf16 ? chain_impl<bf16_t>(G, p, greedy, grouped, consulted, s)
+              : chain_impl<float>(G, p, greedy, grouped, consulted, s);
 }
 
-cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bool greedy, cudaStream_t s) {
-  return bf16 ? tree_impl<bf16_t>(G, p, greedy, s) : tree_impl<float>(G, p, greedy, s);
+cudaError_t launch_tree(const StatsParams& G, const TreeParams& p, bool bf16, bool greedy, bool consulted,
+                        cudaStream_t s) {
+  return bf16 ? tree_impl<bf16_t>(G, p, greedy, consulted, s) : tree_impl<float>(G, p, greedy, consulted, s);
 }
 
 cudaError_t launch_cascade(const StatsParams& G, const CascadeParams& p, bool bf16, bool greedy, cudaStream_t s) {

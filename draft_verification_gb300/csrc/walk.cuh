@@ -257,6 +257,8 @@ struct PassSmem {
   int staged;               // stages issued by earlier passes of this kernel
   int exchanges;            // exchanges completed by earlier passes
   int flt[kMaxCluster];     // fault state of each CTA of the cluster
+  float xv[2][kMaxCluster][4];  // per-CTA values shared across the cluster (double-buffered)
+  float red[2][kWarps][2];      // per-warp (max, sum) of two rows (block reductions)
   int fault;                // a bulk copy here or in a peer did not complete
   float rf;                 // target minus the prefix before the drawn tile
   int owner;                // CTA whose slice holds the drawn tile
@@ -824,6 +826,303 @@ __device__ int cluster_draw(const PassSpec<T>& S, int V, float c, int ntiles, in
     return draw_in_tile(S, V, c, sh, t0, t1 - t0);
   }
   return draw_in_tile(S, V, c, sh);
+}
+
+// ---------------------------------------------------------------------------
+// row statistics computed by the walk itself (consulted-only mode): each CTA
+// of the cluster reduces its slice of a row pair to (max, sum of
+// 2^(x c - M)) or, greedy, to (max, first index); the cluster shares the
+// partials and merges them in rank order, so every CTA holds the same bits
+// ---------------------------------------------------------------------------
+// Fold 8 logits into a running (max, sum): the sum is rescaled to the new
+// maximum once per 8 elements.  NaN propagates into the maximum and +inf
+// makes it infinite, so such a row fails row_stats_ok.
+__device__ __forceinline__ void online8(const float* x, float c, float& m, float& s) {
+  float cm = x[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) cm = fmax_nan(cm, x[e]);
+  const float mn = fmax_nan(m, cm);
+  if (mn == -kInf) return;
+  const float M = scaled_max(mn, c);
+  float acc = (m == -kInf) ? 0.f : __fmul_rn(s, ex2(scaled_max(m, c) - M));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc = __fadd_rn(acc, weight(x[e], c, M));
+  s = acc;
+  m = mn;
+}
+
+// Greedy counterpart: the first index of the maximum (-inf never wins) and
+// whether a NaN or +inf was seen.
+__device__ __forceinline__ void argmax8(const float* x, int e0, float& best, int& bi, bool& bad) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    bad |= !(x[e] < kInf);
+    if (x[e] > best) {
+      best = x[e];
+      bi = e0 + e;
+    }
+  }
+}
+
+// Block reduction of per-thread (max, sum) of two rows into out[0..1] (all
+// threads get the result).
+__device__ __forceinline__ void block_ms2(MaxSum a, MaxSum b, float c, PassSmem& sh, MaxSum* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = ms_warp_reduce(a, c);
+  b = ms_warp_reduce(b, c);
+  if (lane == 0) {
+    sh.red[0][warp][0] = a.m;
+    sh.red[0][warp][1] = a.s;
+    sh.red[1][warp][0] = b.m;
+    sh.red[1][warp][1] = b.s;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    MaxSum t{-kInf, 0.f};
+    for (int w = 0; w < kWarps; ++w) t = ms_merge(t, MaxSum{sh.red[r][w][0], sh.red[r][w][1]}, c);
+    out[r] = t;
+  }
+  __syncthreads();
+}
+
+// Block argmax (lowest index on ties) of one row; bad if any thread saw a
+// NaN or +inf.  out = (value, index), index -1 for a row without a finite
+// maximum.
+__device__ __forceinline__ ArgMax block_argmax(float best, int bi, bool bad, PassSmem& sh, bool* any_bad) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ArgMax t = am_warp_reduce(ArgMax{best, bi});
+  const bool wb = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sh.red[0][warp][0] = t.v;
+    sh.red[0][warp][1] = __int_as_float(t.i);
+    sh.red[1][warp][0] = wb ? 1.f : 0.f;
+  }
+  __syncthreads();
+  ArgMax r{-kInf, -1};
+  bool b = false;
+  for (int w = 0; w < kWarps; ++w) {
+    r = am_merge(r, ArgMax{sh.red[0][w][0], __float_as_int(sh.red[0][w][1])});
+    b |= sh.red[1][w][0] != 0.f;
+  }
+  __syncthreads();
+  *any_bad = b;
+  return r;
+}
+
+// This CTA's (max, sum) of tiles [t0, t1) of rows P and Q (Q may be null)
+// from its resident slice (slice_load's layout, nt = t1 - t0 tiles).
+template <typename T>
+__device__ void resident_row_stats(bool with_q, int nt, float c, PassSmem& sh, MaxSum* out) {
+  const unsigned char* qbuf = dyn_smem + static_cast<size_t>(nt) * kTileElems * sizeof(T);
+  float mp = -kInf, sp = 0.f, mq = -kInf, sq = 0.f;
+  for (int j = 0; j < nt; ++j) {
+    float x[8];
+    slice_get8<T>(dyn_smem, j, x);
+    online8(x, c, mp, sp);
+    if (with_q) {
+      slice_get8<T>(qbuf, j, x);
+      online8(x, c, mq, sq);
+    }
+  }
+  block_ms2(MaxSum{mp, sp}, MaxSum{mq, sq}, c, sh, out);
+}
+
+// Greedy counterpart over the resident target slice (first tile t0).
+template <typename T>
+__device__ ArgMax resident_row_argmax(int t0, int nt, PassSmem& sh, bool* bad) {
+  float best = -kInf;
+  int bi = -1;
+  bool b = false;
+  for (int j = 0; j < nt; ++j) {
+    float x[8];
+    slice_get8<T>(dyn_smem, j, x);
+    argmax8(x, (t0 + j) * kTileElems + 8 * static_cast<int>(threadIdx.x), best, bi, b);
+  }
+  return block_argmax(best, bi, b, sh, bad);
+}
+
+// This CTA's (max, sum) of tiles [t0, t1) of rows P and Q (Q may be null)
+// streamed from global memory through the stage ring (aligned rows) or by
+// plain loads (misaligned rows); the same stage counters as the passes.
+template <typename T>
+__device__ void streamed_row_stats(const T* P, const T* Q, int V, float c, int t0, int t1, PassSmem& sh,
+                                   MaxSum* out) {
+  constexpr int TPS = kStageRowBytes / (kTileElems * static_cast<int>(sizeof(T)));
+  constexpr int R = Load8<T>::kRegs;
+  const int tid = threadIdx.x;
+  const bool useQ = Q != nullptr;
+  float mp = -kInf, sp = 0.f, mq = -kInf, sq = 0.f;
+  const bool aligned = row_is_aligned(P) && (!useQ || row_is_aligned(Q));
+  if (!aligned) {
+    for (int t = t0; t < t1; ++t) {
+      float x[8];
+      const int e0 = t * kTileElems + 8 * tid;
+      load8_misaligned(P, e0, V, x);
+      online8(x, c, mp, sp);
+      if (useQ) {
+        load8_misaligned(Q, e0, V, x);
+        online8(x, c, mq, sq);
+      }
+    }
+    block_ms2(MaxSum{mp, sp}, MaxSum{mq, sq}, c, sh, out);
+    return;
+  }
+  const int nst = (t1 - t0 + TPS - 1) / TPS;
+  const int g0 = sh.staged;
+  const int Vv = vector_end<T>(V);
+  auto issue = [&](int k) {  // thread 0
+    const int ta = t0 + k * TPS, te = min(t1, ta + TPS);
+    const unsigned bytes = static_cast<unsigned>((min(te * kTileElems, Vv) - ta * kTileElems) * sizeof(T));
+    const int b = (g0 + k) % kStages;
+    unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
+    mbar_expect_tx(&sh.bar[b], useQ ? 2 * bytes : bytes);
+    if (bytes == 0) return;
+    bulk_load(buf, P + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
+    if (useQ) bulk_load(buf + kStageRowBytes, Q + static_cast<long long>(ta) * kTileElems, bytes, &sh.bar[b]);
+  };
+  __syncthreads();  // earlier users of the stage region are done with it
+  if (tid == 0) {
+    fence_proxy_async();
+    for (int k = 0; k < min(kStages, nst); ++k) issue(k);
+  }
+  __syncthreads();
+  bool fault = false;
+  for (int k = 0; k < nst; ++k) {
+    const int ta = t0 + k * TPS, nb = min(TPS, t1 - ta);
+    const int b = (g0 + k) % kStages;
+    const unsigned char* buf = dyn_smem + b * 2 * kStageRowBytes;
+    if (!mbar_wait(&sh.bar[b], ((g0 + k) / kStages) & 1)) fault = true;
+#pragma unroll
+    for (int j = 0; j < TPS; ++j) {
+      if (j < nb) {
+        float x[8];
+        if ((ta + j + 1) * kTileElems <= Vv) {
+          uint32_t r[R];
+          stage_load8<T>(buf, j, r);
+          Load8<T>::get(r, x);
+          online8(x, c, mp, sp);
+          if (useQ) {
+            stage_load8<T>(buf + kStageRowBytes, j, r);
+            Load8<T>::get(r, x);
+            online8(x, c, mq, sq);
+          }
+        } else {
+          stage_load8_tail<T>(buf, j, P, ta + j, V, x);
+          online8(x, c, mp, sp);
+          if (useQ) {
+            stage_load8_tail<T>(buf + kStageRowBytes, j, Q, ta + j, V, x);
+            online8(x, c, mq, sq);
+          }
+        }
+      }
+    }
+    __syncthreads();  // buffer b is free
+    if (tid == 0 && k + kStages < nst) {
+      fence_proxy_async();
+      issue(k + kStages);
+    }
+  }
+  if (fault) {
+    for (int k = max(0, nst - kStages); k < nst; ++k)
+      mbar_wait(&sh.bar[(g0 + k) % kStages], ((g0 + k) / kStages) & 1);
+    sh.fault = 1;
+  }
+  if (tid == 0) sh.staged = g0 + nst;
+  block_ms2(MaxSum{mp, sp}, MaxSum{mq, sq}, c, sh, out);
+}
+
+// Share four floats per CTA across the cluster (asynchronous stores counted
+// on the receivers' exchange barriers, like a pass's tile sums).  Returns the
+// buffer of sh.xv that holds every CTA's values, indexed by rank.  Every CTA
+// of the cluster calls it, in the same sequence of exchanges as its passes.
+__device__ __forceinline__ int cluster_share4(float v0, float v1, float v2, float v3, PassSmem& sh) {
+  const int tid = threadIdx.x;
+  const int rank = static_cast<int>(cluster_rank()), n = static_cast<int>(cluster_size());
+  __syncthreads();  // sh.exchanges is current
+  const int x = sh.exchanges;
+  const int xb_i = x & 1;
+  if (tid == 0) {
+    sh.xv[xb_i][rank][0] = v0;
+    sh.xv[xb_i][rank][1] = v1;
+    sh.xv[xb_i][rank][2] = v2;
+    sh.xv[xb_i][rank][3] = v3;
+  }
+  if (n > 1) {
+    if (tid < 32) {
+      uint64_t* xb = &sh.xbar[xb_i];
+      if (tid == 0) {
+        mbar_expect_tx(xb, 20u * static_cast<unsigned>(n - 1));
+        sh.flt[rank] = sh.fault;
+      }
+      __syncwarp();
+      if (tid < n && tid != rank) {
+        const unsigned d = static_cast<unsigned>(tid);
+        st_async_cluster(&sh.xv[xb_i][rank][0], d, __float_as_uint(v0), xb);
+        st_async_cluster(&sh.xv[xb_i][rank][1], d, __float_as_uint(v1), xb);
+        st_async_cluster(&sh.xv[xb_i][rank][2], d, __float_as_uint(v2), xb);
+        st_async_cluster(&sh.xv[xb_i][rank][3], d, __float_as_uint(v3), xb);
+        st_async_cluster(&sh.flt[rank], d, static_cast<uint32_t>(sh.fault), xb);
+      }
+      if (!mbar_wait_cluster(xb, (x >> 1) & 1)) sh.fault = 1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int f = sh.fault;
+      for (int r = 0; r < n; ++r) f |= sh.flt[r];
+      sh.fault = f;
+      sh.exchanges = x + 1;
+    }
+  }
+  __syncthreads();
+  return xb_i;
+}
+
+// Merge the shared (max, sum) pairs of rows 0 and 1 in rank order.
+__device__ __forceinline__ void merge_shared_ms2(int xb_i, float c, PassSmem& sh, MaxSum* out) {
+  const int n = static_cast<int>(cluster_size());
+  MaxSum a{-kInf, 0.f}, b{-kInf, 0.f};
+  for (int r = 0; r < n; ++r) {
+    a = ms_merge(a, MaxSum{sh.xv[xb_i][r][0], sh.xv[xb_i][r][1]}, c);
+    b = ms_merge(b, MaxSum{sh.xv[xb_i][r][2], sh.xv[xb_i][r][3]}, c);
+  }
+  out[0] = a;
+  out[1] = b;
+}
+
+// Merge shared (value, index bits, bad flag) triples in rank order (lowest
+// index on ties).
+__device__ __forceinline__ ArgMax merge_shared_argmax(int xb_i, const PassSmem& sh, bool* bad) {
+  const int n = static_cast<int>(cluster_size());
+  ArgMax r{-kInf, -1};
+  bool b = false;
+  for (int k = 0; k < n; ++k) {
+    r = am_merge(r, ArgMax{sh.xv[xb_i][k][0], __float_as_int(sh.xv[xb_i][k][1])});
+    b |= sh.xv[xb_i][k][2] != 0.f;
+  }
+  *bad = b;
+  return r;
+}
+
+// Greedy: this CTA's argmax of tiles [t0, t1) of row P by plain loads.
+template <typename T>
+__device__ ArgMax direct_row_argmax(const T* P, int V, int t0, int t1, PassSmem& sh, bool* bad) {
+  float best = -kInf;
+  int bi = -1;
+  bool b = false;
+  for (int t = t0; t < t1; ++t) {
+    float x[8];
+    const int e0 = t * kTileElems + 8 * static_cast<int>(threadIdx.x);
+    if (row_is_aligned(P)) {
+      uint32_t r[Load8<T>::kRegs];
+      Load8<T>::issue(P, e0, V, r);
+      Load8<T>::get(r, x);
+    } else {
+      load8_misaligned(P, e0, V, x);
+    }
+    argmax8(x, e0, best, bi, b);
+  }
+  return block_argmax(best, bi, b, sh, bad);
 }
 
 // ---------------------------------------------------------------------------

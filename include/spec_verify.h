@@ -61,14 +61,12 @@
  *    share them; within one thread, do not enqueue a grouped call eagerly
  *    while another of the thread's calls is being captured into a graph
  *    under the global capture mode.
- *    A consulted-only chain call adds one memset of its control words;
+ *    A consulted-only chain call is one kernel (no statistics kernel);
  *    spec_compact_tree_path is one kernel; spec_clasp_layer_select is
  *    L + 2 kernels and L cuBLAS GEMMs; spec_verify_pipeline_async is one
  *    chain verification per stage and a combine kernel (see their sections).
  *  - The workspace holds the row statistics passed from the first kernel of
- *    a call to the second (8 bytes per sequence, row and 8192-element chunk;
- *    a chain's also 4 bytes per sequence and position for its consulted-only
- *    control words, cleared by the call that uses them).
+ *    a call to the second (8 bytes per sequence, row and 8192-element chunk).
  *    Size it with the matching *_workspace_size function; it needs no
  *    initialisation and nothing in it outlives a call.  Two calls that can
  *    run at the same time (other streams) need two workspaces.  Results are
@@ -150,17 +148,16 @@ typedef struct spec_chain_args {
 } spec_chain_args;
 
 /* Consulted-only mode (PipeSpec review, "What carries the argument": the  */
-/* tokens after the first mismatch are rolled back unused).  Position i's   */
-/* target and draft rows are read only while no earlier position of the    */
-/* sequence has been found rejected; the statistics run position by        */
-/* position over the batch, the last chunk of each position tests it, and  */
-/* the rows of later positions of a rejected sequence are skipped.  The     */
-/* decisions, token, rollback and resid_mass are those of the ordinary mode; */
-/* p_at_draft / q_at_draft are NaN after the first rejection, and a NaN or  */
-/* +inf row is an error only when it is read.  Which later rows are skipped */
-/* depends on timing (a row may still be read before its position's        */
-/* predecessor is decided); the outputs do not.  Greedy calls return        */
-/* SPEC_EINVAL in this mode.                                                */
+/* tokens after the first mismatch are rolled back unused).  One cluster   */
+/* per sequence walks the positions in order and computes each position's  */
+/* row statistics itself: position i's target and draft rows are read only */
+/* after positions 0 .. i-1 were kept, and the bonus row only when every    */
+/* draft was kept; no row after the first rejection is read.  One kernel,  */
+/* no statistics kernel; the workspace is not used.  The decisions, token,  */
+/* rollback and resid_mass are those of the ordinary mode; p_at_draft /     */
+/* q_at_draft are NaN after the first rejection, and a NaN or +inf row is   */
+/* an error only when it is read.  Greedy calls return SPEC_EINVAL in this  */
+/* mode.                                                                    */
 size_t spec_chain_workspace_size(int B, int gamma, int V);
 spec_status spec_verify_chain(const spec_chain_args* args, cudaStream_t stream);
 
@@ -230,7 +227,19 @@ typedef struct spec_tree_args {
   int* error_word;             /* in/out, optional                                  */
   void* workspace;
   size_t workspace_bytes;
+  int consulted_only;          /* 0 = every row is read; nonzero = only the rows of */
+                               /* nodes the walk stands at (below)                 */
 } spec_tree_args;
+
+/* Consulted-only tree mode (Staged Speculative Decoding, abstract: the     */
+/* walk keeps one child per level; PipeSpec review, "What carries the       */
+/* argument": tokens after the first mismatch are never used).  One cluster */
+/* per tree walks from the root and computes the statistics of node n's    */
+/* rows when it stands at n: the target row always, the draft row in        */
+/* sampling mode when n has children; rows of nodes off the walked path are */
+/* never read.  One kernel, no statistics kernel; the workspace is not      */
+/* used.  Decisions, path, token and rollback are those of the ordinary     */
+/* mode on finite rows; a NaN or +inf row is an error only when it is read. */
 
 size_t spec_tree_workspace_size(int B, int N, int V);
 spec_status spec_verify_tree(const spec_tree_args* args, cudaStream_t stream);

@@ -147,7 +147,7 @@ def compare_chain(g, o, greedy):
 # tree
 # --------------------------------------------------------------------------
 
-def gpu_tree(w, device, greedy=None, workspace=None):
+def gpu_tree(w, device, greedy=None, workspace=None, consulted_only=False):
     from draft_verification_gb300 import TreePlan
     s = w["spec"]
     greedy = s.greedy if greedy is None else greedy
@@ -156,7 +156,7 @@ def gpu_tree(w, device, greedy=None, workspace=None):
     plan = TreePlan(dev(w["parent"], device), dev(w["tokens"], device), tgt, drf,
                     dev(w["u"], device), dev(w["v"], device), dev(w["prefix_len"], device),
                     max_depth=w["max_depth"], greedy=greedy, temperature=s.temperature,
-                    workspace=workspace)
+                    workspace=workspace, consulted_only=consulted_only)
     return to_np(plan.run())
 
 

@@ -81,8 +81,7 @@ def test_workspace_sizes(lib):
     def size(B, rows, V):
         return (B * rows * -(-V // 8192) * 8 + 255) // 256 * 256
 
-    # the chain adds its consulted-only control words: 4 B per (sequence, position + 1)
-    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256) + 1536 == 91648
+    assert lib.spec_chain_workspace_size(64, 5, 128256) == size(64, 11, 128256) == 90112
     assert lib.spec_tree_workspace_size(16, 64, 50257) == size(16, 128, 50257)
     assert lib.spec_cascade_workspace_size(128, 8, 4, 128256) == size(128, 21, 128256)
     assert lib.spec_chain_workspace_size(0, 5, 10) == 0

@@ -50,11 +50,14 @@ SMALL = [
 def test_consulted_small(cuda_device, spec):
     w = synth.make(spec, seed=8)
     g = H.gpu_chain(w, cuda_device, consulted_only=True)
-    compare(g, oracle(w))
-    # the ordinary mode makes the same decisions on finite inputs
+    o = oracle(w)
+    compare(g, o)
+    # the ordinary mode makes the same decisions on finite inputs (its row
+    # statistics are summed in another order, so not at near ties)
     d = H.gpu_chain(w, cuda_device)
+    keep = ~H.set_aside(o, False)
     for k in ("accept_len", "out_token", "rollback_idx", "seq_error"):
-        assert np.array_equal(g[k], d[k]), k
+        assert np.array_equal(g[k][keep], d[k][keep]), k
 
 
 @pytest.mark.parametrize("name", ["sampling_chain_b64_g5_v128256_bf16_a05", "sampling_chain_b64_g5_v128256_bf16_a60"])
