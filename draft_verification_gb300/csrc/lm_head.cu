@@ -49,19 +49,19 @@ namespace sv {
 namespace {
 
 constexpr int kBK = 64;            // K elements per stage: one 128-byte swizzled row
-constexpr int kBV = 128;           // vocabulary entries per tile (MMA N)
 constexpr int kBR = 128;           // hidden rows per row tile (MMA M)
 constexpr int kMaxRowTiles = 4;    // 4 accumulators of 128 float32 columns: all of TMEM
 constexpr int kRowBlock = kBR * kMaxRowTiles;
-constexpr int kTileBytes = kBR * kBK * 2;  // 16 KB, also a W tile (kBV == kBR)
+constexpr int kTileBytes = kBR * kBK * 2;  // 16 KB: one hidden-state tile
 constexpr int kMaxStages = 6;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 208 * 1024;
 constexpr int kLmThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
 
 struct LmParams {
   int R, V, d;
+  int bv;             // vocabulary entries per tile (MMA N): 256, 160 or 128
   int ntv;            // vocabulary tiles
   int nkb;            // K steps of 64
   int rt_max;         // row tiles of the largest row block
@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(lm_dyn) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  const int stage_bytes = kTileBytes * (1 + P.rt_max);
+  const int wbytes = P.bv * kBK * 2;  // a weight tile
+  const int stage_bytes = wbytes + kTileBytes * P.rt_max;
   const int G = P.chunks, cta = blockIdx.x;
   const int v_t0 = static_cast<int>((static_cast<long long>(cta) * P.ntv) / G);
   const int v_t1 = static_cast<int>((static_cast<long long>(cta + 1) * P.ntv) / G);
@@ -142,10 +143,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
             if (!lm_wait(&empty[s], ph ^ 1u, fault)) break;
             unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
-            mbar_expect_tx(&full[s], static_cast<unsigned>(kTileBytes * (1 + rt)));
-            tma_load_2d(st, &tm_w, kb * kBK, vt * kBV, &full[s]);
+            mbar_expect_tx(&full[s], static_cast<unsigned>(wbytes + kTileBytes * rt));
+            tma_load_2d(st, &tm_w, kb * kBK, vt * P.bv, &full[s]);
             for (int t = 0; t < rt; ++t)
-              tma_load_2d(st + kTileBytes * (1 + t), &tm_x, kb * kBK, rb * kRowBlock + t * kBR, &full[s]);
+              tma_load_2d(st + wbytes + kTileBytes * t, &tm_x, kb * kBK, rb * kRowBlock + t * kBR, &full[s]);
             issued_s = it + 1;
           }
         }
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(kBR, kBV);
+      const uint32_t idesc = umma_idesc_bf16_f32(kBR, P.bv);
       int it = 0, acc = 0;
       for (int rb = 0; rb < nrb && !*fault; ++rb) {
         const int rows = min(kRowBlock, P.R - rb * kRowBlock);
@@ -169,10 +170,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             tc_fence_after();
             const uint32_t st = smem_addr(ring + static_cast<size_t>(s) * stage_bytes);
             for (int t = 0; t < rt; ++t) {
-              const uint32_t xa = st + kTileBytes * (1 + t);
+              const uint32_t xa = st + wbytes + kTileBytes * t;
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
-                umma_bf16(tmem + static_cast<uint32_t>(t * kBV), umma_desc_sw128(xa + 32u * k),
+                umma_bf16(tmem + static_cast<uint32_t>(t * P.bv), umma_desc_sw128(xa + 32u * k),
                           umma_desc_sw128(st + 32u * k), idesc, kb > 0 || k > 0);
             }
             umma_commit(&empty[s]);  // the stage is free once these MMAs are done
@@ -213,12 +214,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
           float* dst = (P.logits && row < P.R) ? P.logits + static_cast<long long>(row) * P.ldl : nullptr;
 #pragma unroll 1
-          for (int cc = 0; cc < kBV / 32; ++cc) {
+          for (int cc = 0; cc < P.bv / 32; ++cc) {
             float v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * kBV + cc * 32),
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * P.bv + cc * 32),
                       v);
-            const int v0 = vt * kBV + cc * 32;
-            const int nv = min(32, P.V - v0);  // >= 1: a tile starts below V
+            const int v0 = vt * P.bv + cc * 32;
+            if (v0 >= P.V) break;  // past the vocabulary in its last, partial tile
+            const int nv = min(32, P.V - v0);
             if (P.greedy) {
               // ascending order with a strict comparison: ties keep the lowest
               // index; -inf never wins (a row of -inf has no argmax)
@@ -320,14 +322,14 @@ EncodeTiled encode_fn() {
 }
 
 // Tensor map of a row-major bfloat16 matrix [rows, cols] (cols contiguous,
-// row stride cols elements): boxes of 128 rows x 64 columns, 128-byte swizzle,
-// out-of-range elements read as zero.
-bool make_map(CUtensorMap* map, const void* base, long long rows, int cols) {
+// row stride cols elements): boxes of box_rows rows x 64 columns, 128-byte
+// swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {kBK, kBR};
+  const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -362,10 +364,23 @@ cudaError_t smem_attribute() {
   return e;
 }
 
+// Partial columns the workspace is sized for: at most one per 128-entry
+// tile (the smallest vocabulary tile) and at most kMaxChunks.
 int lm_chunks(int V) {
-  const int ntv = (V + kBV - 1) / kBV;
+  const int ntv = (V + 127) / 128;
   return ntv < kMaxChunks ? ntv : kMaxChunks;
 }
+
+// Row tiles of the largest row block of a head with R rows.
+int row_tiles(long long R) {
+  const long long t = (R + kBR - 1) / kBR;
+  return static_cast<int>(t < kMaxRowTiles ? t : kMaxRowTiles);
+}
+
+// The vocabulary tile: the widest N (a multiple of 32, at most 256) whose
+// accumulators for all row tiles fit in the 512 TMEM columns, so that every
+// hidden-state tile copied feeds as many products as the accumulators allow.
+int vocab_tile(int rt) { return rt <= 2 ? 256 : (rt == 3 ? 160 : 128); }
 
 long long logit_ld(int V) { return (static_cast<long long>(V) + 3) / 4 * 4; }
 
@@ -387,17 +402,17 @@ LmLayout lm_layout(int B, int gamma, int V, bool greedy) {
 
 cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V, const LmParams& proto,
                         cudaStream_t s) {
-  CUtensorMap tx, tw;
-  if (!make_map(&tx, x, R, d) || !make_map(&tw, w, V, d)) return cudaErrorInvalidValue;
   LmParams P = proto;
   P.R = static_cast<int>(R);
   P.V = V;
   P.d = d;
-  P.ntv = (V + kBV - 1) / kBV;
+  P.rt_max = row_tiles(R);
+  P.bv = vocab_tile(P.rt_max);
+  P.ntv = (V + P.bv - 1) / P.bv;
   P.nkb = (d + kBK - 1) / kBK;
-  const long long row_tiles = (R + kBR - 1) / kBR;
-  P.rt_max = static_cast<int>(row_tiles < kMaxRowTiles ? row_tiles : kMaxRowTiles);
-  const int stage_bytes = kTileBytes * (1 + P.rt_max);
+  CUtensorMap tx, tw;
+  if (!make_map(&tx, x, R, d, kBR) || !make_map(&tw, w, V, d, P.bv)) return cudaErrorInvalidValue;
+  const int stage_bytes = P.bv * kBK * 2 + kTileBytes * P.rt_max;
   P.stages = min(kMaxStages, kSmemBudget / stage_bytes);
   const int dyn = P.stages * stage_bytes + 1024;
   cudaError_t e = smem_attribute();
@@ -441,7 +456,14 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   char* ws = static_cast<char*>(a->workspace);
   const int gamma = a->gamma;
   const int rows_seq = greedy ? gamma + 1 : 2 * gamma + 1;
-  const int chunks = min(lm_chunks(a->V), nsm);
+  // one partial column per CTA; both heads use the same count (the smaller
+  // vocabulary-tile count of the two, at most one CTA per SM)
+  const long long rows_t = static_cast<long long>(a->B) * (gamma + 1);
+  const long long rows_d = static_cast<long long>(a->B) * gamma;
+  int chunks = min(lm_chunks(a->V), nsm);
+  chunks = min(chunks, (a->V + vocab_tile(row_tiles(rows_t)) - 1) / vocab_tile(row_tiles(rows_t)));
+  if (!greedy && gamma > 0)
+    chunks = min(chunks, (a->V + vocab_tile(row_tiles(rows_d)) - 1) / vocab_tile(row_tiles(rows_d)));
   const long long ldl = logit_ld(a->V);
   float* tlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials);
   float* dlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials + L.tlogits);
@@ -460,8 +482,7 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   pt.per = gamma + 1;
   pt.row_off = 0;
   pt.logits = tlog;
-  cudaError_t e = launch_head(a->h_target, static_cast<long long>(a->B) * (gamma + 1), a->d_target, a->w_target,
-                              a->V, pt, stream);
+  cudaError_t e = launch_head(a->h_target, rows_t, a->d_target, a->w_target, a->V, pt, stream);
   if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   if (!greedy && gamma > 0) {
     // draft head: rows (b, i), i < gamma, statistics rows gamma + 1 ..
@@ -469,7 +490,7 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
     pd.per = gamma;
     pd.row_off = gamma + 1;
     pd.logits = dlog;
-    e = launch_head(a->h_draft, static_cast<long long>(a->B) * gamma, a->d_draft, a->w_draft, a->V, pd, stream);
+    e = launch_head(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, pd, stream);
     if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   }
 
