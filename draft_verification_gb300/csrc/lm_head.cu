@@ -61,7 +61,7 @@ constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
 
 struct LmParams {
   int R, V, d;
-  int bv;             // vocabulary entries per tile (MMA N): 256, 160 or 128
+  int bv;             // vocabulary entries per tile (MMA N): a multiple of 16, 64..256
   int ntv;            // vocabulary tiles
   int nkb;            // K steps of 64
   int rt_max;         // row tiles of the largest row block
@@ -214,18 +214,18 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
           float* dst = (P.logits && row < P.R) ? P.logits + static_cast<long long>(row) * P.ldl : nullptr;
 #pragma unroll 1
-          for (int cc = 0; cc < P.bv / 32; ++cc) {
-            float v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * P.bv + cc * 32),
+          for (int cc = 0; cc < P.bv / 16; ++cc) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * P.bv + cc * 16),
                       v);
-            const int v0 = vt * P.bv + cc * 32;
+            const int v0 = vt * P.bv + cc * 16;
             if (v0 >= P.V) break;  // past the vocabulary in its last, partial tile
-            const int nv = min(32, P.V - v0);
+            const int nv = min(16, P.V - v0);
             if (P.greedy) {
               // ascending order with a strict comparison: ties keep the lowest
               // index; -inf never wins (a row of -inf has no argmax)
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
+              for (int j = 0; j < 16; ++j) {
                 if (j < nv) {
                   bad[t] |= !(v[j] < kInf);
                   if (v[j] > m[t]) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             } else {
               float cm = -kInf;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
+              for (int j = 0; j < 16; ++j)
                 if (j < nv) cm = fmax_nan(cm, v[j]);
               const float mn = fmax_nan(m[t], cm);
               if (mn != -kInf) {
@@ -245,19 +245,19 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 const float scale = (m[t] == -kInf) ? 0.f : ex2(scaled_max(m[t], c) - Mn);
                 float sum = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < 16; ++j)
                   if (j < nv) sum = __fadd_rn(sum, weight(v[j], c, Mn));
                 s[t] = __fadd_rn(__fmul_rn(s[t], scale), sum);
                 m[t] = mn;
               }
               if (dst) {
-                if (nv == 32) {
+                if (nv == 16) {
                   float4* d4 = reinterpret_cast<float4*>(dst + v0);
 #pragma unroll
-                  for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                  for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 } else {
 #pragma unroll
-                  for (int j = 0; j < 32; ++j)
+                  for (int j = 0; j < 16; ++j)
                     if (j < nv) dst[v0 + j] = v[j];
                 }
               }
@@ -377,10 +377,27 @@ int row_tiles(long long R) {
   return static_cast<int>(t < kMaxRowTiles ? t : kMaxRowTiles);
 }
 
-// The vocabulary tile: the widest N (a multiple of 32, at most 256) whose
-// accumulators for all row tiles fit in the 512 TMEM columns, so that every
-// hidden-state tile copied feeds as many products as the accumulators allow.
-int vocab_tile(int rt) { return rt <= 2 ? 256 : (rt == 3 ? 160 : 128); }
+// The vocabulary tile N (MMA N, a multiple of 16).  Its accumulators for
+// all row tiles must fit in the 512 TMEM columns.  The busiest CTA works
+// through ceil(ceil(V / N) / G) tiles and copies N * 128 + rt * 16384 bytes
+// per tile and K step (a weight tile and the hidden-state tiles), so N is the
+// width, from 64 up to that limit, that minimises the busiest CTA's bytes
+// (ties: the wider).  Wider tiles feed more products per hidden-state byte;
+// narrower ones can balance the tiles over the CTAs better.
+int vocab_tile(int rt, int V, int G) {
+  const int most = min(256, 512 / rt / 16 * 16);
+  int best = most;
+  long long best_bytes = -1;
+  for (int n = most; n >= 64; n -= 16) {
+    const long long tiles = (V + n - 1) / n;
+    const long long bytes = (tiles + G - 1) / G * (static_cast<long long>(n) * kBK * 2 + rt * kTileBytes);
+    if (best_bytes < 0 || bytes < best_bytes) {
+      best_bytes = bytes;
+      best = n;
+    }
+  }
+  return best;
+}
 
 long long logit_ld(int V) { return (static_cast<long long>(V) + 3) / 4 * 4; }
 
@@ -400,14 +417,14 @@ LmLayout lm_layout(int B, int gamma, int V, bool greedy) {
   return L;
 }
 
-cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V, const LmParams& proto,
+cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V, int bv, const LmParams& proto,
                         cudaStream_t s) {
   LmParams P = proto;
   P.R = static_cast<int>(R);
   P.V = V;
   P.d = d;
   P.rt_max = row_tiles(R);
-  P.bv = vocab_tile(P.rt_max);
+  P.bv = bv;
   P.ntv = (V + P.bv - 1) / P.bv;
   P.nkb = (d + kBK - 1) / kBK;
   CUtensorMap tx, tw;
@@ -460,10 +477,11 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   // vocabulary-tile count of the two, at most one CTA per SM)
   const long long rows_t = static_cast<long long>(a->B) * (gamma + 1);
   const long long rows_d = static_cast<long long>(a->B) * gamma;
-  int chunks = min(lm_chunks(a->V), nsm);
-  chunks = min(chunks, (a->V + vocab_tile(row_tiles(rows_t)) - 1) / vocab_tile(row_tiles(rows_t)));
-  if (!greedy && gamma > 0)
-    chunks = min(chunks, (a->V + vocab_tile(row_tiles(rows_d)) - 1) / vocab_tile(row_tiles(rows_d)));
+  const int slots = min(lm_chunks(a->V), nsm);
+  const int bv_t = vocab_tile(row_tiles(rows_t), a->V, slots);
+  const int bv_d = vocab_tile(row_tiles(rows_d > 0 ? rows_d : 1), a->V, slots);
+  int chunks = min(slots, (a->V + bv_t - 1) / bv_t);
+  if (!greedy && gamma > 0) chunks = min(chunks, (a->V + bv_d - 1) / bv_d);
   const long long ldl = logit_ld(a->V);
   float* tlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials);
   float* dlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials + L.tlogits);
@@ -482,7 +500,7 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   pt.per = gamma + 1;
   pt.row_off = 0;
   pt.logits = tlog;
-  cudaError_t e = launch_head(a->h_target, rows_t, a->d_target, a->w_target, a->V, pt, stream);
+  cudaError_t e = launch_head(a->h_target, rows_t, a->d_target, a->w_target, a->V, bv_t, pt, stream);
   if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   if (!greedy && gamma > 0) {
     // draft head: rows (b, i), i < gamma, statistics rows gamma + 1 ..
@@ -490,7 +508,7 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
     pd.per = gamma;
     pd.row_off = gamma + 1;
     pd.logits = dlog;
-    e = launch_head(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, pd, stream);
+    e = launch_head(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, bv_d, pd, stream);
     if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   }
 
