@@ -37,8 +37,15 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found: set CUDA_HOME or put nvcc on PATH")
 
 
-def lib_path() -> str:
-    return os.path.join(OUT_DIR, LIB_NAME)
+DEBUG_DIR = os.path.join(PKG, "lib_debug")
+
+
+def lib_path(debug_checks: bool | None = None) -> str:
+    """The library to load: the debug-checks build when debug_checks is true,
+    or (None) when the environment variable SPEC_VERIFY_DEBUG_CHECKS is 1."""
+    if debug_checks is None:
+        debug_checks = os.environ.get("SPEC_VERIFY_DEBUG_CHECKS") == "1"
+    return os.path.join(DEBUG_DIR if debug_checks else OUT_DIR, LIB_NAME)
 
 
 def _newer(target: str, deps: list[str]) -> bool:
@@ -48,20 +55,24 @@ def _newer(target: str, deps: list[str]) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile every translation unit and link the library; returns its path."""
+def build(verbose: bool = False, force: bool = False, debug_checks: bool = False) -> str:
+    """Compile every translation unit and link the library; returns its path.
+    debug_checks builds the variant whose vector loads and bulk copies check
+    their alignment preconditions (-DSPEC_DEBUG_CHECKS) into lib_debug/."""
     nvcc = nvcc_path()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    out_dir = DEBUG_DIR if debug_checks else OUT_DIR
+    os.makedirs(out_dir, exist_ok=True)
+    extra = ["-DSPEC_DEBUG_CHECKS"] if debug_checks else []
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "spec_verify.h"))
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or not _newer(o, [s] + headers):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
             jobs.append((src, cmd))
 
     def run(job):
@@ -76,7 +87,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 raise RuntimeError(f"nvcc failed on {name}: {' '.join(cmd)}")
             if verbose:
                 sys.stderr.write(f"[build] {name}\n{r.stderr}")
-    lib = lib_path()
+    lib = lib_path(debug_checks)
     if force or jobs or not os.path.exists(lib):
         cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart", "-lcublas"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -87,4 +98,4 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug_checks="--debug-checks" in sys.argv))

@@ -18,6 +18,22 @@
 
 namespace sv {
 
+// Debug build (SPEC_DEBUG_CHECKS defined; build(debug_checks=True)): the
+// vector loads and bulk copies check their alignment preconditions.  A
+// misaligned 16-byte load returns NaN bits instead of loading (the row is
+// then reported non-finite), and a misaligned bulk copy, L2 prefetch or
+// tensor-map copy is not issued (its barrier's bounded wait then gives up
+// and the sequence reports SPEC_ERR_INTERNAL), so a broken precondition
+// shows up as an error bit instead of a misaligned-address fault.
+#ifdef SPEC_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool misaligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) != 0;
+}
+
 constexpr int kStatsThreads = 256;       // row-statistics kernel: small CTAs, many per SM
 constexpr int kStatsWarps = kStatsThreads / 32;
 constexpr int kVecPerThread = 8;         // 16-byte loads per thread per statistics unit
@@ -43,6 +59,7 @@ __device__ __forceinline__ float load_elem(const bf16_t* p) {
 // 16-byte streaming load that does not allocate in L1 (rows are read once
 // by the statistics pass).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  if (kDebugChecks && misaligned16(p)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -53,6 +70,7 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // 16-byte load through L2 (the walker re-reads rows the statistics pass
 // brought into L2 moments earlier).
 __device__ __forceinline__ uint4 ld16(const void* p) {
+  if (kDebugChecks && misaligned16(p)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -139,6 +157,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
 // Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
 // to this CTA's shared memory; completion is counted on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  if (kDebugChecks && (misaligned16(dst) || misaligned16(src) || (bytes & 15u))) return;
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_addr(dst)),
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
@@ -192,6 +211,7 @@ __device__ __forceinline__ void st_async_cluster(const void* local, unsigned ran
 // Hint the bulk-copy engine to bring `bytes` (a multiple of 16, 16-byte
 // aligned) at `src` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  if (kDebugChecks && (misaligned16(src) || (bytes & 15u))) return;
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 

@@ -129,6 +129,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 // `tmap` (a kernel parameter) into shared memory at `dst`, counting its bytes
 // on `bar`.  x times the element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  // (bf16 tensors: x must be a multiple of 8 elements; the debug build checks)
+  if (kDebugChecks && ((x & 7) != 0 || (smem_addr(dst) & 1023u) != 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_addr(dst)),
