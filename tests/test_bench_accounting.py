@@ -101,3 +101,23 @@ def test_async_launches_per_call_match_the_launch_list():
     spec = synth.PIPELINE_ASYNC_SPECS["pipeline4_async_b128_g8_g6_g4_v128256_bf16"]
     assert bench.async_launches_per_call(spec) == 3 * 8 + 1
     assert 2 * _stats_launches_per_call(spec.name, 5) + 1 == bench.async_launches_per_call(spec)
+
+
+def test_consulted_and_lm_head_launch_counts():
+    # a consulted-only chain or tree call is one walk kernel; the LM-head
+    # chain is one head kernel per head plus the walk
+    import bench
+    from workloads import synth
+    chain = synth.make(synth.with_sizes(synth.SPECS["sampling_chain_b64_g5_v128256_bf16_a05"], B=2, V=100), seed=0)
+    tree = synth.make(synth.with_sizes(synth.SPECS["tree_b16_n64_v50257_bf16"], B=2, V=100), seed=0)
+    old = bench.CONSULTED
+    try:
+        bench.CONSULTED = True
+        assert bench.launches_per_call(chain) == 1 and bench.launches_per_call(tree) == 1
+        bench.CONSULTED = False
+        assert bench.launches_per_call(chain) == 2 and bench.launches_per_call(tree) == 2
+    finally:
+        bench.CONSULTED = old
+    spec = synth.LM_HEAD_SPECS["lm_head_chain_b64_g5_v128256_d4096_bf16"]
+    assert bench.lm_head_flops(spec) == 2 * 128256 * (64 * 6 * 4096 + 64 * 5 * 4096)
+    assert bench.lm_head_bytes(spec) == 2 * 128256 * 4096 * 2 + 64 * (6 + 5) * 4096 * 2

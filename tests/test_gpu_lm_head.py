@@ -184,3 +184,28 @@ def test_lm_head_matches_stored_logit_path(cuda_device):
     flagged = H.set_aside(oc, False)
     for k in ("accept_len", "out_token", "rollback_idx"):
         assert np.array_equal(g[k][~flagged], gc[k][~flagged]), k
+
+
+def test_lm_head_data_errors(cuda_device):
+    # a drafted token out of range, and NaN hidden states (their logit rows
+    # are NaN): those sequences get the data-error bits and empty outputs,
+    # the others are unaffected
+    spec = W(BASE, B=6, gamma=3, V=3000, d_target=128, d_draft=128)
+    w = synth.make(spec, seed=21)
+    nan = synth.bf16_from_float32(np.array([np.nan], np.float32))[0]
+    w["tokens"][1, 2] = spec.V
+    w["h_target"][3, 1, 5] = nan
+    w["h_draft"] = w["h_draft"].copy()
+    w["h_draft"][4, 0, 7] = nan
+    for greedy in (False, True):
+        g, _ = run(w, cuda_device, greedy=greedy)
+        o = oracle(w, np.arange(spec.B), greedy)
+        want = {1: V.ERR_TOKEN, 3: V.ERR_NONFINITE, 4: 0 if greedy else V.ERR_NONFINITE}
+        for b, bit in want.items():
+            assert g["seq_error"][b] == bit == o["error"][b], (greedy, b, g["seq_error"][b], o["error"][b])
+            if bit:
+                assert g["accept_len"][b] == 0 and g["out_token"][b] == -1
+        ok = np.array([b not in want or want[b] == 0 for b in range(spec.B)])
+        flagged = H.set_aside(o, greedy)
+        for k in DECISIONS:
+            assert np.array_equal(g[k][ok & ~flagged], o[k][ok & ~flagged]), (greedy, k)
