@@ -101,22 +101,26 @@ def draft_tokens_per_call(w) -> int:
     return s.B * (s.gamma1 + s.gamma2)
 
 
-def chain_groups(B: int, rows: int, V: int, elt: int) -> int:
-    """Batch groups of one chain call, as the library plans them: at most 4,
-    each with at least 16 sequences and 40 MB of logits."""
-    return max(1, min(4, B // 16, int(B * rows * V * elt / 40e6)))
+def chain_groups(B: int, rows: int, V: int, elt: int, min_seqs: int = 16) -> int:
+    """Batch groups of one chain (or tree) call, as the library plans them:
+    at most 4, each with at least 40 MB of logits and 16 sequences (4 trees)."""
+    return max(1, min(4, B // min_seqs, int(B * rows * V * elt / 40e6)))
 
 
 def launches_per_call(w) -> int:
     """Kernels of the library launched by one verification call: statistics
-    and walk per batch group for chains, statistics and walk for the other
-    kinds, one walk kernel in consulted-only mode."""
+    and walk per batch group for chains and trees, statistics and walk for
+    the other kinds, one walk kernel in consulted-only mode."""
     s = w["spec"]
     if CONSULTED and (w["kind"] == "tree" or (w["kind"] == "chain" and not s.greedy)):
         return 1  # the consulted-only walk computes its own statistics
+    elt = 2 if s.dtype == "bf16" else 4
     if w["kind"] == "chain":
         rows = s.gamma + 1 if s.greedy else 2 * s.gamma + 1
-        return 2 * chain_groups(s.B, rows, s.V, 2 if s.dtype == "bf16" else 4)
+        return 2 * chain_groups(s.B, rows, s.V, elt)
+    if w["kind"] == "tree":
+        n = int(w["parent"].shape[1])
+        return 2 * chain_groups(s.B, n if s.greedy else 2 * n, s.V, elt, min_seqs=4)
     return 2
 
 

@@ -58,6 +58,7 @@ constexpr int kSmemBudget = 208 * 1024;
 constexpr int kLmThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
+constexpr int kPrefetchSteps = 8;  // shallow rings: weight tiles brought into L2 this many K steps ahead
 
 struct LmParams {
   int R, V, d;
@@ -66,6 +67,7 @@ struct LmParams {
   int nkb;            // K steps of 64
   int rt_max;         // row tiles of the largest row block
   int stages;
+  int prefetch;       // K steps of weight tiles requested into L2 ahead of the ring (0: none)
   int per;            // hidden rows per sequence of this head
   int rows_seq;       // statistics rows per sequence
   int row_off;        // this head's first statistics row
@@ -134,11 +136,20 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_w);
       int it = 0;
+      const int slab_steps = (v_t1 - v_t0) * P.nkb;
       for (int rb = 0; rb < nrb && !*fault; ++rb) {
         const int rows = min(kRowBlock, P.R - rb * kRowBlock);
         const int rt = (rows + kBR - 1) / kBR;
+        // a ring of two stages does not cover the weights' HBM latency: then
+        // the first weight tiles are requested into L2 now and every later
+        // one P.prefetch K steps before its copy
+        for (int j = 0; j < min(P.prefetch, slab_steps); ++j)
+          tma_prefetch_l2_2d(&tm_w, (j % P.nkb) * kBK, (v_t0 + j / P.nkb) * P.bv);
         for (int vt = v_t0; vt < v_t1 && !*fault; ++vt) {
           for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+            const int j = (vt - v_t0) * P.nkb + kb + P.prefetch;
+            if (P.prefetch > 0 && j < slab_steps)
+              tma_prefetch_l2_2d(&tm_w, (j % P.nkb) * kBK, (v_t0 + j / P.nkb) * P.bv);
             const int s = it % P.stages;
             const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
             if (!lm_wait(&empty[s], ph ^ 1u, fault)) break;
@@ -431,6 +442,9 @@ cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V,
   if (!make_map(&tx, x, R, d, kBR) || !make_map(&tw, w, V, d, P.bv)) return cudaErrorInvalidValue;
   const int stage_bytes = P.bv * kBK * 2 + kTileBytes * P.rt_max;
   P.stages = min(kMaxStages, kSmemBudget / stage_bytes);
+  // measured: with 3 or more stages the L2 requests only add traffic (B = 4
+  // to 64 at V = 128256 slower); with 2 stages (512-row blocks) they pay
+  P.prefetch = P.stages <= 2 ? kPrefetchSteps : 0;
   const int dyn = P.stages * stage_bytes + 1024;
   cudaError_t e = smem_attribute();
   if (e != cudaSuccess) return e;

@@ -1356,15 +1356,16 @@ cudaError_t launch_chain_walk_resident(const StatsParams& G, const ChainParams& 
 constexpr int kMaxGroups = 4;
 constexpr double kGroupBytes = 40e6;  // logits per group at least
 constexpr int kGroupSeqs = 16;        // sequences per group at least
+constexpr int kTreeGroupSeqs = 4;     // trees per group at least (a tree holds 2N rows)
 
 struct Groups {
   int n;
   int b0[kMaxGroups + 1];
 };
 
-Groups plan_groups(int B, double bytes) {
+Groups plan_groups(int B, double bytes, int min_seqs = kGroupSeqs) {
   Groups g{};
-  int n = min(kMaxGroups, B / kGroupSeqs);
+  int n = min(kMaxGroups, B / min_seqs);
   n = min(n, static_cast<int>(bytes / kGroupBytes));
   g.n = max(n, 1);
   for (int i = 0; i <= g.n; ++i) g.b0[i] = static_cast<int>((static_cast<long long>(B) * i) / g.n);
@@ -1481,6 +1482,26 @@ ChainParams chain_group(const ChainParams& p, int b0, int nb) {
   return g;
 }
 
+template <typename T>
+TreeParams tree_group(const TreeParams& p, int b0, int nb) {
+  TreeParams g = p;
+  const long long n = p.N;
+  g.B = nb;
+  g.target = static_cast<const T*>(p.target) + static_cast<long long>(b0) * n * p.ld;
+  g.draft = p.draft ? static_cast<const T*>(p.draft) + static_cast<long long>(b0) * n * p.ld : nullptr;
+  g.parent = at_seq(p.parent, b0, n);
+  g.tokens = at_seq(p.tokens, b0, n);
+  g.u = at_seq(p.u, b0, n);
+  g.v = at_seq(p.v, b0, 1);
+  g.prefix = at_seq(p.prefix, b0, 1);
+  g.path_len = at_seq(p.path_len, b0, 1);
+  g.path_nodes = at_seq(p.path_nodes, b0, p.max_depth + 1);
+  g.out_token = at_seq(p.out_token, b0, 1);
+  g.rollback = at_seq(p.rollback, b0, 1);
+  g.seq_error = at_seq(p.seq_error, b0, 1);
+  return g;
+}
+
 double logit_bytes(const StatsParams& G, size_t elt) {
   return static_cast<double>(G.B) * G.rows_per_seq * G.V * static_cast<double>(elt);
 }
@@ -1519,6 +1540,23 @@ cudaError_t chain_impl(const StatsParams& G, const ChainParams& p, bool greedy, 
   });
 }
 
+// One group of trees: its statistics, then its walk (priorities as for the
+// chain's groups).
+template <typename T>
+cudaError_t tree_one(const StatsParams& G, const TreeParams& p, bool greedy, cudaStream_t s, int group) {
+  const int sr = group < 0 ? -1 : 1 + group, wr = group < 0 ? -1 : 0;
+  const size_t nodes = static_cast<size_t>(kTreeSmemPerNode) * p.N;
+  const size_t most = static_cast<size_t>(kStageBytes) + static_cast<size_t>(kTreeSmemPerNode) * kMaxNodes;
+  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s, sr) : launch_stats(stats_kernel<T, false>, G, s, sr);
+  if (e != cudaSuccess) return e;
+  if (greedy) {
+    e = smem_limit(reinterpret_cast<const void*>(tree_kernel<T, true, false>), kTreeSmemPerNode * kMaxNodes);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(tree_kernel<T, true, false>, dim3(1, G.B), 0, nodes, G, p, s, wr);
+  }
+  return launch_walk(tree_kernel<T, false, false>, kStageBytes + nodes, most, G, p, s, wr);
+}
+
 template <typename T>
 cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, bool consulted, cudaStream_t s) {
   const size_t nodes = static_cast<size_t>(kTreeSmemPerNode) * p.N;
@@ -1528,14 +1566,12 @@ cudaError_t tree_impl(const StatsParams& G, const TreeParams& p, bool greedy, bo
     if (greedy) return launch_walk(tree_kernel<T, true, true>, kStageBytes + nodes, most, G, p, s);
     return launch_walk(tree_kernel<T, false, true>, kStageBytes + nodes, most, G, p, s);
   }
-  cudaError_t e = greedy ? launch_stats(stats_kernel<T, true>, G, s) : launch_stats(stats_kernel<T, false>, G, s);
-  if (e != cudaSuccess) return e;
-  if (greedy) {
-    e = smem_limit(reinterpret_cast<const void*>(tree_kernel<T, true, false>), kTreeSmemPerNode * kMaxNodes);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(tree_kernel<T, true, false>, dim3(1, G.B), 0, nodes, G, p, s);
-  }
-  return launch_walk(tree_kernel<T, false, false>, kStageBytes + nodes, most, G, p, s);
+  const Groups gr = plan_groups(G.B, logit_bytes(G, sizeof(T)), kTreeGroupSeqs);
+  if (gr.n == 1) return tree_one<T>(G, p, greedy, s, -1);
+  return run_groups(gr, s, [&](int i, cudaStream_t si) {
+    const int b0 = gr.b0[i], nb = gr.b0[i + 1] - b0;
+    return tree_one<T>(stats_group<T>(G, b0, nb), tree_group<T>(p, b0, nb), greedy, si, i);
+  });
 }
 
 template <typename T>

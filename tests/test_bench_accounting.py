@@ -104,8 +104,9 @@ def test_async_launches_per_call_match_the_launch_list():
 
 
 def test_consulted_and_lm_head_launch_counts():
-    # a consulted-only chain or tree call is one walk kernel; the LM-head
-    # chain is one head kernel per head plus the walk
+    # a consulted-only chain or tree call is one walk kernel (a small tree
+    # call is one group: statistics and walk); the LM-head chain is one head
+    # kernel per head plus the walk
     import bench
     from workloads import synth
     chain = synth.make(synth.with_sizes(synth.SPECS["sampling_chain_b64_g5_v128256_bf16_a05"], B=2, V=100), seed=0)
@@ -121,3 +122,17 @@ def test_consulted_and_lm_head_launch_counts():
     spec = synth.LM_HEAD_SPECS["lm_head_chain_b64_g5_v128256_d4096_bf16"]
     assert bench.lm_head_flops(spec) == 2 * 128256 * (64 * 6 * 4096 + 64 * 5 * 4096)
     assert bench.lm_head_bytes(spec) == 2 * 128256 * 4096 * 2 + 64 * (6 + 5) * 4096 * 2
+
+
+def test_tree_launches_per_call_follow_the_grouping_rule():
+    # trees are grouped like chains, with at least 4 trees and 40 MB of
+    # logits per group: the full tree workload (16 trees, 206 MB) runs as 4
+    # groups, 8 trees of 2 x 64 rows at V = 50257 (103 MB) as 2
+    spec = synth.SPECS["tree_b16_n64_v50257_bf16"]
+    w = synth.make(synth.with_sizes(spec, V=100), seed=0)
+    n = w["parent"].shape[1]
+    assert bench.chain_groups(16, 2 * n, 50257, 2, min_seqs=4) == 4
+    assert bench.chain_groups(8, 2 * n, 50257, 2, min_seqs=4) == 2
+    assert bench.chain_groups(3, 2 * n, 50257, 2, min_seqs=4) == 1
+    w = dict(kind="tree", spec=spec, parent=w["parent"])
+    assert bench.launches_per_call(w) == 8
