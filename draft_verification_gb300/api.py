@@ -220,7 +220,7 @@ class LmHeadChainPlan(_Plan):
         # rounded up to 256 bytes), row stride V rounded up to 4
         if self.greedy:
             raise ValueError("greedy calls store no logits")
-        ldl = (self.V + 3) // 4 * 4
+        ldl = (self.V + 7) // 8 * 8
         chunks = min((self.V + 127) // 128, 256)
         part = -(-self.B * (2 * self.gamma + 1) * chunks * 8 // 256) * 256
         tbytes = -(-self.B * (self.gamma + 1) * ldl * 4 // 256) * 256

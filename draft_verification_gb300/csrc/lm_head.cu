@@ -80,6 +80,14 @@ struct LmParams {
   int* error_word;    // optional: SPEC_ERR_INTERNAL when a wait gives up
 };
 
+// 8 floats to global memory in one 32-byte store (dst 32-byte aligned): a
+// whole sector per store, so the rows' scattered writes need no merging
+__device__ __forceinline__ void st_global_v8(float* dst, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
+               "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ bool lm_wait(uint64_t* bar, unsigned parity, volatile int* fault) {
   for (int i = 0; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -233,39 +241,54 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (v0 >= P.V) break;  // past the vocabulary in its last, partial tile
             const int nv = min(16, P.V - v0);
             if (P.greedy) {
-              // ascending order with a strict comparison: ties keep the lowest
-              // index; -inf never wins (a row of -inf has no argmax)
+              // the chunk's maximum, NaN-propagating in two independent
+              // halves: a NaN or +inf anywhere marks the row bad (its
+              // argmax is then not used); otherwise a chunk maximum strictly
+              // above the running one moves the argmax to its first index, so
+              // ties keep the lowest index and -inf never wins (a row of -inf
+              // has no argmax)
+              float ca = -kInf, cb = -kInf;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                if (j < nv) {
-                  bad[t] |= !(v[j] < kInf);
-                  if (v[j] > m[t]) {
-                    m[t] = v[j];
-                    bi[t] = v0 + j;
-                  }
-                }
+              for (int j = 0; j < 16; j += 2) {
+                if (j < nv) ca = fmax_nan(ca, v[j]);
+                if (j + 1 < nv) cb = fmax_nan(cb, v[j + 1]);
+              }
+              const float cm = fmax_nan(ca, cb);
+              bad[t] |= !(cm < kInf);
+              if (cm > m[t] && cm < kInf) {
+                int first = 0;
+#pragma unroll
+                for (int j = 15; j >= 0; --j)
+                  if (j < nv && v[j] == cm) first = j;
+                m[t] = cm;
+                bi[t] = v0 + first;
               }
             } else {
-              float cm = -kInf;
+              // two independent chains (even and odd entries) halve the
+              // dependent latency of the max and of the sum
+              float ca = -kInf, cb = -kInf;
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < nv) cm = fmax_nan(cm, v[j]);
-              const float mn = fmax_nan(m[t], cm);
+              for (int j = 0; j < 16; j += 2) {
+                if (j < nv) ca = fmax_nan(ca, v[j]);
+                if (j + 1 < nv) cb = fmax_nan(cb, v[j + 1]);
+              }
+              const float mn = fmax_nan(m[t], fmax_nan(ca, cb));
               if (mn != -kInf) {
                 const float Mn = scaled_max(mn, c);
                 const float scale = (m[t] == -kInf) ? 0.f : ex2(scaled_max(m[t], c) - Mn);
-                float sum = 0.f;
+                float sa = 0.f, sb = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (j < nv) sum = __fadd_rn(sum, weight(v[j], c, Mn));
-                s[t] = __fadd_rn(__fmul_rn(s[t], scale), sum);
+                for (int j = 0; j < 16; j += 2) {
+                  if (j < nv) sa = __fadd_rn(sa, weight(v[j], c, Mn));
+                  if (j + 1 < nv) sb = __fadd_rn(sb, weight(v[j + 1], c, Mn));
+                }
+                s[t] = __fadd_rn(__fmul_rn(s[t], scale), __fadd_rn(sa, sb));
                 m[t] = mn;
               }
               if (dst) {
                 if (nv == 16) {
-                  float4* d4 = reinterpret_cast<float4*>(dst + v0);
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                  st_global_v8(dst + v0, v);
+                  st_global_v8(dst + v0 + 8, v + 8);
                 } else {
 #pragma unroll
                   for (int j = 0; j < 16; ++j)
@@ -410,7 +433,8 @@ int vocab_tile(int rt, int V, int G) {
   return best;
 }
 
-long long logit_ld(int V) { return (static_cast<long long>(V) + 3) / 4 * 4; }
+// rows start on 32-byte boundaries: the epilogue stores 8 floats at a time
+long long logit_ld(int V) { return (static_cast<long long>(V) + 7) / 8 * 8; }
 
 struct LmLayout {
   size_t partials, tlogits, dlogits, total;

@@ -562,7 +562,7 @@ typedef struct spec_lm_head_chain_args {
 
 /* Partials: 8 bytes per (sequence, statistics row, vocabulary slab), at most */
 /* 256 slabs; sampling adds the float32 logits of every row (row stride V    */
-/* rounded up to a multiple of 4).  0 for sizes outside the limits.          */
+/* rounded up to a multiple of 8).  0 for sizes outside the limits.          */
 size_t spec_lm_head_chain_workspace_size(int B, int gamma, int V, spec_mode mode);
 /* SPEC_EINVAL: a size outside the limits or a NULL required pointer;         */
 /* SPEC_EALIGN: a hidden-state or weight base not 16-byte aligned;            */

@@ -68,3 +68,33 @@ def test_grouped_chain_graph_replays(cuda_device):
         torch.cuda.synchronize()
         H.compare_chain(H.to_np(plan.out), H.oracle_chain(w), False)
     assert dv.workspace_bytes("chain", 64, 5, 128256) <= plan.workspace.numel()
+
+
+def test_grouped_tree_graph_replays(cuda_device):
+    # 16 trees of 64 nodes at V = 50257 (206 MB of logits): the call runs as
+    # four batch groups of four trees on the side streams; replayed from a
+    # graph with new inputs copied into the captured buffers
+    from draft_verification_gb300 import TreePlan
+    spec = S["tree_b16_n64_v50257_bf16"]
+    ws = [synth.make(spec, seed=60 + i) for i in range(2)]
+    w0 = ws[0]
+    plan = TreePlan(H.dev(w0["parent"], cuda_device), H.dev(w0["tokens"], cuda_device),
+                    H.logits_view(H.dev_logits(w0["target"], spec.dtype, cuda_device), spec.V),
+                    H.logits_view(H.dev_logits(w0["draft"], spec.dtype, cuda_device), spec.V),
+                    H.dev(w0["u"], cuda_device), H.dev(w0["v"], cuda_device), H.dev(w0["prefix_len"], cuda_device),
+                    max_depth=w0["max_depth"], temperature=spec.temperature)
+    stream = torch.cuda.Stream(cuda_device)
+    plan.run(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.run(stream)
+    for w in ws[1:] + ws[:1]:
+        for k, x in (("parent", 0), ("tokens", 1), ("u", 4), ("v", 5), ("prefix_len", 6)):
+            plan.keep[x].copy_(H.dev(w[k], cuda_device))
+        plan.keep[2].copy_(H.logits_view(H.dev_logits(w["target"], spec.dtype, cuda_device), spec.V))
+        plan.keep[3].copy_(H.logits_view(H.dev_logits(w["draft"], spec.dtype, cuda_device), spec.V))
+        plan.out["error_word"].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        H.compare_tree(H.to_np(plan.out), H.oracle_tree(w), False)
