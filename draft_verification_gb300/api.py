@@ -217,7 +217,7 @@ class LmHeadChainPlan(_Plan):
     def _logits(self, first_row, rows):
         # the workspace layout of spec_lm_head_chain_workspace_size: the
         # partials, then the target rows, then the draft rows (each part
-        # rounded up to 256 bytes), row stride V rounded up to 4
+        # rounded up to 256 bytes), row stride V rounded up to 8
         if self.greedy:
             raise ValueError("greedy calls store no logits")
         ldl = (self.V + 7) // 8 * 8

@@ -12,15 +12,18 @@
 // lm_head_kernel: logits L = X W^T for one head, X [R, d] (bfloat16 hidden
 // states, one row per position), W [V, d] (bfloat16 LM-head weights), float32
 // accumulation in tensor memory.  One persistent CTA per SM owns a
-// contiguous slab of 128-entry vocabulary tiles.  Per tile and per block of
-// at most 512 hidden rows, the CTA streams K in 64-element steps:
-//   warp 4  (one thread)  TMA copies of the W tile [128 x 64] and the X tiles
+// contiguous slab of N-entry vocabulary tiles (N chosen per call).  Per tile
+// and per block of at most 512 hidden rows, the CTA streams K in 64-element
+// steps:
+//   warp 4  (one thread)  TMA copies of the W tile [N x 64] and the X tiles
 //                         [128 x 64] of the row block into a ring of stages;
-//   warp 5  (one thread)  tcgen05.mma, M = 128 rows, N = 128 vocabulary
-//                         entries, K = 16, one accumulator of 128 columns per
-//                         row tile (at most 4 tiles: all 512 TMEM columns);
-//                         a commit frees each stage, another hands the tile's
-//                         accumulators to the epilogue;
+//   warps 5-7 (one thread each)  tcgen05.mma, M = 128 rows, N vocabulary
+//                         entries, K = 16, one accumulator of N columns per
+//                         row tile (at most 4 tiles within the 512 TMEM
+//                         columns); warp 5 + i issues the row tiles t with
+//                         t % 3 == i, so three instruction streams feed the
+//                         tensor pipe; each issuer's commits free the stages
+//                         and hand the tile's accumulators to the epilogue;
 //   warps 0-3             the epilogue: thread t of warp w owns TMEM lane
 //                         32 w + t, i.e. one hidden row of every row tile, and
 //                         folds the tile's 128 logits into that row's running
@@ -55,7 +58,8 @@ constexpr int kRowBlock = kBR * kMaxRowTiles;
 constexpr int kTileBytes = kBR * kBK * 2;  // 16 KB: one hidden-state tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 208 * 1024;
-constexpr int kLmThreads = 192;
+constexpr int kLmThreads = 256;
+constexpr int kIssuers = 3;        // MMA-issuing warps (5, 6, 7): one thread's issue rate was the limit
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
 constexpr int kPrefetchSteps = 8;  // shallow rings: weight tiles brought into L2 this many K steps ahead
@@ -120,11 +124,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kIssuers);
     }
-    mbar_init(&tfull, 1);
+    mbar_init(&tfull, kIssuers);
     mbar_init(&tempty, 4);
-    mbar_init(&drain, 1);
+    mbar_init(&drain, kIssuers);
     fault_s = 0;
     issued_s = 0;
     mbar_fence_init();
@@ -171,8 +175,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp >= 5 && warp < 5 + kIssuers) {
+    // ---------------- MMA issuers: row tiles t with t % kIssuers == warp - 5 ----------------
+    const int me = warp - 5;
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16_f32(kBR, P.bv);
       int it = 0, acc = 0;
@@ -188,12 +193,19 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (!lm_wait(&full[s], ph, fault)) break;
             tc_fence_after();
             const uint32_t st = smem_addr(ring + static_cast<size_t>(s) * stage_bytes);
-            for (int t = 0; t < rt; ++t) {
-              const uint32_t xa = st + wbytes + kTileBytes * t;
+            // descriptors of the stage's tiles, built once: a K step of 16
+            // elements adds 32 bytes (2 in the start-address field), a row
+            // tile 16 KB (1024)
+            const uint64_t dw = umma_desc_sw128(st);
+            const uint64_t dx = umma_desc_sw128(st + wbytes);
 #pragma unroll
-              for (int k = 0; k < kBK / 16; ++k)
-                umma_bf16(tmem + static_cast<uint32_t>(t * P.bv), umma_desc_sw128(xa + 32u * k),
-                          umma_desc_sw128(st + 32u * k), idesc, kb > 0 || k > 0);
+            for (int t = 0; t < kMaxRowTiles; ++t) {
+              if (t < rt && t % kIssuers == me) {
+                const uint64_t dxt = dx + static_cast<uint64_t>(t * (kTileBytes >> 4));
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  umma_bf16(tmem + static_cast<uint32_t>(t * P.bv), dxt + 2u * k, dw + 2u * k, idesc, kb > 0 || k > 0);
+              }
             }
             umma_commit(&empty[s]);  // the stage is free once these MMAs are done
           }
