@@ -15,23 +15,26 @@
 // contiguous slab of N-entry vocabulary tiles (N chosen per call).  Per tile
 // and per block of at most 512 hidden rows, the CTA streams K in 64-element
 // steps:
-//   warp 4  (one thread)  TMA copies of the W tile [N x 64] and the X tiles
+//   warp 8  (one thread)  TMA copies of the W tile [N x 64] and the X tiles
 //                         [128 x 64] of the row block into a ring of stages;
-//   warps 5-7 (one thread each)  tcgen05.mma, M = 128 rows, N vocabulary
+//   warps 9-11 (one thread each)  tcgen05.mma, M = 128 rows, N vocabulary
 //                         entries, K = 16, one accumulator of N columns per
 //                         row tile (at most 4 tiles within the 512 TMEM
-//                         columns); warp 5 + i issues the row tiles t with
+//                         columns); warp 9 + i issues the row tiles t with
 //                         t % 3 == i, so three instruction streams feed the
 //                         tensor pipe; each issuer's commits free the stages
 //                         and hand the tile's accumulators to the epilogue;
-//   warps 0-3             the epilogue: thread t of warp w owns TMEM lane
-//                         32 w + t, i.e. one hidden row of every row tile, and
-//                         folds the tile's 128 logits into that row's running
+//   warps 0-7             the epilogue: thread t of warps w and w + 4 owns
+//                         TMEM lane 32 w + t, i.e. one hidden row of every
+//                         row tile; warp w takes the first half of the tile's
+//                         16-column chunks, warp w + 4 the second half; each
+//                         folds its logits into the row's running
 //                         (max, sum of 2^(x c - M)) (sampling) or (max, first
 //                         index) (greedy), in ascending vocabulary order, and
 //                         in sampling mode stores the float32 logits for the
 //                         walk's residual or bonus draw.
-// After its slab the CTA writes one partial per row in the statistics
+// At the end of a row block the two halves' states are merged and the CTA
+// writes one partial per row in the statistics
 // kernel's format, so the chain walk merges them exactly like the partials of
 // stored logits.  Greedy calls store no logits at all: the walk needs only
 // the argmaxes.
@@ -58,8 +61,11 @@ constexpr int kRowBlock = kBR * kMaxRowTiles;
 constexpr int kTileBytes = kBR * kBK * 2;  // 16 KB: one hidden-state tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 208 * 1024;
-constexpr int kLmThreads = 256;
-constexpr int kIssuers = 3;        // MMA-issuing warps (5, 6, 7): one thread's issue rate was the limit
+constexpr int kEpiWarps = 8;       // two epilogue warps per TMEM lane quarter, each half of a tile's columns
+constexpr int kProdWarp = kEpiWarps;
+constexpr int kIssuer0 = kEpiWarps + 1;
+constexpr int kLmThreads = 32 * (kEpiWarps + 4);
+constexpr int kIssuers = 3;        // MMA-issuing warps (9, 10, 11): one thread's issue rate was the limit
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxChunks = 256;    // partial columns per row (persistent CTAs)
 constexpr int kPrefetchSteps = 8;  // shallow rings: weight tiles brought into L2 this many K steps ahead
@@ -109,6 +115,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __shared__ uint32_t tmem_s;
   __shared__ int fault_s;
   __shared__ int issued_s;  // stages the producer issued
+  __shared__ float2 xch[kMaxRowTiles][kBR];          // second-half epilogue states, handed over per row block
+  __shared__ unsigned char xbad[kMaxRowTiles][kBR];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(lm_dyn) + 1023) &
@@ -127,13 +135,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       mbar_init(&empty[s], kIssuers);
     }
     mbar_init(&tfull, kIssuers);
-    mbar_init(&tempty, 4);
+    mbar_init(&tempty, kEpiWarps);
     mbar_init(&drain, kIssuers);
     fault_s = 0;
     issued_s = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == kIssuer0) {
     tmem_alloc(&tmem_s, kTmemCols);
     tmem_relinquish();
   }
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_s;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
@@ -175,9 +183,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
       }
     }
-  } else if (warp >= 5 && warp < 5 + kIssuers) {
-    // ---------------- MMA issuers: row tiles t with t % kIssuers == warp - 5 ----------------
-    const int me = warp - 5;
+  } else if (warp >= kIssuer0 && warp < kIssuer0 + kIssuers) {
+    // ---------------- MMA issuers: row tiles t with t % kIssuers == warp - kIssuer0 ----------------
+    const int me = warp - kIssuer0;
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16_f32(kBR, P.bv);
       int it = 0, acc = 0;
@@ -234,6 +242,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         bi[t] = -1;
         bad[t] = false;
       }
+      const int q = warp & 3, h = warp >> 2;  // TMEM lane quarter, column half
+      const int nch16 = P.bv / 16;
+      const int c_lo = h ? (nch16 + 1) / 2 : 0, c_hi = h ? nch16 : (nch16 + 1) / 2;
       for (int vt = v_t0; vt < v_t1; ++vt, ++acc) {
         // the warp decides together: the TMEM loads below are warp-wide
         const bool ready = __all_sync(0xffffffffu, lm_wait(&tfull, static_cast<unsigned>(acc) & 1u, fault));
@@ -242,12 +253,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 #pragma unroll
         for (int t = 0; t < kMaxRowTiles; ++t) {
           if (t >= rt) break;
-          const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
+          const int row = rb * kRowBlock + t * kBR + q * 32 + lane;
           float* dst = (P.logits && row < P.R) ? P.logits + static_cast<long long>(row) * P.ldl : nullptr;
 #pragma unroll 1
-          for (int cc = 0; cc < P.bv / 16; ++cc) {
+          for (int cc = c_lo; cc < c_hi; ++cc) {
             float v[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(t * P.bv + cc * 16),
+            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(t * P.bv + cc * 16),
                       v);
             const int v0 = vt * P.bv + cc * 16;
             if (v0 >= P.V) break;  // past the vocabulary in its last, partial tile
@@ -314,19 +325,44 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty);
       }
-      // one partial per row of the block for this CTA's slab
+      // the second half's warps hand their state to the first half's, which
+      // merge it (larger maximum wins, ties to the lower index) and write one
+      // partial per row of the block for this CTA's slab
+      if (h) {
 #pragma unroll
-      for (int t = 0; t < kMaxRowTiles; ++t) {
-        if (t >= rt) break;
-        const int row = rb * kRowBlock + t * kBR + warp * 32 + lane;
-        if (row >= P.R) continue;
-        const long long prow = static_cast<long long>(row / P.per) * P.rows_seq + P.row_off + row % P.per;
-        float2 out;
-        if (*fault) out = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
-        else if (P.greedy) out = make_float2(bad[t] ? __int_as_float(0x7fc00000) : m[t], __int_as_float(bi[t]));
-        else out = make_float2(m[t], s[t]);
-        P.partials[prow * P.chunks + cta] = out;
+        for (int t = 0; t < kMaxRowTiles; ++t) {
+          if (t >= rt) break;
+          xch[t][q * 32 + lane] = P.greedy ? make_float2(m[t], __int_as_float(bi[t])) : make_float2(m[t], s[t]);
+          xbad[t][q * 32 + lane] = bad[t] ? 1 : 0;
+        }
       }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (!h) {
+#pragma unroll
+        for (int t = 0; t < kMaxRowTiles; ++t) {
+          if (t >= rt) break;
+          const int row = rb * kRowBlock + t * kBR + q * 32 + lane;
+          if (row >= P.R) continue;
+          const long long prow = static_cast<long long>(row / P.per) * P.rows_seq + P.row_off + row % P.per;
+          const float2 o = xch[t][q * 32 + lane];
+          float2 out;
+          if (P.greedy) {
+            const int oi = __float_as_int(o.y);
+            if (oi >= 0 && (bi[t] < 0 || o.x > m[t] || (o.x == m[t] && oi < bi[t]))) {
+              m[t] = o.x;
+              bi[t] = oi;
+            }
+            const bool b = bad[t] || xbad[t][q * 32 + lane];
+            out = make_float2(b ? __int_as_float(0x7fc00000) : m[t], __int_as_float(bi[t]));
+          } else {
+            const MaxSum ms = ms_merge(MaxSum{m[t], s[t]}, MaxSum{o.x, o.y}, c);
+            out = make_float2(ms.m, ms.s);
+          }
+          if (*fault) out = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+          P.partials[prow * P.chunks + cta] = out;
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     }
   }
 
@@ -340,7 +376,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (P.error_word) atomicOr(P.error_word, SPEC_ERR_INTERNAL);
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kIssuer0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
