@@ -209,3 +209,31 @@ def test_lm_head_data_errors(cuda_device):
         flagged = H.set_aside(o, greedy)
         for k in DECISIONS:
             assert np.array_equal(g[k][ok & ~flagged], o[k][ok & ~flagged]), (greedy, k)
+
+
+def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device):
+    # Identical weight rows give bit-identical logits (same operands, same
+    # accumulation order in every column), so each hidden row's maximum is
+    # an exact tie between those vocabulary entries and the greedy argmax
+    # must be the lowest of them (the first-index rule of the oracle's
+    # argmax).  With V = 40000 and 4 rows the head kernel's tiles are 144
+    # entries wide and one CTA of a 152-SM part owns tiles 1 and 2; its first
+    # epilogue half sees entry 300 (tile 2) and its second half entry 230
+    # (tile 1), so the merge of the two halves must pick 230.
+    from draft_verification_gb300 import LmHeadChainPlan
+    rng = np.random.default_rng(5)
+    B, g, V, d = 2, 1, 40000, 64
+    h = synth.bf16_from_float32((np.abs(rng.normal(size=(B, g + 1, d))) + 0.5).astype(np.float32))
+    w = synth.bf16_from_float32((0.01 * rng.normal(size=(V, d))).astype(np.float32))
+    ties = [230, 300, 35000, 39999]
+    w[ties] = synth.bf16_from_float32(np.ones(d, np.float32))
+    tokens = np.full((B, g), 7, np.int32)  # never the argmax: the first test rejects
+    zeros = np.zeros((B, g), np.float32)
+    plan = LmHeadChainPlan(_bf16_dev(h, cuda_device), _bf16_dev(h[:, :g], cuda_device), _bf16_dev(w, cuda_device),
+                           _bf16_dev(w, cuda_device), H.dev(tokens, cuda_device), H.dev(zeros, cuda_device),
+                           H.dev(np.zeros(B, np.float32), cuda_device), H.dev(np.zeros(B, np.int32), cuda_device),
+                           greedy=True)
+    out = H.to_np(plan.run())
+    assert (out["seq_error"] == 0).all()
+    assert (out["accept_len"] == 0).all()
+    assert (out["out_token"] == min(ties)).all(), out["out_token"]
