@@ -216,12 +216,13 @@ class LmHeadChainPlan(_Plan):
 
     def _logits(self, first_row, rows):
         # the workspace layout of spec_lm_head_chain_workspace_size: the
-        # partials, then the target rows, then the draft rows (each part
+        # partials (two columns per 256-entry vocabulary tile, at most 256),
+        # then the target rows, then the draft rows (each part
         # rounded up to 256 bytes), row stride V rounded up to 8
         if self.greedy:
             raise ValueError("greedy calls store no logits")
         ldl = (self.V + 7) // 8 * 8
-        chunks = min((self.V + 127) // 128, 256)
+        chunks = min(2 * ((self.V + 255) // 256), 256)
         part = -(-self.B * (2 * self.gamma + 1) * chunks * 8 // 256) * 256
         tbytes = -(-self.B * (self.gamma + 1) * ldl * 4 // 256) * 256
         off = part + (0 if first_row == 0 else tbytes)

@@ -383,6 +383,343 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// lm_head_pair_kernel: the same product and partials on CTA pairs.  A
+// cluster of two CTAs owns a slab of 256-entry vocabulary tiles; per tile,
+// row block and 64-element K step the pair issues M = 256 products with the
+// weights as A (the even CTA holds vocabulary rows 0-127 of the tile, the
+// odd CTA rows 128-255) and the hidden rows as B, in one or two chunks of
+// Nc <= 256 rows (the even CTA holds the first Nc/2 rows of each chunk, the
+// odd CTA the rest).  Each CTA therefore copies 16 KB of weights and half of
+// the hidden rows per stage, and its tensor pipe reads half of B.  Warps 5
+// and 6 of the even CTA each issue one chunk's products.  The accumulators
+// land with one vocabulary entry per TMEM lane and one hidden row per
+// column; the epilogue (warps 0-3 of each CTA) transposes each 32 x 32 block
+// through shared memory, so that lane l folds row l's 32 vocabulary entries
+// in order into a per-warp running state; at the end of a row block the four
+// warps' states are merged into one partial per row and CTA.
+// ---------------------------------------------------------------------------
+constexpr int kPairM = 256;              // vocabulary entries per pair tile
+constexpr int kPairMaxRows = 512;        // hidden rows per row block (TMEM columns)
+constexpr int kPairRing = 168 * 1024;    // ring budget per CTA
+constexpr int kPairMaxStages = 12;
+// CTA pairs for calls whose target head has at least this many rows (the
+// products dominate: c3-sized heads 3-4 % faster, 2304 rows 15 %); smaller
+// calls stream the weights faster on single CTAs (B = 4 and 16: 15-20 %)
+constexpr int kPairMinRows = 256;
+constexpr int kPairWBytes = 128 * kBK * 2;  // a CTA's weight tile: 16 KB
+constexpr int kPairIssuers = 2;          // warps 9 and 10 of the even CTA: one chunk each
+constexpr int kPairEpi = 8;              // epilogue warps: two per TMEM lane quarter
+constexpr int kPairProd = kPairEpi;      // the TMA producer warp
+constexpr int kPairIss0 = kPairEpi + 1;  // the first MMA-issuing warp
+constexpr int kPairThreads = 32 * (kPairEpi + 1 + kPairIssuers);
+constexpr int kPairScr = 32 * 33;        // floats of one warp's transpose block
+constexpr int kPairExtra = 4 * kPairMaxRows * 8 + 4 * kPairMaxRows + kPairEpi * kPairScr * 4;  // states, flags, blocks
+
+struct LmPairParams {
+  int R, V, d, nkb;
+  int nc;             // hidden rows per chunk (MMA N): a multiple of 16, <= 256
+  int nch;            // chunks per full row block (1 or 2)
+  int ntv;            // 256-entry vocabulary tiles
+  int stages;
+  int per, rows_seq, row_off;
+  int chunks;         // CTAs of the launch: one partial column each
+  int greedy;
+  float c;
+  float2* partials;
+  float* logits;
+  long long ldl;
+  int* error_word;
+};
+
+// Bounded wait with acquire semantics at cluster scope (arrivals come from
+// the peer CTA).
+__device__ __forceinline__ bool lm_wait_cluster(uint64_t* bar, unsigned parity, volatile int* fault) {
+  for (int i = 0; i < kMaxPolls; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kPollNs)
+        : "memory");
+    if (ok) return true;
+    if (*fault) return false;
+  }
+  *fault = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    lm_head_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                        const LmPairParams P) {
+  extern __shared__ __align__(1024) unsigned char lp_dyn[];
+  __shared__ uint64_t full[kPairMaxStages], empty[kPairMaxStages], tfull, tempty, drain;
+  __shared__ uint32_t tmem_s;
+  __shared__ int fault_s;
+  __shared__ int issued_s;       // stages this CTA's producer issued
+  __shared__ int peer_issued_s;  // (even CTA) stages the odd CTA's producer issued
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const bool lead = rank == 0;
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(lp_dyn) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const int xhalf = P.nc / 2 * kBK * 2;  // one CTA's half of a chunk of hidden rows, one K step
+  const int stage_bytes = kPairWBytes + P.nch * xhalf;
+  float2* state = reinterpret_cast<float2*>(ring + static_cast<size_t>(P.stages) * stage_bytes);
+  unsigned char* sbad = reinterpret_cast<unsigned char*>(state + 4 * kPairMaxRows);
+  float* scratch = reinterpret_cast<float*>(sbad + 4 * kPairMaxRows);
+  const int pairs = static_cast<int>(gridDim.x) / 2, pair = static_cast<int>(blockIdx.x) / 2;
+  const int v_t0 = static_cast<int>((static_cast<long long>(pair) * P.ntv) / pairs);
+  const int v_t1 = static_cast<int>((static_cast<long long>(pair + 1) * P.ntv) / pairs);
+  const int rbrows = P.nc * P.nch;
+  const int nrb = (P.R + rbrows - 1) / rbrows;
+  volatile int* fault = &fault_s;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kPairIssuers);
+    }
+    mbar_init(&tfull, kPairIssuers);
+    mbar_init(&tempty, 2 * kPairEpi);  // the epilogue warps of both CTAs of the pair
+    mbar_init(&drain, kPairIssuers);
+    fault_s = 0;
+    issued_s = 0;
+    peer_issued_s = 0;
+    mbar_fence_init();
+  }
+  if (warp == kPairIss0) {
+    tmem_alloc_pair(&tmem_s, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive();  // both CTAs' barriers are initialised before either signals the other's
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+
+  if (warp == kPairProd) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      int it = 0;
+      for (int rb = 0; rb < nrb && !*fault; ++rb) {
+        const int rows = min(rbrows, P.R - rb * rbrows);
+        const int nch = (rows + P.nc - 1) / P.nc;
+        for (int vt = v_t0; vt < v_t1 && !*fault; ++vt) {
+          for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+            const int s = it % P.stages;
+            const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
+            if (!lm_wait(&empty[s], ph ^ 1u, fault)) break;
+            unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
+            const uint32_t fb = cluster_addr(&full[s], 0);
+            // the even CTA's barrier counts both CTAs' bytes
+            if (lead) mbar_expect_tx(&full[s], 2u * static_cast<unsigned>(kPairWBytes + nch * xhalf));
+            tma_load_2d_pair(st, &tm_w, kb * kBK, vt * kPairM + rank * 128, fb);
+            for (int j = 0; j < nch; ++j)
+              tma_load_2d_pair(st + kPairWBytes + j * xhalf, &tm_x, kb * kBK, rb * rbrows + j * P.nc + rank * (P.nc / 2),
+                               fb);
+            issued_s = it + 1;
+          }
+        }
+      }
+    }
+  } else if (warp >= kPairIss0) {
+    // ---------------- MMA issuers (even CTA): chunk j = warp - kPairIss0 ----------------
+    const int j = warp - kPairIss0;
+    if (lead && lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16_f32(kPairM, P.nc);
+      int it = 0, acc = 0;
+      for (int rb = 0; rb < nrb && !*fault; ++rb) {
+        const int rows = min(rbrows, P.R - rb * rbrows);
+        const bool mine = j < (rows + P.nc - 1) / P.nc;
+        for (int vt = v_t0; vt < v_t1 && !*fault; ++vt, ++acc) {
+          // both CTAs' epilogues have read the previous tile's accumulators
+          if (!lm_wait_cluster(&tempty, (static_cast<unsigned>(acc) & 1u) ^ 1u, fault)) break;
+          tc_fence_after();
+          for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+            const int s = it % P.stages;
+            const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
+            if (!lm_wait(&full[s], ph, fault)) break;
+            tc_fence_after();
+            if (mine) {
+              // descriptors built once per stage: a K step adds 2 to the
+              // start-address field
+              const uint32_t st = smem_addr(ring + static_cast<size_t>(s) * stage_bytes);
+              const uint64_t dw = umma_desc_sw128(st);
+              const uint64_t dx = umma_desc_sw128(st + kPairWBytes + j * xhalf);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16_pair(tmem + static_cast<uint32_t>(j * P.nc), dw + 2u * k, dx + 2u * k, idesc,
+                               kb > 0 || k > 0);
+            }
+            umma_commit_pair(&empty[s], 3);  // the stage is free in both CTAs once these products are done
+          }
+          if (*fault) break;
+          umma_commit_pair(&tfull, 3);  // the tile's accumulators are complete in both CTAs
+        }
+      }
+      umma_commit_pair(&drain, 3);
+    }
+    if (lane == 0) mbar_wait(&drain, 0);  // no product of the pair still reads or writes this CTA's memory
+  } else {
+    // ---------------- epilogue (warps 0-7, both CTAs) ----------------
+    // warps q and q + 4 read TMEM lane quarter q; warp q + 4h takes the
+    // 32-row groups g with g % 2 == h
+    const float c = P.c;
+    const int q = warp & 3, h = warp >> 2;
+    float2* my = state + q * kPairMaxRows;  // the quarter's running state of every row of the block
+    unsigned char* mybad = sbad + q * kPairMaxRows;
+    float* scr = scratch + warp * kPairScr;
+    int acc = 0;
+    for (int rb = 0; rb < nrb; ++rb) {
+      const int rows = min(rbrows, P.R - rb * rbrows);
+      const int ngrp = (rows + 31) / 32;
+      for (int g = h; g < ngrp; g += 2) {
+        my[g * 32 + lane] = P.greedy ? make_float2(-kInf, __int_as_float(-1)) : make_float2(-kInf, 0.f);
+        mybad[g * 32 + lane] = 0;
+      }
+      for (int vt = v_t0; vt < v_t1; ++vt, ++acc) {
+        // the warp decides together: the TMEM loads below are warp-wide
+        const bool ready = __all_sync(0xffffffffu, lm_wait(&tfull, static_cast<unsigned>(acc) & 1u, fault));
+        if (!ready) break;
+        tc_fence_after();
+        const int vw = vt * kPairM + rank * 128 + q * 32;  // the quarter's first vocabulary entry
+        const int nv = max(0, min(32, P.V - vw));            // of its 32 entries, those below V
+        for (int g = h; g < ngrp; g += 2) {
+          float x[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * 32), x);
+          const int r0 = rb * rbrows + g * 32;  // hidden row of column 0 of the group
+          // transpose: lane l then holds row r0 + l's values at the
+          // quarter's 32 vocabulary entries, in ascending order
+#pragma unroll
+          for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = x[j];
+          __syncwarp();
+          float y[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) y[e] = scr[e * 33 + lane];
+          __syncwarp();
+          if (P.logits && r0 + lane < P.R) {
+            // row r0 + lane: 32 consecutive float32 logits, whole 32-byte sectors
+            float* dst = P.logits + static_cast<long long>(r0 + lane) * P.ldl + vw;
+            if (nv == 32) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 8) st_global_v8(dst + e, y + e);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e < nv) dst[e] = y[e];
+            }
+          }
+          const float2 cur = my[g * 32 + lane];
+          if (P.greedy) {
+            // NaN-propagating maximum in two chains; NaN or +inf marks the
+            // row bad; a maximum strictly above the running one moves the
+            // argmax to its first entry (ties keep the lowest index)
+            float ca = -kInf, cb = -kInf;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              if (e < nv) ca = fmax_nan(ca, y[e]);
+              if (e + 1 < nv) cb = fmax_nan(cb, y[e + 1]);
+            }
+            const float cm = fmax_nan(ca, cb);
+            if (!(cm < kInf) && nv > 0) mybad[g * 32 + lane] = 1;
+            if (cm > cur.x && cm < kInf) {
+              int first = 0;
+#pragma unroll
+              for (int e = 31; e >= 0; --e)
+                if (e < nv && y[e] == cm) first = e;
+              my[g * 32 + lane] = make_float2(cm, __int_as_float(vw + first));
+            }
+          } else {
+            float ca = -kInf, cb = -kInf;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              if (e < nv) ca = fmax_nan(ca, y[e]);
+              if (e + 1 < nv) cb = fmax_nan(cb, y[e + 1]);
+            }
+            const float mn = fmax_nan(cur.x, fmax_nan(ca, cb));
+            if (mn != -kInf) {
+              const float Mn = scaled_max(mn, c);
+              const float scale = (cur.x == -kInf) ? 0.f : ex2(scaled_max(cur.x, c) - Mn);
+              float sa = 0.f, sb = 0.f;
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                if (e < nv) sa = __fadd_rn(sa, weight(y[e], c, Mn));
+                if (e + 1 < nv) sb = __fadd_rn(sb, weight(y[e + 1], c, Mn));
+              }
+              my[g * 32 + lane] = make_float2(mn, __fadd_rn(__fmul_rn(cur.y, scale), __fadd_rn(sa, sb)));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (lead) mbar_arrive(&tempty);
+          else mbar_arrive_remote(cluster_addr(&tempty, 0));
+        }
+      }
+      // merge the four warps' states of each row, in warp order, into this
+      // CTA's partial (one column per CTA of the launch)
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpi * 32) : "memory");
+      for (int r = static_cast<int>(threadIdx.x); r < rows; r += kPairEpi * 32) {
+        const int row = rb * rbrows + r;
+        const long long prow = static_cast<long long>(row / P.per) * P.rows_seq + P.row_off + row % P.per;
+        float2 out;
+        if (P.greedy) {
+          ArgMax m2{-kInf, -1};
+          bool bad = false;
+          for (int w = 0; w < 4; ++w) {
+            const float2 st = state[w * kPairMaxRows + r];
+            m2 = am_merge(m2, ArgMax{st.x, __float_as_int(st.y)});
+            bad |= sbad[w * kPairMaxRows + r] != 0;
+          }
+          out = make_float2(bad ? __int_as_float(0x7fc00000) : m2.v, __int_as_float(m2.i));
+        } else {
+          MaxSum m2{-kInf, 0.f};
+          for (int w = 0; w < 4; ++w) {
+            const float2 st = state[w * kPairMaxRows + r];
+            m2 = ms_merge(m2, MaxSum{st.x, st.y}, c);
+          }
+          out = make_float2(m2.m, m2.s);
+        }
+        if (*fault) out = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+        P.partials[prow * P.chunks + blockIdx.x] = out;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpi * 32) : "memory");
+    }
+  }
+
+  __syncthreads();
+  if (!lead && threadIdx.x == 0) {
+    // tell the even CTA how many stages this CTA's producer issued: their
+    // copies count on its barriers
+    const uint32_t dst = cluster_addr(&peer_issued_s, 0);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(issued_s) : "memory");
+  }
+  cluster_arrive();
+  cluster_wait();
+  if (*fault && lead && threadIdx.x == 0) {
+    // copies still in flight (this CTA's or the odd CTA's) land before
+    // either CTA exits: wait (bounded) for the last phase of every stage
+    const int issued = max(issued_s, peer_issued_s);
+    for (int k = max(0, issued - P.stages); k < issued; ++k)
+      mbar_wait(&full[k % P.stages], static_cast<unsigned>(k / P.stages) & 1u);
+  }
+  if (*fault && threadIdx.x == 0 && P.error_word) atomicOr(P.error_word, SPEC_ERR_INTERNAL);
+  __syncthreads();
+  cluster_arrive();  // neither CTA leaves while the other may still signal or read it
+  cluster_wait();
+  if (warp == kPairIss0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -446,11 +783,11 @@ cudaError_t smem_attribute() {
   return e;
 }
 
-// Partial columns the workspace is sized for: at most one per 128-entry
-// tile (the smallest vocabulary tile) and at most kMaxChunks.
+// Partial columns the workspace is sized for: two per 256-entry tile (a CTA
+// pair's; at least one per 128-entry tile) and at most kMaxChunks.
 int lm_chunks(int V) {
-  const int ntv = (V + 127) / 128;
-  return ntv < kMaxChunks ? ntv : kMaxChunks;
+  const int n = 2 * ((V + kPairM - 1) / kPairM);
+  return n < kMaxChunks ? n : kMaxChunks;
 }
 
 // Row tiles of the largest row block of a head with R rows.
@@ -524,6 +861,76 @@ cudaError_t launch_head(const void* x, long long R, int d, const void* w, int V,
   return cudaGetLastError();
 }
 
+// CTA pairs of lm_head_pair_kernel that can be resident at once (a pair
+// must fit in one GPC), cached per device.
+cudaError_t pair_slots(int* out) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  const int dyn = kPairRing + kPairExtra + 1024;
+  e = cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, lm_head_pair_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  cache[dev] = n;
+  *out = n;
+  return cudaSuccess;
+}
+
+// One head on `pairs` CTA pairs.  Rows are taken in blocks of up to 512 (two
+// chunks of up to 256 when a block holds more than 256 rows); the chunk width
+// is the block's rows split evenly, rounded up to a multiple of 16.
+cudaError_t launch_head_pair(const void* x, long long R, int d, const void* w, int V, int pairs,
+                             const LmPairParams& proto, cudaStream_t s) {
+  LmPairParams P = proto;
+  P.R = static_cast<int>(R);
+  P.V = V;
+  P.d = d;
+  P.nkb = (d + kBK - 1) / kBK;
+  const int rb = static_cast<int>(R < kPairMaxRows ? R : kPairMaxRows);
+  P.nch = rb > 256 ? 2 : 1;
+  P.nc = ((rb + P.nch - 1) / P.nch + 15) / 16 * 16;
+  P.ntv = (V + kPairM - 1) / kPairM;
+  CUtensorMap tx, tw;
+  if (!make_map(&tx, x, R, d, P.nc / 2) || !make_map(&tw, w, V, d, 128)) return cudaErrorInvalidValue;
+  const int stage_bytes = kPairWBytes + P.nch * (P.nc / 2) * kBK * 2;
+  P.stages = min(kPairMaxStages, kPairRing / stage_bytes);
+  const int dyn = P.stages * stage_bytes + kPairExtra + 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lm_head_pair_kernel, tx, tw, P);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -568,6 +975,14 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   const int bv_d = vocab_tile(row_tiles(rows_d > 0 ? rows_d : 1), a->V, slots);
   int chunks = min(slots, (a->V + bv_t - 1) / bv_t);
   if (!greedy && gamma > 0) chunks = min(chunks, (a->V + bv_d - 1) / bv_d);
+  int pairs = 0;
+  const bool use_pair = rows_t >= kPairMinRows;
+  if (use_pair) {
+    cudaError_t pe = pair_slots(&pairs);
+    if (pe != cudaSuccess || pairs < 1) return SPEC_ECUDA;
+    pairs = min(pairs, (a->V + kPairM - 1) / kPairM);
+    chunks = 2 * pairs;
+  }
   const long long ldl = logit_ld(a->V);
   float* tlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials);
   float* dlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials + L.tlogits);
@@ -582,11 +997,25 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   proto.error_word = a->error_word;
 
   // target head: rows (b, i), i <= gamma, statistics rows 0 .. gamma
+  LmPairParams pp{};
+  pp.rows_seq = rows_seq;
+  pp.chunks = chunks;
+  pp.greedy = proto.greedy;
+  pp.c = proto.c;
+  pp.partials = proto.partials;
+  pp.ldl = ldl;
+  pp.error_word = a->error_word;
   LmParams pt = proto;
   pt.per = gamma + 1;
   pt.row_off = 0;
   pt.logits = tlog;
-  cudaError_t e = launch_head(a->h_target, rows_t, a->d_target, a->w_target, a->V, bv_t, pt, stream);
+  LmPairParams ppt = pp;
+  ppt.per = gamma + 1;
+  ppt.row_off = 0;
+  ppt.logits = tlog;
+  cudaError_t e = use_pair
+                      ? launch_head_pair(a->h_target, rows_t, a->d_target, a->w_target, a->V, pairs, ppt, stream)
+                      : launch_head(a->h_target, rows_t, a->d_target, a->w_target, a->V, bv_t, pt, stream);
   if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   if (!greedy && gamma > 0) {
     // draft head: rows (b, i), i < gamma, statistics rows gamma + 1 ..
@@ -594,7 +1023,12 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
     pd.per = gamma;
     pd.row_off = gamma + 1;
     pd.logits = dlog;
-    e = launch_head(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, bv_d, pd, stream);
+    LmPairParams ppd = pp;
+    ppd.per = gamma;
+    ppd.row_off = gamma + 1;
+    ppd.logits = dlog;
+    e = use_pair ? launch_head_pair(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, pairs, ppd, stream)
+                     : launch_head(a->h_draft, rows_d, a->d_draft, a->w_draft, a->V, bv_d, pd, stream);
     if (e != cudaSuccess) return e == cudaErrorInvalidValue ? SPEC_EINVAL : SPEC_ECUDA;
   }
 

@@ -123,6 +123,61 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 }
 
 // ---------------------------------------------------------------------------
+// CTA pairs (cta_group::2): the two CTAs of a cluster of two act as one MMA
+// unit.  A of an M = 256 product is split by rows (rows 0-127 in the even
+// CTA's shared memory, 128-255 in the odd CTA's, at the same address), B by
+// its N rows (the first N/2 in the even CTA, the rest in the odd one), and D
+// by rows (each CTA's TMEM lanes 0-127 hold its 128 rows, all N columns).
+// Threads of the even CTA issue the MMAs.  Allocation, relinquishing and
+// deallocation are collective: one warp of each CTA of the pair executes
+// them.  Within a kernel every tcgen05 instruction uses the same group size.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A * B^T over the pair, M = 256, N x 16, bfloat16 in, float32 out.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+
+// Arrive once, when every pair MMA this thread issued so far has completed,
+// on the mbarrier at `bar`'s offset in each CTA of `cta_mask` (cluster ranks).
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Address of `local`'s counterpart in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, unsigned rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
+  return a;
+}
+
+// One arrival on an mbarrier of another CTA of the cluster (address from
+// cluster_addr), ordered after this thread's earlier memory accesses.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // tensor-map bulk copies
 // ---------------------------------------------------------------------------
 // Copy the box at element coordinates (x, y) of the 2-D tensor described by
@@ -143,6 +198,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
                : "memory");
+}
+
+// Pair form of tma_load_2d: the box lands in this CTA's shared memory at
+// `dst`, and its bytes are counted on the mbarrier at cluster address
+// `cluster_bar`, which may be the peer CTA's (the even CTA of the pair
+// counts both CTAs' operand copies).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, int x, int y, uint32_t cluster_bar) {
+  if (kDebugChecks && ((x & 7) != 0 || (smem_addr(dst) & 1023u) != 0)) return;
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -370,12 +370,12 @@ def test_lm_head_argument_errors_and_workspace(lib):
     assert greedy == -(-64 * 6 * 256 * 8 // 256) * 256
     assert lib.spec_lm_head_chain_workspace_size(0, 5, 100, _lib.SPEC_SAMPLE) == 0
     assert lib.spec_lm_head_chain_workspace_size(4, 33, 100, _lib.SPEC_SAMPLE) == 0
-    # the layout the binding's logits views assume: one partial column per
-    # 128-entry vocabulary tile (at most 256), then the target and draft rows
+    # the layout the binding's logits views assume: two partial columns per
+    # 256-entry vocabulary tile (at most 256), then the target and draft rows
     # with a row stride of V rounded up to 8, each part rounded up to 256 B
     for B, g, V in ((6, 4, 9000), (5, 3, 5000), (3, 4, 1000), (2, 0, 100), (7, 2, 257), (64, 5, 128256)):
         up = lambda n: -(-n // 256) * 256
-        chunks = min((V + 127) // 128, 256)
+        chunks = min(2 * ((V + 255) // 256), 256)
         ldl = (V + 7) // 8 * 8
         part = up(B * (2 * g + 1) * chunks * 8)
         assert lib.spec_lm_head_chain_workspace_size(B, g, V, _lib.SPEC_SAMPLE) == \

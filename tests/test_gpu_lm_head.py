@@ -134,6 +134,9 @@ CASES = [
     W(BASE, name="v5000_dt200_dd104_g3", B=5, gamma=3, V=5000, d_target=200, d_draft=104),
     W(BASE, name="rows180_v3001_d128", B=30, gamma=5, V=3001, d_target=128, d_draft=128, temperature=1.0),
     W(BASE, name="rows560_two_row_blocks", B=80, gamma=6, V=3000, d_target=128, d_draft=64),
+    # 270 / 216 rows: CTA pairs, chunks of 144 / 112 rows partly past the
+    # last row, a ragged vocabulary tile and a ragged last K step
+    W(BASE, name="pairs_rows270_v5001_d200", B=54, gamma=4, V=5001, d_target=200, d_draft=200),
     W(BASE, name="g0_bonus_only", B=6, gamma=0, V=2000, d_target=64, d_draft=64),
     W(BASE, name="v40000_d1024_T1.3", B=4, gamma=5, V=40000, d_target=1024, d_draft=1024, temperature=1.3),
 ]
@@ -186,11 +189,12 @@ def test_lm_head_matches_stored_logit_path(cuda_device):
         assert np.array_equal(g[k][~flagged], gc[k][~flagged]), k
 
 
-def test_lm_head_data_errors(cuda_device):
+@pytest.mark.parametrize("B", [6, 64], ids=["single_cta", "cta_pairs"])
+def test_lm_head_data_errors(cuda_device, B):
     # a drafted token out of range, and NaN hidden states (their logit rows
     # are NaN): those sequences get the data-error bits and empty outputs,
-    # the others are unaffected
-    spec = W(BASE, B=6, gamma=3, V=3000, d_target=128, d_draft=128)
+    # the others are unaffected (B = 64: 256 target rows, the CTA-pair kernel)
+    spec = W(BASE, B=B, gamma=3, V=3000, d_target=128, d_draft=128)
     w = synth.make(spec, seed=21)
     nan = synth.bf16_from_float32(np.array([np.nan], np.float32))[0]
     w["tokens"][1, 2] = spec.V
@@ -211,7 +215,9 @@ def test_lm_head_data_errors(cuda_device):
             assert np.array_equal(g[k][ok & ~flagged], o[k][ok & ~flagged]), (greedy, k)
 
 
-def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device):
+@pytest.mark.parametrize("B,ties", [(2, [230, 300, 35000, 39999]), (128, [100, 260, 35000, 39999])],
+                         ids=["single_cta", "cta_pairs"])
+def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device, B, ties):
     # Identical weight rows give bit-identical logits (same operands, same
     # accumulation order in every column), so each hidden row's maximum is
     # an exact tie between those vocabulary entries and the greedy argmax
@@ -219,13 +225,16 @@ def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device):
     # argmax).  With V = 40000 and 4 rows the head kernel's tiles are 144
     # entries wide and one CTA of a 152-SM part owns tiles 1 and 2; its first
     # epilogue half sees entry 300 (tile 2) and its second half entry 230
-    # (tile 1), so the merge of the two halves must pick 230.
+    # (tile 1), so the merge of the two halves must pick 230.  With 256 rows
+    # (B = 128) the CTA-pair kernel runs: the even CTA of the first pair holds
+    # entries 0-127 (tile 0) and 256-383 (tile 1); its lane quarter 0 sees 260
+    # and its quarter 3 sees 100, and the per-row merge of the quarters (in
+    # quarter order) must pick 100.
     from draft_verification_gb300 import LmHeadChainPlan
     rng = np.random.default_rng(5)
-    B, g, V, d = 2, 1, 40000, 64
+    g, V, d = 1, 40000, 64
     h = synth.bf16_from_float32((np.abs(rng.normal(size=(B, g + 1, d))) + 0.5).astype(np.float32))
     w = synth.bf16_from_float32((0.01 * rng.normal(size=(V, d))).astype(np.float32))
-    ties = [230, 300, 35000, 39999]
     w[ties] = synth.bf16_from_float32(np.ones(d, np.float32))
     tokens = np.full((B, g), 7, np.int32)  # never the argmax: the first test rejects
     zeros = np.zeros((B, g), np.float32)
