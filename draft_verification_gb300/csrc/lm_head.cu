@@ -402,9 +402,10 @@ constexpr int kPairM = 256;              // vocabulary entries per pair tile
 constexpr int kPairMaxRows = 512;        // hidden rows per row block (TMEM columns)
 constexpr int kPairRing = 168 * 1024;    // ring budget per CTA
 constexpr int kPairMaxStages = 12;
-// CTA pairs for calls whose target head has at least this many rows (the
-// products dominate: c3-sized heads 3-4 % faster, 2304 rows 15 %); smaller
-// calls stream the weights faster on single CTAs (B = 4 and 16: 15-20 %)
+// CTA pairs only for calls whose target head has at least this many rows
+// (the products dominate; smaller calls stream the weights faster on single
+// CTAs: B = 4 and 16 at V = 128256 15-20 %), and only when the pairs' coarser
+// 256-entry tiles do not balance worse than the single-CTA tiles (below)
 constexpr int kPairMinRows = 256;
 constexpr int kPairWBytes = 128 * kBK * 2;  // a CTA's weight tile: 16 KB
 constexpr int kPairIssuers = 2;          // warps 9 and 10 of the even CTA: one chunk each
@@ -976,13 +977,20 @@ extern "C" spec_status spec_verify_chain_lm_head(const spec_lm_head_chain_args* 
   int chunks = min(slots, (a->V + bv_t - 1) / bv_t);
   if (!greedy && gamma > 0) chunks = min(chunks, (a->V + bv_d - 1) / bv_d);
   int pairs = 0;
-  const bool use_pair = rows_t >= kPairMinRows;
+  bool use_pair = rows_t >= kPairMinRows;
   if (use_pair) {
     cudaError_t pe = pair_slots(&pairs);
     if (pe != cudaSuccess || pairs < 1) return SPEC_ECUDA;
     pairs = min(pairs, (a->V + kPairM - 1) / kPairM);
-    chunks = 2 * pairs;
+    // the busier of the two launches' slowest unit: a pair's 256-entry
+    // tile takes about 36 us at 384 rows, a CTA's tile about 46 us per 144
+    // entries (measured); the pairs' coarser tiles can balance worse
+    const int ntv_pair = (a->V + kPairM - 1) / kPairM;
+    const double t_pair = 36.0 * static_cast<double>((ntv_pair + pairs - 1) / pairs);
+    const double t_single = 46.0 / 144.0 * bv_t * static_cast<double>(((a->V + bv_t - 1) / bv_t + chunks - 1) / chunks);
+    use_pair = t_pair < t_single;
   }
+  if (use_pair) chunks = 2 * pairs;
   const long long ldl = logit_ld(a->V);
   float* tlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials);
   float* dlog = greedy ? nullptr : reinterpret_cast<float*>(ws + L.partials + L.tlogits);

@@ -215,9 +215,9 @@ def test_lm_head_data_errors(cuda_device, B):
             assert np.array_equal(g[k][ok & ~flagged], o[k][ok & ~flagged]), (greedy, k)
 
 
-@pytest.mark.parametrize("B,ties", [(2, [230, 300, 35000, 39999]), (128, [100, 260, 35000, 39999])],
+@pytest.mark.parametrize("B,V,ties", [(2, 40000, [230, 300, 35000, 39999]), (128, 75776, [100, 260, 35000, 39999])],
                          ids=["single_cta", "cta_pairs"])
-def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device, B, ties):
+def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device, B, V, ties):
     # Identical weight rows give bit-identical logits (same operands, same
     # accumulation order in every column), so each hidden row's maximum is
     # an exact tie between those vocabulary entries and the greedy argmax
@@ -226,13 +226,15 @@ def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device, B, ties):
     # entries wide and one CTA of a 152-SM part owns tiles 1 and 2; its first
     # epilogue half sees entry 300 (tile 2) and its second half entry 230
     # (tile 1), so the merge of the two halves must pick 230.  With 256 rows
-    # (B = 128) the CTA-pair kernel runs: the even CTA of the first pair holds
+    # (B = 128) and V = 75776 the CTA-pair kernel runs (on a 152-SM part its
+    # 296 tiles balance better over 76 pairs than the single-CTA tiles over
+    # 152 CTAs): the even CTA of the first pair holds
     # entries 0-127 (tile 0) and 256-383 (tile 1); its lane quarter 0 sees 260
     # and its quarter 3 sees 100, and the per-row merge of the quarters (in
     # quarter order) must pick 100.
     from draft_verification_gb300 import LmHeadChainPlan
     rng = np.random.default_rng(5)
-    g, V, d = 1, 40000, 64
+    g, d = 1, 64
     h = synth.bf16_from_float32((np.abs(rng.normal(size=(B, g + 1, d))) + 0.5).astype(np.float32))
     w = synth.bf16_from_float32((0.01 * rng.normal(size=(V, d))).astype(np.float32))
     w[ties] = synth.bf16_from_float32(np.ones(d, np.float32))
