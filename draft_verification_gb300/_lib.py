@@ -142,6 +142,7 @@ SIGNATURES = {
     "spec_clasp_layer_select": (C.c_int, [C.POINTER(ClaspArgs), _vp]),
     "spec_status_string": (C.c_char_p, [C.c_int]),
     "spec_test_inject_copy_timeout": (C.c_int, [C.c_int]),
+    "spec_test_inject_head_copy_timeout": (C.c_int, [C.c_int]),
     "spec_lm_head_chain_workspace_size": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spec_verify_chain_lm_head": (C.c_int, [C.POINTER(LmHeadChainArgs), _vp]),
 }

@@ -98,6 +98,12 @@ __device__ __forceinline__ void st_global_v8(float* dst, const float* v) {
                : "memory");
 }
 
+// Test hook (spec_test_inject_head_copy_timeout): nonzero makes every stage
+// of both head kernels expect 16 bytes that never come (on the even CTA's
+// barrier for a pair), so that the MMA issuers' bounded waits give up.  Zero
+// in normal operation.
+__device__ int g_lm_copy_timeout_test = 0;
+
 __device__ __forceinline__ bool lm_wait(uint64_t* bar, unsigned parity, volatile int* fault) {
   for (int i = 0; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_w);
+      const unsigned extra_tx = g_lm_copy_timeout_test ? 16u : 0u;
       int it = 0;
       const int slab_steps = (v_t1 - v_t0) * P.nkb;
       for (int rb = 0; rb < nrb && !*fault; ++rb) {
@@ -174,7 +181,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const unsigned ph = static_cast<unsigned>(it / P.stages) & 1u;
             if (!lm_wait(&empty[s], ph ^ 1u, fault)) break;
             unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
-            mbar_expect_tx(&full[s], static_cast<unsigned>(wbytes + kTileBytes * rt));
+            mbar_expect_tx(&full[s], static_cast<unsigned>(wbytes + kTileBytes * rt) + extra_tx);
             tma_load_2d(st, &tm_w, kb * kBK, vt * P.bv, &full[s]);
             for (int t = 0; t < rt; ++t)
               tma_load_2d(st + wbytes + kTileBytes * t, &tm_x, kb * kBK, rb * kRowBlock + t * kBR, &full[s]);
@@ -506,6 +513,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_w);
+      const unsigned extra_tx = g_lm_copy_timeout_test ? 16u : 0u;
       int it = 0;
       for (int rb = 0; rb < nrb && !*fault; ++rb) {
         const int rows = min(rbrows, P.R - rb * rbrows);
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
             const uint32_t fb = cluster_addr(&full[s], 0);
             // the even CTA's barrier counts both CTAs' bytes
-            if (lead) mbar_expect_tx(&full[s], 2u * static_cast<unsigned>(kPairWBytes + nch * xhalf));
+            if (lead) mbar_expect_tx(&full[s], 2u * static_cast<unsigned>(kPairWBytes + nch * xhalf) + extra_tx);
             tma_load_2d_pair(st, &tm_w, kb * kBK, vt * kPairM + rank * 128, fb);
             for (int j = 0; j < nch; ++j)
               tma_load_2d_pair(st + kPairWBytes + j * xhalf, &tm_x, kb * kBK, rb * rbrows + j * P.nc + rank * (P.nc / 2),
@@ -935,7 +943,13 @@ cudaError_t launch_head_pair(const void* x, long long R, int d, const void* w, i
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
 }  // namespace sv
+
+extern "C" spec_status spec_test_inject_head_copy_timeout(int enable) {
+  const int v = enable ? 1 : 0;
+  return cudaMemcpyToSymbol(sv::g_lm_copy_timeout_test, &v, sizeof(v)) == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
 
 extern "C" size_t spec_lm_head_chain_workspace_size(int B, int gamma, int V, spec_mode mode) {
   if (B < 1 || gamma < 0 || gamma > 32 || V < 1) return 0;

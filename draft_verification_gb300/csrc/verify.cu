@@ -80,13 +80,18 @@ __device__ __forceinline__ const T* stats_row(const StatsParams& G, int b, int r
 }
 
 // Row statistics of sequence b.  The chunk partials of a group of rows are
-// loaded at once (at most 4 per thread) into `stage`, then one thread merges
-// each row in chunk order and calls emit(row, stats, ok): stats is (max,
-// sum), or (unused, argmax bits) in greedy mode; ok is false for a row with a
-// NaN or +inf, or without a finite entry.
-template <bool kGreedy, typename Emit>
+// loaded at once (at most 4 per thread) into `stage`; then each row is
+// merged in a fixed order, so every CTA of a cluster gets the same bits.
+// kWide false: one thread per row, in chunk order (the statistics kernel's
+// few chunks per row; a shuffle tree is no faster there).  kWide true: one
+// warp per row, each lane merging its chunks k, k + 32, ... in order and the
+// warp combining them with shuffles (the LM head's up to 256 partials per
+// row).  One thread per row calls emit(row, stats, ok): stats is (max, sum),
+// or (unused, argmax bits) in greedy mode; ok is false for a row with a NaN
+// or +inf, or without a finite entry.
+template <bool kGreedy, bool kWide, typename Emit>
 __device__ void merge_stats(const StatsParams& G, int b, float2* stage, Emit emit) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = G.chunks, R = G.rows_per_seq;
   const int rpg = max(1, kStage / C);
   const float2* part = G.partials + static_cast<long long>(b) * R * C;
@@ -106,14 +111,36 @@ __device__ void merge_stats(const StatsParams& G, int b, float2* stage, Emit emi
       if (i < n) stage[i] = v[q];
     }
     __syncthreads();
-    for (int r = tid; r < nr; r += kThreads) {
-      if constexpr (kGreedy) {
-        bool bad;
-        const ArgMax am = combine_row_argmax(stage + r * C, C, bad);
-        emit(r0 + r, make_float2(0.f, __int_as_float(am.i)), !bad && am.i >= 0);
-      } else {
-        const MaxSum ms = combine_row(stage + r * C, C, G.c);
-        emit(r0 + r, make_float2(ms.m, ms.s), row_stats_ok(ms));
+    if constexpr (!kWide) {
+      for (int r = tid; r < nr; r += kThreads) {
+        if constexpr (kGreedy) {
+          bool bad;
+          const ArgMax am = combine_row_argmax(stage + r * C, C, bad);
+          emit(r0 + r, make_float2(0.f, __int_as_float(am.i)), !bad && am.i >= 0);
+        } else {
+          const MaxSum ms = combine_row(stage + r * C, C, G.c);
+          emit(r0 + r, make_float2(ms.m, ms.s), row_stats_ok(ms));
+        }
+      }
+    } else {
+      for (int r = warp; r < nr; r += kThreads / 32) {  // warp-uniform
+        const float2* pr = stage + r * C;
+        if constexpr (kGreedy) {
+          ArgMax acc{-kInf, -1};
+          bool bad = false;
+          for (int k = lane; k < C; k += 32) {
+            if (pr[k].x != pr[k].x) bad = true;
+            acc = am_merge(acc, ArgMax{pr[k].x, __float_as_int(pr[k].y)});
+          }
+          acc = am_warp_reduce(acc);
+          bad = __any_sync(0xffffffffu, bad);
+          if (lane == 0) emit(r0 + r, make_float2(0.f, __int_as_float(acc.i)), !bad && acc.i >= 0);
+        } else {
+          MaxSum acc{-kInf, 0.f};
+          for (int k = lane; k < C; k += 32) acc = ms_merge(acc, MaxSum{pr[k].x, pr[k].y}, G.c);
+          acc = ms_warp_reduce(acc, G.c);
+          if (lane == 0) emit(r0 + r, make_float2(acc.m, acc.s), row_stats_ok(acc));
+        }
       }
     }
     __syncthreads();
@@ -121,10 +148,10 @@ __device__ void merge_stats(const StatsParams& G, int b, float2* stage, Emit emi
 }
 
 // Statistics into separate arrays; returns the error bits (or'ed into *err_s).
-template <bool kGreedy>
+template <bool kGreedy, bool kWide = false>
 __device__ int gather_stats(const StatsParams& G, int b, float* st_m, float* st_s, int* st_arg, int* err_s,
                             float2* stage) {
-  merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
+  merge_stats<kGreedy, kWide>(G, b, stage, [&](int r, float2 v, bool ok) {
     if (kGreedy) {
       st_arg[r] = __float_as_int(v.y);
     } else {
@@ -242,7 +269,8 @@ __device__ void chain_error_out(const ChainParams& P, int b, int err) {
   }
 }
 
-template <typename T>
+// kWide: the row partials come from the LM head (many chunks per row).
+template <typename T, bool kWide = false>
 __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParams G, const ChainParams P) {
   __shared__ ChainSmem cs;
   __shared__ float2 stage[kStage];
@@ -250,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParam
   const int g = P.gamma;
   chain_inputs<T>(P, b, cs, false);
   pdl_wait();
-  const int err = gather_stats<true>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  const int err = gather_stats<true, kWide>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
   if (err) {
     chain_error_out(P, b, err);
     return;
@@ -277,8 +305,9 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_kernel(const StatsParam
 // dynamic shared memory at once (one bulk-copy round trip instead of a ring
 // of stages) and the drawing CTA finds the element there; used where the
 // walk runs after the statistics have been read (the last batch group), so
-// its larger shared memory does not crowd the statistics kernel.
-template <typename T, bool kResident>
+// its larger shared memory does not crowd the statistics kernel.  kWide:
+// the row partials come from the LM head (many chunks per row).
+template <typename T, bool kResident, bool kWide = false>
 __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsParams G, const ChainParams P) {
   __shared__ ChainSmem cs;
   __shared__ PassSmem ps;
@@ -297,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_walk_kernel(const StatsPara
   cluster_enter();
   chain_inputs<T>(P, b, cs, true);
   pdl_wait();  // the statistics are complete and visible from here on
-  const int err = gather_stats<false>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
+  const int err = gather_stats<false, kWide>(G, b, cs.st_m, cs.st_s, cs.st_arg, &cs.err, stage);
   cluster_ready();
   if (err) {  // every CTA of the cluster sees the same error; the lead reports it
     if (lead) chain_error_out(P, b, err);
@@ -947,7 +976,7 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const StatsParams G, con
   }
   if constexpr (!kConsulted) {
     pdl_wait();
-    merge_stats<kGreedy>(G, b, stage, [&](int r, float2 v, bool ok) {
+    merge_stats<kGreedy, false>(G, b, stage, [&](int r, float2 v, bool ok) {
       ts.st[r] = v;
       if (!ok) atomicOr(&err_s, SPEC_ERR_NONFINITE);
     });
@@ -1630,8 +1659,8 @@ cudaError_t launch_cascade(const StatsParams& G, const CascadeParams& p, bool bf
 cudaError_t launch_chain_walk_f32(const StatsParams& G, const ChainParams& p, bool greedy, cudaStream_t s) {
   // plain stream order: the walk reads the logits at the drafted tokens
   // before it waits, and here those logits come from the preceding kernel
-  if (greedy) return launch_dependent(chain_greedy_kernel<float>, dim3(G.B), 0, 0, G, p, s, -1, false);
-  return launch_walk(chain_walk_kernel<float, false>, kStageBytes, kStageBytes, G, p, s, -1, false);
+  if (greedy) return launch_dependent(chain_greedy_kernel<float, true>, dim3(G.B), 0, 0, G, p, s, -1, false);
+  return launch_walk(chain_walk_kernel<float, false, true>, kStageBytes, kStageBytes, G, p, s, -1, false);
 }
 
 }  // namespace sv

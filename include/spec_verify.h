@@ -527,8 +527,8 @@ spec_status spec_clasp_layer_select(const spec_clasp_args* args, cudaStream_t st
 /*    accept tests; the walk reads just those rows.                          */
 /*  - Same outputs, data-error bits and rules as spec_verify_chain (outputs  */
 /*    as in spec_chain_args).  A bounded wait in the head kernel that gives  */
-/*    up marks its rows non-finite (bit 4 on the affected sequences) and     */
-/*    sets SPEC_ERR_INTERNAL in *error_word.                                 */
+/*    up marks its rows non-finite (SPEC_ERR_NONFINITE on the affected       */
+/*    sequences) and sets SPEC_ERR_INTERNAL in *error_word.                  */
 /*  - Launches: one head kernel per head (the draft head only in sampling    */
 /*    mode with gamma > 0), then one walk kernel.                            */
 /* ---------------------------------------------------------------------- */
@@ -587,6 +587,19 @@ const char* spec_status_string(spec_status status);
 /* SPEC_ECUDA if the copy fails.                                           */
 /* ---------------------------------------------------------------------- */
 spec_status spec_test_inject_copy_timeout(int enable);
+
+/* ---------------------------------------------------------------------- */
+/* The same kind of test hook for spec_verify_chain_lm_head.  While enabled */
+/* on the current device, every pipeline stage of the head kernels (single */
+/* CTAs or CTA pairs) expects 16 bytes more than it copies, so the MMA      */
+/* issuers give up after about 65 ms: every row of the head comes out      */
+/* non-finite (SPEC_ERR_NONFINITE on every sequence, with empty outputs)   */
+/* and *error_word gets SPEC_ERR_INTERNAL.  Nothing faults and nothing is  */
+/* left in flight.  Synchronous; affects calls launched after it returns.  */
+/* Tests only: leave it disabled (the default) in any other use.           */
+/* SPEC_ECUDA if the copy fails.                                           */
+/* ---------------------------------------------------------------------- */
+spec_status spec_test_inject_head_copy_timeout(int enable);
 
 #ifdef __cplusplus
 }

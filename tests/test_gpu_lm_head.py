@@ -215,6 +215,35 @@ def test_lm_head_data_errors(cuda_device, B):
             assert np.array_equal(g[k][ok & ~flagged], o[k][ok & ~flagged]), (greedy, k)
 
 
+@pytest.mark.parametrize("B", [4, 64], ids=["single_cta", "cta_pairs"])
+def test_lm_head_wait_gives_up_with_internal_error(cuda_device, B):
+    # The head's copy-timeout test hook: every stage of the head kernel
+    # expects 16 bytes that never come, so its MMA issuers' bounded waits
+    # give up (about 65 ms, then a bounded wait for the stages already
+    # issued).  Every row comes out non-finite, so every sequence reports
+    # SPEC_ERR_NONFINITE with empty outputs, and the head sets
+    # SPEC_ERR_INTERNAL in the error word.  B = 4: 16 target rows, single
+    # CTAs; B = 64: 256 rows, CTA pairs (both CTAs of a pair give up, and the
+    # even one waits for the odd one's copies before either leaves).
+    # Afterwards the same calls, hook off, are correct.
+    from draft_verification_gb300 import _lib
+    lib = _lib.lib()
+    spec = W(BASE, B=B, gamma=3, V=3000 if B == 64 else 5001, d_target=128 if B == 64 else 256,
+             d_draft=128 if B == 64 else 256)
+    w = synth.make(spec, seed=23)
+    for greedy in (False, True):
+        assert lib.spec_test_inject_head_copy_timeout(1) == _lib.SPEC_OK
+        try:
+            g, _ = run(w, cuda_device, greedy=greedy)
+        finally:
+            assert lib.spec_test_inject_head_copy_timeout(0) == _lib.SPEC_OK
+        assert (g["seq_error"] == _lib.ERR_NONFINITE).all(), (greedy, g["seq_error"])
+        assert g["error_word"][0] & _lib.ERR_INTERNAL, (greedy, g["error_word"])
+        assert (g["accept_len"] == 0).all() and (g["out_token"] == -1).all()
+        assert np.array_equal(g["rollback_idx"], w["prefix_len"])
+    check(w, cuda_device, np.arange(spec.B))
+
+
 @pytest.mark.parametrize("B,V,ties", [(2, 40000, [230, 300, 35000, 39999]), (128, 75776, [100, 260, 35000, 39999])],
                          ids=["single_cta", "cta_pairs"])
 def test_lm_head_greedy_ties_go_to_the_lowest_index(cuda_device, B, V, ties):
