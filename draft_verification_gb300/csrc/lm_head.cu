@@ -397,13 +397,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 // odd CTA rows 128-255) and the hidden rows as B, in one or two chunks of
 // Nc <= 256 rows (the even CTA holds the first Nc/2 rows of each chunk, the
 // odd CTA the rest).  Each CTA therefore copies 16 KB of weights and half of
-// the hidden rows per stage, and its tensor pipe reads half of B.  Warps 5
-// and 6 of the even CTA each issue one chunk's products.  The accumulators
+// the hidden rows per stage, and its tensor pipe reads half of B.  Warps 17
+// and 18 of the even CTA each issue one chunk's products.  The accumulators
 // land with one vocabulary entry per TMEM lane and one hidden row per
-// column; the epilogue (warps 0-3 of each CTA) transposes each 32 x 32 block
-// through shared memory, so that lane l folds row l's 32 vocabulary entries
-// in order into a per-warp running state; at the end of a row block the four
-// warps' states are merged into one partial per row and CTA.
+// column; the epilogue (warps 0-15 of each CTA, four per TMEM lane quarter)
+// transposes each 32-entry x 16-row block through shared memory, so that
+// lanes l and l + 16 hold 16 entries each of one row, fold them and combine
+// by one shuffle into the quarter's running state of the row; at the end of
+// a row block the four quarters' states are merged into one partial per row
+// and CTA.
 // ---------------------------------------------------------------------------
 constexpr int kPairM = 256;              // vocabulary entries per pair tile
 constexpr int kPairMaxRows = 512;        // hidden rows per row block (TMEM columns)
@@ -415,12 +417,12 @@ constexpr int kPairMaxStages = 12;
 // 256-entry tiles do not balance worse than the single-CTA tiles (below)
 constexpr int kPairMinRows = 256;
 constexpr int kPairWBytes = 128 * kBK * 2;  // a CTA's weight tile: 16 KB
-constexpr int kPairIssuers = 2;          // warps 9 and 10 of the even CTA: one chunk each
-constexpr int kPairEpi = 8;              // epilogue warps: two per TMEM lane quarter
+constexpr int kPairIssuers = 2;          // warps 17 and 18 of the even CTA: one chunk each
+constexpr int kPairEpi = 16;             // epilogue warps: four per TMEM lane quarter
 constexpr int kPairProd = kPairEpi;      // the TMA producer warp
 constexpr int kPairIss0 = kPairEpi + 1;  // the first MMA-issuing warp
 constexpr int kPairThreads = 32 * (kPairEpi + 1 + kPairIssuers);
-constexpr int kPairScr = 32 * 33;        // floats of one warp's transpose block
+constexpr int kPairScr = 32 * 17;        // floats of one warp's transpose block (32 x 16, padded)
 constexpr int kPairExtra = 4 * kPairMaxRows * 8 + 4 * kPairMaxRows + kPairEpi * kPairScr * 4;  // states, flags, blocks
 
 struct LmPairParams {
@@ -575,19 +577,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     if (lane == 0) mbar_wait(&drain, 0);  // no product of the pair still reads or writes this CTA's memory
   } else {
-    // ---------------- epilogue (warps 0-7, both CTAs) ----------------
-    // warps q and q + 4 read TMEM lane quarter q; warp q + 4h takes the
-    // 32-row groups g with g % 2 == h
+    // ---------------- epilogue (warps 0-15, both CTAs) ----------------
+    // warps q, q + 4, q + 8 and q + 12 read TMEM lane quarter q; warp
+    // q + 4h takes the 32-row groups g with g % 4 == h
     const float c = P.c;
     const int q = warp & 3, h = warp >> 2;
+    constexpr int kPerQ = kPairEpi / 4;
     float2* my = state + q * kPairMaxRows;  // the quarter's running state of every row of the block
     unsigned char* mybad = sbad + q * kPairMaxRows;
     float* scr = scratch + warp * kPairScr;
+    const int rr = lane & 15, eh = lane >> 4;  // after the transpose: row rr of a half group, entries 16 eh ..
     int acc = 0;
     for (int rb = 0; rb < nrb; ++rb) {
       const int rows = min(rbrows, P.R - rb * rbrows);
       const int ngrp = (rows + 31) / 32;
-      for (int g = h; g < ngrp; g += 2) {
+      for (int g = h; g < ngrp; g += kPerQ) {
         my[g * 32 + lane] = P.greedy ? make_float2(-kInf, __int_as_float(-1)) : make_float2(-kInf, 0.f);
         mybad[g * 32 + lane] = 0;
       }
@@ -598,69 +602,74 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         tc_fence_after();
         const int vw = vt * kPairM + rank * 128 + q * 32;  // the quarter's first vocabulary entry
         const int nv = max(0, min(32, P.V - vw));            // of its 32 entries, those below V
-        for (int g = h; g < ngrp; g += 2) {
+        const int e0 = eh * 16;                              // this lane's first entry after the transpose
+        const int nl = max(0, min(16, nv - e0));             // of its 16 entries, those below V
+        for (int g = h; g < ngrp; g += kPerQ) {
           float x[32];
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * 32), x);
-          const int r0 = rb * rbrows + g * 32;  // hidden row of column 0 of the group
-          // transpose: lane l then holds row r0 + l's values at the
-          // quarter's 32 vocabulary entries, in ascending order
 #pragma unroll
-          for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = x[j];
-          __syncwarp();
-          float y[32];
+          for (int hh = 0; hh < 2; ++hh) {
+            // transpose the quarter's 32 entries x 16 rows: lane l then holds
+            // entries e0 .. e0 + 15 of row rr of the half group, in order
 #pragma unroll
-          for (int e = 0; e < 32; ++e) y[e] = scr[e * 33 + lane];
-          __syncwarp();
-          if (P.logits && r0 + lane < P.R) {
-            // row r0 + lane: 32 consecutive float32 logits, whole 32-byte sectors
-            float* dst = P.logits + static_cast<long long>(r0 + lane) * P.ldl + vw;
-            if (nv == 32) {
+            for (int j = 0; j < 16; ++j) scr[lane * 17 + j] = x[hh * 16 + j];
+            __syncwarp();
+            float y[16];
 #pragma unroll
-              for (int e = 0; e < 32; e += 8) st_global_v8(dst + e, y + e);
+            for (int i = 0; i < 16; ++i) y[i] = scr[(e0 + i) * 17 + rr];
+            __syncwarp();
+            const int si = g * 32 + hh * 16 + rr;  // the row's index within the block
+            const int row = rb * rbrows + si;      // its hidden row
+            if (P.logits && row < P.R) {
+              // 16 consecutive float32 logits: whole 32-byte sectors
+              float* dst = P.logits + static_cast<long long>(row) * P.ldl + vw + e0;
+              if (nl == 16) {
+                st_global_v8(dst, y);
+                st_global_v8(dst + 8, y + 8);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (i < nl) dst[i] = y[i];
+              }
+            }
+            const float2 cur = my[si];
+            // the row's maximum over its 32 entries, NaN-propagating: two
+            // chains per lane, then the lane pair (l, l ^ 16)
+            float ca = -kInf, cb = -kInf;
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              if (i < nl) ca = fmax_nan(ca, y[i]);
+              if (i + 1 < nl) cb = fmax_nan(cb, y[i + 1]);
+            }
+            float cm = fmax_nan(ca, cb);
+            cm = fmax_nan(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+            if (P.greedy) {
+              // NaN or +inf marks the row bad; a maximum strictly above the
+              // running one moves the argmax to its first entry (ties keep
+              // the lowest index)
+              if (!(cm < kInf) && eh == 0) mybad[si] = 1;
+              const bool up = cm > cur.x && cm < kInf;
+              int first = 32;
+#pragma unroll
+              for (int i = 15; i >= 0; --i)
+                if (up && i < nl && y[i] == cm) first = e0 + i;
+              first = min(first, __shfl_xor_sync(0xffffffffu, first, 16));
+              if (up && eh == 0) my[si] = make_float2(cm, __int_as_float(vw + first));
             } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (e < nv) dst[e] = y[e];
-            }
-          }
-          const float2 cur = my[g * 32 + lane];
-          if (P.greedy) {
-            // NaN-propagating maximum in two chains; NaN or +inf marks the
-            // row bad; a maximum strictly above the running one moves the
-            // argmax to its first entry (ties keep the lowest index)
-            float ca = -kInf, cb = -kInf;
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              if (e < nv) ca = fmax_nan(ca, y[e]);
-              if (e + 1 < nv) cb = fmax_nan(cb, y[e + 1]);
-            }
-            const float cm = fmax_nan(ca, cb);
-            if (!(cm < kInf) && nv > 0) mybad[g * 32 + lane] = 1;
-            if (cm > cur.x && cm < kInf) {
-              int first = 0;
-#pragma unroll
-              for (int e = 31; e >= 0; --e)
-                if (e < nv && y[e] == cm) first = e;
-              my[g * 32 + lane] = make_float2(cm, __int_as_float(vw + first));
-            }
-          } else {
-            float ca = -kInf, cb = -kInf;
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              if (e < nv) ca = fmax_nan(ca, y[e]);
-              if (e + 1 < nv) cb = fmax_nan(cb, y[e + 1]);
-            }
-            const float mn = fmax_nan(cur.x, fmax_nan(ca, cb));
-            if (mn != -kInf) {
-              const float Mn = scaled_max(mn, c);
-              const float scale = (cur.x == -kInf) ? 0.f : ex2(scaled_max(cur.x, c) - Mn);
+              const float mn = fmax_nan(cur.x, cm);
+              const float Mn = (mn == -kInf) ? 0.f : scaled_max(mn, c);
               float sa = 0.f, sb = 0.f;
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                if (e < nv) sa = __fadd_rn(sa, weight(y[e], c, Mn));
-                if (e + 1 < nv) sb = __fadd_rn(sb, weight(y[e + 1], c, Mn));
+              for (int i = 0; i < 16; i += 2) {
+                if (i < nl) sa = __fadd_rn(sa, weight(y[i], c, Mn));
+                if (i + 1 < nl) sb = __fadd_rn(sb, weight(y[i + 1], c, Mn));
               }
-              my[g * 32 + lane] = make_float2(mn, __fadd_rn(__fmul_rn(cur.y, scale), __fadd_rn(sa, sb)));
+              float sp = __fadd_rn(sa, sb);
+              sp = __fadd_rn(sp, __shfl_xor_sync(0xffffffffu, sp, 16));  // the same bits in both lanes
+              if (mn != -kInf && eh == 0) {
+                const float scale = (cur.x == -kInf) ? 0.f : ex2(scaled_max(cur.x, c) - Mn);
+                my[si] = make_float2(mn, __fadd_rn(__fmul_rn(cur.y, scale), sp));
+              }
             }
           }
         }
@@ -671,7 +680,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           else mbar_arrive_remote(cluster_addr(&tempty, 0));
         }
       }
-      // merge the four warps' states of each row, in warp order, into this
+      // merge the four quarters' states of each row, in quarter order, into this
       // CTA's partial (one column per CTA of the launch)
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpi * 32) : "memory");
       for (int r = static_cast<int>(threadIdx.x); r < rows; r += kPairEpi * 32) {
