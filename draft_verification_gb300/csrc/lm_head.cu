@@ -422,7 +422,8 @@ constexpr int kPairEpi = 16;             // epilogue warps: four per TMEM lane q
 constexpr int kPairProd = kPairEpi;      // the TMA producer warp
 constexpr int kPairIss0 = kPairEpi + 1;  // the first MMA-issuing warp
 constexpr int kPairThreads = 32 * (kPairEpi + 1 + kPairIssuers);
-constexpr int kPairScr = 32 * 17;        // floats of one warp's transpose block (32 x 16, padded)
+constexpr int kPairScrLd = 36;           // floats per row of a warp's transpose block (32 entries, padded)
+constexpr int kPairScr = 16 * kPairScrLd;  // floats of one warp's transpose block (16 rows x 32 entries)
 constexpr int kPairExtra = 4 * kPairMaxRows * 8 + 4 * kPairMaxRows + kPairEpi * kPairScr * 4;  // states, flags, blocks
 
 struct LmPairParams {
@@ -440,6 +441,40 @@ struct LmPairParams {
   long long ldl;
   int* error_word;
 };
+
+// Folds of one lane's 16 consecutive logits of a row, of which the first nl
+// are inside the vocabulary; kFull: all 16 are (no per-entry tests).
+// NaN-propagating maximum, in two independent chains.
+template <bool kFull>
+__device__ __forceinline__ float max16(const float* y, int nl) {
+  float ca = -kInf, cb = -kInf;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    if (kFull || i < nl) ca = fmax_nan(ca, y[i]);
+    if (kFull || i + 1 < nl) cb = fmax_nan(cb, y[i + 1]);
+  }
+  return fmax_nan(ca, cb);
+}
+// Sum of 2^(y c - Mn), in two independent chains.
+template <bool kFull>
+__device__ __forceinline__ float sum16(const float* y, int nl, float c, float Mn) {
+  float sa = 0.f, sb = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    if (kFull || i < nl) sa = __fadd_rn(sa, weight(y[i], c, Mn));
+    if (kFull || i + 1 < nl) sb = __fadd_rn(sb, weight(y[i + 1], c, Mn));
+  }
+  return __fadd_rn(sa, sb);
+}
+// The first i with y[i] == m, or 16.
+template <bool kFull>
+__device__ __forceinline__ int first16(const float* y, int nl, float m) {
+  int f = 16;
+#pragma unroll
+  for (int i = 15; i >= 0; --i)
+    if ((kFull || i < nl) && y[i] == m) f = i;
+  return f;
+}
 
 // Bounded wait with acquire semantics at cluster scope (arrivals come from
 // the peer CTA).
@@ -609,14 +644,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * 32), x);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            // transpose the quarter's 32 entries x 16 rows: lane l then holds
-            // entries e0 .. e0 + 15 of row rr of the half group, in order
+            // transpose the quarter's 32 entries x 16 rows: lane l writes
+            // its entry of every row, then reads entries e0 .. e0 + 15 of
+            // row rr of the half group (four 16-byte loads; the padded rows
+            // keep both sides free of bank conflicts)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) scr[lane * 17 + j] = x[hh * 16 + j];
+            for (int j = 0; j < 16; ++j) scr[j * kPairScrLd + lane] = x[hh * 16 + j];
             __syncwarp();
             float y[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = scr[(e0 + i) * 17 + rr];
+            for (int k = 0; k < 4; ++k) {
+              const float4 v = *reinterpret_cast<const float4*>(scr + rr * kPairScrLd + e0 + 4 * k);
+              y[4 * k] = v.x;
+              y[4 * k + 1] = v.y;
+              y[4 * k + 2] = v.z;
+              y[4 * k + 3] = v.w;
+            }
             __syncwarp();
             const int si = g * 32 + hh * 16 + rr;  // the row's index within the block
             const int row = rb * rbrows + si;      // its hidden row
@@ -633,15 +676,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               }
             }
             const float2 cur = my[si];
-            // the row's maximum over its 32 entries, NaN-propagating: two
-            // chains per lane, then the lane pair (l, l ^ 16)
-            float ca = -kInf, cb = -kInf;
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              if (i < nl) ca = fmax_nan(ca, y[i]);
-              if (i + 1 < nl) cb = fmax_nan(cb, y[i + 1]);
-            }
-            float cm = fmax_nan(ca, cb);
+            // the row's maximum over its 32 entries, NaN-propagating: each
+            // lane's 16, then the lane pair (l, l ^ 16)
+            float cm = nl == 16 ? max16<true>(y, nl) : max16<false>(y, nl);
             cm = fmax_nan(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
             if (P.greedy) {
               // NaN or +inf marks the row bad; a maximum strictly above the
@@ -650,21 +687,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               if (!(cm < kInf) && eh == 0) mybad[si] = 1;
               const bool up = cm > cur.x && cm < kInf;
               int first = 32;
-#pragma unroll
-              for (int i = 15; i >= 0; --i)
-                if (up && i < nl && y[i] == cm) first = e0 + i;
+              if (up) {
+                const int f = nl == 16 ? first16<true>(y, nl, cm) : first16<false>(y, nl, cm);
+                if (f < 16) first = e0 + f;
+              }
               first = min(first, __shfl_xor_sync(0xffffffffu, first, 16));
               if (up && eh == 0) my[si] = make_float2(cm, __int_as_float(vw + first));
             } else {
               const float mn = fmax_nan(cur.x, cm);
               const float Mn = (mn == -kInf) ? 0.f : scaled_max(mn, c);
-              float sa = 0.f, sb = 0.f;
-#pragma unroll
-              for (int i = 0; i < 16; i += 2) {
-                if (i < nl) sa = __fadd_rn(sa, weight(y[i], c, Mn));
-                if (i + 1 < nl) sb = __fadd_rn(sb, weight(y[i + 1], c, Mn));
-              }
-              float sp = __fadd_rn(sa, sb);
+              float sp = nl == 16 ? sum16<true>(y, nl, c, Mn) : sum16<false>(y, nl, c, Mn);
               sp = __fadd_rn(sp, __shfl_xor_sync(0xffffffffu, sp, 16));  // the same bits in both lanes
               if (mn != -kInf && eh == 0) {
                 const float scale = (cur.x == -kInf) ? 0.f : ex2(scaled_max(cur.x, c) - Mn);
