@@ -618,7 +618,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const float c = P.c;
     const int q = warp & 3, h = warp >> 2;
     constexpr int kPerQ = kPairEpi / 4;
-    float2* my = state + q * kPairMaxRows;  // the quarter's running state of every row of the block
+    constexpr int kGrpW = kPairMaxRows / 32 / kPerQ;  // 32-row groups per warp and row block, at most
+    float2* my = state + q * kPairMaxRows;  // the quarter's state of every row of the block, at its end
     unsigned char* mybad = sbad + q * kPairMaxRows;
     float* scr = scratch + warp * kPairScr;
     const int rr = lane & 15, eh = lane >> 4;  // after the transpose: row rr of a half group, entries 16 eh ..
@@ -626,10 +627,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int rb = 0; rb < nrb; ++rb) {
       const int rows = min(rbrows, P.R - rb * rbrows);
       const int ngrp = (rows + 31) / 32;
-      for (int g = h; g < ngrp; g += kPerQ) {
-        my[g * 32 + lane] = P.greedy ? make_float2(-kInf, __int_as_float(-1)) : make_float2(-kInf, 0.f);
-        mybad[g * 32 + lane] = 0;
-      }
+      // the running states of this lane's rows (group h + kPerQ k, half hh,
+      // row rr), the same bits in lanes l and l ^ 16; bit 2k + hh of bad
+      // marks a row that saw a NaN or +inf
+      float2 st[kGrpW][2];
+      unsigned bad = 0;
+#pragma unroll
+      for (int k = 0; k < kGrpW; ++k)
+        st[k][0] = st[k][1] = P.greedy ? make_float2(-kInf, __int_as_float(-1)) : make_float2(-kInf, 0.f);
       for (int vt = v_t0; vt < v_t1; ++vt, ++acc) {
         // the warp decides together: the TMEM loads below are warp-wide
         const bool ready = __all_sync(0xffffffffu, lm_wait(&tfull, static_cast<unsigned>(acc) & 1u, fault));
@@ -639,7 +644,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int nv = max(0, min(32, P.V - vw));            // of its 32 entries, those below V
         const int e0 = eh * 16;                              // this lane's first entry after the transpose
         const int nl = max(0, min(16, nv - e0));             // of its 16 entries, those below V
-        for (int g = h; g < ngrp; g += kPerQ) {
+#pragma unroll
+        for (int k = 0; k < kGrpW; ++k) {
+          const int g = h + kPerQ * k;
+          if (g >= ngrp) break;
           float x[32];
           tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(g * 32), x);
 #pragma unroll
@@ -661,8 +669,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               y[4 * k + 3] = v.w;
             }
             __syncwarp();
-            const int si = g * 32 + hh * 16 + rr;  // the row's index within the block
-            const int row = rb * rbrows + si;      // its hidden row
+            const int row = rb * rbrows + g * 32 + hh * 16 + rr;  // the lane's hidden row
             if (P.logits && row < P.R) {
               // 16 consecutive float32 logits: whole 32-byte sectors
               float* dst = P.logits + static_cast<long long>(row) * P.ldl + vw + e0;
@@ -675,7 +682,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                   if (i < nl) dst[i] = y[i];
               }
             }
-            const float2 cur = my[si];
+            const float2 cur = st[k][hh];
             // the row's maximum over its 32 entries, NaN-propagating: each
             // lane's 16, then the lane pair (l, l ^ 16)
             float cm = nl == 16 ? max16<true>(y, nl) : max16<false>(y, nl);
@@ -684,7 +691,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               // NaN or +inf marks the row bad; a maximum strictly above the
               // running one moves the argmax to its first entry (ties keep
               // the lowest index)
-              if (!(cm < kInf) && eh == 0) mybad[si] = 1;
+              if (!(cm < kInf)) bad |= 1u << (2 * k + hh);
               const bool up = cm > cur.x && cm < kInf;
               int first = 32;
               if (up) {
@@ -692,15 +699,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (f < 16) first = e0 + f;
               }
               first = min(first, __shfl_xor_sync(0xffffffffu, first, 16));
-              if (up && eh == 0) my[si] = make_float2(cm, __int_as_float(vw + first));
+              if (up) st[k][hh] = make_float2(cm, __int_as_float(vw + first));
             } else {
               const float mn = fmax_nan(cur.x, cm);
               const float Mn = (mn == -kInf) ? 0.f : scaled_max(mn, c);
               float sp = nl == 16 ? sum16<true>(y, nl, c, Mn) : sum16<false>(y, nl, c, Mn);
               sp = __fadd_rn(sp, __shfl_xor_sync(0xffffffffu, sp, 16));  // the same bits in both lanes
-              if (mn != -kInf && eh == 0) {
+              if (mn != -kInf) {
                 const float scale = (cur.x == -kInf) ? 0.f : ex2(scaled_max(cur.x, c) - Mn);
-                my[si] = make_float2(mn, __fadd_rn(__fmul_rn(cur.y, scale), sp));
+                st[k][hh] = make_float2(mn, __fadd_rn(__fmul_rn(cur.y, scale), sp));
               }
             }
           }
@@ -710,6 +717,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (lane == 0) {
           if (lead) mbar_arrive(&tempty);
           else mbar_arrive_remote(cluster_addr(&tempty, 0));
+        }
+      }
+      // this warp's rows into the quarter's states (lanes 0-15 of the pairs)
+      if (eh == 0) {
+#pragma unroll
+        for (int k = 0; k < kGrpW; ++k) {
+          const int g = h + kPerQ * k;
+          if (g >= ngrp) break;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            my[g * 32 + hh * 16 + rr] = st[k][hh];
+            mybad[g * 32 + hh * 16 + rr] = (bad >> (2 * k + hh)) & 1u;
+          }
         }
       }
       // merge the four quarters' states of each row, in quarter order, into this
