@@ -1454,7 +1454,7 @@ def run_lm_head(args, w):
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                 "peak_source": hbm_src, "algorithmic_bytes": nbytes}
     launches = 2 if (s.greedy or s.gamma == 0) else 3
-    roof.update({"kernel": "whole call: lm_head_kernel per head + chain walk", "unit_of_work": "one call",
+    roof.update({"kernel": "whole call: one head kernel per head (lm_head_pair_kernel on CTA pairs or lm_head_kernel, as the library picks) + chain walk", "unit_of_work": "one call",
                  "kernel_ms": ms,
                  "other": {"tensor_TFLOPs": tfs, "tensor_frac": tfs / tc_peak, "weights_GBps": gbs,
                            "hbm_frac": gbs / hbm_peak},
