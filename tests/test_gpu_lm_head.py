@@ -139,6 +139,12 @@ CASES = [
     W(BASE, name="pairs_rows270_v5001_d200", B=54, gamma=4, V=5001, d_target=200, d_draft=200),
     W(BASE, name="g0_bonus_only", B=6, gamma=0, V=2000, d_target=64, d_draft=64),
     W(BASE, name="v40000_d1024_T1.3", B=4, gamma=5, V=40000, d_target=1024, d_draft=1024, temperature=1.3),
+    # the interface's limits: the largest vocabulary (one partial per CTA and
+    # row, one CTA per SM, merged by the walk's warp-per-row form; d = 8 is
+    # one K step, mostly zero-filled by the copy engine) and the widest
+    # hidden state (1024 K steps per tile)
+    W(BASE, name="vmax_2097152_d8", B=2, gamma=1, V=2097152, d_target=8, d_draft=8),
+    W(BASE, name="dmax_65536_v1000", B=2, gamma=2, V=1000, d_target=65536, d_draft=65536),
 ]
 
 
