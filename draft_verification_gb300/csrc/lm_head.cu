@@ -661,12 +661,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             __syncwarp();
             float y[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float4 v = *reinterpret_cast<const float4*>(scr + rr * kPairScrLd + e0 + 4 * k);
-              y[4 * k] = v.x;
-              y[4 * k + 1] = v.y;
-              y[4 * k + 2] = v.z;
-              y[4 * k + 3] = v.w;
+            for (int f = 0; f < 4; ++f) {
+              const float4 v = *reinterpret_cast<const float4*>(scr + rr * kPairScrLd + e0 + 4 * f);
+              y[4 * f] = v.x;
+              y[4 * f + 1] = v.y;
+              y[4 * f + 2] = v.z;
+              y[4 * f + 3] = v.w;
             }
             __syncwarp();
             const int row = rb * rbrows + g * 32 + hh * 16 + rr;  // the lane's hidden row
@@ -741,18 +741,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         float2 out;
         if (P.greedy) {
           ArgMax m2{-kInf, -1};
-          bool bad = false;
+          bool rbad = false;
           for (int w = 0; w < 4; ++w) {
-            const float2 st = state[w * kPairMaxRows + r];
-            m2 = am_merge(m2, ArgMax{st.x, __float_as_int(st.y)});
-            bad |= sbad[w * kPairMaxRows + r] != 0;
+            const float2 sw = state[w * kPairMaxRows + r];
+            m2 = am_merge(m2, ArgMax{sw.x, __float_as_int(sw.y)});
+            rbad |= sbad[w * kPairMaxRows + r] != 0;
           }
-          out = make_float2(bad ? __int_as_float(0x7fc00000) : m2.v, __int_as_float(m2.i));
+          out = make_float2(rbad ? __int_as_float(0x7fc00000) : m2.v, __int_as_float(m2.i));
         } else {
           MaxSum m2{-kInf, 0.f};
           for (int w = 0; w < 4; ++w) {
-            const float2 st = state[w * kPairMaxRows + r];
-            m2 = ms_merge(m2, MaxSum{st.x, st.y}, c);
+            const float2 sw = state[w * kPairMaxRows + r];
+            m2 = ms_merge(m2, MaxSum{sw.x, sw.y}, c);
           }
           out = make_float2(m2.m, m2.s);
         }
