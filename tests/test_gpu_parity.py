@@ -36,6 +36,12 @@ CHAIN_SMALL = [
     W(S["sampling_chain_b32_g8_v32000_bf16"], name="f32_v12000_g32", B=3, gamma=32, V=12000, dtype="f32"),
     W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_f32_v4097_pad2", B=7, gamma=6, V=4097, pad=2),
     W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_bf16_v50257", B=5, gamma=4, V=50257, dtype="bf16"),
+    # the interface's limits: the largest vocabulary (128 statistics chunks
+    # per row) and the largest batch (65535 sequences of a tiny vocabulary:
+    # launch grids 65535 deep, one single-CTA cluster per sequence)
+    W(S["sampling_chain_b32_g8_v32000_bf16"], name="bf16_vmax_2097152_g2", B=2, gamma=2, V=2097152),
+    W(S["sampling_chain_b32_g8_v32000_bf16"], name="bf16_bmax_65535_v16_g1", B=65535, gamma=1, V=16),
+    W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_f32_bmax_65535_v16", B=65535, gamma=1, V=16),
 ]
 
 
