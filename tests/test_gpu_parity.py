@@ -37,9 +37,13 @@ CHAIN_SMALL = [
     W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_f32_v4097_pad2", B=7, gamma=6, V=4097, pad=2),
     W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_bf16_v50257", B=5, gamma=4, V=50257, dtype="bf16"),
     # the interface's limits: the largest vocabulary (128 statistics chunks
-    # per row) and the largest batch (65535 sequences of a tiny vocabulary:
-    # launch grids 65535 deep, one single-CTA cluster per sequence)
-    W(S["sampling_chain_b32_g8_v32000_bf16"], name="bf16_vmax_2097152_g2", B=2, gamma=2, V=2097152),
+    # per row; a low temperature concentrates the softmax on a few tokens, so
+    # that draws and accept tests do not fall within the near-tie margins,
+    # which a flat distribution over 2^21 tokens would) and the largest batch
+    # (65535 sequences of a tiny vocabulary: launch grids 65535 deep, one
+    # single-CTA cluster per sequence)
+    W(S["sampling_chain_b32_g8_v32000_bf16"], name="bf16_vmax_2097152_g2", B=2, gamma=2, V=2097152,
+      temperature=0.05),
     W(S["sampling_chain_b32_g8_v32000_bf16"], name="bf16_bmax_65535_v16_g1", B=65535, gamma=1, V=16),
     W(S["greedy_chain_b4_g4_v1000_f32"], name="greedy_f32_bmax_65535_v16", B=65535, gamma=1, V=16),
 ]
@@ -168,6 +172,13 @@ TREE_SMALL = [
     W(S["tree_b16_n64_v50257_bf16"], name="tree_f32_v999_n40", B=4, V=999, dtype="f32", n_nodes=40),
     W(S["tree_b16_n64_v50257_bf16"], name="tree_wide_root", B=4, V=4000, n_nodes=9, branching=(8,)),
     W(S["tree_b16_n64_v50257_bf16"], name="tree_greedy_v20000", B=6, V=20000, greedy=True),
+    # the interface's limits: the most nodes (1024, a binary tree ten levels
+    # deep) and the largest vocabulary (at a low temperature, as for chains)
+    W(S["tree_b16_n64_v50257_bf16"], name="tree_nmax_1024_v64", B=2, V=64, n_nodes=1024, branching=(2,) * 10),
+    W(S["tree_b16_n64_v50257_bf16"], name="tree_greedy_nmax_1024_v64", B=2, V=64, n_nodes=1024,
+      branching=(2,) * 10, greedy=True),
+    W(S["tree_b16_n64_v50257_bf16"], name="tree_vmax_2097152_n6", B=1, V=2097152, n_nodes=6, branching=(2, 2),
+      temperature=0.05),
 ]
 
 
@@ -225,6 +236,9 @@ CASCADE_SMALL = [
     W(S["cascade_b128_g8_g4_v128256_bf16"], name="cascade_g3_g4_v30000", B=8, gamma1=3, gamma2=4, V=30000),
     W(S["cascade_b128_g8_g4_v128256_bf16"], name="cascade_f32_v4000", B=6, V=4000, dtype="f32"),
     W(S["cascade_b128_g8_g4_v128256_bf16"], name="cascade_greedy_v16000", B=8, V=16000, greedy=True),
+    # the largest vocabulary the interface accepts (at a low temperature, as
+    # for chains)
+    W(S["cascade_b128_g8_g4_v128256_bf16"], name="cascade_vmax_2097152", B=2, V=2097152, temperature=0.05),
 ]
 
 
