@@ -517,10 +517,13 @@ spec_status spec_clasp_layer_select(const spec_clasp_args* args, cudaStream_t st
 /*    at the gamma positions H_d W_d^T: bfloat16 hidden states and weights,  */
 /*    float32 accumulation on the tensor cores (so a logit differs from the  */
 /*    exact product by float32 rounding of a d-term sum).                    */
-/*  - Each head is one persistent kernel (one CTA per SM, a slab of the      */
-/*    vocabulary each) whose epilogue folds every 128-entry tile of logits   */
-/*    into per-row (max, sum of exponentials) (sampling) or argmax (greedy)  */
-/*    partials, the format the chain walk merges; then the chain walk.       */
+/*  - Each head is one persistent kernel whose CTAs (or CTA pairs) own a     */
+/*    slab of the vocabulary each and fold every tile of logits into per-row */
+/*    (max, sum of exponentials) (sampling) or argmax (greedy) partials, the */
+/*    format the chain walk merges; then the chain walk.  When the target    */
+/*    head has 256 rows or more and the pairs' 256-entry tiles balance       */
+/*    better than the single CTAs' tiles, both heads run on CTA pairs        */
+/*    (tcgen05 cta_group::2); otherwise on one CTA per SM.                   */
 /*  - Greedy mode writes no logits anywhere.  Sampling mode stores the       */
 /*    float32 logits of every row in the workspace, because the residual or */
 /*    bonus draw reads one or two rows per sequence chosen only after the    */
