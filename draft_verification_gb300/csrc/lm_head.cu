@@ -38,6 +38,13 @@
 // kernel's format, so the chain walk merges them exactly like the partials of
 // stored logits.  Greedy calls store no logits at all: the walk needs only
 // the argmaxes.
+//
+// lm_head_pair_kernel (described at its definition): the same product and
+// partials on clusters of two CTAs issuing cta_group::2 products over
+// 256-entry vocabulary tiles, which halves each CTA's tensor-pipe operand
+// reads.  The host picks it when the target head has at least 256 rows and
+// its tiles balance better over the pairs than the single-CTA tiles over the
+// SMs; both heads of a call then use it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
