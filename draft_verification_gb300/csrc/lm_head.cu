@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPairM = 256;              // vocabulary entries per pair tile
 constexpr int kPairMaxRows = 512;        // hidden rows per row block (TMEM columns)
-constexpr int kPairRing = 168 * 1024;    // ring budget per CTA
+constexpr int kPairRing = 188 * 1024;    // ring budget per CTA
 constexpr int kPairMaxStages = 12;
 // CTA pairs only for calls whose target head has at least this many rows
 // (the products dominate; smaller calls stream the weights faster on single
@@ -431,7 +431,9 @@ constexpr int kPairIss0 = kPairEpi + 1;  // the first MMA-issuing warp
 constexpr int kPairThreads = 32 * (kPairEpi + 1 + kPairIssuers);
 constexpr int kPairScrLd = 36;           // floats per row of a warp's transpose block (32 entries, padded)
 constexpr int kPairScr = 16 * kPairScrLd;  // floats of one warp's transpose block (16 rows x 32 entries)
-constexpr int kPairExtra = 4 * kPairMaxRows * 8 + 4 * kPairMaxRows + kPairEpi * kPairScr * 4;  // states, flags, blocks
+constexpr int kPairExtra = kPairEpi * kPairScr * 4;  // the epilogue warps' transpose blocks
+// a row block's quarter states and bad-row flags reuse the transpose blocks
+static_assert(4 * kPairMaxRows * 8 + 4 * kPairMaxRows <= kPairExtra, "quarter states fit the transpose blocks");
 
 struct LmPairParams {
   int R, V, d, nkb;
@@ -518,9 +520,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                                          ~static_cast<uintptr_t>(1023));
   const int xhalf = P.nc / 2 * kBK * 2;  // one CTA's half of a chunk of hidden rows, one K step
   const int stage_bytes = kPairWBytes + P.nch * xhalf;
-  float2* state = reinterpret_cast<float2*>(ring + static_cast<size_t>(P.stages) * stage_bytes);
+  float* scratch = reinterpret_cast<float*>(ring + static_cast<size_t>(P.stages) * stage_bytes);
+  // at the end of a row block, once every epilogue warp is past its
+  // transposes, the same bytes hold the quarter states and bad-row flags
+  float2* state = reinterpret_cast<float2*>(scratch);
   unsigned char* sbad = reinterpret_cast<unsigned char*>(state + 4 * kPairMaxRows);
-  float* scratch = reinterpret_cast<float*>(sbad + 4 * kPairMaxRows);
   const int pairs = static_cast<int>(gridDim.x) / 2, pair = static_cast<int>(blockIdx.x) / 2;
   const int v_t0 = static_cast<int>((static_cast<long long>(pair) * P.ntv) / pairs);
   const int v_t1 = static_cast<int>((static_cast<long long>(pair + 1) * P.ntv) / pairs);
@@ -726,7 +730,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           else mbar_arrive_remote(cluster_addr(&tempty, 0));
         }
       }
-      // this warp's rows into the quarter's states (lanes 0-15 of the pairs)
+      // this warp's rows into the quarter's states (lanes 0-15 of the pairs),
+      // which overlay the transpose blocks: every warp is past its last
+      // transpose of the block first
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpi * 32) : "memory");
       if (eh == 0) {
 #pragma unroll
         for (int k = 0; k < kGrpW; ++k) {
